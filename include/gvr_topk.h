@@ -1,0 +1,150 @@
+/*
+ * gvr_topk.h -- C ABI of libgvrtopk: exact per-row top-K over fp32 sparse-attention indexer
+ * scores by hint-free Guess-Verify-Refine (GVR) self-sampling, on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation.  For every row r the library returns the K window-local indices of the K
+ * largest scores of that row's valid window W_r = [a_r, a_r + nv_r) of
+ * logits[r * row_stride + ...]:
+ *   - "exact (tie-interchangeable) top-K": when several scores tie at the K-th largest value
+ *     tau, any choice among the tied entries is correct; -0 and +0 are one tie class; +inf and
+ *     -inf are ordinary values ("Block-skip fast path for self-sampling GVR top-K decode",
+ *     TensorRT-LLM PR #18122, commit log "Contract" and "run_varlen");
+ *   - a window with nv_r <= K yields the identity 0, 1, ..., nv_r - 1 followed by -1 pads
+ *     ("Self-sampling GVR V2 prefill indexer top-K", PR #18702, section "Kernel");
+ *   - the K indices of a longer row come in no particular order;
+ *   - scores outside the window (padding, other requests, +inf/NaN/3e38/-inf poison) never
+ *     influence the result; NaN inside a window is outside the contract: the result is then K
+ *     distinct in-window indices, but which ones is unspecified.
+ * How it is computed ("GVR K=2048 reg_clus with block64 sampling and parallel rescue",
+ * PR #20998, sections "Why the GLM row overflows" and "What changes"): uniform block64
+ * sampling of exactly K scores gives a value bracket [GMIN, GMAX]; a value histogram over the
+ * bracket finds the bin that crosses tau; the members of that bin go to a bounded candidate
+ * buffer and an exact refine picks the remaining winners; an invalid bracket or an overflowing
+ * buffer sends the row to an exact radix rescue that runs on every CTA of the row's cluster.
+ *
+ * Conventions shared by every entry point.
+ *   - All pointers except `options` are DEVICE pointers into memory the caller owns.  The
+ *     library allocates nothing, never reads device memory on the host and never
+ *     synchronizes: each call validates its arguments on the host and enqueues ONE kernel on
+ *     `stream` (a cudaStream_t; NULL is the legacy default stream).  The result is ready when
+ *     the stream reaches that point.  The first call on a device sets kernel attributes once.
+ *   - logits is fp32 [num_rows][row_stride], row-major with unit inner stride; its base must
+ *     be 16-byte aligned and row_stride a multiple of 4 (float4 rows), 4 <= row_stride <
+ *     2^31.  Reads stay inside each row's window, widened at its start only down to the
+ *     16-byte boundary (never past the window's last score).
+ *   - indices is int32 [num_rows][k] (row stride exactly k); values (when non-NULL) is fp32
+ *     [num_rows][k].  Every one of the k slots of every row is written.
+ *   - k must be 512, 1024 or 2048.
+ *   - num_rows == 0 is a no-op that returns GVR_OK.
+ *   - Errors are returned, never raised on the device: argument errors are detected on the
+ *     host before anything is enqueued; GVR_ERR_LAUNCH reports a failed launch.
+ *   - Calls may run concurrently on different streams: no state is shared between calls.
+ */
+#ifndef GVR_TOPK_H
+#define GVR_TOPK_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gvr_status {
+  GVR_OK = 0,
+  GVR_ERR_NULL = 1,   /* a required pointer is NULL */
+  GVR_ERR_ALIGN = 2,  /* logits is not 16-byte aligned, or indices/values not 4-byte aligned */
+  GVR_ERR_STRIDE = 3, /* row_stride is not a multiple of 4, below 4, or not below 2^31 */
+  GVR_ERR_K = 4,      /* k is not 512, 1024 or 2048 */
+  GVR_ERR_ARG = 5,    /* a negative row count, next_n < 1, compress_ratio < 1, bad options */
+  GVR_ERR_LAUNCH = 6  /* the kernel launch failed (no device, bad configuration, ...) */
+} gvr_status;
+
+/*
+ * Decode top-K.  Row r belongs to request r / next_n and has
+ *   n_r = (kv_lens[r / next_n] - next_n + r % next_n + 1) / compress_ratio
+ * valid scores logits[r][0 .. n_r) (integer division), with n_r = 0 when
+ * kv_lens[r / next_n] < next_n and n_r clamped to row_stride.  This is the MTP window formula
+ * of "Block-skip fast path for self-sampling GVR top-K decode" (PR #18122, commit
+ * "run_varlen"): kv_lens holds each request's total uncompressed cache length, and the
+ * empty-row rule is from its commit "engine/reference convention alignment".
+ *   kv_lens  int32 [ceil(num_rows / next_n)], device, read on the device only.
+ *   indices  int32 [num_rows][k]: window indices (= column indices for decode), -1 pads.
+ *   values   optional fp32 [num_rows][k]: the score at each returned index, bit-exact copied
+ *            from logits; -FLT_MAX in -1 slots ("values output" commit of PR #18122).
+ */
+gvr_status topk_decode(const float* logits, int64_t row_stride, int64_t num_rows,
+                       const int32_t* kv_lens, int32_t next_n, int32_t compress_ratio, int32_t k,
+                       int32_t* indices, float* values, void* stream);
+
+/*
+ * Prefill top-K.  Row r selects over the window [row_starts[r], row_ends[r]) of its own row
+ * (compressed column units) and writes LOCAL indices (column - row_starts[r]) with a trailing
+ * -1 pad; nv <= k yields the identity 0..nv-1 ("Self-sampling GVR V2 prefill indexer top-K",
+ * PR #18702, section "Kernel").  The window start need not be 16-byte aligned: the loads start
+ * at the aligned column below it and the lead lanes are excluded by position.  A start below 0
+ * is treated as 0, an end beyond row_stride as row_stride, and an end at or before the start
+ * as an empty window.
+ *   row_starts, row_ends  int32 [num_rows], device.
+ *   indices               int32 [num_rows][k].
+ */
+gvr_status topk_prefill(const float* logits, int64_t row_stride, int64_t num_rows,
+                        const int32_t* row_starts, const int32_t* row_ends, int32_t k,
+                        int32_t* indices, void* stream);
+
+/* Tuning and diagnostics for the *_ex entry points (the plain entry points use all zeros). */
+enum {
+  GVR_FLAG_FORCE_RESCUE = 1, /* skip the histogram: every long row takes the exact rescue */
+  GVR_FLAG_NO_FLOOR = 2,     /* count every bin of the value histogram (no sampled floor) */
+  GVR_FLAG_ZERO_CAP = 4,     /* candidate buffer of 0 slots: every long row overflows to rescue */
+  GVR_FLAG_RADIX_REFINE = 8  /* refine every candidate set by radix select (not by ranking) */
+};
+
+typedef struct gvr_options {
+  int32_t cluster_size;       /* CTAs per row: 0 = automatic, else 1, 2, 4 or 8 */
+  int32_t vectors_per_thread; /* float4 registers per thread: 0 = automatic, else 1, 2, 4, 8 */
+  int32_t flags;              /* GVR_FLAG_* bits; results stay exact under every flag */
+  int32_t reserved;           /* must be 0 */
+  int32_t* row_stats;         /* optional device int32 [num_rows][4]: path (GVR_PATH_*),
+                                 candidate count m, histogram rounds, winners above the
+                                 crossing bin */
+} gvr_options;
+
+/* Values of row_stats[r][0]. */
+enum {
+  GVR_PATH_SHORT = 0,           /* nv <= k: identity and -1 pad */
+  GVR_PATH_REFINE = 1,          /* histogram, crossing bin, candidates, exact refine */
+  GVR_PATH_RESCUE_BRACKET = 2,  /* invalid sampled bracket: exact rescue */
+  GVR_PATH_RESCUE_OVERFLOW = 3, /* crossing bin exceeded the candidate buffer: exact rescue */
+  GVR_PATH_RESCUE_FORCED = 4    /* GVR_FLAG_FORCE_RESCUE */
+};
+
+/* topk_decode with tuning/diagnostic options (NULL = automatic, identical to topk_decode). */
+gvr_status topk_decode_ex(const float* logits, int64_t row_stride, int64_t num_rows,
+                          const int32_t* kv_lens, int32_t next_n, int32_t compress_ratio,
+                          int32_t k, int32_t* indices, float* values, void* stream,
+                          const gvr_options* options);
+
+/* topk_prefill with tuning/diagnostic options (NULL = automatic, identical to topk_prefill). */
+gvr_status topk_prefill_ex(const float* logits, int64_t row_stride, int64_t num_rows,
+                           const int32_t* row_starts, const int32_t* row_ends, int32_t k,
+                           int32_t* indices, void* stream, const gvr_options* options);
+
+/* Static English text for a status code; never NULL. */
+const char* gvr_status_string(gvr_status status);
+
+/*
+ * The launch geometry the library would choose for a call on the current device (host
+ * only, no device work): CTAs per row (cluster size), float4 registers per thread, threads
+ * per CTA and dynamic shared memory bytes.  Returns the GVR_ERR_* code the entry points would
+ * return for these arguments.  sm_count > 0 overrides the device's SM count (for planning
+ * without a device); any output pointer may be NULL.
+ */
+gvr_status gvr_plan(int64_t row_stride, int64_t num_rows, int32_t k, const gvr_options* options,
+                    int32_t sm_count, int32_t* cluster_size, int32_t* vectors_per_thread,
+                    int32_t* threads, int32_t* smem_bytes);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GVR_TOPK_H */

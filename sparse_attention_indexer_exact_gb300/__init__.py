@@ -1,0 +1,204 @@
+"""Exact per-row top-K for a DSA sparse-attention indexer on one GB300 (sm_103a).
+
+A thin Python binding over the C ABI of ``libgvrtopk.so`` (declared in
+``include/gvr_topk.h``).  Every step of the selection runs in the library's
+CUDA kernel; this module only checks tensor types, takes device pointers and
+the current CUDA stream, and forwards them.  PyTorch is used for device
+memory and streams only.  There is no CPU fallback: if the library has not
+been built (``python -m sparse_attention_indexer_exact_gb300._build`` or
+``__graft_entry__.build()``), every call raises.
+
+Entry points (same names as the C ABI):
+
+* ``topk_decode(logits, kv_lens, next_n, compress_ratio, k, ...)`` -- decode
+  rows, n = (kv_len - next_n + row % next_n + 1) // compress_ratio valid
+  scores per row ("Block-skip fast path for self-sampling GVR top-K decode",
+  TensorRT-LLM PR #18122, commit "run_varlen");
+* ``topk_prefill(logits, row_starts, row_ends, k, ...)`` -- per-row windows
+  [row_starts, row_ends) written in the local frame with a -1 pad
+  ("Self-sampling GVR V2 prefill indexer top-K", PR #18702, "Kernel").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = ["topk_decode", "topk_prefill", "topk_decode_raw", "topk_prefill_raw", "plan", "Options",
+           "GvrError", "library_path", "load_library", "FLAG_FORCE_RESCUE", "FLAG_NO_FLOOR", "FLAG_ZERO_CAP",
+           "FLAG_RADIX_REFINE", "PATH_NAMES", "SUPPORTED_K"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libgvrtopk.so")
+_lock = threading.Lock()
+_lib = None
+
+FLAG_FORCE_RESCUE, FLAG_NO_FLOOR, FLAG_ZERO_CAP, FLAG_RADIX_REFINE = 1, 2, 4, 8
+PATH_NAMES = {0: "short", 1: "refine", 2: "rescue_bracket", 3: "rescue_overflow", 4: "rescue_forced"}
+SUPPORTED_K = (512, 1024, 2048)
+EXPORTED_SYMBOLS = ("topk_decode", "topk_prefill", "topk_decode_ex", "topk_prefill_ex", "gvr_status_string",
+                    "gvr_plan")
+
+
+class GvrError(RuntimeError):
+    """A non-zero gvr_status returned by the library."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"gvr status {status}: {message}")
+        self.status = status
+
+
+class Options(ctypes.Structure):
+    """Mirror of ``gvr_options`` (tuning and diagnostics of the *_ex entry points)."""
+    _fields_ = [("cluster_size", ctypes.c_int32), ("vectors_per_thread", ctypes.c_int32),
+                ("flags", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("row_stats", ctypes.c_void_p)]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _declare(lib):
+    i64, i32, p = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+    lib.topk_decode.argtypes = [p, i64, i64, p, i32, i32, i32, p, p, p]
+    lib.topk_decode_ex.argtypes = [p, i64, i64, p, i32, i32, i32, p, p, p, ctypes.POINTER(Options)]
+    lib.topk_prefill.argtypes = [p, i64, i64, p, p, i32, p, p]
+    lib.topk_prefill_ex.argtypes = [p, i64, i64, p, p, i32, p, p, ctypes.POINTER(Options)]
+    lib.gvr_plan.argtypes = [i64, i64, i32, ctypes.POINTER(Options), i32] + [ctypes.POINTER(i32)] * 4
+    for f in (lib.topk_decode, lib.topk_decode_ex, lib.topk_prefill, lib.topk_prefill_ex, lib.gvr_plan):
+        f.restype = ctypes.c_int
+    lib.gvr_status_string.argtypes = [ctypes.c_int]
+    lib.gvr_status_string.restype = ctypes.c_char_p
+    return lib
+
+
+def load_library(path: str | None = None):
+    """Load libgvrtopk.so; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if path is not None:
+            return _declare(ctypes.CDLL(path))
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(f"{_LIB_PATH} is missing: build it with "
+                                   "`python -m sparse_attention_indexer_exact_gb300._build` (no CPU fallback exists)")
+            _lib = _declare(ctypes.CDLL(_LIB_PATH))
+        return _lib
+
+
+def _check(status: int):
+    if status != 0:
+        lib = load_library()
+        raise GvrError(status, lib.gvr_status_string(status).decode())
+
+
+# ----------------------------------------------------------------------------- raw pointers
+def topk_decode_raw(logits_ptr: int, row_stride: int, num_rows: int, kv_lens_ptr: int, next_n: int,
+                    compress_ratio: int, k: int, indices_ptr: int, values_ptr: int | None, stream: int,
+                    options: Options | None = None) -> None:
+    """``topk_decode`` / ``topk_decode_ex`` on raw device addresses (enqueue only)."""
+    lib = load_library()
+    if options is None:
+        st = lib.topk_decode(logits_ptr, row_stride, num_rows, kv_lens_ptr, next_n, compress_ratio, k,
+                             indices_ptr, values_ptr, stream)
+    else:
+        st = lib.topk_decode_ex(logits_ptr, row_stride, num_rows, kv_lens_ptr, next_n, compress_ratio, k,
+                                indices_ptr, values_ptr, stream, ctypes.byref(options))
+    _check(st)
+
+
+def topk_prefill_raw(logits_ptr: int, row_stride: int, num_rows: int, row_starts_ptr: int, row_ends_ptr: int,
+                     k: int, indices_ptr: int, stream: int, options: Options | None = None) -> None:
+    """``topk_prefill`` / ``topk_prefill_ex`` on raw device addresses (enqueue only)."""
+    lib = load_library()
+    if options is None:
+        st = lib.topk_prefill(logits_ptr, row_stride, num_rows, row_starts_ptr, row_ends_ptr, k, indices_ptr,
+                              stream)
+    else:
+        st = lib.topk_prefill_ex(logits_ptr, row_stride, num_rows, row_starts_ptr, row_ends_ptr, k, indices_ptr,
+                                 stream, ctypes.byref(options))
+    _check(st)
+
+
+def plan(row_stride: int, num_rows: int, k: int, options: Options | None = None, sm_count: int = 0) -> dict:
+    """Launch geometry the library would choose (host only)."""
+    lib = load_library()
+    outs = [ctypes.c_int32(0) for _ in range(4)]
+    st = lib.gvr_plan(row_stride, num_rows, k, ctypes.byref(options) if options is not None else None, sm_count,
+                      *[ctypes.byref(o) for o in outs])
+    _check(st)
+    cs, vpt, threads, smem = (o.value for o in outs)
+    return {"cluster_size": cs, "vectors_per_thread": vpt, "threads": threads, "smem_bytes": smem}
+
+
+# ----------------------------------------------------------------------------- torch tensors
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream) -> int:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _rows_2d(logits):
+    torch = _torch()
+    if not isinstance(logits, torch.Tensor) or not logits.is_cuda:
+        raise TypeError("logits must be a CUDA tensor")
+    if logits.dtype != torch.float32:
+        raise TypeError("logits must be float32")
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be 2-D with unit inner stride")
+    return logits.shape[0], logits.stride(0)
+
+
+def _int32_vec(t, n, name):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.int32:
+        raise TypeError(f"{name} must be a CUDA int32 tensor")
+    if t.dim() != 1 or t.stride(0) != 1 or t.numel() < n:
+        raise ValueError(f"{name} must be 1-D contiguous with at least {n} entries")
+
+
+def _out(t, rows, k, dtype, device, name):
+    torch = _torch()
+    if t is None:
+        return torch.empty((rows, k), dtype=dtype, device=device)
+    if t.dtype != dtype or not t.is_cuda or t.shape != (rows, k) or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor of shape ({rows}, {k})")
+    return t
+
+
+def topk_decode(logits, kv_lens, next_n: int, compress_ratio: int, k: int, indices=None, values=None, *,
+                want_values: bool = False, stream=None, options: Options | None = None):
+    """Decode top-K of each row of ``logits`` [rows, >=n]; returns (indices, values or None).
+
+    ``logits.stride(0)`` is the row stride.  ``kv_lens`` is int32 [ceil(rows / next_n)].
+    """
+    rows, stride = _rows_2d(logits)
+    _int32_vec(kv_lens, (rows + next_n - 1) // max(next_n, 1), "kv_lens")
+    indices = _out(indices, rows, k, _torch().int32, logits.device, "indices")
+    if values is None and want_values:
+        values = _out(None, rows, k, _torch().float32, logits.device, "values")
+    elif values is not None:
+        values = _out(values, rows, k, _torch().float32, logits.device, "values")
+    topk_decode_raw(logits.data_ptr(), stride, rows, kv_lens.data_ptr(), next_n, compress_ratio, k,
+                    indices.data_ptr(), values.data_ptr() if values is not None else None,
+                    _stream_handle(stream), options)
+    return indices, values
+
+
+def topk_prefill(logits, row_starts, row_ends, k: int, indices=None, *, stream=None,
+                 options: Options | None = None):
+    """Prefill top-K over per-row windows [row_starts, row_ends); returns local indices [rows, k]."""
+    rows, stride = _rows_2d(logits)
+    _int32_vec(row_starts, rows, "row_starts")
+    _int32_vec(row_ends, rows, "row_ends")
+    indices = _out(indices, rows, k, _torch().int32, logits.device, "indices")
+    topk_prefill_raw(logits.data_ptr(), stride, rows, row_starts.data_ptr(), row_ends.data_ptr(), k,
+                     indices.data_ptr(), _stream_handle(stream), options)
+    return indices

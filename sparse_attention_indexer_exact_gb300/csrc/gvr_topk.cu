@@ -1,0 +1,251 @@
+// gvr_topk.cu -- host side of libgvrtopk: argument validation, launch geometry and the
+// C entry points declared in include/gvr_topk.h.
+//
+// Every entry point checks its arguments on the host, picks a launch geometry from host-known
+// quantities only (row stride, row count, k, the device's SM count) and enqueues one
+// cluster launch of gvr_topk_kernel on the caller's stream.  Nothing is allocated, no device
+// memory is read on the host and nothing synchronizes, so a call costs one launch.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "gvr_kernel.cuh"
+#include "gvr_topk.h"
+
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kMaxDevices = 64;
+constexpr int kMaxVpt = 8;
+constexpr int kMaxCluster = 8;
+
+struct DeviceState {
+  std::once_flag once;
+  cudaError_t err = cudaSuccess;
+  int sms = 0;
+};
+DeviceState g_devices[kMaxDevices];
+
+template <int VPT>
+cudaError_t set_attributes() {
+  return cudaFuncSetAttribute(gvr::gvr_topk_kernel<kThreads, VPT>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(gvr::Smem)));
+}
+
+// One-time per-device set-up: kernel attributes and the SM count.
+cudaError_t device_state(int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  DeviceState& st = g_devices[dev];
+  std::call_once(st.once, [&st, dev]() {
+    cudaError_t r = cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (r == cudaSuccess) r = set_attributes<1>();
+    if (r == cudaSuccess) r = set_attributes<2>();
+    if (r == cudaSuccess) r = set_attributes<4>();
+    if (r == cudaSuccess) r = set_attributes<8>();
+    st.err = r;
+  });
+  *sms = st.sms;
+  return st.err;
+}
+
+bool is_pow2_upto8(int v) { return v == 1 || v == 2 || v == 4 || v == 8; }
+
+int pow2_ceil(int64_t v) {
+  int p = 1;
+  while (p < v && p < (1 << 30)) p <<= 1;
+  return p;
+}
+
+gvr_status check_common(int64_t row_stride, int64_t num_rows, int32_t k, const gvr_options* o) {
+  if (num_rows < 0) return GVR_ERR_ARG;
+  if (row_stride < 4 || row_stride % 4 != 0 || row_stride >= (int64_t(1) << 31)) return GVR_ERR_STRIDE;
+  if (k != 512 && k != 1024 && k != 2048) return GVR_ERR_K;
+  if (o) {
+    if (o->reserved != 0) return GVR_ERR_ARG;
+    if (o->cluster_size != 0 && !is_pow2_upto8(o->cluster_size)) return GVR_ERR_ARG;
+    if (o->vectors_per_thread != 0 && !is_pow2_upto8(o->vectors_per_thread)) return GVR_ERR_ARG;
+    if (o->flags & ~(GVR_FLAG_FORCE_RESCUE | GVR_FLAG_NO_FLOOR | GVR_FLAG_ZERO_CAP | GVR_FLAG_RADIX_REFINE))
+      return GVR_ERR_ARG;
+  }
+  return GVR_OK;
+}
+
+// Launch geometry.  A row's window never exceeds row_stride, so the cluster must hold
+// row_stride / 4 vectors: cluster_size * threads * vpt >= row_stride / 4 (beyond 8 CTAs of 8
+// vectors per thread the kernel streams its share in chunks).  Few rows spread each row over
+// more CTAs (more SMs pulling one row); many rows keep the CTAs per row low.
+void plan_geometry(int64_t row_stride, int64_t num_rows, int sms, const gvr_options* o, int* cs_out,
+                   int* vpt_out) {
+  const int64_t need_vec = row_stride / 4;
+  const int64_t per_cta_max = int64_t(kThreads) * kMaxVpt;
+  int cs;
+  if (o && o->cluster_size) {
+    cs = o->cluster_size;
+  } else {
+    int cs_min = pow2_ceil((need_vec + per_cta_max - 1) / per_cta_max);
+    if (cs_min > kMaxCluster) cs_min = kMaxCluster;
+    int cs_max = pow2_ceil((need_vec + kThreads - 1) / kThreads);
+    if (cs_max > kMaxCluster) cs_max = kMaxCluster;
+    if (cs_max < cs_min) cs_max = cs_min;
+    const int64_t slots = 2 * int64_t(sms > 0 ? sms : 148);  // two 512-thread CTAs per SM
+    cs = cs_min;
+    while (cs < cs_max && num_rows * cs * 2 <= slots) cs *= 2;
+  }
+  int vpt;
+  if (o && o->vectors_per_thread) {
+    vpt = o->vectors_per_thread;
+  } else {
+    vpt = kMaxVpt;
+    for (int v = 1; v <= kMaxVpt; v *= 2) {
+      if (int64_t(cs) * kThreads * v >= need_vec) {
+        vpt = v;
+        break;
+      }
+    }
+  }
+  *cs_out = cs;
+  *vpt_out = vpt;
+}
+
+gvr_status launch(const gvr::Params& prm, int64_t num_rows, const gvr_options* o, void* stream) {
+  int sms = 0;
+  if (device_state(&sms) != cudaSuccess) return GVR_ERR_LAUNCH;
+  int cs = 1, vpt = 1;
+  plan_geometry(prm.row_stride, num_rows, sms, o, &cs, &vpt);
+  const int64_t blocks = num_rows * cs;
+  if (blocks > 0x7fffffffLL) return GVR_ERR_ARG;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(blocks), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = sizeof(gvr::Smem);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(cs);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+
+  cudaError_t e = cudaErrorInvalidValue;
+  switch (vpt) {
+    case 1: e = cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<kThreads, 1>, prm); break;
+    case 2: e = cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<kThreads, 2>, prm); break;
+    case 4: e = cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<kThreads, 4>, prm); break;
+    case 8: e = cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<kThreads, 8>, prm); break;
+    default: break;
+  }
+  return e == cudaSuccess ? GVR_OK : GVR_ERR_LAUNCH;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+gvr_status topk_decode_ex(const float* logits, int64_t row_stride, int64_t num_rows,
+                          const int32_t* kv_lens, int32_t next_n, int32_t compress_ratio,
+                          int32_t k, int32_t* indices, float* values, void* stream,
+                          const gvr_options* options) {
+  gvr_status s = check_common(row_stride, num_rows, k, options);
+  if (s != GVR_OK) return s;
+  if (next_n < 1 || compress_ratio < 1) return GVR_ERR_ARG;
+  if (num_rows == 0) return GVR_OK;
+  if (!logits || !kv_lens || !indices) return GVR_ERR_NULL;
+  if (!aligned(logits, 16) || !aligned(indices, 4) || !aligned(kv_lens, 4) ||
+      (values && !aligned(values, 4)))
+    return GVR_ERR_ALIGN;
+  gvr::Params prm = {};
+  prm.logits = logits;
+  prm.row_stride = row_stride;
+  prm.kv_lens = kv_lens;
+  prm.indices = indices;
+  prm.values = values;
+  prm.row_stats = options ? options->row_stats : nullptr;
+  prm.next_n = next_n;
+  prm.compress_ratio = compress_ratio;
+  prm.k = k;
+  prm.mode = gvr::MODE_DECODE;
+  prm.flags = options ? options->flags : 0;
+  return launch(prm, num_rows, options, stream);
+}
+
+gvr_status topk_decode(const float* logits, int64_t row_stride, int64_t num_rows,
+                       const int32_t* kv_lens, int32_t next_n, int32_t compress_ratio, int32_t k,
+                       int32_t* indices, float* values, void* stream) {
+  return topk_decode_ex(logits, row_stride, num_rows, kv_lens, next_n, compress_ratio, k, indices,
+                        values, stream, nullptr);
+}
+
+gvr_status topk_prefill_ex(const float* logits, int64_t row_stride, int64_t num_rows,
+                           const int32_t* row_starts, const int32_t* row_ends, int32_t k,
+                           int32_t* indices, void* stream, const gvr_options* options) {
+  gvr_status s = check_common(row_stride, num_rows, k, options);
+  if (s != GVR_OK) return s;
+  if (num_rows == 0) return GVR_OK;
+  if (!logits || !row_starts || !row_ends || !indices) return GVR_ERR_NULL;
+  if (!aligned(logits, 16) || !aligned(indices, 4) || !aligned(row_starts, 4) || !aligned(row_ends, 4))
+    return GVR_ERR_ALIGN;
+  gvr::Params prm = {};
+  prm.logits = logits;
+  prm.row_stride = row_stride;
+  prm.row_starts = row_starts;
+  prm.row_ends = row_ends;
+  prm.indices = indices;
+  prm.values = nullptr;
+  prm.row_stats = options ? options->row_stats : nullptr;
+  prm.next_n = 1;
+  prm.compress_ratio = 1;
+  prm.k = k;
+  prm.mode = gvr::MODE_PREFILL;
+  prm.flags = options ? options->flags : 0;
+  return launch(prm, num_rows, options, stream);
+}
+
+gvr_status topk_prefill(const float* logits, int64_t row_stride, int64_t num_rows,
+                        const int32_t* row_starts, const int32_t* row_ends, int32_t k,
+                        int32_t* indices, void* stream) {
+  return topk_prefill_ex(logits, row_stride, num_rows, row_starts, row_ends, k, indices, stream, nullptr);
+}
+
+const char* gvr_status_string(gvr_status status) {
+  switch (status) {
+    case GVR_OK: return "ok";
+    case GVR_ERR_NULL: return "a required pointer is NULL";
+    case GVR_ERR_ALIGN: return "logits must be 16-byte aligned and int32/fp32 buffers 4-byte aligned";
+    case GVR_ERR_STRIDE: return "row_stride must be a multiple of 4 in [4, 2^31)";
+    case GVR_ERR_K: return "k must be 512, 1024 or 2048";
+    case GVR_ERR_ARG: return "invalid argument (row count, next_n, compress_ratio or options)";
+    case GVR_ERR_LAUNCH: return "kernel launch failed";
+  }
+  return "unknown status";
+}
+
+gvr_status gvr_plan(int64_t row_stride, int64_t num_rows, int32_t k, const gvr_options* options,
+                    int32_t sm_count, int32_t* cluster_size, int32_t* vectors_per_thread,
+                    int32_t* threads, int32_t* smem_bytes) {
+  gvr_status s = check_common(row_stride, num_rows, k, options);
+  if (s != GVR_OK) return s;
+  int sms = sm_count;
+  if (sms <= 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return GVR_ERR_LAUNCH;
+  }
+  int cs = 1, vpt = 1;
+  plan_geometry(row_stride, num_rows, sms, options, &cs, &vpt);
+  if (cluster_size) *cluster_size = cs;
+  if (vectors_per_thread) *vectors_per_thread = vpt;
+  if (threads) *threads = kThreads;
+  if (smem_bytes) *smem_bytes = int32_t(sizeof(gvr::Smem));
+  return GVR_OK;
+}
+
+}  // extern "C"

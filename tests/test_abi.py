@@ -1,0 +1,141 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must build for sm_103a, load, export every function that
+include/gvr_topk.h declares, reject bad arguments with the documented status
+codes before touching the device, and choose launch geometries whose register
+capacity covers the row envelope.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gvr_topk.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_attention_indexer_exact_gb300 import _build
+    _build.build_library()
+    import sparse_attention_indexer_exact_gb300 as gvr
+    return gvr.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for want in ("topk_decode", "topk_prefill", "topk_decode_ex", "topk_prefill_ex", "gvr_status_string",
+                 "gvr_plan"):
+        assert want in names, names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libgvrtopk.so does not export {name}"
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        s = lib.gvr_status_string(code)
+        assert s and len(s) > 1
+    assert lib.gvr_status_string(0) == b"ok"
+    assert lib.gvr_status_string(99) == b"unknown status"
+
+
+# Fake, never-dereferenced device addresses: validation must reject before any device work.
+ALIGNED = 0x10000
+K = 512
+
+
+def test_decode_argument_errors(lib):
+    f = lib.topk_decode
+    ok = (ALIGNED, 1024, 4, ALIGNED, 1, 1, K, ALIGNED, None, None)
+
+    def call(**kw):
+        args = list(ok)
+        names = ["logits", "row_stride", "num_rows", "kv_lens", "next_n", "cr", "k", "indices", "values", "stream"]
+        for key, v in kw.items():
+            args[names.index(key)] = v
+        return f(*args)
+
+    assert call(logits=None) == 1
+    assert call(kv_lens=None) == 1
+    assert call(indices=None) == 1
+    assert call(logits=ALIGNED + 4) == 2
+    assert call(indices=ALIGNED + 2) == 2
+    assert call(values=ALIGNED + 1) == 2
+    assert call(row_stride=1026) == 3
+    assert call(row_stride=0) == 3
+    assert call(row_stride=1 << 31) == 3
+    for bad_k in (0, 1, 256, 511, 513, 4096):
+        assert call(k=bad_k) == 4
+    assert call(num_rows=-1) == 5
+    assert call(next_n=0) == 5
+    assert call(cr=0) == 5
+    assert call(num_rows=0, logits=None, indices=None, kv_lens=None) == 0  # empty batch: no-op
+
+
+def test_prefill_argument_errors(lib):
+    f = lib.topk_prefill
+    assert f(None, 1024, 4, ALIGNED, ALIGNED, K, ALIGNED, None) == 1
+    assert f(ALIGNED, 1024, 4, None, ALIGNED, K, ALIGNED, None) == 1
+    assert f(ALIGNED, 1024, 4, ALIGNED, None, K, ALIGNED, None) == 1
+    assert f(ALIGNED + 8, 1024, 4, ALIGNED, ALIGNED, K, ALIGNED, None) == 2
+    assert f(ALIGNED, 1022, 4, ALIGNED, ALIGNED, K, ALIGNED, None) == 3
+    assert f(ALIGNED, 1024, 4, ALIGNED, ALIGNED, 1000, ALIGNED, None) == 4
+    assert f(ALIGNED, 1024, -3, ALIGNED, ALIGNED, K, ALIGNED, None) == 5
+    assert f(None, 1024, 0, None, None, K, None, None) == 0
+
+
+def test_option_errors(lib):
+    import sparse_attention_indexer_exact_gb300 as gvr
+    for bad in (dict(cluster_size=3), dict(cluster_size=16), dict(vectors_per_thread=5), dict(reserved=1),
+                dict(flags=64)):
+        o = gvr.Options(**bad)
+        st = lib.topk_decode_ex(ALIGNED, 1024, 4, ALIGNED, 1, 1, K, ALIGNED, None, None, ctypes.byref(o))
+        assert st == 5, bad
+
+
+@pytest.mark.parametrize("stride", [4, 64, 1024, 8192, 14848, 65536, 131072, 131076, 262144, 1 << 20])
+@pytest.mark.parametrize("rows", [1, 4, 64, 128, 4096])
+@pytest.mark.parametrize("k", [512, 2048])
+def test_plan_covers_the_row_envelope(lib, stride, rows, k):
+    import sparse_attention_indexer_exact_gb300 as gvr
+    p = gvr.plan(stride, rows, k, sm_count=152)
+    assert p["cluster_size"] in (1, 2, 4, 8) and p["vectors_per_thread"] in (1, 2, 4, 8)
+    cap = p["cluster_size"] * p["threads"] * p["vectors_per_thread"] * 4
+    if stride <= 8 * 512 * 8 * 4:
+        assert cap >= stride, p  # whole rows stay in registers
+    else:
+        assert p["cluster_size"] == 8 and p["vectors_per_thread"] == 8  # streamed in chunks
+    assert p["smem_bytes"] <= 227 * 1024
+
+
+def test_plan_respects_overrides(lib):
+    import sparse_attention_indexer_exact_gb300 as gvr
+    o = gvr.Options(cluster_size=2, vectors_per_thread=4)
+    p = gvr.plan(131072, 1, 1024, o, sm_count=152)
+    assert p["cluster_size"] == 2 and p["vectors_per_thread"] == 4
+
+
+def test_product_path_has_no_oracle_dependency():
+    """The CUDA path and its binding never import or link the oracle (and vice versa)."""
+    pkg = os.path.join(ROOT, "sparse_attention_indexer_exact_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert "oracle" not in text.lower(), f"{fn} mentions the oracle"
+    for fn in os.listdir(os.path.join(ROOT, "oracle")):
+        if fn.endswith((".py", ".c")):
+            text = open(os.path.join(ROOT, "oracle", fn)).read()
+            assert "sparse_attention_indexer_exact_gb300" not in text and "gvr_topk.h" not in text

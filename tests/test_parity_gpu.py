@@ -1,0 +1,293 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, tie-aware.
+
+Every case runs the library on cuda:0 and the oracle on the host over the same
+seeded inputs, then compares row by row with tests/tiecheck.py (short rows by
+exact equality; long rows by the set of winners above tau, the exact selected
+value multiset and index validity).  The bar is 0 inexact rows.
+
+Cases: the five workloads (single decode row, the 128-row decode batch at full
+size, the 4096-row prefill tile, the adversarial row and its variants, sweep
+cells), every launch geometry including streamed shares, every forced path of
+the method (rescue on an invalid bracket, rescue on overflow, no floor, radix
+refine), and the edge cases: empty and short rows at nv in {0, 1, K-1, K, K+1},
+misaligned prefill windows with the -inf tie class, clamped windows, MTP rows
+with kv_len < next_n, more than 65535 rows, and NaN inside a window (safety
+only: K distinct in-window indices).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from tiecheck import compare_rows, decode_windows, prefill_windows
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gvr():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_attention_indexer_exact_gb300 import _build
+    _build.build_library()
+    import sparse_attention_indexer_exact_gb300 as mod
+    mod.load_library()
+    torch.cuda.set_device(0)
+    return mod
+
+
+DEV = "cuda:0"
+
+
+def run_decode(gvr, case, *, values=True, options=None, stats=False):
+    lg = torch.from_numpy(case.logits).to(DEV)
+    kv = torch.from_numpy(case.kv_lens).to(DEV)
+    st = None
+    if stats:
+        st = torch.full((case.rows, 4), -7, dtype=torch.int32, device=DEV)
+        options = options or gvr.Options()
+        options.row_stats = st.data_ptr()
+    idx, vals = gvr.topk_decode(lg, kv, case.next_n, case.compress_ratio, case.k, want_values=values,
+                                options=options)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), (vals.cpu().numpy() if vals is not None else None), \
+        (st.cpu().numpy() if st is not None else None)
+
+
+def run_prefill(gvr, case, *, options=None, stats=False):
+    lg = torch.from_numpy(case.logits).to(DEV)
+    ks = torch.from_numpy(case.row_starts).to(DEV)
+    ke = torch.from_numpy(case.row_ends).to(DEV)
+    st = None
+    if stats:
+        st = torch.full((case.rows, 4), -7, dtype=torch.int32, device=DEV)
+        options = options or gvr.Options()
+        options.row_stats = st.data_ptr()
+    idx = gvr.topk_prefill(lg, ks, ke, case.k, options=options)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), (st.cpu().numpy() if st is not None else None)
+
+
+def assert_decode_exact(gvr, case, **kw):
+    got, vals, st = run_decode(gvr, case, **kw)
+    ref, _, _ = oracle.topk_decode(case.logits, case.kv_lens, case.next_n, case.compress_ratio, case.k)
+    bad, why = compare_rows(decode_windows(case.logits, case.kv_lens, case.next_n, case.compress_ratio), case.k,
+                            got, ref, got_values=vals)
+    assert bad == 0, f"{case.name}: {bad} inexact rows: {why}"
+    return st
+
+
+def assert_prefill_exact(gvr, case, **kw):
+    got, st = run_prefill(gvr, case, **kw)
+    ref, _ = oracle.topk_prefill(case.logits, case.row_starts, case.row_ends, case.k)
+    bad, why = compare_rows(prefill_windows(case.logits, case.row_starts, case.row_ends), case.k, got, ref)
+    assert bad == 0, f"{case.name}: {bad} inexact rows: {why}"
+    return st
+
+
+# ----------------------------------------------------------------------------- the workloads
+@pytest.mark.parametrize("values", [False, True])
+def test_single_decode_row(gvr, values):
+    assert_decode_exact(gvr, workloads.single_decode_row(), values=values)
+
+
+def test_decode_batch_full_size(gvr):
+    st = assert_decode_exact(gvr, workloads.decode_batch(), stats=True)
+    n = workloads.decode_batch().row_lengths()
+    assert (st[n <= 1024, 0] == 0).all() and (st[n > 1024, 0] >= 1).all()
+
+
+def test_decode_batch_with_empty_request(gvr):
+    case = workloads.decode_batch(requests=64, empty_request=True, stride=32768, kv_hi=131072)
+    assert_decode_exact(gvr, case)
+
+
+def test_prefill_tile_full_size(gvr):
+    st = assert_prefill_exact(gvr, workloads.prefill_tile(), stats=True)
+    assert (st[:, 0] <= 1).all(), "an ordinary N(0,1) tile should never need the rescue"
+
+
+@pytest.mark.parametrize("variant", workloads.ADVERSARIAL_VARIANTS)
+def test_adversarial_row(gvr, variant):
+    st = assert_decode_exact(gvr, workloads.adversarial_row(variant), stats=True)
+    path = int(st[0, 0])
+    if variant == "all_equal":
+        assert path == 2  # GMIN == GMAX: invalid bracket
+    if variant == "two_valued":
+        assert path == 3  # the top bin holds ~n/2 candidates: overflow
+
+
+@pytest.mark.parametrize("bs,n,k", [(1, 16384, 512), (4, 32768, 1024), (16, 65536, 2048), (4, 131072, 512),
+                                    (1, 131072, 2048), (64, 16384, 1024)])
+def test_sweep_cells_decode(gvr, bs, n, k):
+    assert_decode_exact(gvr, workloads.sweep_decode(bs, n, k))
+
+
+@pytest.mark.parametrize("bs,n,k", [(4, 16384, 512), (16, 32768, 2048), (4, 131072, 1024)])
+def test_sweep_cells_prefill(gvr, bs, n, k):
+    assert_prefill_exact(gvr, workloads.sweep_prefill(bs, n, k))
+
+
+# ----------------------------------------------------------------------------- geometry and paths
+@pytest.mark.parametrize("cs", [1, 2, 4, 8])
+@pytest.mark.parametrize("vpt", [1, 2, 4, 8])
+def test_every_geometry(gvr, cs, vpt):
+    """Every cluster size x registers per thread, including shares streamed in several chunks."""
+    case = workloads.decode_batch(seed=77, requests=6, next_n=2, cr=1, k=1024, stride=40960, kv_lo=900,
+                                  kv_hi=40960, boundary=False)
+    assert_decode_exact(gvr, case, options=gvr.Options(cluster_size=cs, vectors_per_thread=vpt))
+    pc = workloads.prefill_tile(seed=78, rows=24, k=512, lengths=(700, 2100, 5000, 9000))
+    assert_prefill_exact(gvr, pc, options=gvr.Options(cluster_size=cs, vectors_per_thread=vpt))
+
+
+@pytest.mark.parametrize("flags,expect", [(1, {4}), (4, {3}), (2, {1}), (8, {1}), (2 | 8, {1})])
+def test_forced_paths(gvr, flags, expect):
+    case = workloads.decode_batch(seed=5, requests=8, next_n=2, cr=4, k=1024, stride=131072,
+                                  boundary=False)
+    st = assert_decode_exact(gvr, case, options=gvr.Options(flags=flags), stats=True)
+    long_rows = case.row_lengths() > case.k
+    assert set(np.unique(st[long_rows, 0]).tolist()) <= expect, st[:, 0]
+    adv = workloads.adversarial_row("base")
+    assert_decode_exact(gvr, adv, options=gvr.Options(flags=flags))
+    pc = workloads.prefill_tile(seed=9, rows=32, k=512, lengths=(600, 1800, 3000, 6000))
+    assert_prefill_exact(gvr, pc, options=gvr.Options(flags=flags))
+
+
+def test_radix_refine_large_candidate_sets(gvr):
+    """Coarse plateaus give crossing bins with hundreds to thousands of members."""
+    g = np.random.default_rng(21)
+    rows, stride, k = 12, 65536, 2048
+    lg = np.round(g.standard_normal((rows, stride)) * (2.0 + np.arange(rows)[:, None] * 3)).astype(np.float32)
+    case = workloads.DecodeCase("plateaus", lg, np.full(rows, stride, np.int32), 1, 1, k)
+    st = assert_decode_exact(gvr, case, stats=True)
+    assert (st[:, 1] > 256).any(), st
+
+
+# ----------------------------------------------------------------------------- edge cases
+@pytest.mark.parametrize("k", [512, 1024, 2048])
+def test_short_row_boundaries(gvr, k):
+    ns = [0, 1, k - 1, k, k + 1, k + 2, 2 * k + 3]
+    stride = workloads.roundup(2 * k + 8, 64)
+    g = np.random.default_rng(k)
+    lg = np.empty((len(ns), stride), np.float32)
+    for r, n in enumerate(ns):
+        lg[r] = g.standard_normal(stride).astype(np.float32)
+        lg[r, n:] = workloads.DECODE_POISON[np.arange(n, stride) % 3]
+    case = workloads.DecodeCase("short", lg, np.array(ns, np.int32), 1, 1, k)
+    assert_decode_exact(gvr, case)
+
+
+def test_prefill_misaligned_neg_inf_class(gvr):
+    """ks % 4 in {0,1,2,3} crossed with a -inf tie class that holds tau; poison all around."""
+    g = np.random.default_rng(3)
+    k, stride = 512, 8192
+    rows = []
+    for s in range(4):
+        for nv in (513, 700, 3000, 7000):
+            ks = 4 * int(g.integers(0, 50)) + s
+            nv = min(nv, stride - ks)
+            row = workloads.PREFILL_POISON[np.arange(stride) % 4].copy()
+            w = g.standard_normal(nv).astype(np.float32)
+            w[g.choice(nv, nv - k + 40, replace=False)] = -np.inf
+            row[ks:ks + nv] = w
+            rows.append((row, ks, ks + nv))
+    lg = np.stack([r[0] for r in rows])
+    case = workloads.PrefillCase("neg_inf_lead", lg, np.array([r[1] for r in rows], np.int32),
+                                 np.array([r[2] for r in rows], np.int32), k)
+    got, _ = run_prefill(gvr, case)
+    assert got.min() >= 0
+    assert_prefill_exact(gvr, case)
+
+
+def test_prefill_clamped_windows(gvr):
+    g = np.random.default_rng(4)
+    k, stride = 512, 4096
+    lg = g.standard_normal((6, stride)).astype(np.float32)
+    ks = np.array([-5, 3000, 100, 2000, -100, 4090], np.int32)
+    ke = np.array([1000, 5000, 50, 2000, 9000, 4100], np.int32)
+    case = workloads.PrefillCase("clamped", lg, ks, ke, k)
+    assert_prefill_exact(gvr, case)
+
+
+@pytest.mark.parametrize("next_n", [1, 2, 3, 4])
+@pytest.mark.parametrize("cr", [1, 4])
+def test_mtp_rows(gvr, next_n, cr):
+    g = np.random.default_rng(100 * next_n + cr)
+    reqs, stride, k = 9, 16384, 512
+    kv = g.integers(0, stride * cr, reqs).astype(np.int32)
+    kv[0], kv[1], kv[2] = next_n - 1, next_n, cr * k + next_n - 1  # empty, tiny, boundary
+    rows = reqs * next_n
+    lg = g.standard_normal((rows, stride)).astype(np.float32)
+    case = workloads.DecodeCase("mtp", lg, kv, next_n, cr, k)
+    n = case.row_lengths()
+    for r in range(rows):
+        lg[r, n[r]:] = workloads.DECODE_POISON[np.arange(n[r], stride) % 3]
+    assert_decode_exact(gvr, case)
+
+
+def test_more_than_65535_rows(gvr):
+    rows, stride, k = 70000, 64, 512
+    g = np.random.default_rng(6)
+    lg = g.standard_normal((rows, stride)).astype(np.float32)
+    kv = g.integers(0, stride + 1, rows).astype(np.int32)
+    case = workloads.DecodeCase("many_rows", lg, kv, 1, 1, k)
+    assert_decode_exact(gvr, case, values=False)
+
+
+def test_mixed_row_independence(gvr):
+    """304 rows of random, full-length, short, empty and boundary lengths under next_n = 4."""
+    g = np.random.default_rng(304)
+    next_n, cr, k, stride = 4, 4, 1024, 65536
+    kv = g.integers(1, stride * cr, 76).astype(np.int32)
+    kv[:6] = [stride * cr, 3, 4, cr * k + 3, cr * (k + 1) + 3, 4 * stride * cr]
+    rows = 76 * next_n
+    lg = np.empty((rows, stride), np.float32)
+    n = workloads.DecodeCase("x", lg, kv, next_n, cr, k).row_lengths()
+    for r in range(rows):
+        lg[r] = g.standard_normal(stride).astype(np.float32) * (1 + r % 7)
+        lg[r, n[r]:] = workloads.DECODE_POISON[np.arange(n[r], stride) % 3]
+    assert_decode_exact(gvr, workloads.DecodeCase("mixed", lg, kv, next_n, cr, k))
+
+
+def test_nan_inside_window_is_safe(gvr):
+    g = np.random.default_rng(8)
+    rows, stride, k = 4, 8192, 512
+    lg = g.standard_normal((rows, stride)).astype(np.float32)
+    lg[0, g.choice(stride, 50, replace=False)] = np.nan
+    lg[1, :] = np.nan
+    lg[2, g.choice(stride, stride - 100, replace=False)] = np.nan
+    lg[3, ::2] = np.nan
+    lg_t = torch.from_numpy(lg).to(DEV)
+    kv = torch.full((rows,), stride, dtype=torch.int32, device=DEV)
+    idx, _ = gvr.topk_decode(lg_t, kv, 1, 1, k)
+    got = idx.cpu().numpy()
+    for r in range(rows):
+        assert got[r].min() >= 0 and got[r].max() < stride and np.unique(got[r]).size == k
+
+
+def test_empty_batch_and_side_stream(gvr):
+    lg = torch.zeros((0, 1024), device=DEV)
+    kv = torch.zeros((1,), dtype=torch.int32, device=DEV)
+    idx, _ = gvr.topk_decode(lg, kv, 1, 1, 512)
+    assert idx.shape == (0, 512)
+    case = workloads.single_decode_row(seed=55)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        lg = torch.from_numpy(case.logits).to(DEV)
+        kv = torch.from_numpy(case.kv_lens).to(DEV)
+        idx, _ = gvr.topk_decode(lg, kv, 1, 1, case.k)
+    s.synchronize()
+    ref, _, _ = oracle.topk_decode(case.logits, case.kv_lens, 1, 1, case.k)
+    bad, why = compare_rows(decode_windows(case.logits, case.kv_lens, 1, 1), case.k, idx.cpu().numpy(), ref)
+    assert bad == 0, why
+
+
+def test_signed_zero_and_inf_classes(gvr):
+    for variant in ("signed_zero_tau", "pos_inf_class", "neg_inf_tau"):
+        case = workloads.adversarial_row(variant)
+        for flags in (0, 1, 4):
+            assert_decode_exact(gvr, case, options=gvr.Options(flags=flags))

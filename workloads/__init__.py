@@ -160,7 +160,8 @@ def prefill_tile(seed: int = 1003, rows: int = 4096, k: int = 2048,
 
     Request q starts at column off_q with a gap of q poisoned columns before
     it, so off = (0, 513, 2051, 6150) for the default lengths.  Tile row i is
-    query position floor(3.5 i) of the ungapped packed sequence; its window is
+    query position floor(i * total / rows) of the ungapped packed sequence
+    (floor(3.5 i) for the default 4096 rows of 14336 tokens); its window is
     [off_q, off_q + pos + 1).  Rows 4090..4095 are overridden to positions
     2046, 2047, 2048 of requests 2 and 3 (nv = K-1, K, K+1).  Stride is the
     width plus >=256 floats of slack rounded to 256 floats (1024 B).
@@ -175,7 +176,7 @@ def prefill_tile(seed: int = 1003, rows: int = 4096, k: int = 2048,
     ks = np.empty(rows, np.int32)
     ke = np.empty(rows, np.int32)
     for i in range(rows):
-        p = min(int(np.floor(3.5 * i)), total - 1)
+        p = min(i * total // rows, total - 1)  # floor(3.5 i) for 4096 rows of 14336 tokens
         q = int(np.searchsorted(ends, p, side="right"))
         pos = p - (int(ends[q - 1]) if q else 0)
         ks[i], ke[i] = offs[q], offs[q] + pos + 1
