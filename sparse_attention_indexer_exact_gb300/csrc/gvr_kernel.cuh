@@ -1,8 +1,9 @@
 // gvr_kernel.cuh -- the GVR (Guess-Verify-Refine) exact per-row top-K kernel for sm_103a.
 //
 // One thread-block cluster selects one row.  The row's valid window is split evenly over the
-// cluster's CTAs; every CTA holds its share of the row in registers as float4 vectors (read
-// from HBM exactly once), so all later passes run over registers.  Per row:
+// cluster's CTAs; each CTA stages its share in shared memory with bulk asynchronous copies
+// (TMA, completion on an mbarrier), so the row is read from HBM exactly once and every later
+// pass reads shared memory.  Per row:
 //
 //   Guess   uniform block64 sampling: K scores in K/64 runs of 64 consecutive scores whose
 //           starts spread evenly over the window, first run at 0, last run ending at nv.
@@ -20,23 +21,29 @@
 //           over all CTAs of the cluster through distributed shared memory -- the parallel
 //           rescue of PR #20998, in the same launch, with no host synchronization.
 //
-// Two implementation choices keep the per-score work to a compare or two:
+// Implementation choices that keep the per-score work to about one compare:
 //  * sampled histogram floor: the samples also give a floor bin F below which, by the sample
 //    quantile, the crossing should not lie; only scores in bins >= F are counted.  A score's
 //    bin is >= F exactly when the score is >= v_F, the smallest float whose bin is >= F (found
 //    by a 32-way search over float keys), so the floor test is one float compare.  If fewer
 //    than K scores reach the floor, the bins below it are counted in a second round, so the
 //    result never depends on the floor.
-//  * warp-aggregated shared-memory atomics (__match_any_sync) for every histogram update,
-//    so tie-heavy rows cost one atomic per distinct bin per warp instruction.
+//  * above-floor bitmask: each thread compares its (at most 32) staged scores with v_F once
+//    and keeps a 32-bit mask of the few that pass; the histogram and the collect step then
+//    visit only the set bits, reading those scores back from shared memory.  A warp whose
+//    masks are dense (tie-heavy rows) counts with warp-aggregated atomics (__match_any_sync)
+//    instead, one shared-memory atomic per distinct bin per warp instruction.
 //
 // The bin function is monotone non-decreasing in the score (IEEE round-to-nearest subtract and
 // multiply by a positive scale, clamp, truncate), which is all the crossing-bin logic needs;
 // it is evaluated with the same instruction sequence everywhere, so every pass and every CTA
-// classifies a score identically.
+// classifies a score identically.  Positions outside the window (the lead lanes below an
+// unaligned window start, the lanes past its end) are never compared: they are staged as NaN,
+// which fails every `>=` / `<` test, and the key-space rescue masks them by position.
 #pragma once
 
 #include <cfloat>
+#include <cstddef>
 #include <cstdint>
 
 #include "gvr_device.cuh"
@@ -49,10 +56,15 @@ constexpr int COARSE_SHIFT = 3;       // NB / NCOARSE == 8
 constexpr int CAP = 4096;             // candidate slots in cluster rank 0
 constexpr int RANK_REFINE_MAX = 256;  // m at or below: refine by pairwise ranking
 constexpr int MAX_K = 2048;
+constexpr int MAX_VPT = 8;            // staged float4 per thread per chunk: a 32-bit score mask
+constexpr int SPARSE_MAX = 8;         // above-floor scores per thread beyond which a warp goes dense
+constexpr uint32_t COPY_PIECE = 16384;             // bytes per bulk copy instruction
+constexpr uint64_t WAIT_LIMIT_NS = 500000000ull;   // bound on any wait for staged data (0.5 s)
 
 enum : int32_t { MODE_DECODE = 0, MODE_PREFILL = 1 };
 enum : int32_t { FLAG_FORCE_RESCUE = 1, FLAG_NO_FLOOR = 2, FLAG_ZERO_CAP = 4, FLAG_RADIX_REFINE = 8 };
 enum : int32_t {
+  PATH_DEVICE_ERROR = -1,
   PATH_SHORT = 0,
   PATH_REFINE = 1,
   PATH_RESCUE_BRACKET = 2,
@@ -74,6 +86,7 @@ struct Params {
   int32_t k;
   int32_t mode;
   int32_t flags;
+  int32_t slice_vec;          // float4 slots of the shared-memory stage per CTA (T * vpt)
 };
 
 struct Crossing {
@@ -86,7 +99,7 @@ struct Crossing {
 };
 
 struct alignas(16) Smem {
-  uint32_t hist[NB];
+  uint32_t hist[NB];  // first: 16-byte aligned groups of 4 bins are read as one vector
   uint32_t dhist[2][256];
   uint32_t shist[NCOARSE];
   float cand_v[CAP];
@@ -95,13 +108,22 @@ struct alignas(16) Smem {
   float wmin[32];
   float wmax[32];
   Crossing cross;
-  float vfloor;
+  float vthr;
   int32_t floor_bin;
   uint32_t dsel, dabove, dcnt;
   uint32_t ctr_win, ctr_cand;   // this CTA's slot counters (refine path)
   uint32_t ctr_rwin, ctr_rtie;  // rank 0's counters for its own radix refine
   uint32_t rc_win, rc_tie;      // rank 0's counters shared by the cluster in rescue
+  uint32_t tout;                // this CTA gave up waiting for staged data
+  uint32_t err;                 // rank 0: some CTA of the cluster gave up
+  uint64_t bar;                 // completion of the bulk copies of the current stage
 };
+static_assert(offsetof(Smem, hist) % 16 == 0, "histogram groups are read as 16-byte vectors");
+static_assert(offsetof(Smem, bar) % 8 == 0, "mbarrier must be 8-byte aligned");
+
+constexpr int SMEM_FIXED = int((sizeof(Smem) + 127) / 128 * 128);
+
+__host__ __device__ constexpr int smem_bytes(int slice_vec) { return SMEM_FIXED + 16 * slice_vec; }
 
 // Monotone bin of a score in [GMIN, GMAX] with NB bins; NaN maps to bin 0.
 __device__ __forceinline__ int value_bin(float v, float gmin, float sc) {
@@ -284,18 +306,20 @@ __device__ __forceinline__ void digit_cross(Smem& S, int buf, uint32_t c0, uint3
   __syncthreads();
 }
 
-template <int T, int VPT>
-__global__ void __launch_bounds__(T, 1024 / T) gvr_topk_kernel(const Params p) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+template <int T>
+__global__ void __launch_bounds__(T, 2) gvr_topk_kernel(const Params p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
+  float4* sdata = reinterpret_cast<float4*>(smem_raw + SMEM_FIXED);
+  const float* sdataf = reinterpret_cast<const float*>(smem_raw + SMEM_FIXED);
   constexpr int NW = T / 32;
-  constexpr int CH = T * VPT;               // vectors per chunk of a CTA's share
   constexpr int KPT = (MAX_K + T - 1) / T;  // samples per thread at most
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t cs = cluster_size();
   const uint32_t rank = cluster_rank();
   const int64_t row = cluster_id_x();
   const int32_t k = p.k;
+  const float qnan = __int_as_float(0x7fffffff);
 
   // ---------------------------------------------------------------- row geometry
   // row_stride < 2^31, so window offsets and lengths fit in 32 bits.
@@ -336,14 +360,17 @@ __global__ void __launch_bounds__(T, 1024 / T) gvr_topk_kernel(const Params p) {
   if (tid == 0) {
     S.ctr_win = S.ctr_cand = S.ctr_rwin = S.ctr_rtie = 0;
     S.rc_win = S.rc_tie = 0;
+    S.tout = S.err = 0;
     S.cross = Crossing{};
     S.dsel = S.dabove = S.dcnt = 0;
+    mbar_init(&S.bar, 1);
+    mbar_init_fence();
   }
 
   // ---------------------------------------------------------------- this CTA's share
   // Vectors are 16-byte aligned float4s starting at the aligned column at or below the
-  // window start; the first `lead` lanes of vector 0 and the lanes past the window end in the
-  // last vector are outside the window and are masked by position.
+  // window start.  The share [vb, ve) is staged in chunks of slice_vec vectors; with one chunk
+  // (the usual case) it is staged once and stays resident for every pass.
   const int32_t lead = a & 3;
   const float* base = rowp + (a - lead);
   const int32_t span = lead + nv;
@@ -351,44 +378,87 @@ __global__ void __launch_bounds__(T, 1024 / T) gvr_topk_kernel(const Params p) {
   const int32_t tailn = span & 3;   // in-window scalars of the partial last vector
   const int32_t nvec = ffull + (tailn ? 1 : 0);
   const int32_t per = int32_t((nvec + int32_t(cs) - 1) / int32_t(cs));
-  const int32_t vb = int32_t(rank) * per;
+  const int32_t vb = int32_t(rank) * per < nvec ? int32_t(rank) * per : nvec;
   const int32_t ve = vb + per < nvec ? vb + per : nvec;
-  const int32_t nchunks = ve > vb ? (ve - vb + CH - 1) / CH : 0;
+  const int32_t cap_vec = p.slice_vec;
+  const int32_t nloc = ve - vb;
+  const int nchunks = nloc > 0 ? (nloc + cap_vec - 1) / cap_vec : 0;
   const bool resident = nchunks <= 1;
+  uint32_t phase = 0;
 
-  float4 x[VPT];
-  auto vec_index = [&](int ch, int i) -> int32_t { return vb + ch * CH + i * T + tid; };
-  auto load_chunk = [&](int ch) {
-#pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      const int32_t f = vec_index(ch, i);
-      if (f < ve && f < ffull) {
-        x[i] = ld_stream_v4(base + 4 * size_t(f));
-      } else if (f < ve) {  // the partial last vector: read only its in-window scalars
-        const float* q = base + 4 * size_t(f);
-        float4 t = f4_zero();
-        t.x = q[0];
-        if (tailn > 1) t.y = q[1];
-        if (tailn > 2) t.z = q[2];
-        x[i] = t;
-      } else {
-        x[i] = f4_zero();
+  auto chunk_begin = [&](int ch) -> int32_t { return vb + ch * cap_vec; };
+  auto chunk_count = [&](int ch) -> int32_t {
+    const int32_t c0 = vb + ch * cap_vec;
+    return (c0 + cap_vec < ve ? c0 + cap_vec : ve) - c0;
+  };
+  // Stage chunk ch: bulk copies of its whole vectors (thread 0) and the in-window scalars of
+  // the partial last vector.  Returns whether bulk copies were issued (same on all threads).
+  auto issue_chunk = [&](int ch) -> bool {
+    const int32_t c0 = chunk_begin(ch), c1 = c0 + chunk_count(ch);
+    const int32_t fe = c1 < ffull ? c1 : ffull;
+    const int32_t nfull = fe > c0 ? fe - c0 : 0;
+    if (tid == 0 && nfull > 0) {
+      fence_proxy_async_smem();
+      const uint32_t bytes = uint32_t(nfull) * 16u;
+      mbar_arrive_expect_tx(&S.bar, bytes);
+      const char* src = reinterpret_cast<const char*>(base + 4 * size_t(c0));
+      char* dst = reinterpret_cast<char*>(sdata);
+      for (uint32_t off = 0; off < bytes; off += COPY_PIECE) {
+        const uint32_t n = bytes - off < COPY_PIECE ? bytes - off : COPY_PIECE;
+        bulk_copy_g2s(dst + off, src + off, n, &S.bar);
       }
     }
+    if (tid == 32 && tailn && ffull >= c0 && ffull < c1) {
+      const float* q = base + 4 * size_t(ffull);
+      sdata[ffull - c0] = make_float4(q[0], tailn > 1 ? q[1] : qnan, tailn > 2 ? q[2] : qnan, qnan);
+    }
+    return nfull > 0;
   };
-  auto lane_mask = [&](int32_t f) -> uint32_t {
-    if (f >= ve) return 0u;
-    uint32_t m = 0xFu;
-    if (f == 0) m &= (0xFu << lead) & 0xFu;
-    if (f == ffull) m &= (1u << tailn) - 1u;
-    return m;
+  // Wait (bounded) for chunk ch, blank the lead lanes below the window start, publish.
+  auto wait_chunk = [&](int ch, bool armed) {
+    bool late = false;
+    if (armed) {
+      if (!mbar_wait_bounded(&S.bar, phase, WAIT_LIMIT_NS)) {
+        mbar_wait_bounded(&S.bar, phase, WAIT_LIMIT_NS);  // let copies in flight land
+        late = true;
+      }
+      phase ^= 1u;
+    }
+    if (tid == 0 && lead > 0 && chunk_begin(ch) == 0 && chunk_count(ch) > 0) {
+      float* v0 = reinterpret_cast<float*>(sdata);
+      for (int l = 0; l < lead; ++l) v0[l] = qnan;
+    }
+    if (__syncthreads_or(late) && tid == 0) S.tout = 1;
   };
-  if (nchunks == 1) {
-    load_chunk(0);  // stays in registers for every pass
-  } else {
+  // After a cluster barrier: tell rank 0 that this CTA gave up waiting (rank 0 marks the row).
+  auto report_timeout = [&]() {
+    if (tid == 0 && S.tout) dsmem_st_u32(dsmem_map(smem_u32(&S.err), 0), 1u);
+  };
+  // Mask of this thread's staged scores that are >= thr (below == false) or < thr (below ==
+  // true); bit 4i+l is lane l of the thread's i-th vector (chunk vector i*T + tid).
+  auto build_bits = [&](int32_t cnt, float thr, bool below) -> uint32_t {
+    uint32_t bits = 0;
 #pragma unroll
-    for (int i = 0; i < VPT; ++i) x[i] = f4_zero();
-  }
+    for (int i = 0; i < MAX_VPT; ++i) {
+      const int32_t f = i * T + tid;
+      if (f < cnt) {
+        const float4 v = sdata[f];
+        uint32_t b;
+        if (!below)
+          b = uint32_t(v.x >= thr) | (uint32_t(v.y >= thr) << 1) | (uint32_t(v.z >= thr) << 2) |
+              (uint32_t(v.w >= thr) << 3);
+        else
+          b = uint32_t(v.x < thr) | (uint32_t(v.y < thr) << 1) | (uint32_t(v.z < thr) << 2) |
+              (uint32_t(v.w < thr) << 3);
+        bits |= b << (4 * i);
+      }
+    }
+    return bits;
+  };
+  auto bit_score = [&](int j) -> float { return sdataf[4 * ((j >> 2) * T + tid) + (j & 3)]; };
+
+  bool armed0 = false;
+  if (nchunks == 1) armed0 = issue_chunk(0);  // overlaps the sampling below
 
   // ---------------------------------------------------------------- guess: block64 sample
   const int nblk = k >> 6;
@@ -397,7 +467,7 @@ __global__ void __launch_bounds__(T, 1024 / T) gvr_topk_kernel(const Params p) {
 #pragma unroll
   for (int q = 0; q < KPT; ++q) {
     const int i = q * T + tid;
-    sv[q] = __int_as_float(0x7fffffff);
+    sv[q] = qnan;
     if (i < k) {
       const int64_t blk = i >> 6;
       const int32_t s = int32_t(blk * (nv - 64) / (nblk - 1));
@@ -435,15 +505,14 @@ __global__ void __launch_bounds__(T, 1024 / T) gvr_topk_kernel(const Params p) {
   float sc = 0.f;
   float vfloor = -INFINITY;
   int fbin = 0;
-  Crossing cr{};
-  int rounds = 0;
   if (path == PATH_REFINE) {
     sc = __fdiv_rn(float(NB), __fsub_rn(gmax, gmin));
     // ------------------------------------------------------------ sampled floor
     if (!(p.flags & FLAG_NO_FLOOR)) {
-      // about k*k/nv samples are expected above tau; keep twice that plus a margin
-      const int64_t want64 = 2 * int64_t(k) * k / nv + 32;
-      const uint32_t want = uint32_t(want64 < k ? want64 : k);
+      // mu = k*k/nv samples are expected above tau; keep mu + 3 sqrt(mu) + 16 above the floor
+      const float mu = float(k) * float(k) / float(nv);
+      const float want_f = mu + 3.0f * sqrtf(mu) + 16.0f;
+      const uint32_t want = want_f < float(k) ? uint32_t(want_f) : uint32_t(k);
 #pragma unroll
       for (int q = 0; q < KPT; ++q)
         if (!isnan(sv[q])) atomicAdd(&S.shist[value_bin(sv[q], gmin, sc) >> COARSE_SHIFT], 1u);
@@ -484,32 +553,58 @@ __global__ void __launch_bounds__(T, 1024 / T) gvr_topk_kernel(const Params p) {
         const float vf = fb > 0 ? floor_value(fb, gmin, sc) : -INFINITY;
         if (lane == 0) {
           S.floor_bin = fb;
-          S.vfloor = vf;
+          S.vthr = vf;
         }
       }
       __syncthreads();
       fbin = S.floor_bin;
-      vfloor = S.vfloor;
+      vfloor = S.vthr;
     }
+  }
 
+  if (nchunks == 1) wait_chunk(0, armed0);
+
+  Crossing cr{};
+  int rounds = 0;
+  uint32_t mbits = 0;  // resident share: this thread's scores >= vfloor
+  if (path == PATH_REFINE) {
     // ------------------------------------------------------------ verify: value histogram
+    auto count_bits = [&](uint32_t bits) {
+      const bool dense = __any_sync(FULL_MASK, __popc(bits) > SPARSE_MAX);
+      if (!dense) {
+        while (bits) {
+          const int j = __ffs(bits) - 1;
+          bits &= bits - 1;
+          atomicAdd(&S.hist[value_bin(bit_score(j), gmin, sc)], 1u);
+        }
+      } else {
+#pragma unroll 4
+        for (int j = 0; j < 4 * MAX_VPT; ++j) {
+          const bool pr = (bits >> j) & 1u;
+          const float e = pr ? bit_score(j) : 0.f;
+          hist_add(S.hist, pr, pr ? uint32_t(value_bin(e, gmin, sc)) : 0u);
+        }
+      }
+    };
     for (int round = 0; round < 2; ++round) {
       const bool upper = round == 0;
       ++rounds;
-      for (int ch = 0; ch < nchunks; ++ch) {
-        if (!resident) load_chunk(ch);
-#pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-          const uint32_t m = lane_mask(vec_index(ch, i));
-#pragma unroll
-          for (int l = 0; l < 4; ++l) {
-            const float e = f4_get(x[i], l);
-            const bool pr = ((m >> l) & 1u) && (upper ? e >= vfloor : e < vfloor);
-            hist_add(S.hist, pr, uint32_t(pr ? value_bin(e, gmin, sc) : 0));
-          }
+      if (resident) {
+        if (nchunks == 1) {
+          const uint32_t b = build_bits(nloc, vfloor, !upper);
+          if (upper) mbits = b;
+          count_bits(b);
+        }
+      } else {
+        for (int ch = 0; ch < nchunks; ++ch) {
+          const bool armed = issue_chunk(ch);
+          wait_chunk(ch, armed);
+          count_bits(build_bits(chunk_count(ch), vfloor, !upper));
+          __syncthreads();
         }
       }
       cluster_sync();
+      report_timeout();
       cr = reduce_crossing<T>(S, cs, rank, uint32_t(k), upper ? fbin : 0);
       if (cr.total >= uint32_t(k)) break;
       if (!upper || fbin == 0) break;  // fewer than k countable scores (NaN in the window)
@@ -520,40 +615,50 @@ __global__ void __launch_bounds__(T, 1024 / T) gvr_topk_kernel(const Params p) {
 
   if (path == PATH_REFINE) {
     // ------------------------------------------------------------ collect
-    const float thr = rounds > 1 ? -INFINITY : vfloor;  // every counted score is >= thr
     const int bstar = cr.bin;
+    float thr = vfloor;
+    if (rounds > 1) {  // scores below the floor were counted too: select bins >= b* afresh
+      if (warp == 0) {
+        const float t = bstar > 0 ? floor_value(bstar, gmin, sc) : -INFINITY;
+        if (lane == 0) S.vthr = t;
+      }
+      __syncthreads();
+      thr = S.vthr;
+    }
     const uint32_t rv = dsmem_map(smem_u32(&S.cand_v[0]), 0);
     const uint32_t rj = dsmem_map(smem_u32(&S.cand_j[0]), 0);
-    for (int ch = 0; ch < nchunks; ++ch) {
-      if (!resident) load_chunk(ch);
-#pragma unroll
-      for (int i = 0; i < VPT; ++i) {
-        const int32_t f = vec_index(ch, i);
-        const uint32_t m = lane_mask(f);
-#pragma unroll
-        for (int l = 0; l < 4; ++l) {
-          const float e = f4_get(x[i], l);
-          const bool pr = ((m >> l) & 1u) && e >= thr;
-          const int b = pr ? value_bin(e, gmin, sc) : -1;
-          const int32_t j = 4 * f + l - lead;
-          const uint32_t ws = warp_alloc_local(&S.ctr_win, b > bstar);
-          if (b > bstar) {
-            const uint32_t slot = cr.base_above + ws;
-            if (slot < uint32_t(k)) {  // always true: counts match the histogram's
-              out[slot] = j;
-              if (outv) outv[slot] = e;
-            }
+    auto collect_bits = [&](uint32_t bits, int32_t c0) {
+      while (bits) {
+        const int j = __ffs(bits) - 1;
+        bits &= bits - 1;
+        const float e = bit_score(j);
+        const int b = value_bin(e, gmin, sc);
+        const int32_t jw = 4 * (c0 + (j >> 2) * T + tid) + (j & 3) - lead;
+        if (b > bstar) {
+          const uint32_t slot = cr.base_above + atomicAdd(&S.ctr_win, 1u);
+          if (slot < uint32_t(k)) {  // always true: counts match the histogram's
+            out[slot] = jw;
+            if (outv) outv[slot] = e;
           }
-          const uint32_t cslot = warp_alloc_local(&S.ctr_cand, b == bstar);
-          if (b == bstar) {
-            const uint32_t s = cr.base_cand + cslot;
-            if (s < uint32_t(CAP)) {  // always true: m <= CAP on this path
-              dsmem_st_u32(rv + 4u * s, __float_as_uint(e));
-              dsmem_st_u32(rj + 4u * s, uint32_t(j));
-            }
+        } else if (b == bstar) {
+          const uint32_t c = cr.base_cand + atomicAdd(&S.ctr_cand, 1u);
+          if (c < uint32_t(CAP)) {  // always true: m <= CAP on this path
+            dsmem_st_u32(rv + 4u * c, __float_as_uint(e));
+            dsmem_st_u32(rj + 4u * c, uint32_t(jw));
           }
         }
       }
+    };
+    if (resident) {
+      if (nchunks == 1) collect_bits(rounds > 1 ? build_bits(nloc, thr, false) : mbits, vb);
+    } else {
+      for (int ch = 0; ch < nchunks; ++ch) {
+        const bool armed = issue_chunk(ch);
+        wait_chunk(ch, armed);
+        collect_bits(build_bits(chunk_count(ch), thr, false), chunk_begin(ch));
+        __syncthreads();
+      }
+      report_timeout();
     }
     cluster_sync();  // every candidate has landed in rank 0's buffer
     if (rank != 0) return;
@@ -623,8 +728,12 @@ __global__ void __launch_bounds__(T, 1024 / T) gvr_topk_kernel(const Params p) {
         }
       }
     }
+    __syncthreads();
+    const bool failed = S.err || S.tout;
+    if (failed)
+      for (int i = tid; i < k; i += T) out[i] = -2;
     if (stats) {
-      stats[0] = PATH_REFINE;
+      stats[0] = failed ? PATH_DEVICE_ERROR : PATH_REFINE;
       stats[1] = int32_t(cr.m);
       stats[2] = rounds;
       stats[3] = int32_t(cr.above);
@@ -633,6 +742,30 @@ __global__ void __launch_bounds__(T, 1024 / T) gvr_topk_kernel(const Params p) {
   }
 
   // ---------------------------------------------------------------- rescue: cluster radix select
+  // Every staged score of the window takes part; positions outside the window are masked here
+  // by position (their staged NaN would otherwise have a key).
+  auto key_pass = [&](auto&& visit) {
+    for (int ch = 0; ch < nchunks; ++ch) {
+      if (!resident) {
+        const bool armed = issue_chunk(ch);
+        wait_chunk(ch, armed);
+      }
+      const int32_t c0 = chunk_begin(ch), cnt = chunk_count(ch);
+#pragma unroll 1
+      for (int i = 0; i < MAX_VPT; ++i) {
+        const int32_t f = i * T + tid;
+        const bool in = f < cnt;
+        const float4 v = in ? sdata[f] : f4_zero();
+        const int32_t g = c0 + f;  // vector index from the aligned window base
+#pragma unroll
+        for (int l = 0; l < 4; ++l) {
+          const bool valid = in && (g != 0 || l >= lead) && (g != ffull || l < tailn);
+          visit(f4_get(v, l), valid, 4 * g + l - lead);
+        }
+      }
+      if (!resident) __syncthreads();
+    }
+  };
   uint32_t prefix = 0, pmask = 0, need = uint32_t(k);
   bool ge = false;
   for (int pass = 0; pass < 4; ++pass) {
@@ -640,20 +773,13 @@ __global__ void __launch_bounds__(T, 1024 / T) gvr_topk_kernel(const Params p) {
     const int buf = pass & 1;
     for (int i = tid; i < 256; i += T) S.dhist[buf][i] = 0;
     __syncthreads();
-    for (int ch = 0; ch < nchunks; ++ch) {
-      if (!resident) load_chunk(ch);
-#pragma unroll
-      for (int i = 0; i < VPT; ++i) {
-        const uint32_t m = lane_mask(vec_index(ch, i));
-#pragma unroll
-        for (int l = 0; l < 4; ++l) {
-          const uint32_t key = order_key(f4_get(x[i], l));
-          const bool pr = ((m >> l) & 1u) && (key & pmask) == prefix;
-          hist_add(S.dhist[buf], pr, (key >> shift) & 255u);
-        }
-      }
-    }
+    key_pass([&](float e, bool valid, int32_t) {
+      const uint32_t key = order_key(e);
+      const bool pr = valid && (key & pmask) == prefix;
+      hist_add(S.dhist[buf], pr, (key >> shift) & 255u);
+    });
     cluster_sync();
+    report_timeout();
     digit_cross<T>(S, buf, 0, cs, need);
     const uint32_t d = S.dsel, ab = S.dabove, cnt = S.dcnt;
     prefix |= d << shift;
@@ -668,39 +794,33 @@ __global__ void __launch_bounds__(T, 1024 / T) gvr_topk_kernel(const Params p) {
   const uint32_t tie_base = uint32_t(k) - nties;
   const uint32_t rwin = dsmem_map(smem_u32(&S.rc_win), 0);
   const uint32_t rtie = dsmem_map(smem_u32(&S.rc_tie), 0);
-  for (int ch = 0; ch < nchunks; ++ch) {
-    if (!resident) load_chunk(ch);
-#pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      const int32_t f = vec_index(ch, i);
-      const uint32_t m = lane_mask(f);
-#pragma unroll
-      for (int l = 0; l < 4; ++l) {
-        const float e = f4_get(x[i], l);
-        const uint32_t key = order_key(e);
-        const bool valid = (m >> l) & 1u;
-        const bool win = valid && (ge ? (key & pmask) >= prefix : key > prefix);
-        const bool tie = valid && !ge && key == prefix;
-        const int32_t j = 4 * f + l - lead;
-        const uint32_t ws = warp_alloc_remote(rwin, win);
-        if (win && ws < tie_base) {
-          out[ws] = j;
-          if (outv) outv[ws] = e;
-        }
-        const uint32_t ts = warp_alloc_remote(rtie, tie);
-        if (tie && ts < nties) {
-          out[tie_base + ts] = j;
-          if (outv) outv[tie_base + ts] = e;
-        }
-      }
+  key_pass([&](float e, bool valid, int32_t jw) {
+    const uint32_t key = order_key(e);
+    const bool win = valid && (ge ? (key & pmask) >= prefix : key > prefix);
+    const bool tie = valid && !ge && key == prefix;
+    const uint32_t ws = warp_alloc_remote(rwin, win);
+    if (win && ws < tie_base) {
+      out[ws] = jw;
+      if (outv) outv[ws] = e;
     }
-  }
+    const uint32_t ts = warp_alloc_remote(rtie, tie);
+    if (tie && ts < nties) {
+      out[tie_base + ts] = jw;
+      if (outv) outv[tie_base + ts] = e;
+    }
+  });
+  report_timeout();
   cluster_sync();  // rank 0's counters stay alive until every CTA is done with them
-  if (stats) {
-    stats[0] = path;
-    stats[1] = int32_t(cr.m);
-    stats[2] = rounds;
-    stats[3] = 0;
+  if (rank == 0) {
+    const bool failed = S.err || S.tout;
+    if (failed)
+      for (int i = tid; i < k; i += T) out[i] = -2;
+    if (stats) {
+      stats[0] = failed ? PATH_DEVICE_ERROR : path;
+      stats[1] = int32_t(cr.m);
+      stats[2] = rounds;
+      stats[3] = 0;
+    }
   }
 }
 

@@ -17,7 +17,7 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kMaxDevices = 64;
-constexpr int kMaxVpt = 8;
+constexpr int kMaxVpt = gvr::MAX_VPT;
 constexpr int kMaxCluster = 8;
 
 struct DeviceState {
@@ -27,10 +27,9 @@ struct DeviceState {
 };
 DeviceState g_devices[kMaxDevices];
 
-template <int VPT>
 cudaError_t set_attributes() {
-  return cudaFuncSetAttribute(gvr::gvr_topk_kernel<kThreads, VPT>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(gvr::Smem)));
+  return cudaFuncSetAttribute(gvr::gvr_topk_kernel<kThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              gvr::smem_bytes(kThreads * gvr::MAX_VPT));
 }
 
 // One-time per-device set-up: kernel attributes and the SM count.
@@ -42,10 +41,7 @@ cudaError_t device_state(int* sms) {
   DeviceState& st = g_devices[dev];
   std::call_once(st.once, [&st, dev]() {
     cudaError_t r = cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev);
-    if (r == cudaSuccess) r = set_attributes<1>();
-    if (r == cudaSuccess) r = set_attributes<2>();
-    if (r == cudaSuccess) r = set_attributes<4>();
-    if (r == cudaSuccess) r = set_attributes<8>();
+    if (r == cudaSuccess) r = set_attributes();
     st.err = r;
   });
   *sms = st.sms;
@@ -74,10 +70,10 @@ gvr_status check_common(int64_t row_stride, int64_t num_rows, int32_t k, const g
   return GVR_OK;
 }
 
-// Launch geometry.  A row's window never exceeds row_stride, so the cluster must hold
-// row_stride / 4 vectors: cluster_size * threads * vpt >= row_stride / 4 (beyond 8 CTAs of 8
-// vectors per thread the kernel streams its share in chunks).  Few rows spread each row over
-// more CTAs (more SMs pulling one row); many rows keep the CTAs per row low.
+// Launch geometry.  A row's window never exceeds row_stride, so to stage a whole row in shared
+// memory the cluster needs cluster_size * threads * vpt >= row_stride / 4 float4 slots (beyond
+// 8 CTAs of 8 slots per thread the kernel stages its share in several chunks).  Few rows spread
+// each row over more CTAs (more SMs pulling one row); many rows keep the CTAs per row low.
 void plan_geometry(int64_t row_stride, int64_t num_rows, int sms, const gvr_options* o, int* cs_out,
                    int* vpt_out) {
   const int64_t need_vec = row_stride / 4;
@@ -122,7 +118,7 @@ gvr_status launch(const gvr::Params& prm, int64_t num_rows, const gvr_options* o
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(blocks), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = sizeof(gvr::Smem);
+  cfg.dynamicSmemBytes = size_t(gvr::smem_bytes(kThreads * vpt));
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -132,14 +128,9 @@ gvr_status launch(const gvr::Params& prm, int64_t num_rows, const gvr_options* o
   cfg.attrs = attr;
   cfg.numAttrs = 1;
 
-  cudaError_t e = cudaErrorInvalidValue;
-  switch (vpt) {
-    case 1: e = cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<kThreads, 1>, prm); break;
-    case 2: e = cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<kThreads, 2>, prm); break;
-    case 4: e = cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<kThreads, 4>, prm); break;
-    case 8: e = cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<kThreads, 8>, prm); break;
-    default: break;
-  }
+  gvr::Params q = prm;
+  q.slice_vec = kThreads * vpt;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<kThreads>, q);
   return e == cudaSuccess ? GVR_OK : GVR_ERR_LAUNCH;
 }
 
@@ -244,7 +235,7 @@ gvr_status gvr_plan(int64_t row_stride, int64_t num_rows, int32_t k, const gvr_o
   if (cluster_size) *cluster_size = cs;
   if (vectors_per_thread) *vectors_per_thread = vpt;
   if (threads) *threads = kThreads;
-  if (smem_bytes) *smem_bytes = int32_t(sizeof(gvr::Smem));
+  if (smem_bytes) *smem_bytes = int32_t(gvr::smem_bytes(kThreads * vpt));
   return GVR_OK;
 }
 
