@@ -101,7 +101,7 @@ enum {
 
 typedef struct gvr_options {
   int32_t cluster_size;       /* CTAs per row: 0 = automatic, else 1, 2, 4 or 8 */
-  int32_t vectors_per_thread; /* float4 registers per thread: 0 = automatic, else 1, 2, 4, 8 */
+  int32_t reserved0;          /* must be 0 */
   int32_t flags;              /* GVR_FLAG_* bits; results stay exact under every flag */
   int32_t reserved;           /* must be 0 */
   int32_t* row_stats;         /* optional device int32 [num_rows][4]: path (GVR_PATH_*),
@@ -109,8 +109,10 @@ typedef struct gvr_options {
                                  crossing bin */
 } gvr_options;
 
-/* Values of row_stats[r][0]. */
+/* Values of row_stats[r][0].  GVR_PATH_DEVICE_ERROR means a CTA gave up waiting (0.5 s) for
+ * its staged scores; every index of that row is then -2.  It is not expected to happen. */
 enum {
+  GVR_PATH_DEVICE_ERROR = -1,
   GVR_PATH_SHORT = 0,           /* nv <= k: identity and -1 pad */
   GVR_PATH_REFINE = 1,          /* histogram, crossing bin, candidates, exact refine */
   GVR_PATH_RESCUE_BRACKET = 2,  /* invalid sampled bracket: exact rescue */
@@ -134,14 +136,14 @@ const char* gvr_status_string(gvr_status status);
 
 /*
  * The launch geometry the library would choose for a call on the current device (host
- * only, no device work): CTAs per row (cluster size), float4 registers per thread, threads
- * per CTA and dynamic shared memory bytes.  Returns the GVR_ERR_* code the entry points would
- * return for these arguments.  sm_count > 0 overrides the device's SM count (for planning
- * without a device); any output pointer may be NULL.
+ * only, no device work): CTAs per row (cluster size), bytes per shared-memory ring stage,
+ * threads per CTA and dynamic shared memory bytes per CTA.  Returns the GVR_ERR_* code the
+ * entry points would return for these arguments.  sm_count > 0 overrides the device's SM
+ * count (for planning without a device); any output pointer may be NULL.
  */
 gvr_status gvr_plan(int64_t row_stride, int64_t num_rows, int32_t k, const gvr_options* options,
-                    int32_t sm_count, int32_t* cluster_size, int32_t* vectors_per_thread,
-                    int32_t* threads, int32_t* smem_bytes);
+                    int32_t sm_count, int32_t* cluster_size, int32_t* stage_bytes, int32_t* threads,
+                    int32_t* smem_bytes);
 
 #ifdef __cplusplus
 }

@@ -1,9 +1,10 @@
 // gvr_kernel.cuh -- the GVR (Guess-Verify-Refine) exact per-row top-K kernel for sm_103a.
 //
 // One thread-block cluster selects one row.  The row's valid window is split evenly over the
-// cluster's CTAs; each CTA stages its share in shared memory with bulk asynchronous copies
-// (TMA, completion on an mbarrier), so the row is read from HBM exactly once and every later
-// pass reads shared memory.  Per row:
+// cluster's CTAs; each CTA streams its share through a small ring of shared-memory stages
+// filled by bulk asynchronous copies (TMA, completion on one mbarrier per stage), so the row
+// is read from HBM once and each CTA needs little shared memory: several CTAs -- several rows
+// -- are resident on every SM at a time.  Per row:
 //
 //   Guess   uniform block64 sampling: K scores in K/64 runs of 64 consecutive scores whose
 //           starts spread evenly over the window, first run at 0, last run ending at nv.
@@ -22,24 +23,21 @@
 //           rescue of PR #20998, in the same launch, with no host synchronization.
 //
 // Implementation choices that keep the per-score work to about one compare:
-//  * sampled histogram floor: the samples also give a floor bin F below which, by the sample
-//    quantile, the crossing should not lie; only scores in bins >= F are counted.  A score's
-//    bin is >= F exactly when the score is >= v_F, the smallest float whose bin is >= F (found
-//    by a 32-way search over float keys), so the floor test is one float compare.  If fewer
-//    than K scores reach the floor, the bins below it are counted in a second round, so the
-//    result never depends on the floor.
-//  * above-floor bitmask: each thread compares its (at most 32) staged scores with v_F once
-//    and keeps a 32-bit mask of the few that pass; the histogram and the collect step then
-//    visit only the set bits, reading those scores back from shared memory.  A warp whose
-//    masks are dense (tie-heavy rows) counts with warp-aggregated atomics (__match_any_sync)
-//    instead, one shared-memory atomic per distinct bin per warp instruction.
+//  * sampled histogram floor: the samples also give a floor t below which, by the sample
+//    quantile, the crossing should not lie; only scores >= t are counted, and they are kept in
+//    a small shared-memory list for the collect step (no second read of the row).  Bins above
+//    bin(t) are then complete, bin(t) itself is partial.  If the crossing lands in bin(t) or
+//    below, the scores below t are counted in a second pass, so the result never depends on
+//    the floor.
+//  * warp-aggregated shared-memory atomics (__match_any_sync) for every histogram update and
+//    ballot-aggregated slot allocation for list, winner and candidate slots, so tie-heavy rows
+//    cost one atomic per distinct bin per warp instruction.
 //
 // The bin function is monotone non-decreasing in the score (IEEE round-to-nearest subtract and
 // multiply by a positive scale, clamp, truncate), which is all the crossing-bin logic needs;
 // it is evaluated with the same instruction sequence everywhere, so every pass and every CTA
 // classifies a score identically.  Positions outside the window (the lead lanes below an
-// unaligned window start, the lanes past its end) are never compared: they are staged as NaN,
-// which fails every `>=` / `<` test, and the key-space rescue masks them by position.
+// unaligned window start, the lanes past its end) are excluded by position in every pass.
 #pragma once
 
 #include <cfloat>
@@ -50,16 +48,19 @@
 
 namespace gvr {
 
+constexpr int THREADS = 256;          // threads per CTA
 constexpr int NB = 2048;              // value-histogram bins over [GMIN, GMAX]
 constexpr int NCOARSE = 256;          // bins of the sample histogram that sets the floor
 constexpr int COARSE_SHIFT = 3;       // NB / NCOARSE == 8
-constexpr int CAP = 4096;             // candidate slots in cluster rank 0
+constexpr int VPS = 2;                // float4 per thread per stage
+constexpr int STAGE_VEC = THREADS * VPS;  // 512 float4 = 8 KB per stage
+constexpr int NSTAGE = 3;             // stages in the ring
+constexpr int LIST_CAP = 1024;        // above-floor scores kept per CTA for the collect step
+constexpr int CAP = 1024;             // candidate slots in cluster rank 0
 constexpr int RANK_REFINE_MAX = 256;  // m at or below: refine by pairwise ranking
+constexpr int SPARSE_MAX = 4;         // above-floor scores of a thread per stage before a warp aggregates
 constexpr int MAX_K = 2048;
-constexpr int MAX_VPT = 8;            // staged float4 per thread per chunk: a 32-bit score mask
-constexpr int SPARSE_MAX = 8;         // above-floor scores per thread beyond which a warp goes dense
-constexpr uint32_t COPY_PIECE = 16384;             // bytes per bulk copy instruction
-constexpr uint64_t WAIT_LIMIT_NS = 500000000ull;   // bound on any wait for staged data (0.5 s)
+constexpr uint64_t WAIT_LIMIT_NS = 500000000ull;  // bound on any wait for staged data (0.5 s)
 
 enum : int32_t { MODE_DECODE = 0, MODE_PREFILL = 1 };
 enum : int32_t { FLAG_FORCE_RESCUE = 1, FLAG_NO_FLOOR = 2, FLAG_ZERO_CAP = 4, FLAG_RADIX_REFINE = 8 };
@@ -86,7 +87,6 @@ struct Params {
   int32_t k;
   int32_t mode;
   int32_t flags;
-  int32_t slice_vec;          // float4 slots of the shared-memory stage per CTA (T * vpt)
 };
 
 struct Crossing {
@@ -99,31 +99,35 @@ struct Crossing {
 };
 
 struct alignas(16) Smem {
-  uint32_t hist[NB];  // first: 16-byte aligned groups of 4 bins are read as one vector
-  uint32_t dhist[2][256];
-  uint32_t shist[NCOARSE];
+  uint32_t hist[NB];                  // first: groups of 4 bins are read as 16-byte vectors
+  float4 ring[NSTAGE][STAGE_VEC];     // bulk-copy destinations (16-byte aligned)
+  float list_v[LIST_CAP];
+  int32_t list_j[LIST_CAP];
   float cand_v[CAP];
   int32_t cand_j[CAP];
+  uint32_t dhist[2][256];
+  uint32_t shist[NCOARSE];
   uint32_t wsum[2][32];
   float wmin[32];
   float wmax[32];
+  float4 tail;                        // the partial last vector of the window, NaN-padded
   Crossing cross;
   float vthr;
-  int32_t floor_bin;
+  int32_t fpart;
   uint32_t dsel, dabove, dcnt;
-  uint32_t ctr_win, ctr_cand;   // this CTA's slot counters (refine path)
-  uint32_t ctr_rwin, ctr_rtie;  // rank 0's counters for its own radix refine
-  uint32_t rc_win, rc_tie;      // rank 0's counters shared by the cluster in rescue
-  uint32_t tout;                // this CTA gave up waiting for staged data
-  uint32_t err;                 // rank 0: some CTA of the cluster gave up
-  uint64_t bar;                 // completion of the bulk copies of the current stage
+  uint32_t list_n;                    // scores appended to the list (may exceed LIST_CAP)
+  uint32_t ctr_win, ctr_cand;         // this CTA's slot counters (refine path)
+  uint32_t ctr_rwin, ctr_rtie;        // rank 0's counters for its own radix refine
+  uint32_t rc_win, rc_tie;            // rank 0's counters shared by the cluster in rescue
+  uint32_t tout;                      // this CTA gave up waiting for staged data
+  uint32_t err;                       // rank 0: some CTA of the cluster gave up
+  uint64_t bar[NSTAGE];               // one mbarrier per ring stage
 };
 static_assert(offsetof(Smem, hist) % 16 == 0, "histogram groups are read as 16-byte vectors");
-static_assert(offsetof(Smem, bar) % 8 == 0, "mbarrier must be 8-byte aligned");
+static_assert(offsetof(Smem, ring) % 16 == 0, "bulk-copy destinations must be 16-byte aligned");
+static_assert(offsetof(Smem, bar) % 8 == 0, "mbarriers must be 8-byte aligned");
 
-constexpr int SMEM_FIXED = int((sizeof(Smem) + 127) / 128 * 128);
-
-__host__ __device__ constexpr int smem_bytes(int slice_vec) { return SMEM_FIXED + 16 * slice_vec; }
+constexpr int SMEM_BYTES = int((sizeof(Smem) + 127) / 128 * 128);
 
 // Monotone bin of a score in [GMIN, GMAX] with NB bins; NaN maps to bin 0.
 __device__ __forceinline__ int value_bin(float v, float gmin, float sc) {
@@ -204,17 +208,30 @@ __device__ __forceinline__ Crossing reduce_crossing(Smem& S, uint32_t cs, uint32
   for (int j = 0; j < BPT; ++j) tot[j] = pre[j] = 0;
   if (lo_bin + BPT - 1 >= fbin) {
     const uint32_t local = smem_u32(&S.hist[lo_bin]);
-    for (uint32_t c = 0; c < cs; ++c) {
-      const uint32_t addr = dsmem_map(local, c);
+    constexpr int G = 4;  // remote ranks whose loads are in flight together
+    for (uint32_t c0 = 0; c0 < cs; c0 += G) {
+      uint4 v[G][BPT / 4];
 #pragma unroll
-      for (int q = 0; q < BPT / 4; ++q) {
-        const uint4 v = dsmem_ld_v4(addr + 16u * q);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      for (int g = 0; g < G; ++g) {
+        if (c0 + g < cs) {
+          const uint32_t addr = dsmem_map(local, c0 + g);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = BPT - 1 - (4 * q + e);  // descending position of bin lo_bin + 4q + e
-          tot[j] += w[e];
-          if (c < rank) pre[j] += w[e];
+          for (int q = 0; q < BPT / 4; ++q) v[g][q] = dsmem_ld_v4(addr + 16u * q);
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        if (c0 + g < cs) {
+#pragma unroll
+          for (int q = 0; q < BPT / 4; ++q) {
+            const uint32_t w[4] = {v[g][q].x, v[g][q].y, v[g][q].z, v[g][q].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j = BPT - 1 - (4 * q + e);  // descending position of bin lo_bin + 4q + e
+              tot[j] += w[e];
+              if (c0 + g < rank) pre[j] += w[e];
+            }
+          }
         }
       }
     }
@@ -306,47 +323,47 @@ __device__ __forceinline__ void digit_cross(Smem& S, int buf, uint32_t c0, uint3
   __syncthreads();
 }
 
-template <int T>
-__global__ void __launch_bounds__(T, 2) gvr_topk_kernel(const Params p) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  Smem& S = *reinterpret_cast<Smem*>(smem_raw);
-  float4* sdata = reinterpret_cast<float4*>(smem_raw + SMEM_FIXED);
-  const float* sdataf = reinterpret_cast<const float*>(smem_raw + SMEM_FIXED);
+__global__ void __launch_bounds__(THREADS, 4) gvr_topk_kernel(const Params p) {
+  constexpr int T = THREADS;
   constexpr int NW = T / 32;
   constexpr int KPT = (MAX_K + T - 1) / T;  // samples per thread at most
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  Smem& S = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t cs = cluster_size();
   const uint32_t rank = cluster_rank();
-  const int64_t row = cluster_id_x();
+  const uint32_t row = cluster_id_x();
   const int32_t k = p.k;
   const float qnan = __int_as_float(0x7fffffff);
 
   // ---------------------------------------------------------------- row geometry
-  // row_stride < 2^31, so window offsets and lengths fit in 32 bits.
-  int32_t a = 0, nv = 0;
+  // row_stride < 2^31 and every count below fits in 32 bits.
+  const uint32_t stride = uint32_t(p.row_stride);
+  uint32_t a = 0, nv = 0;
   if (p.mode == MODE_DECODE) {
-    const int64_t kv = p.kv_lens[row / p.next_n];
-    int64_t n = 0;
-    if (kv >= p.next_n) n = (kv - p.next_n + row % p.next_n + 1) / p.compress_ratio;
-    nv = int32_t(n < p.row_stride ? n : p.row_stride);
+    const uint32_t nn = uint32_t(p.next_n);
+    const uint32_t req = row / nn;
+    const int32_t kv = p.kv_lens[req];
+    if (kv >= p.next_n) nv = (uint32_t(kv) - nn + (row - req * nn) + 1u) / uint32_t(p.compress_ratio);
+    nv = nv < stride ? nv : stride;
   } else {
-    const int64_t ks = p.row_starts[row];
-    const int64_t ke = p.row_ends[row];
-    const int64_t s = ks > 0 ? ks : 0;
-    const int64_t e = ke < p.row_stride ? ke : p.row_stride;
-    a = int32_t(s < p.row_stride ? s : p.row_stride);
-    nv = int32_t(e > s ? e - s : 0);
+    const int32_t ks = p.row_starts[row];
+    const int32_t ke = p.row_ends[row];
+    const uint32_t s = ks > 0 ? uint32_t(ks) : 0u;
+    const uint32_t e = ke > 0 ? (uint32_t(ke) < stride ? uint32_t(ke) : stride) : 0u;
+    a = s < stride ? s : stride;
+    nv = e > a ? e - a : 0u;
   }
-  const float* rowp = p.logits + row * p.row_stride;
-  int32_t* out = p.indices + row * int64_t(k);
-  float* outv = p.values ? p.values + row * int64_t(k) : nullptr;
-  int32_t* stats = (p.row_stats && rank == 0 && tid == 0) ? p.row_stats + 4 * row : nullptr;
+  const float* rowp = p.logits + int64_t(row) * p.row_stride;
+  int32_t* out = p.indices + int64_t(row) * k;
+  float* outv = p.values ? p.values + int64_t(row) * k : nullptr;
+  int32_t* stats = (p.row_stats && rank == 0 && tid == 0) ? p.row_stats + 4 * int64_t(row) : nullptr;
 
   // ---------------------------------------------------------------- short row: identity
-  if (nv <= k) {
+  if (nv <= uint32_t(k)) {
     for (int i = int(rank) * T + tid; i < k; i += int(cs) * T) {
-      out[i] = i < nv ? i : -1;
-      if (outv) outv[i] = i < nv ? rowp[a + i] : -FLT_MAX;
+      out[i] = uint32_t(i) < nv ? i : -1;
+      if (outv) outv[i] = uint32_t(i) < nv ? rowp[a + i] : -FLT_MAX;
     }
     if (stats) {
       stats[0] = PATH_SHORT;
@@ -355,123 +372,147 @@ __global__ void __launch_bounds__(T, 2) gvr_topk_kernel(const Params p) {
     return;
   }
 
+  // ---------------------------------------------------------------- this CTA's stages
+  // Vectors are 16-byte aligned float4s from the aligned column at or below the window start:
+  // vector g holds window positions 4g - lead .. 4g + 3 - lead.  The first `lead` lanes of
+  // vector 0 and the lanes past the window end in the partial last vector are masked.  The row
+  // is cut into stages of STAGE_VEC vectors dealt round-robin to the cluster's CTAs (stage s to
+  // rank s % cs), so every CTA sees the whole row evenly, however the scores drift with position.
+  const int32_t lead = int32_t(a & 3u);
+  const float* base = rowp + (a - uint32_t(lead));
+  const int32_t span = lead + int32_t(nv);
+  const int32_t ffull = span >> 2;        // whole vectors inside [col0, window end)
+  const int32_t tailn = span & 3;         // in-window scalars of the partial last vector
+  const int32_t nvec = ffull + (tailn ? 1 : 0);
+  const int32_t nrow_stages = (nvec + STAGE_VEC - 1) / STAGE_VEC;
+  const int32_t nstages = int32_t(rank) < nrow_stages
+                              ? (nrow_stages - int32_t(rank) + int32_t(cs) - 1) / int32_t(cs)
+                              : 0;
+  auto stage_first = [&](int32_t s) -> int32_t {  // first vector of this CTA's s-th stage
+    return (int32_t(rank) + s * int32_t(cs)) * STAGE_VEC;
+  };
+
   for (int i = tid; i < NB; i += T) S.hist[i] = 0;
   for (int i = tid; i < NCOARSE; i += T) S.shist[i] = 0;
   if (tid == 0) {
+    S.list_n = 0;
     S.ctr_win = S.ctr_cand = S.ctr_rwin = S.ctr_rtie = 0;
     S.rc_win = S.rc_tie = 0;
     S.tout = S.err = 0;
     S.cross = Crossing{};
     S.dsel = S.dabove = S.dcnt = 0;
-    mbar_init(&S.bar, 1);
+#pragma unroll
+    for (int s = 0; s < NSTAGE; ++s) mbar_init(&S.bar[s], 1);
     mbar_init_fence();
   }
-
-  // ---------------------------------------------------------------- this CTA's share
-  // Vectors are 16-byte aligned float4s starting at the aligned column at or below the
-  // window start.  The share [vb, ve) is staged in chunks of slice_vec vectors; with one chunk
-  // (the usual case) it is staged once and stays resident for every pass.
-  const int32_t lead = a & 3;
-  const float* base = rowp + (a - lead);
-  const int32_t span = lead + nv;
-  const int32_t ffull = span >> 2;  // whole vectors inside [col0, window end)
-  const int32_t tailn = span & 3;   // in-window scalars of the partial last vector
-  const int32_t nvec = ffull + (tailn ? 1 : 0);
-  const int32_t per = int32_t((nvec + int32_t(cs) - 1) / int32_t(cs));
-  const int32_t vb = int32_t(rank) * per < nvec ? int32_t(rank) * per : nvec;
-  const int32_t ve = vb + per < nvec ? vb + per : nvec;
-  const int32_t cap_vec = p.slice_vec;
-  const int32_t nloc = ve - vb;
-  const int nchunks = nloc > 0 ? (nloc + cap_vec - 1) / cap_vec : 0;
-  const bool resident = nchunks <= 1;
-  uint32_t phase = 0;
-
-  auto chunk_begin = [&](int ch) -> int32_t { return vb + ch * cap_vec; };
-  auto chunk_count = [&](int ch) -> int32_t {
-    const int32_t c0 = vb + ch * cap_vec;
-    return (c0 + cap_vec < ve ? c0 + cap_vec : ve) - c0;
-  };
-  // Stage chunk ch: bulk copies of its whole vectors (thread 0) and the in-window scalars of
-  // the partial last vector.  Returns whether bulk copies were issued (same on all threads).
-  auto issue_chunk = [&](int ch) -> bool {
-    const int32_t c0 = chunk_begin(ch), c1 = c0 + chunk_count(ch);
-    const int32_t fe = c1 < ffull ? c1 : ffull;
-    const int32_t nfull = fe > c0 ? fe - c0 : 0;
-    if (tid == 0 && nfull > 0) {
-      fence_proxy_async_smem();
-      const uint32_t bytes = uint32_t(nfull) * 16u;
-      mbar_arrive_expect_tx(&S.bar, bytes);
-      const char* src = reinterpret_cast<const char*>(base + 4 * size_t(c0));
-      char* dst = reinterpret_cast<char*>(sdata);
-      for (uint32_t off = 0; off < bytes; off += COPY_PIECE) {
-        const uint32_t n = bytes - off < COPY_PIECE ? bytes - off : COPY_PIECE;
-        bulk_copy_g2s(dst + off, src + off, n, &S.bar);
-      }
-    }
-    if (tid == 32 && tailn && ffull >= c0 && ffull < c1) {
+  if (tid == 32) {  // the partial last vector is read with scalar loads, never past the window
+    S.tail = make_float4(qnan, qnan, qnan, qnan);
+    if (tailn && (ffull / STAGE_VEC) % int32_t(cs) == int32_t(rank)) {
       const float* q = base + 4 * size_t(ffull);
-      sdata[ffull - c0] = make_float4(q[0], tailn > 1 ? q[1] : qnan, tailn > 2 ? q[2] : qnan, qnan);
+      S.tail = make_float4(q[0], tailn > 1 ? q[1] : qnan, tailn > 2 ? q[2] : qnan, qnan);
     }
-    return nfull > 0;
+  }
+
+  // ---------------------------------------------------------------- streaming ring
+  // The CTA's stages of every pass go through the ring in one sequence q = qbase + s: slot
+  // q % NSTAGE, mbarrier phase (q / NSTAGE) & 1.  Thread 0 refills a slot after all threads
+  // have left it.
+  uint32_t qbase = 0;
+  bool late = false;
+  auto stage_full = [&](int32_t s) -> int32_t {  // whole vectors of stage s (bulk-copied)
+    const int32_t c0 = stage_first(s);
+    const int32_t c1 = c0 + STAGE_VEC < nvec ? c0 + STAGE_VEC : nvec;
+    const int32_t fe = c1 < ffull ? c1 : ffull;
+    return fe > c0 ? fe - c0 : 0;
   };
-  // Wait (bounded) for chunk ch, blank the lead lanes below the window start, publish.
-  auto wait_chunk = [&](int ch, bool armed) {
-    bool late = false;
-    if (armed) {
-      if (!mbar_wait_bounded(&S.bar, phase, WAIT_LIMIT_NS)) {
-        mbar_wait_bounded(&S.bar, phase, WAIT_LIMIT_NS);  // let copies in flight land
+  // Every stage completes exactly one phase of its slot's barrier, even a stage with no whole
+  // vector (only the partial tail), so slot phases stay in step with q.
+  auto issue_stage = [&](int32_t s) {  // thread 0 only
+    const int32_t nfull = stage_full(s);
+    const uint32_t slot = (qbase + uint32_t(s)) % NSTAGE;
+    if (nfull > 0) {
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(&S.bar[slot], uint32_t(nfull) * 16u);
+      bulk_copy_g2s(&S.ring[slot][0], base + 4 * size_t(stage_first(s)), uint32_t(nfull) * 16u,
+                    &S.bar[slot]);
+    } else {
+      mbar_arrive(&S.bar[slot]);
+    }
+  };
+  // One pass over this CTA's stages: visit(slot, c0) once per stage, after the stage has landed
+  // in ring slot `slot`; c0 is the row vector index of the stage's first vector.  All threads
+  // call visit the same number of times, so visitors may use warp collectives.
+  auto stream_pass = [&](bool primed, auto&& visit) {
+    if (tid == 0 && !primed)
+      for (int32_t s = 0; s < NSTAGE && s < nstages; ++s) issue_stage(s);
+    for (int32_t s = 0; s < nstages; ++s) {
+      const uint32_t q = qbase + uint32_t(s);
+      const uint32_t slot = q % NSTAGE;
+      if (!mbar_wait_bounded(&S.bar[slot], (q / NSTAGE) & 1u, WAIT_LIMIT_NS)) {
+        mbar_wait_bounded(&S.bar[slot], (q / NSTAGE) & 1u, WAIT_LIMIT_NS);  // let copies land
         late = true;
       }
-      phase ^= 1u;
+      visit(slot, stage_first(s));
+      __syncthreads();  // every thread is done with this slot
+      if (tid == 0 && s + NSTAGE < nstages) issue_stage(s + NSTAGE);
     }
-    if (tid == 0 && lead > 0 && chunk_begin(ch) == 0 && chunk_count(ch) > 0) {
-      float* v0 = reinterpret_cast<float*>(sdata);
-      for (int l = 0; l < lead; ++l) v0[l] = qnan;
-    }
+    qbase += uint32_t(nstages);
     if (__syncthreads_or(late) && tid == 0) S.tout = 1;
+  };
+  // The i-th vector of this thread in the stage at (slot, c0): its share index g, its values
+  // and the 4-bit mask of its in-window lanes (0 past the share).
+  auto stage_vec = [&](uint32_t slot, int32_t c0, int i, int32_t& g, float4& v) -> uint32_t {
+    const int32_t f = i * T + tid;
+    g = c0 + f;
+    v = f4_zero();
+    if (g >= nvec) return 0u;
+    uint32_t lanes = 0xFu;
+    if (g < ffull) {
+      v = S.ring[slot][f];
+    } else {
+      v = S.tail;
+      lanes = (1u << tailn) - 1u;
+    }
+    if (g == 0) lanes &= (0xFu << lead) & 0xFu;
+    return lanes;
+  };
+  // Score j (bit j = 4i + l of a stage mask) of this thread in the stage at (slot, c0).
+  auto stage_score = [&](uint32_t slot, int32_t c0, int j) -> float {
+    const int32_t f = (j >> 2) * T + tid;
+    if (c0 + f >= ffull) return f4_get(S.tail, j & 3);
+    return reinterpret_cast<const float*>(&S.ring[slot][0])[4 * f + (j & 3)];
+  };
+  // Per-lane walk of one stage for the rarely taken passes: f(e, g, valid, l) for every lane of
+  // every vector slot of this thread (warp-uniform call count).
+  auto each_lane = [&](uint32_t slot, int32_t c0, auto&& f) {
+#pragma unroll
+    for (int i = 0; i < VPS; ++i) {
+      int32_t g;
+      float4 v;
+      const uint32_t lanes = stage_vec(slot, c0, i, g, v);
+#pragma unroll
+      for (int l = 0; l < 4; ++l) f(f4_get(v, l), g, ((lanes >> l) & 1u) != 0, l);
+    }
   };
   // After a cluster barrier: tell rank 0 that this CTA gave up waiting (rank 0 marks the row).
   auto report_timeout = [&]() {
     if (tid == 0 && S.tout) dsmem_st_u32(dsmem_map(smem_u32(&S.err), 0), 1u);
   };
-  // Mask of this thread's staged scores that are >= thr (below == false) or < thr (below ==
-  // true); bit 4i+l is lane l of the thread's i-th vector (chunk vector i*T + tid).
-  auto build_bits = [&](int32_t cnt, float thr, bool below) -> uint32_t {
-    uint32_t bits = 0;
-#pragma unroll
-    for (int i = 0; i < MAX_VPT; ++i) {
-      const int32_t f = i * T + tid;
-      if (f < cnt) {
-        const float4 v = sdata[f];
-        uint32_t b;
-        if (!below)
-          b = uint32_t(v.x >= thr) | (uint32_t(v.y >= thr) << 1) | (uint32_t(v.z >= thr) << 2) |
-              (uint32_t(v.w >= thr) << 3);
-        else
-          b = uint32_t(v.x < thr) | (uint32_t(v.y < thr) << 1) | (uint32_t(v.z < thr) << 2) |
-              (uint32_t(v.w < thr) << 3);
-        bits |= b << (4 * i);
-      }
-    }
-    return bits;
-  };
-  auto bit_score = [&](int j) -> float { return sdataf[4 * ((j >> 2) * T + tid) + (j & 3)]; };
-
-  bool armed0 = false;
-  if (nchunks == 1) armed0 = issue_chunk(0);  // overlaps the sampling below
 
   // ---------------------------------------------------------------- guess: block64 sample
-  const int nblk = k >> 6;
+  const uint32_t nblk = uint32_t(k) >> 6;
+  const uint32_t sq = (nv - 64u) / (nblk - 1u), sr = (nv - 64u) % (nblk - 1u);
   float sv[KPT];
   float lmin = INFINITY, lmax = -INFINITY;
 #pragma unroll
   for (int q = 0; q < KPT; ++q) {
-    const int i = q * T + tid;
+    const uint32_t i = uint32_t(q * T + tid);
     sv[q] = qnan;
-    if (i < k) {
-      const int64_t blk = i >> 6;
-      const int32_t s = int32_t(blk * (nv - 64) / (nblk - 1));
-      const float v = __ldg(rowp + a + s + (i & 63));
+    if (i < uint32_t(k)) {
+      const uint32_t blk = i >> 6;
+      // start of run blk = floor(blk * (nv - 64) / (nblk - 1)) without 64-bit arithmetic
+      const uint32_t s = blk * sq + (blk * sr) / (nblk - 1u);
+      const float v = __ldg(rowp + a + s + (i & 63u));
       sv[q] = v;
       if (isfinite(v)) {
         lmin = fminf(lmin, v);
@@ -479,6 +520,9 @@ __global__ void __launch_bounds__(T, 2) gvr_topk_kernel(const Params p) {
       }
     }
   }
+  // The sample loads go out first; the ring's bulk copies queue behind them.
+  if (tid == 0)
+    for (int32_t s = 0; s < NSTAGE && s < nstages; ++s) issue_stage(s);  // overlaps the sampling
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     lmin = fminf(lmin, __shfl_xor_sync(FULL_MASK, lmin, o));
@@ -503,11 +547,10 @@ __global__ void __launch_bounds__(T, 2) gvr_topk_kernel(const Params p) {
   else if (!bracket_ok) path = PATH_RESCUE_BRACKET;
 
   float sc = 0.f;
-  float vfloor = -INFINITY;
-  int fbin = 0;
+  float thr = -INFINITY;  // floor: scores >= thr are counted (and listed) in the first pass
+  int fpart = -1;         // bin(thr): the one partially counted bin; -1 = no floor
   if (path == PATH_REFINE) {
     sc = __fdiv_rn(float(NB), __fsub_rn(gmax, gmin));
-    // ------------------------------------------------------------ sampled floor
     if (!(p.flags & FLAG_NO_FLOOR)) {
       // mu = k*k/nv samples are expected above tau; keep mu + 3 sqrt(mu) + 16 above the floor
       const float mu = float(k) * float(k) / float(nv);
@@ -549,115 +592,128 @@ __global__ void __launch_bounds__(T, 2) gvr_topk_kernel(const Params p) {
           }
           fc = __shfl_sync(FULL_MASK, fc, src);
         }
-        const int fb = fc << COARSE_SHIFT;
-        const float vf = fb > 0 ? floor_value(fb, gmin, sc) : -INFINITY;
         if (lane == 0) {
-          S.floor_bin = fb;
-          S.vthr = vf;
+          // any threshold works: bins above bin(t) are complete, bin(t) is partial
+          const float t = fc > 0 ? __fadd_rn(gmin, __fdiv_rn(float(fc << COARSE_SHIFT), sc)) : -INFINITY;
+          S.vthr = t;
+          S.fpart = fc > 0 ? value_bin(t, gmin, sc) : -1;
         }
       }
       __syncthreads();
-      fbin = S.floor_bin;
-      vfloor = S.vthr;
+      thr = S.vthr;
+      fpart = S.fpart;
     }
   }
 
-  if (nchunks == 1) wait_chunk(0, armed0);
-
   Crossing cr{};
   int rounds = 0;
-  uint32_t mbits = 0;  // resident share: this thread's scores >= vfloor
+  bool listed = false;  // the list holds every score >= thr of this CTA's share
   if (path == PATH_REFINE) {
     // ------------------------------------------------------------ verify: value histogram
-    auto count_bits = [&](uint32_t bits) {
-      const bool dense = __any_sync(FULL_MASK, __popc(bits) > SPARSE_MAX);
-      if (!dense) {
-        while (bits) {
+    // Pass 1 counts (and lists) the scores >= thr; pass 2, only when the crossing falls in
+    // the partial bin or below, counts the rest.
+    stream_pass(true, [&](uint32_t slot, int32_t c0) {
+      uint32_t bits = 0;  // bit 4i+l: lane l of this thread's i-th vector is >= thr
+#pragma unroll
+      for (int i = 0; i < VPS; ++i) {
+        int32_t g;
+        float4 v;
+        const uint32_t lanes = stage_vec(slot, c0, i, g, v);
+        const uint32_t b = uint32_t(v.x >= thr) | (uint32_t(v.y >= thr) << 1) | (uint32_t(v.z >= thr) << 2) |
+                           (uint32_t(v.w >= thr) << 3);
+        bits |= (b & lanes) << (4 * i);
+      }
+      if (!__any_sync(FULL_MASK, __popc(bits) > SPARSE_MAX)) {
+        while (bits) {  // the usual case: a few scores per thread, plain atomics
           const int j = __ffs(bits) - 1;
           bits &= bits - 1;
-          atomicAdd(&S.hist[value_bin(bit_score(j), gmin, sc)], 1u);
+          const float e = stage_score(slot, c0, j);
+          atomicAdd(&S.hist[value_bin(e, gmin, sc)], 1u);
+          const uint32_t at = atomicAdd(&S.list_n, 1u);
+          if (at < uint32_t(LIST_CAP)) {
+            S.list_v[at] = e;
+            S.list_j[at] = 4 * (c0 + (j >> 2) * T + tid) + (j & 3) - lead;
+          }
         }
-      } else {
-#pragma unroll 4
-        for (int j = 0; j < 4 * MAX_VPT; ++j) {
-          const bool pr = (bits >> j) & 1u;
-          const float e = pr ? bit_score(j) : 0.f;
-          hist_add(S.hist, pr, pr ? uint32_t(value_bin(e, gmin, sc)) : 0u);
-        }
-      }
-    };
-    for (int round = 0; round < 2; ++round) {
-      const bool upper = round == 0;
-      ++rounds;
-      if (resident) {
-        if (nchunks == 1) {
-          const uint32_t b = build_bits(nloc, vfloor, !upper);
-          if (upper) mbits = b;
-          count_bits(b);
-        }
-      } else {
-        for (int ch = 0; ch < nchunks; ++ch) {
-          const bool armed = issue_chunk(ch);
-          wait_chunk(ch, armed);
-          count_bits(build_bits(chunk_count(ch), vfloor, !upper));
-          __syncthreads();
+      } else {  // tie-heavy warp: aggregate per distinct bin and per warp
+#pragma unroll
+        for (int j = 0; j < 4 * VPS; ++j) {
+          const bool hit = (bits >> j) & 1u;
+          const float e = hit ? stage_score(slot, c0, j) : 0.f;
+          const uint32_t at = warp_alloc_local(&S.list_n, hit);
+          if (hit && at < uint32_t(LIST_CAP)) {
+            S.list_v[at] = e;
+            S.list_j[at] = 4 * (c0 + (j >> 2) * T + tid) + (j & 3) - lead;
+          }
+          hist_add(S.hist, hit, hit ? uint32_t(value_bin(e, gmin, sc)) : 0u);
         }
       }
+    });
+    listed = S.list_n <= uint32_t(LIST_CAP);
+    rounds = 1;
+    cluster_sync();
+    report_timeout();
+    cr = reduce_crossing<T>(S, cs, rank, uint32_t(k), fpart > 0 ? fpart : 0);
+    if (fpart >= 0 && (cr.total < uint32_t(k) || cr.bin <= fpart)) {
+      rounds = 2;
+      stream_pass(false, [&](uint32_t slot, int32_t c0) {
+        each_lane(slot, c0, [&](float e, int32_t, bool valid, int) {
+          const bool hit = valid && e < thr;
+          if (__any_sync(FULL_MASK, hit)) hist_add(S.hist, hit, uint32_t(value_bin(e, gmin, sc)));
+        });
+      });
       cluster_sync();
       report_timeout();
-      cr = reduce_crossing<T>(S, cs, rank, uint32_t(k), upper ? fbin : 0);
-      if (cr.total >= uint32_t(k)) break;
-      if (!upper || fbin == 0) break;  // fewer than k countable scores (NaN in the window)
+      cr = reduce_crossing<T>(S, cs, rank, uint32_t(k), 0);
     }
     const uint32_t cap = (p.flags & FLAG_ZERO_CAP) ? 0u : uint32_t(CAP);
-    if (cr.total < uint32_t(k) || cr.m > cap) path = PATH_RESCUE_OVERFLOW;
+    if (cr.total < uint32_t(k) || cr.m > cap) path = PATH_RESCUE_OVERFLOW;  // < k: NaN in window
   }
 
   if (path == PATH_REFINE) {
     // ------------------------------------------------------------ collect
     const int bstar = cr.bin;
-    float thr = vfloor;
-    if (rounds > 1) {  // scores below the floor were counted too: select bins >= b* afresh
+    const uint32_t rv = dsmem_map(smem_u32(&S.cand_v[0]), 0);
+    const uint32_t rj = dsmem_map(smem_u32(&S.cand_j[0]), 0);
+    auto place = [&](float e, int32_t jw, bool valid) {  // warp-collective
+      const int b = valid ? value_bin(e, gmin, sc) : -1;
+      const uint32_t ws = warp_alloc_local(&S.ctr_win, b > bstar);
+      if (b > bstar) {
+        const uint32_t slot = cr.base_above + ws;
+        if (slot < uint32_t(k)) {  // always true: counts match the histogram's
+          out[slot] = jw;
+          if (outv) outv[slot] = e;
+        }
+      }
+      const uint32_t cslot = warp_alloc_local(&S.ctr_cand, b == bstar);
+      if (b == bstar) {
+        const uint32_t c = cr.base_cand + cslot;
+        if (c < uint32_t(CAP)) {  // always true: m <= CAP on this path
+          dsmem_st_u32(rv + 4u * c, __float_as_uint(e));
+          dsmem_st_u32(rj + 4u * c, uint32_t(jw));
+        }
+      }
+    };
+    if (rounds == 1 && listed) {
+      const uint32_t n = S.list_n;
+      for (uint32_t b0 = 0; b0 < n; b0 += T) {
+        const uint32_t i = b0 + tid;
+        const bool in = i < n;
+        place(in ? S.list_v[i] : 0.f, in ? S.list_j[i] : 0, in);
+      }
+    } else {  // the list overflowed or scores below the floor count: read the share again
       if (warp == 0) {
         const float t = bstar > 0 ? floor_value(bstar, gmin, sc) : -INFINITY;
         if (lane == 0) S.vthr = t;
       }
       __syncthreads();
-      thr = S.vthr;
-    }
-    const uint32_t rv = dsmem_map(smem_u32(&S.cand_v[0]), 0);
-    const uint32_t rj = dsmem_map(smem_u32(&S.cand_j[0]), 0);
-    auto collect_bits = [&](uint32_t bits, int32_t c0) {
-      while (bits) {
-        const int j = __ffs(bits) - 1;
-        bits &= bits - 1;
-        const float e = bit_score(j);
-        const int b = value_bin(e, gmin, sc);
-        const int32_t jw = 4 * (c0 + (j >> 2) * T + tid) + (j & 3) - lead;
-        if (b > bstar) {
-          const uint32_t slot = cr.base_above + atomicAdd(&S.ctr_win, 1u);
-          if (slot < uint32_t(k)) {  // always true: counts match the histogram's
-            out[slot] = jw;
-            if (outv) outv[slot] = e;
-          }
-        } else if (b == bstar) {
-          const uint32_t c = cr.base_cand + atomicAdd(&S.ctr_cand, 1u);
-          if (c < uint32_t(CAP)) {  // always true: m <= CAP on this path
-            dsmem_st_u32(rv + 4u * c, __float_as_uint(e));
-            dsmem_st_u32(rj + 4u * c, uint32_t(jw));
-          }
-        }
-      }
-    };
-    if (resident) {
-      if (nchunks == 1) collect_bits(rounds > 1 ? build_bits(nloc, thr, false) : mbits, vb);
-    } else {
-      for (int ch = 0; ch < nchunks; ++ch) {
-        const bool armed = issue_chunk(ch);
-        wait_chunk(ch, armed);
-        collect_bits(build_bits(chunk_count(ch), thr, false), chunk_begin(ch));
-        __syncthreads();
-      }
+      const float tb = S.vthr;  // scores >= tb are exactly those in bins >= b*
+      stream_pass(false, [&](uint32_t slot, int32_t c0) {
+        each_lane(slot, c0, [&](float e, int32_t g, bool valid, int l) {
+          const bool hit = valid && e >= tb;
+          if (__any_sync(FULL_MASK, hit)) place(e, 4 * g + l - lead, hit);
+        });
+      });
       report_timeout();
     }
     cluster_sync();  // every candidate has landed in rank 0's buffer
@@ -742,42 +798,23 @@ __global__ void __launch_bounds__(T, 2) gvr_topk_kernel(const Params p) {
   }
 
   // ---------------------------------------------------------------- rescue: cluster radix select
-  // Every staged score of the window takes part; positions outside the window are masked here
-  // by position (their staged NaN would otherwise have a key).
-  auto key_pass = [&](auto&& visit) {
-    for (int ch = 0; ch < nchunks; ++ch) {
-      if (!resident) {
-        const bool armed = issue_chunk(ch);
-        wait_chunk(ch, armed);
-      }
-      const int32_t c0 = chunk_begin(ch), cnt = chunk_count(ch);
-#pragma unroll 1
-      for (int i = 0; i < MAX_VPT; ++i) {
-        const int32_t f = i * T + tid;
-        const bool in = f < cnt;
-        const float4 v = in ? sdata[f] : f4_zero();
-        const int32_t g = c0 + f;  // vector index from the aligned window base
-#pragma unroll
-        for (int l = 0; l < 4; ++l) {
-          const bool valid = in && (g != 0 || l >= lead) && (g != ffull || l < tailn);
-          visit(f4_get(v, l), valid, 4 * g + l - lead);
-        }
-      }
-      if (!resident) __syncthreads();
-    }
-  };
+  // Every score of the window takes part; positions outside the window are masked by position.
   uint32_t prefix = 0, pmask = 0, need = uint32_t(k);
   bool ge = false;
+  bool primed = rounds == 0;  // the first pass of a row that skipped the histogram is primed
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
     const int buf = pass & 1;
     for (int i = tid; i < 256; i += T) S.dhist[buf][i] = 0;
     __syncthreads();
-    key_pass([&](float e, bool valid, int32_t) {
-      const uint32_t key = order_key(e);
-      const bool pr = valid && (key & pmask) == prefix;
-      hist_add(S.dhist[buf], pr, (key >> shift) & 255u);
+    stream_pass(primed, [&](uint32_t slot, int32_t c0) {
+      each_lane(slot, c0, [&](float e, int32_t, bool valid, int) {
+        const uint32_t key = order_key(e);
+        const bool pr = valid && (key & pmask) == prefix;
+        hist_add(S.dhist[buf], pr, (key >> shift) & 255u);
+      });
     });
+    primed = false;
     cluster_sync();
     report_timeout();
     digit_cross<T>(S, buf, 0, cs, need);
@@ -794,20 +831,23 @@ __global__ void __launch_bounds__(T, 2) gvr_topk_kernel(const Params p) {
   const uint32_t tie_base = uint32_t(k) - nties;
   const uint32_t rwin = dsmem_map(smem_u32(&S.rc_win), 0);
   const uint32_t rtie = dsmem_map(smem_u32(&S.rc_tie), 0);
-  key_pass([&](float e, bool valid, int32_t jw) {
-    const uint32_t key = order_key(e);
-    const bool win = valid && (ge ? (key & pmask) >= prefix : key > prefix);
-    const bool tie = valid && !ge && key == prefix;
-    const uint32_t ws = warp_alloc_remote(rwin, win);
-    if (win && ws < tie_base) {
-      out[ws] = jw;
-      if (outv) outv[ws] = e;
-    }
-    const uint32_t ts = warp_alloc_remote(rtie, tie);
-    if (tie && ts < nties) {
-      out[tie_base + ts] = jw;
-      if (outv) outv[tie_base + ts] = e;
-    }
+  stream_pass(false, [&](uint32_t slot, int32_t c0) {
+    each_lane(slot, c0, [&](float e, int32_t g, bool valid, int l) {
+      const uint32_t key = order_key(e);
+      const bool win = valid && (ge ? (key & pmask) >= prefix : key > prefix);
+      const bool tie = valid && !ge && key == prefix;
+      const int32_t jw = 4 * g + l - lead;
+      const uint32_t ws = warp_alloc_remote(rwin, win);
+      if (win && ws < tie_base) {
+        out[ws] = jw;
+        if (outv) outv[ws] = e;
+      }
+      const uint32_t ts = warp_alloc_remote(rtie, tie);
+      if (tie && ts < nties) {
+        out[tie_base + ts] = jw;
+        if (outv) outv[tie_base + ts] = e;
+      }
+    });
   });
   report_timeout();
   cluster_sync();  // rank 0's counters stay alive until every CTA is done with them

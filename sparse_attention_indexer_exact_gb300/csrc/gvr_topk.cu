@@ -15,10 +15,10 @@
 
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = gvr::THREADS;
 constexpr int kMaxDevices = 64;
-constexpr int kMaxVpt = gvr::MAX_VPT;
 constexpr int kMaxCluster = 8;
+constexpr int64_t kShareVec = 4096;  // target float4 per CTA when a row spans several CTAs
 
 struct DeviceState {
   std::once_flag once;
@@ -28,8 +28,8 @@ struct DeviceState {
 DeviceState g_devices[kMaxDevices];
 
 cudaError_t set_attributes() {
-  return cudaFuncSetAttribute(gvr::gvr_topk_kernel<kThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              gvr::smem_bytes(kThreads * gvr::MAX_VPT));
+  return cudaFuncSetAttribute(gvr::gvr_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              gvr::SMEM_BYTES);
 }
 
 // One-time per-device set-up: kernel attributes and the SM count.
@@ -63,62 +63,47 @@ gvr_status check_common(int64_t row_stride, int64_t num_rows, int32_t k, const g
   if (o) {
     if (o->reserved != 0) return GVR_ERR_ARG;
     if (o->cluster_size != 0 && !is_pow2_upto8(o->cluster_size)) return GVR_ERR_ARG;
-    if (o->vectors_per_thread != 0 && !is_pow2_upto8(o->vectors_per_thread)) return GVR_ERR_ARG;
+    if (o->reserved0 != 0) return GVR_ERR_ARG;
     if (o->flags & ~(GVR_FLAG_FORCE_RESCUE | GVR_FLAG_NO_FLOOR | GVR_FLAG_ZERO_CAP | GVR_FLAG_RADIX_REFINE))
       return GVR_ERR_ARG;
   }
   return GVR_OK;
 }
 
-// Launch geometry.  A row's window never exceeds row_stride, so to stage a whole row in shared
-// memory the cluster needs cluster_size * threads * vpt >= row_stride / 4 float4 slots (beyond
-// 8 CTAs of 8 slots per thread the kernel stages its share in several chunks).  Few rows spread
-// each row over more CTAs (more SMs pulling one row); many rows keep the CTAs per row low.
-void plan_geometry(int64_t row_stride, int64_t num_rows, int sms, const gvr_options* o, int* cs_out,
-                   int* vpt_out) {
+// Launch geometry.  Each CTA streams its share of a row through a fixed shared-memory ring,
+// so any share length works; the cluster size only balances work.  A row is split so that a
+// CTA's share is about kShareVec float4 (8 CTAs cover a 131072-score row); few rows spread each
+// row over more CTAs (more SMs pulling one row), down to one ring stage per CTA.
+void plan_geometry(int64_t row_stride, int64_t num_rows, int sms, const gvr_options* o, int* cs_out) {
   const int64_t need_vec = row_stride / 4;
-  const int64_t per_cta_max = int64_t(kThreads) * kMaxVpt;
   int cs;
   if (o && o->cluster_size) {
     cs = o->cluster_size;
   } else {
-    int cs_min = pow2_ceil((need_vec + per_cta_max - 1) / per_cta_max);
+    int cs_min = pow2_ceil((need_vec + kShareVec - 1) / kShareVec);
     if (cs_min > kMaxCluster) cs_min = kMaxCluster;
-    int cs_max = pow2_ceil((need_vec + kThreads - 1) / kThreads);
+    int cs_max = pow2_ceil((need_vec + gvr::STAGE_VEC - 1) / gvr::STAGE_VEC);
     if (cs_max > kMaxCluster) cs_max = kMaxCluster;
     if (cs_max < cs_min) cs_max = cs_min;
-    const int64_t slots = 2 * int64_t(sms > 0 ? sms : 148);  // two 512-thread CTAs per SM
+    const int64_t slots = 4 * int64_t(sms > 0 ? sms : 148);  // four 256-thread CTAs per SM
     cs = cs_min;
     while (cs < cs_max && num_rows * cs * 2 <= slots) cs *= 2;
   }
-  int vpt;
-  if (o && o->vectors_per_thread) {
-    vpt = o->vectors_per_thread;
-  } else {
-    vpt = kMaxVpt;
-    for (int v = 1; v <= kMaxVpt; v *= 2) {
-      if (int64_t(cs) * kThreads * v >= need_vec) {
-        vpt = v;
-        break;
-      }
-    }
-  }
   *cs_out = cs;
-  *vpt_out = vpt;
 }
 
 gvr_status launch(const gvr::Params& prm, int64_t num_rows, const gvr_options* o, void* stream) {
   int sms = 0;
   if (device_state(&sms) != cudaSuccess) return GVR_ERR_LAUNCH;
-  int cs = 1, vpt = 1;
-  plan_geometry(prm.row_stride, num_rows, sms, o, &cs, &vpt);
+  int cs = 1;
+  plan_geometry(prm.row_stride, num_rows, sms, o, &cs);
   const int64_t blocks = num_rows * cs;
   if (blocks > 0x7fffffffLL) return GVR_ERR_ARG;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(blocks), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = size_t(gvr::smem_bytes(kThreads * vpt));
+  cfg.dynamicSmemBytes = size_t(gvr::SMEM_BYTES);
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -128,9 +113,7 @@ gvr_status launch(const gvr::Params& prm, int64_t num_rows, const gvr_options* o
   cfg.attrs = attr;
   cfg.numAttrs = 1;
 
-  gvr::Params q = prm;
-  q.slice_vec = kThreads * vpt;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<kThreads>, q);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel, prm);
   return e == cudaSuccess ? GVR_OK : GVR_ERR_LAUNCH;
 }
 
@@ -219,8 +202,8 @@ const char* gvr_status_string(gvr_status status) {
 }
 
 gvr_status gvr_plan(int64_t row_stride, int64_t num_rows, int32_t k, const gvr_options* options,
-                    int32_t sm_count, int32_t* cluster_size, int32_t* vectors_per_thread,
-                    int32_t* threads, int32_t* smem_bytes) {
+                    int32_t sm_count, int32_t* cluster_size, int32_t* stage_bytes, int32_t* threads,
+                    int32_t* smem_bytes) {
   gvr_status s = check_common(row_stride, num_rows, k, options);
   if (s != GVR_OK) return s;
   int sms = sm_count;
@@ -230,12 +213,12 @@ gvr_status gvr_plan(int64_t row_stride, int64_t num_rows, int32_t k, const gvr_o
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return GVR_ERR_LAUNCH;
   }
-  int cs = 1, vpt = 1;
-  plan_geometry(row_stride, num_rows, sms, options, &cs, &vpt);
+  int cs = 1;
+  plan_geometry(row_stride, num_rows, sms, options, &cs);
   if (cluster_size) *cluster_size = cs;
-  if (vectors_per_thread) *vectors_per_thread = vpt;
+  if (stage_bytes) *stage_bytes = int32_t(gvr::STAGE_VEC * 16);
   if (threads) *threads = kThreads;
-  if (smem_bytes) *smem_bytes = int32_t(gvr::smem_bytes(kThreads * vpt));
+  if (smem_bytes) *smem_bytes = int32_t(gvr::SMEM_BYTES);
   return GVR_OK;
 }
 

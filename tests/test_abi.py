@@ -98,7 +98,7 @@ def test_prefill_argument_errors(lib):
 
 def test_option_errors(lib):
     import sparse_attention_indexer_exact_gb300 as gvr
-    for bad in (dict(cluster_size=3), dict(cluster_size=16), dict(vectors_per_thread=5), dict(reserved=1),
+    for bad in (dict(cluster_size=3), dict(cluster_size=16), dict(reserved0=5), dict(reserved=1),
                 dict(flags=64)):
         o = gvr.Options(**bad)
         st = lib.topk_decode_ex(ALIGNED, 1024, 4, ALIGNED, 1, 1, K, ALIGNED, None, None, ctypes.byref(o))
@@ -108,23 +108,26 @@ def test_option_errors(lib):
 @pytest.mark.parametrize("stride", [4, 64, 1024, 8192, 14848, 65536, 131072, 131076, 262144, 1 << 20])
 @pytest.mark.parametrize("rows", [1, 4, 64, 128, 4096])
 @pytest.mark.parametrize("k", [512, 2048])
-def test_plan_covers_the_row_envelope(lib, stride, rows, k):
+def test_plan_geometry(lib, stride, rows, k):
     import sparse_attention_indexer_exact_gb300 as gvr
     p = gvr.plan(stride, rows, k, sm_count=152)
-    assert p["cluster_size"] in (1, 2, 4, 8) and p["vectors_per_thread"] in (1, 2, 4, 8)
-    cap = p["cluster_size"] * p["threads"] * p["vectors_per_thread"] * 4
-    if stride <= 8 * 512 * 8 * 4:
-        assert cap >= stride, p  # whole rows stay in registers
-    else:
-        assert p["cluster_size"] == 8 and p["vectors_per_thread"] == 8  # streamed in chunks
-    assert p["smem_bytes"] <= 227 * 1024
+    cs = p["cluster_size"]
+    assert cs in (1, 2, 4, 8)
+    share_vec = -(-(stride // 4) // cs)
+    if stride // 4 >= 8 * 4096:
+        assert cs == 8  # long rows always spread over a full cluster
+    if rows * 8 * 2 <= 4 * 152 and stride // 4 >= 8 * 512:
+        assert cs == 8  # few rows: spread each row wide
+    assert share_vec <= max(4096, -(-(stride // 4) // 8))  # balanced shares
+    assert p["threads"] == 256 and p["stage_bytes"] == 8192
+    assert p["smem_bytes"] <= 227 * 1024 // 4  # four CTAs fit on an SM
 
 
 def test_plan_respects_overrides(lib):
     import sparse_attention_indexer_exact_gb300 as gvr
-    o = gvr.Options(cluster_size=2, vectors_per_thread=4)
+    o = gvr.Options(cluster_size=2)
     p = gvr.plan(131072, 1, 1024, o, sm_count=152)
-    assert p["cluster_size"] == 2 and p["vectors_per_thread"] == 4
+    assert p["cluster_size"] == 2
 
 
 def test_product_path_has_no_oracle_dependency():

@@ -134,14 +134,37 @@ def test_sweep_cells_prefill(gvr, bs, n, k):
 
 # ----------------------------------------------------------------------------- geometry and paths
 @pytest.mark.parametrize("cs", [1, 2, 4, 8])
-@pytest.mark.parametrize("vpt", [1, 2, 4, 8])
-def test_every_geometry(gvr, cs, vpt):
-    """Every cluster size x registers per thread, including shares streamed in several chunks."""
+def test_every_cluster_size(gvr, cs):
+    """Every cluster size: shares from a fraction of one ring stage to many stages."""
     case = workloads.decode_batch(seed=77, requests=6, next_n=2, cr=1, k=1024, stride=40960, kv_lo=900,
                                   kv_hi=40960, boundary=False)
-    assert_decode_exact(gvr, case, options=gvr.Options(cluster_size=cs, vectors_per_thread=vpt))
+    assert_decode_exact(gvr, case, options=gvr.Options(cluster_size=cs))
     pc = workloads.prefill_tile(seed=78, rows=24, k=512, lengths=(700, 2100, 5000, 9000))
-    assert_prefill_exact(gvr, pc, options=gvr.Options(cluster_size=cs, vectors_per_thread=vpt))
+    assert_prefill_exact(gvr, pc, options=gvr.Options(cluster_size=cs))
+
+
+@pytest.mark.parametrize("cs", [1, 2, 4])
+def test_stage_holding_only_the_partial_vector(gvr, cs):
+    """Windows whose last ring stage holds nothing but the partial last vector (every lead)."""
+    g = np.random.default_rng(31)
+    k, stride = 512, 16384
+    rows = []
+    for lead in range(4):
+        for nfull in (512, 1024, 1536, 2048, 3584):  # whole vectors per CTA share multiple of a stage
+            for tailn in (1, 2, 3):
+                span = 4 * nfull * cs + tailn
+                if span > stride:
+                    continue
+                ks = lead
+                ke = span  # window [lead, span): span - lead scores
+                row = workloads.PREFILL_POISON[np.arange(stride) % 4].copy()
+                row[ks:ke] = g.standard_normal(ke - ks).astype(np.float32)
+                rows.append((row, ks, ke))
+    lg = np.stack([r[0] for r in rows])
+    case = workloads.PrefillCase("tail_stage", lg, np.array([r[1] for r in rows], np.int32),
+                                 np.array([r[2] for r in rows], np.int32), k)
+    assert_prefill_exact(gvr, case, options=gvr.Options(cluster_size=cs))
+    assert_prefill_exact(gvr, case, options=gvr.Options(cluster_size=cs, flags=1))
 
 
 @pytest.mark.parametrize("flags,expect", [(1, {4}), (4, {3}), (2, {1}), (8, {1}), (2 | 8, {1})])
