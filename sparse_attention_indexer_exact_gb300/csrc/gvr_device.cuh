@@ -181,3 +181,22 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 }  // namespace gvr
+
+namespace gvr {
+
+// Fire-and-forget add into another CTA's shared memory (DSMEM address).
+__device__ __forceinline__ void dsmem_red_add(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Split cluster barrier: arrive (publishing earlier shared-memory writes) ...
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+// ... and wait for every CTA of the cluster to have arrived.
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+}  // namespace gvr

@@ -48,15 +48,15 @@
 
 namespace gvr {
 
-constexpr int THREADS = 256;          // threads per CTA
-constexpr int NB = 2048;              // value-histogram bins over [GMIN, GMAX]
-constexpr int NCOARSE = 256;          // bins of the sample histogram that sets the floor
-constexpr int COARSE_SHIFT = 3;       // NB / NCOARSE == 8
+constexpr int THREADS = 128;          // threads per CTA
+constexpr int NB = 1024;              // value-histogram bins over [GMIN, GMAX]
+constexpr int COARSE_SHIFT = 3;       // the floor's sample histogram has NB >> 3 bins
+constexpr int NCOARSE = NB >> COARSE_SHIFT;
 constexpr int VPS = 2;                // float4 per thread per stage
-constexpr int STAGE_VEC = THREADS * VPS;  // 512 float4 = 8 KB per stage
+constexpr int STAGE_VEC = THREADS * VPS;  // 256 float4 = 4 KB per stage
 constexpr int NSTAGE = 3;             // stages in the ring
-constexpr int LIST_CAP = 1024;        // above-floor scores kept per CTA for the collect step
-constexpr int CAP = 1024;             // candidate slots in cluster rank 0
+constexpr int LIST_CAP = 768;         // above-floor scores kept per CTA for the collect step
+constexpr int CAP = 512;              // candidate slots in cluster rank 0
 constexpr int RANK_REFINE_MAX = 256;  // m at or below: refine by pairwise ranking
 constexpr int SPARSE_MAX = 4;         // above-floor scores of a thread per stage before a warp aggregates
 constexpr int MAX_K = 2048;
@@ -93,39 +93,47 @@ struct Crossing {
   int32_t bin;          // b*
   uint32_t above;       // cluster-wide count in bins above b*
   uint32_t m;           // cluster-wide count in b*
-  uint32_t base_above;  // count in bins above b* held by lower-ranked CTAs
-  uint32_t base_cand;   // count in b* held by lower-ranked CTAs
-  uint32_t total;       // cluster-wide count over the bins examined
+  uint32_t my_above;    // this CTA's count in bins above b*
+  uint32_t my_cand;     // this CTA's count in b*
+  uint32_t total;       // cluster-wide count over all bins
 };
 
 struct alignas(16) Smem {
-  uint32_t hist[NB];                  // first: groups of 4 bins are read as 16-byte vectors
-  float4 ring[NSTAGE][STAGE_VEC];     // bulk-copy destinations (16-byte aligned)
-  float list_v[LIST_CAP];
+  uint32_t hist[NB];               // this CTA's counts (groups of 4 bins read as 16-byte vectors)
+  uint32_t tot[NB];                // cluster-wide counts, pushed here by every CTA of the cluster;
+                                   // the rescue's two 256-bin digit histograms reuse it
+  float4 ring[NSTAGE][STAGE_VEC];  // bulk-copy destinations (16-byte aligned)
+  float list_v[LIST_CAP];          // the floor's sample histogram reuses it before the first pass
   int32_t list_j[LIST_CAP];
   float cand_v[CAP];
   int32_t cand_j[CAP];
-  uint32_t dhist[2][256];
-  uint32_t shist[NCOARSE];
-  uint32_t wsum[2][32];
-  float wmin[32];
-  float wmax[32];
-  float4 tail;                        // the partial last vector of the window, NaN-padded
+  uint32_t wsum[2][8];
+  float wmin[8];
+  float wmax[8];
+  float4 tail;                     // the partial last vector of the window, NaN-padded
   Crossing cross;
   float vthr;
   int32_t fpart;
   uint32_t dsel, dabove, dcnt;
-  uint32_t list_n;                    // scores appended to the list (may exceed LIST_CAP)
-  uint32_t ctr_win, ctr_cand;         // this CTA's slot counters (refine path)
-  uint32_t ctr_rwin, ctr_rtie;        // rank 0's counters for its own radix refine
-  uint32_t rc_win, rc_tie;            // rank 0's counters shared by the cluster in rescue
-  uint32_t tout;                      // this CTA gave up waiting for staged data
-  uint32_t err;                       // rank 0: some CTA of the cluster gave up
-  uint64_t bar[NSTAGE];               // one mbarrier per ring stage
+  uint32_t list_n;                 // scores appended to the list (may exceed LIST_CAP)
+  uint32_t ctr_win, ctr_cand;      // this CTA's slot counters (refine path)
+  uint32_t gctr_above, gctr_cand;  // rank 0: hands out each CTA's winner / candidate slot bases
+  uint32_t base_above, base_cand;  // this CTA's slot bases
+  uint32_t ctr_rwin, ctr_rtie;     // rank 0's counters for its own radix refine
+  uint32_t rc_win, rc_tie;         // rank 0's counters shared by the cluster in rescue
+  uint32_t saved;                  // count of the partial floor bin before the second pass
+  uint32_t tout;                   // this CTA gave up waiting for staged data
+  uint32_t err;                    // rank 0: some CTA of the cluster gave up
+  uint64_t bar[NSTAGE];            // one mbarrier per ring stage
 };
-static_assert(offsetof(Smem, hist) % 16 == 0, "histogram groups are read as 16-byte vectors");
+static_assert(offsetof(Smem, hist) % 16 == 0 && offsetof(Smem, tot) % 16 == 0,
+              "histograms are read as 16-byte vectors");
 static_assert(offsetof(Smem, ring) % 16 == 0, "bulk-copy destinations must be 16-byte aligned");
 static_assert(offsetof(Smem, bar) % 8 == 0, "mbarriers must be 8-byte aligned");
+static_assert(2 * 256 <= NB && NCOARSE <= LIST_CAP, "aliased arrays must fit");
+
+__device__ __forceinline__ uint32_t* digit_hist(Smem& S, int buf) { return S.tot + 256 * buf; }
+__device__ __forceinline__ uint32_t* sample_hist(Smem& S) { return reinterpret_cast<uint32_t*>(S.list_v); }
 
 constexpr int SMEM_BYTES = int((sizeof(Smem) + 127) / 128 * 128);
 
@@ -192,97 +200,76 @@ __device__ __forceinline__ uint32_t warp_alloc_remote(uint32_t ctr_addr, bool wa
   return base + __popc(mask & lanemask_lt());
 }
 
-// Sum the value histograms of cluster ranks [0, cs) over bins >= fbin and find the crossing
-// bin: the highest b with sum_{bins >= b} count >= k.  Thread t owns the NB/T bins
-// NB-1-(NB/T)t down to NB-(NB/T)(t+1), so thread order is descending bin order.
+// Find the crossing bin in the cluster-wide totals S.tot: the highest b with
+// sum_{bins >= b} tot >= k, with this CTA's own counts above and at b (from S.hist).  Thread t
+// owns the NB/T bins NB-1-(NB/T)t down to NB-(NB/T)(t+1), so thread order is descending order.
 template <int T>
-__device__ __forceinline__ Crossing reduce_crossing(Smem& S, uint32_t cs, uint32_t rank, uint32_t k,
-                                                    int fbin) {
+__device__ __forceinline__ Crossing scan_crossing(Smem& S, uint32_t k) {
   constexpr int BPT = NB / T;
   constexpr int NW = T / 32;
-  static_assert(BPT == 4 || BPT == 8, "threads per CTA must be 256 or 512");
+  static_assert(BPT % 4 == 0 && NW <= 8, "bins per thread must be a multiple of 4");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int lo_bin = NB - BPT * (tid + 1);
-  uint32_t tot[BPT], pre[BPT];
+  uint32_t tot[BPT], loc[BPT];
 #pragma unroll
-  for (int j = 0; j < BPT; ++j) tot[j] = pre[j] = 0;
-  if (lo_bin + BPT - 1 >= fbin) {
-    const uint32_t local = smem_u32(&S.hist[lo_bin]);
-    constexpr int G = 4;  // remote ranks whose loads are in flight together
-    for (uint32_t c0 = 0; c0 < cs; c0 += G) {
-      uint4 v[G][BPT / 4];
+  for (int q = 0; q < BPT / 4; ++q) {
+    const uint4 t4 = *reinterpret_cast<const uint4*>(&S.tot[lo_bin + 4 * q]);
+    const uint4 l4 = *reinterpret_cast<const uint4*>(&S.hist[lo_bin + 4 * q]);
+    const uint32_t tw[4] = {t4.x, t4.y, t4.z, t4.w};
+    const uint32_t lw[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        if (c0 + g < cs) {
-          const uint32_t addr = dsmem_map(local, c0 + g);
-#pragma unroll
-          for (int q = 0; q < BPT / 4; ++q) v[g][q] = dsmem_ld_v4(addr + 16u * q);
-        }
-      }
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        if (c0 + g < cs) {
-#pragma unroll
-          for (int q = 0; q < BPT / 4; ++q) {
-            const uint32_t w[4] = {v[g][q].x, v[g][q].y, v[g][q].z, v[g][q].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j = BPT - 1 - (4 * q + e);  // descending position of bin lo_bin + 4q + e
-              tot[j] += w[e];
-              if (c0 + g < rank) pre[j] += w[e];
-            }
-          }
-        }
-      }
+    for (int e = 0; e < 4; ++e) {
+      tot[BPT - 1 - (4 * q + e)] = tw[e];  // descending position of bin lo_bin + 4q + e
+      loc[BPT - 1 - (4 * q + e)] = lw[e];
     }
   }
-  uint32_t st = 0, sp = 0;
+  uint32_t st = 0, sl = 0;
 #pragma unroll
   for (int j = 0; j < BPT; ++j) {
     st += tot[j];
-    sp += pre[j];
+    sl += loc[j];
   }
-  uint32_t it = st, ip = sp;
+  uint32_t it = st, il = sl;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const uint32_t a = __shfl_up_sync(FULL_MASK, it, o);
-    const uint32_t b = __shfl_up_sync(FULL_MASK, ip, o);
+    const uint32_t b = __shfl_up_sync(FULL_MASK, il, o);
     if (lane >= o) {
       it += a;
-      ip += b;
+      il += b;
     }
   }
   if (lane == 31) {
     S.wsum[0][warp] = it;
-    S.wsum[1][warp] = ip;
+    S.wsum[1][warp] = il;
   }
   __syncthreads();
-  uint32_t wt = 0, wp = 0, total = 0;
+  uint32_t wt = 0, wl = 0, total = 0;
 #pragma unroll
   for (int w = 0; w < NW; ++w) {
     const uint32_t x = S.wsum[0][w];
     if (w < warp) {
       wt += x;
-      wp += S.wsum[1][w];
+      wl += S.wsum[1][w];
     }
     total += x;
   }
-  const uint32_t et = wt + it - st;  // count in bins above this thread's bins
-  const uint32_t ep = wp + ip - sp;
+  const uint32_t et = wt + it - st;  // cluster-wide count in bins above this thread's bins
+  const uint32_t el = wl + il - sl;  // this CTA's count there
   if (et < k && et + st >= k) {
-    uint32_t cum = et, cp = ep;
+    uint32_t cum = et, cl = el;
 #pragma unroll
     for (int j = 0; j < BPT; ++j) {
       if (cum + tot[j] >= k) {
         S.cross.bin = lo_bin + BPT - 1 - j;
         S.cross.above = cum;
         S.cross.m = tot[j];
-        S.cross.base_above = cp;
-        S.cross.base_cand = pre[j];
+        S.cross.my_above = cl;
+        S.cross.my_cand = loc[j];
         break;
       }
       cum += tot[j];
-      cp += pre[j];
+      cl += loc[j];
     }
   }
   __syncthreads();
@@ -291,39 +278,56 @@ __device__ __forceinline__ Crossing reduce_crossing(Smem& S, uint32_t cs, uint32
   return r;
 }
 
-// Sum the 256-bin digit histograms dhist[buf] of cluster ranks [c0, c0 + cn) and find the
+// Sum the 256-bin digit histograms digit_hist(buf) of cluster ranks [c0, c0 + cn) and find the
 // digit d (scanning from 255 down) where the running count reaches `need`; publishes d, the
-// count above d and the count at d in S.dsel / S.dabove / S.dcnt.
+// count above d and the count at d in S.dsel / S.dabove / S.dcnt.  Thread t owns digits
+// 255 - DPT t down to 256 - DPT (t + 1).
 template <int T>
 __device__ __forceinline__ void digit_cross(Smem& S, int buf, uint32_t c0, uint32_t cn, uint32_t need) {
-  static_assert(T >= 256, "one thread per digit");
+  constexpr int DPT = 256 / T;
+  constexpr int NW = T / 32;
+  static_assert(DPT * T == 256 && NW <= 8, "threads must divide 256");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t tot = 0;
-  const int d = 255 - tid;
-  if (tid < 256) {
-    const uint32_t local = smem_u32(&S.dhist[buf][d]);
-    for (uint32_t c = c0; c < c0 + cn; ++c) tot += dsmem_ld_u32(dsmem_map(local, c));
+  uint32_t cnt[DPT];
+  uint32_t st = 0;
+#pragma unroll
+  for (int j = 0; j < DPT; ++j) {
+    const int d = 255 - DPT * tid - j;
+    const uint32_t local = smem_u32(&digit_hist(S, buf)[d]);
+    uint32_t t = 0;
+    for (uint32_t c = c0; c < c0 + cn; ++c) t += dsmem_ld_u32(dsmem_map(local, c));
+    cnt[j] = t;
+    st += t;
   }
-  uint32_t incl = tot;
+  uint32_t incl = st;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const uint32_t a = __shfl_up_sync(FULL_MASK, incl, o);
     if (lane >= o) incl += a;
   }
-  if (lane == 31 && warp < 8) S.wsum[0][warp] = incl;
+  if (lane == 31) S.wsum[0][warp] = incl;
   __syncthreads();
   uint32_t before = 0;
-  for (int w = 0; w < warp && w < 8; ++w) before += S.wsum[0][w];
-  const uint32_t excl = before + incl - tot;
-  if (tid < 256 && excl < need && excl + tot >= need) {
-    S.dsel = uint32_t(d);
-    S.dabove = excl;
-    S.dcnt = tot;
+#pragma unroll
+  for (int w = 0; w < NW; ++w)
+    if (w < warp) before += S.wsum[0][w];
+  uint32_t excl = before + incl - st;
+  if (excl < need && excl + st >= need) {
+#pragma unroll
+    for (int j = 0; j < DPT; ++j) {
+      if (excl + cnt[j] >= need) {
+        S.dsel = uint32_t(255 - DPT * tid - j);
+        S.dabove = excl;
+        S.dcnt = cnt[j];
+        break;
+      }
+      excl += cnt[j];
+    }
   }
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(THREADS, 4) gvr_topk_kernel(const Params p) {
+__global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   constexpr int T = THREADS;
   constexpr int NW = T / 32;
   constexpr int KPT = (MAX_K + T - 1) / T;  // samples per thread at most
@@ -392,25 +396,12 @@ __global__ void __launch_bounds__(THREADS, 4) gvr_topk_kernel(const Params p) {
     return (int32_t(rank) + s * int32_t(cs)) * STAGE_VEC;
   };
 
-  for (int i = tid; i < NB; i += T) S.hist[i] = 0;
-  for (int i = tid; i < NCOARSE; i += T) S.shist[i] = 0;
+  // The ring's barriers are initialized before anything else so that its first stages can be
+  // in flight while the row is sampled.
   if (tid == 0) {
-    S.list_n = 0;
-    S.ctr_win = S.ctr_cand = S.ctr_rwin = S.ctr_rtie = 0;
-    S.rc_win = S.rc_tie = 0;
-    S.tout = S.err = 0;
-    S.cross = Crossing{};
-    S.dsel = S.dabove = S.dcnt = 0;
 #pragma unroll
     for (int s = 0; s < NSTAGE; ++s) mbar_init(&S.bar[s], 1);
     mbar_init_fence();
-  }
-  if (tid == 32) {  // the partial last vector is read with scalar loads, never past the window
-    S.tail = make_float4(qnan, qnan, qnan, qnan);
-    if (tailn && (ffull / STAGE_VEC) % int32_t(cs) == int32_t(rank)) {
-      const float* q = base + 4 * size_t(ffull);
-      S.tail = make_float4(q[0], tailn > 1 ? q[1] : qnan, tailn > 2 ? q[2] : qnan, qnan);
-    }
   }
 
   // ---------------------------------------------------------------- streaming ring
@@ -499,30 +490,50 @@ __global__ void __launch_bounds__(THREADS, 4) gvr_topk_kernel(const Params p) {
     if (tid == 0 && S.tout) dsmem_st_u32(dsmem_map(smem_u32(&S.err), 0), 1u);
   };
 
+  if (tid == 0)
+    for (int32_t s = 0; s < NSTAGE && s < nstages; ++s) issue_stage(s);  // overlaps the sampling
+
   // ---------------------------------------------------------------- guess: block64 sample
   const uint32_t nblk = uint32_t(k) >> 6;
+  // Start of run b = floor(b (nv - 64) / (nblk - 1)), one run per lane (nblk <= 32), with no
+  // 64-bit arithmetic: b (nv - 64) = b sq (nblk - 1) + b sr.
   const uint32_t sq = (nv - 64u) / (nblk - 1u), sr = (nv - 64u) % (nblk - 1u);
+  const uint32_t run_start = uint32_t(lane) * sq + (uint32_t(lane) * sr) / (nblk - 1u);
   float sv[KPT];
+#pragma unroll
+  for (int q = 0; q < KPT; ++q) {  // the 64 samples of a run are 64 consecutive threads' slots
+    const uint32_t i = uint32_t(q * T + tid);
+    const uint32_t blk = i >> 6;
+    const uint32_t s = __shfl_sync(FULL_MASK, run_start, blk & 31u);
+    sv[q] = i < uint32_t(k) ? __ldg(rowp + a + s + (i & 63u)) : qnan;
+  }
+  // Zero the counters while the samples are in flight (global loads are not waited for here).
+  for (int i = tid; i < NB; i += T) S.hist[i] = S.tot[i] = 0;
+  for (int i = tid; i < NCOARSE; i += T) sample_hist(S)[i] = 0;
+  if (tid == 0) {
+    S.list_n = 0;
+    S.ctr_win = S.ctr_cand = S.ctr_rwin = S.ctr_rtie = 0;
+    S.gctr_above = S.gctr_cand = 0;
+    S.rc_win = S.rc_tie = 0;
+    S.tout = S.err = 0;
+    S.cross = Crossing{};
+    S.dsel = S.dabove = S.dcnt = 0;
+  }
+  if (tid == 32) {  // the partial last vector is read with scalar loads, never past the window
+    S.tail = make_float4(qnan, qnan, qnan, qnan);
+    if (tailn && (ffull / STAGE_VEC) % int32_t(cs) == int32_t(rank)) {
+      const float* q = base + 4 * size_t(ffull);
+      S.tail = make_float4(q[0], tailn > 1 ? q[1] : qnan, tailn > 2 ? q[2] : qnan, qnan);
+    }
+  }
   float lmin = INFINITY, lmax = -INFINITY;
 #pragma unroll
   for (int q = 0; q < KPT; ++q) {
-    const uint32_t i = uint32_t(q * T + tid);
-    sv[q] = qnan;
-    if (i < uint32_t(k)) {
-      const uint32_t blk = i >> 6;
-      // start of run blk = floor(blk * (nv - 64) / (nblk - 1)) without 64-bit arithmetic
-      const uint32_t s = blk * sq + (blk * sr) / (nblk - 1u);
-      const float v = __ldg(rowp + a + s + (i & 63u));
-      sv[q] = v;
-      if (isfinite(v)) {
-        lmin = fminf(lmin, v);
-        lmax = fmaxf(lmax, v);
-      }
+    if (isfinite(sv[q])) {
+      lmin = fminf(lmin, sv[q]);
+      lmax = fmaxf(lmax, sv[q]);
     }
   }
-  // The sample loads go out first; the ring's bulk copies queue behind them.
-  if (tid == 0)
-    for (int32_t s = 0; s < NSTAGE && s < nstages; ++s) issue_stage(s);  // overlaps the sampling
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     lmin = fminf(lmin, __shfl_xor_sync(FULL_MASK, lmin, o));
@@ -533,6 +544,20 @@ __global__ void __launch_bounds__(THREADS, 4) gvr_topk_kernel(const Params p) {
     S.wmax[warp] = lmax;
   }
   __syncthreads();
+  // Every CTA's totals and rank 0's counters are now zero; no CTA of the cluster adds to them
+  // before it has waited on this (split) barrier, right before its first remote update.
+  cluster_arrive();
+  bool init_waited = false;
+  auto wait_init = [&]() {
+    if (!init_waited) {
+      cluster_wait();
+      init_waited = true;
+    }
+  };
+  auto csync = [&]() {
+    wait_init();
+    cluster_sync();
+  };
   float gmin = INFINITY, gmax = -INFINITY;
 #pragma unroll
   for (int w = 0; w < NW; ++w) {
@@ -558,14 +583,15 @@ __global__ void __launch_bounds__(THREADS, 4) gvr_topk_kernel(const Params p) {
       const uint32_t want = want_f < float(k) ? uint32_t(want_f) : uint32_t(k);
 #pragma unroll
       for (int q = 0; q < KPT; ++q)
-        if (!isnan(sv[q])) atomicAdd(&S.shist[value_bin(sv[q], gmin, sc) >> COARSE_SHIFT], 1u);
+        if (!isnan(sv[q])) atomicAdd(&sample_hist(S)[value_bin(sv[q], gmin, sc) >> COARSE_SHIFT], 1u);
       __syncthreads();
       if (warp == 0) {
-        uint32_t c[8];
+        constexpr int CPL = NCOARSE / 32;  // coarse bins per lane, descending
+        uint32_t c[CPL];
         uint32_t s = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          c[i] = S.shist[NCOARSE - 1 - 8 * lane - i];
+        for (int i = 0; i < CPL; ++i) {
+          c[i] = sample_hist(S)[NCOARSE - 1 - CPL * lane - i];
           s += c[i];
         }
         uint32_t incl = s;
@@ -582,10 +608,10 @@ __global__ void __launch_bounds__(THREADS, 4) gvr_topk_kernel(const Params p) {
           if (lane == src) {
             uint32_t cum = excl;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < CPL; ++i) {
               cum += c[i];
               if (cum >= want) {
-                fc = NCOARSE - 1 - 8 * lane - i;
+                fc = NCOARSE - 1 - CPL * lane - i;
                 break;
               }
             }
@@ -623,17 +649,28 @@ __global__ void __launch_bounds__(THREADS, 4) gvr_topk_kernel(const Params p) {
                            (uint32_t(v.w >= thr) << 3);
         bits |= (b & lanes) << (4 * i);
       }
-      if (!__any_sync(FULL_MASK, __popc(bits) > SPARSE_MAX)) {
-        while (bits) {  // the usual case: a few scores per thread, plain atomics
+      const uint32_t nhit = __popc(bits);
+      if (!__any_sync(FULL_MASK, nhit > SPARSE_MAX)) {
+        // the usual case: a few scores per thread; list slots from one atomic per warp
+        uint32_t incl = nhit;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t t = __shfl_up_sync(FULL_MASK, incl, o);
+          if (lane >= o) incl += t;
+        }
+        uint32_t wbase = 0;
+        if (lane == 31 && incl) wbase = atomicAdd(&S.list_n, incl);
+        uint32_t at = __shfl_sync(FULL_MASK, wbase, 31) + incl - nhit;
+        while (bits) {
           const int j = __ffs(bits) - 1;
           bits &= bits - 1;
           const float e = stage_score(slot, c0, j);
           atomicAdd(&S.hist[value_bin(e, gmin, sc)], 1u);
-          const uint32_t at = atomicAdd(&S.list_n, 1u);
           if (at < uint32_t(LIST_CAP)) {
             S.list_v[at] = e;
             S.list_j[at] = 4 * (c0 + (j >> 2) * T + tid) + (j & 3) - lead;
           }
+          ++at;
         }
       } else {  // tie-heavy warp: aggregate per distinct bin and per warp
 #pragma unroll
@@ -651,20 +688,42 @@ __global__ void __launch_bounds__(THREADS, 4) gvr_topk_kernel(const Params p) {
     });
     listed = S.list_n <= uint32_t(LIST_CAP);
     rounds = 1;
-    cluster_sync();
+    // Push this CTA's counts of bins [b0, b1] into every CTA's totals (fire-and-forget).
+    auto push = [&](int b0, int b1) {
+      wait_init();
+      for (int b = b0 + tid; b <= b1; b += T) {
+        const uint32_t v = S.hist[b];
+        if (v) {
+          const uint32_t local = smem_u32(&S.tot[b]);
+          for (uint32_t c = 0; c < cs; ++c) dsmem_red_add(dsmem_map(local, c), v);
+        }
+      }
+    };
+    push(fpart > 0 ? fpart : 0, NB - 1);
+    csync();
     report_timeout();
-    cr = reduce_crossing<T>(S, cs, rank, uint32_t(k), fpart > 0 ? fpart : 0);
+    cr = scan_crossing<T>(S, uint32_t(k));
     if (fpart >= 0 && (cr.total < uint32_t(k) || cr.bin <= fpart)) {
+      // The crossing is in the partial floor bin or below: count the scores below the floor,
+      // push only these new counts, then scan the complete totals.
       rounds = 2;
+      if (tid == 0) {
+        S.saved = S.hist[fpart];
+        S.hist[fpart] = 0;
+      }
+      csync();  // every CTA has finished reading its totals before new counts arrive
       stream_pass(false, [&](uint32_t slot, int32_t c0) {
         each_lane(slot, c0, [&](float e, int32_t, bool valid, int) {
           const bool hit = valid && e < thr;
           if (__any_sync(FULL_MASK, hit)) hist_add(S.hist, hit, uint32_t(value_bin(e, gmin, sc)));
         });
       });
-      cluster_sync();
+      push(0, fpart);
+      csync();
       report_timeout();
-      cr = reduce_crossing<T>(S, cs, rank, uint32_t(k), 0);
+      if (tid == 0) S.hist[fpart] += S.saved;
+      __syncthreads();
+      cr = scan_crossing<T>(S, uint32_t(k));
     }
     const uint32_t cap = (p.flags & FLAG_ZERO_CAP) ? 0u : uint32_t(CAP);
     if (cr.total < uint32_t(k) || cr.m > cap) path = PATH_RESCUE_OVERFLOW;  // < k: NaN in window
@@ -672,6 +731,10 @@ __global__ void __launch_bounds__(THREADS, 4) gvr_topk_kernel(const Params p) {
 
   if (path == PATH_REFINE) {
     // ------------------------------------------------------------ collect
+    // Rank 0 hands each CTA a contiguous block of winner slots and of candidate slots.
+    if (tid == 0) S.base_above = dsmem_atom_add(dsmem_map(smem_u32(&S.gctr_above), 0), cr.my_above);
+    if (tid == 32) S.base_cand = dsmem_atom_add(dsmem_map(smem_u32(&S.gctr_cand), 0), cr.my_cand);
+    __syncthreads();
     const int bstar = cr.bin;
     const uint32_t rv = dsmem_map(smem_u32(&S.cand_v[0]), 0);
     const uint32_t rj = dsmem_map(smem_u32(&S.cand_j[0]), 0);
@@ -679,7 +742,7 @@ __global__ void __launch_bounds__(THREADS, 4) gvr_topk_kernel(const Params p) {
       const int b = valid ? value_bin(e, gmin, sc) : -1;
       const uint32_t ws = warp_alloc_local(&S.ctr_win, b > bstar);
       if (b > bstar) {
-        const uint32_t slot = cr.base_above + ws;
+        const uint32_t slot = S.base_above + ws;
         if (slot < uint32_t(k)) {  // always true: counts match the histogram's
           out[slot] = jw;
           if (outv) outv[slot] = e;
@@ -687,7 +750,7 @@ __global__ void __launch_bounds__(THREADS, 4) gvr_topk_kernel(const Params p) {
       }
       const uint32_t cslot = warp_alloc_local(&S.ctr_cand, b == bstar);
       if (b == bstar) {
-        const uint32_t c = cr.base_cand + cslot;
+        const uint32_t c = S.base_cand + cslot;
         if (c < uint32_t(CAP)) {  // always true: m <= CAP on this path
           dsmem_st_u32(rv + 4u * c, __float_as_uint(e));
           dsmem_st_u32(rj + 4u * c, uint32_t(jw));
@@ -716,7 +779,7 @@ __global__ void __launch_bounds__(THREADS, 4) gvr_topk_kernel(const Params p) {
       });
       report_timeout();
     }
-    cluster_sync();  // every candidate has landed in rank 0's buffer
+    csync();  // every candidate has landed in rank 0's buffer
     if (rank != 0) return;
 
     // ------------------------------------------------------------ refine (rank 0)
@@ -743,14 +806,14 @@ __global__ void __launch_bounds__(THREADS, 4) gvr_topk_kernel(const Params p) {
       bool ge = false;
       for (int pass = 0; pass < 4; ++pass) {
         const int shift = 24 - 8 * pass;
-        for (int i = tid; i < 256; i += T) S.dhist[0][i] = 0;
+        for (int i = tid; i < 256; i += T) digit_hist(S, 0)[i] = 0;
         __syncthreads();
         for (uint32_t b0 = 0; b0 < mm; b0 += T) {
           const uint32_t i = b0 + tid;
           const bool in = i < mm;
           const uint32_t key = in ? order_key(S.cand_v[i]) : 0u;
           const bool pr = in && (key & pmask) == prefix;
-          hist_add(S.dhist[0], pr, (key >> shift) & 255u);
+          hist_add(digit_hist(S, 0), pr, (key >> shift) & 255u);
         }
         __syncthreads();
         digit_cross<T>(S, 0, rank, 1, rneed);
@@ -805,17 +868,17 @@ __global__ void __launch_bounds__(THREADS, 4) gvr_topk_kernel(const Params p) {
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
     const int buf = pass & 1;
-    for (int i = tid; i < 256; i += T) S.dhist[buf][i] = 0;
+    for (int i = tid; i < 256; i += T) digit_hist(S, buf)[i] = 0;
     __syncthreads();
     stream_pass(primed, [&](uint32_t slot, int32_t c0) {
       each_lane(slot, c0, [&](float e, int32_t, bool valid, int) {
         const uint32_t key = order_key(e);
         const bool pr = valid && (key & pmask) == prefix;
-        hist_add(S.dhist[buf], pr, (key >> shift) & 255u);
+        hist_add(digit_hist(S, buf), pr, (key >> shift) & 255u);
       });
     });
     primed = false;
-    cluster_sync();
+    csync();
     report_timeout();
     digit_cross<T>(S, buf, 0, cs, need);
     const uint32_t d = S.dsel, ab = S.dabove, cnt = S.dcnt;
@@ -850,7 +913,7 @@ __global__ void __launch_bounds__(THREADS, 4) gvr_topk_kernel(const Params p) {
     });
   });
   report_timeout();
-  cluster_sync();  // rank 0's counters stay alive until every CTA is done with them
+  csync();  // rank 0's counters stay alive until every CTA is done with them
   if (rank == 0) {
     const bool failed = S.err || S.tout;
     if (failed)

@@ -85,7 +85,7 @@ void plan_geometry(int64_t row_stride, int64_t num_rows, int sms, const gvr_opti
     int cs_max = pow2_ceil((need_vec + gvr::STAGE_VEC - 1) / gvr::STAGE_VEC);
     if (cs_max > kMaxCluster) cs_max = kMaxCluster;
     if (cs_max < cs_min) cs_max = cs_min;
-    const int64_t slots = 4 * int64_t(sms > 0 ? sms : 148);  // four 256-thread CTAs per SM
+    const int64_t slots = 7 * int64_t(sms > 0 ? sms : 148);  // seven 128-thread CTAs per SM
     cs = cs_min;
     while (cs < cs_max && num_rows * cs * 2 <= slots) cs *= 2;
   }

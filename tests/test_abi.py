@@ -116,11 +116,11 @@ def test_plan_geometry(lib, stride, rows, k):
     share_vec = -(-(stride // 4) // cs)
     if stride // 4 >= 8 * 4096:
         assert cs == 8  # long rows always spread over a full cluster
-    if rows * 8 * 2 <= 4 * 152 and stride // 4 >= 8 * 512:
+    if rows * 8 * 2 <= 7 * 152 and stride // 4 >= 8 * 256:
         assert cs == 8  # few rows: spread each row wide
     assert share_vec <= max(4096, -(-(stride // 4) // 8))  # balanced shares
-    assert p["threads"] == 256 and p["stage_bytes"] == 8192
-    assert p["smem_bytes"] <= 227 * 1024 // 4  # four CTAs fit on an SM
+    assert p["threads"] == 128 and p["stage_bytes"] == 4096
+    assert 7 * (p["smem_bytes"] + 1024) <= 228 * 1024  # seven CTAs fit on an SM
 
 
 def test_plan_respects_overrides(lib):
