@@ -101,7 +101,8 @@ enum {
 
 typedef struct gvr_options {
   int32_t cluster_size;       /* CTAs per row: 0 = automatic, else 1, 2, 4 or 8 */
-  int32_t reserved0;          /* must be 0 */
+  int32_t ring_stages;        /* shared-memory ring stages of 4 KB per CTA: 0 = automatic,
+                                 else 3..16 */
   int32_t flags;              /* GVR_FLAG_* bits; results stay exact under every flag */
   int32_t reserved;           /* must be 0 */
   int32_t* row_stats;         /* optional device int32 [num_rows][4]: path (GVR_PATH_*),
@@ -136,13 +137,14 @@ const char* gvr_status_string(gvr_status status);
 
 /*
  * The launch geometry the library would choose for a call on the current device (host
- * only, no device work): CTAs per row (cluster size), bytes per shared-memory ring stage,
- * threads per CTA and dynamic shared memory bytes per CTA.  Returns the GVR_ERR_* code the
- * entry points would return for these arguments.  sm_count > 0 overrides the device's SM
- * count (for planning without a device); any output pointer may be NULL.
+ * only, no device work): CTAs per row (cluster size), 4 KB stages of each CTA's shared-memory
+ * ring, threads per CTA and dynamic shared memory bytes per CTA.  Returns the GVR_ERR_* code
+ * the entry points would return for these arguments.  sm_count > 0 plans for a GB300-class
+ * device with that many SMs (228 KB shared memory per SM) without touching a device; any
+ * output pointer may be NULL.
  */
 gvr_status gvr_plan(int64_t row_stride, int64_t num_rows, int32_t k, const gvr_options* options,
-                    int32_t sm_count, int32_t* cluster_size, int32_t* stage_bytes, int32_t* threads,
+                    int32_t sm_count, int32_t* cluster_size, int32_t* ring_stages, int32_t* threads,
                     int32_t* smem_bytes);
 
 #ifdef __cplusplus

@@ -50,7 +50,7 @@ class GvrError(RuntimeError):
 
 class Options(ctypes.Structure):
     """Mirror of ``gvr_options`` (tuning and diagnostics of the *_ex entry points)."""
-    _fields_ = [("cluster_size", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+    _fields_ = [("cluster_size", ctypes.c_int32), ("ring_stages", ctypes.c_int32),
                 ("flags", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("row_stats", ctypes.c_void_p)]
 
@@ -128,8 +128,8 @@ def plan(row_stride: int, num_rows: int, k: int, options: Options | None = None,
     st = lib.gvr_plan(row_stride, num_rows, k, ctypes.byref(options) if options is not None else None, sm_count,
                       *[ctypes.byref(o) for o in outs])
     _check(st)
-    cs, stage, threads, smem = (o.value for o in outs)
-    return {"cluster_size": cs, "stage_bytes": stage, "threads": threads, "smem_bytes": smem}
+    cs, stages, threads, smem = (o.value for o in outs)
+    return {"cluster_size": cs, "ring_stages": stages, "threads": threads, "smem_bytes": smem}
 
 
 # ----------------------------------------------------------------------------- torch tensors

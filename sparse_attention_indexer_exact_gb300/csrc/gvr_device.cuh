@@ -200,3 +200,15 @@ __device__ __forceinline__ void cluster_wait() {
 }
 
 }  // namespace gvr
+
+namespace gvr {
+
+__device__ __forceinline__ void dsmem_red_min(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.min.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void dsmem_red_max(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.max.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+}  // namespace gvr

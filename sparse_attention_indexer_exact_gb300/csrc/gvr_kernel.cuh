@@ -50,11 +50,10 @@ namespace gvr {
 
 constexpr int THREADS = 128;          // threads per CTA
 constexpr int NB = 1024;              // value-histogram bins over [GMIN, GMAX]
-constexpr int COARSE_SHIFT = 3;       // the floor's sample histogram has NB >> 3 bins
-constexpr int NCOARSE = NB >> COARSE_SHIFT;
 constexpr int VPS = 2;                // float4 per thread per stage
 constexpr int STAGE_VEC = THREADS * VPS;  // 256 float4 = 4 KB per stage
-constexpr int NSTAGE = 3;             // stages in the ring
+constexpr int MIN_STAGES = 3;         // ring depth bounds (the host picks the depth per launch)
+constexpr int MAX_STAGES = 16;
 constexpr int LIST_CAP = 768;         // above-floor scores kept per CTA for the collect step
 constexpr int CAP = 512;              // candidate slots in cluster rank 0
 constexpr int RANK_REFINE_MAX = 256;  // m at or below: refine by pairwise ranking
@@ -87,6 +86,7 @@ struct Params {
   int32_t k;
   int32_t mode;
   int32_t flags;
+  int32_t nstage;             // ring depth, MIN_STAGES..MAX_STAGES
 };
 
 struct Crossing {
@@ -102,8 +102,7 @@ struct alignas(16) Smem {
   uint32_t hist[NB];               // this CTA's counts (groups of 4 bins read as 16-byte vectors)
   uint32_t tot[NB];                // cluster-wide counts, pushed here by every CTA of the cluster;
                                    // the rescue's two 256-bin digit histograms reuse it
-  float4 ring[NSTAGE][STAGE_VEC];  // bulk-copy destinations (16-byte aligned)
-  float list_v[LIST_CAP];          // the floor's sample histogram reuses it before the first pass
+  float list_v[LIST_CAP];
   int32_t list_j[LIST_CAP];
   float cand_v[CAP];
   int32_t cand_j[CAP];
@@ -114,7 +113,8 @@ struct alignas(16) Smem {
   Crossing cross;
   float vthr;
   int32_t fpart;
-  uint32_t dsel, dabove, dcnt;
+  uint32_t dsel, dabove, dcnt, dmy_above, dmy_at;
+  uint32_t kmin_loc, kmax_loc;     // rescue: smallest / largest key of this CTA's matching scores
   uint32_t list_n;                 // scores appended to the list (may exceed LIST_CAP)
   uint32_t ctr_win, ctr_cand;      // this CTA's slot counters (refine path)
   uint32_t gctr_above, gctr_cand;  // rank 0: hands out each CTA's winner / candidate slot bases
@@ -124,18 +124,19 @@ struct alignas(16) Smem {
   uint32_t saved;                  // count of the partial floor bin before the second pass
   uint32_t tout;                   // this CTA gave up waiting for staged data
   uint32_t err;                    // rank 0: some CTA of the cluster gave up
-  uint64_t bar[NSTAGE];            // one mbarrier per ring stage
+  uint64_t bar[MAX_STAGES];        // one mbarrier per ring stage
 };
 static_assert(offsetof(Smem, hist) % 16 == 0 && offsetof(Smem, tot) % 16 == 0,
               "histograms are read as 16-byte vectors");
-static_assert(offsetof(Smem, ring) % 16 == 0, "bulk-copy destinations must be 16-byte aligned");
 static_assert(offsetof(Smem, bar) % 8 == 0, "mbarriers must be 8-byte aligned");
-static_assert(2 * 256 <= NB && NCOARSE <= LIST_CAP, "aliased arrays must fit");
+static_assert(2 * 256 + 4 <= NB, "the rescue's digit totals and key bounds live in tot");
 
 __device__ __forceinline__ uint32_t* digit_hist(Smem& S, int buf) { return S.tot + 256 * buf; }
-__device__ __forceinline__ uint32_t* sample_hist(Smem& S) { return reinterpret_cast<uint32_t*>(S.list_v); }
 
-constexpr int SMEM_BYTES = int((sizeof(Smem) + 127) / 128 * 128);
+// Dynamic shared memory: the fixed part, then the ring of nstage stages (bulk-copy
+// destinations, 128-byte aligned).
+constexpr int SMEM_FIXED = int((sizeof(Smem) + 127) / 128 * 128);
+__host__ __device__ constexpr int smem_bytes(int nstage) { return SMEM_FIXED + nstage * STAGE_VEC * 16; }
 
 // Monotone bin of a score in [GMIN, GMAX] with NB bins; NaN maps to bin 0.
 __device__ __forceinline__ int value_bin(float v, float gmin, float sc) {
@@ -282,6 +283,126 @@ __device__ __forceinline__ Crossing scan_crossing(Smem& S, uint32_t k) {
 // digit d (scanning from 255 down) where the running count reaches `need`; publishes d, the
 // count above d and the count at d in S.dsel / S.dabove / S.dcnt.  Thread t owns digits
 // 255 - DPT t down to 256 - DPT (t + 1).
+// The highest bin b of arr[0..NB) with sum_{bins >= b} arr >= want, or -1 when the total is
+// below want.  Block-collective; thread t owns bins NB-1-(NB/T)t down to NB-(NB/T)(t+1).
+template <int T>
+__device__ __forceinline__ int suffix_cross(Smem& S, const uint32_t* arr, uint32_t want) {
+  constexpr int BPT = NB / T;
+  constexpr int NW = T / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int lo_bin = NB - BPT * (tid + 1);
+  uint32_t c[BPT];
+  uint32_t st = 0;
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) {
+    c[j] = arr[lo_bin + BPT - 1 - j];
+    st += c[j];
+  }
+  uint32_t it = st;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t a = __shfl_up_sync(FULL_MASK, it, o);
+    if (lane >= o) it += a;
+  }
+  if (lane == 31) S.wsum[0][warp] = it;
+  if (tid == 0) S.dsel = 0xffffffffu;
+  __syncthreads();
+  uint32_t before = 0;
+#pragma unroll
+  for (int w = 0; w < NW; ++w)
+    if (w < warp) before += S.wsum[0][w];
+  const uint32_t ex = before + it - st;
+  if (ex < want && ex + st >= want) {
+    uint32_t cum = ex;
+#pragma unroll
+    for (int j = 0; j < BPT; ++j) {
+      cum += c[j];
+      if (cum >= want) {
+        S.dsel = uint32_t(lo_bin + BPT - 1 - j);
+        break;
+      }
+    }
+  }
+  __syncthreads();
+  const int r = int(S.dsel);
+  __syncthreads();
+  return r;
+}
+
+struct DigitCross {
+  uint32_t digit;     // d*
+  uint32_t above;     // cluster-wide count of digits above d* (among the matching keys)
+  uint32_t cnt;       // cluster-wide count at d*
+  uint32_t my_above;  // this CTA's count above d*
+  uint32_t my_at;     // this CTA's count at d*
+  uint32_t my_all;    // this CTA's count over every digit (its matching keys)
+};
+
+// Digit crossing over pushed cluster-wide digit counts dtot (local) and this CTA's own counts
+// dloc: the digit d (scanning from 255 down) where the running cluster count reaches `need`.
+// Thread t owns digits 255 - DPT t down to 256 - DPT (t + 1).
+template <int T>
+__device__ __forceinline__ DigitCross digit_scan(Smem& S, const uint32_t* dtot, const uint32_t* dloc,
+                                                 uint32_t need) {
+  constexpr int DPT = 256 / T;
+  constexpr int NW = T / 32;
+  static_assert(DPT * T == 256 && NW <= 8, "threads must divide 256");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t tot[DPT], loc[DPT];
+  uint32_t st = 0, sl = 0;
+#pragma unroll
+  for (int j = 0; j < DPT; ++j) {
+    const int d = 255 - DPT * tid - j;
+    tot[j] = dtot[d];
+    loc[j] = dloc[d];
+    st += tot[j];
+    sl += loc[j];
+  }
+  uint32_t it = st, il = sl;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t a = __shfl_up_sync(FULL_MASK, it, o);
+    const uint32_t b = __shfl_up_sync(FULL_MASK, il, o);
+    if (lane >= o) {
+      it += a;
+      il += b;
+    }
+  }
+  if (lane == 31) {
+    S.wsum[0][warp] = it;
+    S.wsum[1][warp] = il;
+  }
+  __syncthreads();
+  uint32_t wt = 0, wl = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    if (w < warp) {
+      wt += S.wsum[0][w];
+      wl += S.wsum[1][w];
+    }
+    all += S.wsum[1][w];
+  }
+  const uint32_t et = wt + it - st, el = wl + il - sl;
+  if (et < need && et + st >= need) {
+    uint32_t cum = et, cl = el;
+#pragma unroll
+    for (int j = 0; j < DPT; ++j) {
+      if (cum + tot[j] >= need) {
+        S.dsel = uint32_t(255 - DPT * tid - j);
+        S.dabove = cum;
+        S.dcnt = tot[j];
+        S.dmy_above = cl;
+        S.dmy_at = loc[j];
+        break;
+      }
+      cum += tot[j];
+      cl += loc[j];
+    }
+  }
+  __syncthreads();
+  return DigitCross{S.dsel, S.dabove, S.dcnt, S.dmy_above, S.dmy_at, all};
+}
+
 template <int T>
 __device__ __forceinline__ void digit_cross(Smem& S, int buf, uint32_t c0, uint32_t cn, uint32_t need) {
   constexpr int DPT = 256 / T;
@@ -333,6 +454,8 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   constexpr int KPT = (MAX_K + T - 1) / T;  // samples per thread at most
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
+  float4 (*ring)[STAGE_VEC] = reinterpret_cast<float4 (*)[STAGE_VEC]>(smem_raw + SMEM_FIXED);
+  const int32_t nst = p.nstage;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t cs = cluster_size();
   const uint32_t rank = cluster_rank();
@@ -400,13 +523,14 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   // in flight while the row is sampled.
   if (tid == 0) {
 #pragma unroll
-    for (int s = 0; s < NSTAGE; ++s) mbar_init(&S.bar[s], 1);
+    for (int s = 0; s < MAX_STAGES; ++s)
+      if (s < nst) mbar_init(&S.bar[s], 1);
     mbar_init_fence();
   }
 
   // ---------------------------------------------------------------- streaming ring
   // The CTA's stages of every pass go through the ring in one sequence q = qbase + s: slot
-  // q % NSTAGE, mbarrier phase (q / NSTAGE) & 1.  Thread 0 refills a slot after all threads
+  // q % nst, mbarrier phase (q / nst) & 1.  Thread 0 refills a slot after all threads
   // have left it.
   uint32_t qbase = 0;
   bool late = false;
@@ -420,11 +544,11 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   // vector (only the partial tail), so slot phases stay in step with q.
   auto issue_stage = [&](int32_t s) {  // thread 0 only
     const int32_t nfull = stage_full(s);
-    const uint32_t slot = (qbase + uint32_t(s)) % NSTAGE;
+    const uint32_t slot = (qbase + uint32_t(s)) % uint32_t(nst);
     if (nfull > 0) {
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(&S.bar[slot], uint32_t(nfull) * 16u);
-      bulk_copy_g2s(&S.ring[slot][0], base + 4 * size_t(stage_first(s)), uint32_t(nfull) * 16u,
+      bulk_copy_g2s(&ring[slot][0], base + 4 * size_t(stage_first(s)), uint32_t(nfull) * 16u,
                     &S.bar[slot]);
     } else {
       mbar_arrive(&S.bar[slot]);
@@ -433,21 +557,27 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   // One pass over this CTA's stages: visit(slot, c0) once per stage, after the stage has landed
   // in ring slot `slot`; c0 is the row vector index of the stage's first vector.  All threads
   // call visit the same number of times, so visitors may use warp collectives.
+  // A share that fits in the ring stays resident after its first pass: later passes reuse the
+  // same slots (their barriers' phases are already complete) instead of copying it again.
+  const bool ring_resident = nstages <= nst;
+  bool loaded = false;
   auto stream_pass = [&](bool primed, auto&& visit) {
-    if (tid == 0 && !primed)
-      for (int32_t s = 0; s < NSTAGE && s < nstages; ++s) issue_stage(s);
+    if (tid == 0 && !primed && !(ring_resident && loaded))
+      for (int32_t s = 0; s < nst && s < nstages; ++s) issue_stage(s);
     for (int32_t s = 0; s < nstages; ++s) {
       const uint32_t q = qbase + uint32_t(s);
-      const uint32_t slot = q % NSTAGE;
-      if (!mbar_wait_bounded(&S.bar[slot], (q / NSTAGE) & 1u, WAIT_LIMIT_NS)) {
-        mbar_wait_bounded(&S.bar[slot], (q / NSTAGE) & 1u, WAIT_LIMIT_NS);  // let copies land
+      const uint32_t slot = q % uint32_t(nst);
+      const uint32_t ph = (q / uint32_t(nst)) & 1u;
+      if (!mbar_wait_bounded(&S.bar[slot], ph, WAIT_LIMIT_NS)) {
+        mbar_wait_bounded(&S.bar[slot], ph, WAIT_LIMIT_NS);  // let copies land
         late = true;
       }
       visit(slot, stage_first(s));
       __syncthreads();  // every thread is done with this slot
-      if (tid == 0 && s + NSTAGE < nstages) issue_stage(s + NSTAGE);
+      if (tid == 0 && s + nst < nstages) issue_stage(s + nst);
     }
-    qbase += uint32_t(nstages);
+    if (!ring_resident) qbase += uint32_t(nstages);
+    loaded = true;
     if (__syncthreads_or(late) && tid == 0) S.tout = 1;
   };
   // The i-th vector of this thread in the stage at (slot, c0): its share index g, its values
@@ -459,7 +589,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     if (g >= nvec) return 0u;
     uint32_t lanes = 0xFu;
     if (g < ffull) {
-      v = S.ring[slot][f];
+      v = ring[slot][f];
     } else {
       v = S.tail;
       lanes = (1u << tailn) - 1u;
@@ -471,7 +601,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   auto stage_score = [&](uint32_t slot, int32_t c0, int j) -> float {
     const int32_t f = (j >> 2) * T + tid;
     if (c0 + f >= ffull) return f4_get(S.tail, j & 3);
-    return reinterpret_cast<const float*>(&S.ring[slot][0])[4 * f + (j & 3)];
+    return reinterpret_cast<const float*>(&ring[slot][0])[4 * f + (j & 3)];
   };
   // Per-lane walk of one stage for the rarely taken passes: f(e, g, valid, l) for every lane of
   // every vector slot of this thread (warp-uniform call count).
@@ -491,7 +621,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   };
 
   if (tid == 0)
-    for (int32_t s = 0; s < NSTAGE && s < nstages; ++s) issue_stage(s);  // overlaps the sampling
+    for (int32_t s = 0; s < nst && s < nstages; ++s) issue_stage(s);  // overlaps the sampling
 
   // ---------------------------------------------------------------- guess: block64 sample
   const uint32_t nblk = uint32_t(k) >> 6;
@@ -509,7 +639,6 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   }
   // Zero the counters while the samples are in flight (global loads are not waited for here).
   for (int i = tid; i < NB; i += T) S.hist[i] = S.tot[i] = 0;
-  for (int i = tid; i < NCOARSE; i += T) sample_hist(S)[i] = 0;
   if (tid == 0) {
     S.list_n = 0;
     S.ctr_win = S.ctr_cand = S.ctr_rwin = S.ctr_rtie = 0;
@@ -577,54 +706,24 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   if (path == PATH_REFINE) {
     sc = __fdiv_rn(float(NB), __fsub_rn(gmax, gmin));
     if (!(p.flags & FLAG_NO_FLOOR)) {
-      // mu = k*k/nv samples are expected above tau; keep mu + 3 sqrt(mu) + 16 above the floor
+      // mu = k*k/nv samples are expected above tau; keep mu + 3 sqrt(mu) + 6 above the floor
       const float mu = float(k) * float(k) / float(nv);
-      const float want_f = mu + 3.0f * sqrtf(mu) + 16.0f;
+      const float want_f = mu + 3.0f * sqrtf(mu) + 6.0f;
       const uint32_t want = want_f < float(k) ? uint32_t(want_f) : uint32_t(k);
+      // The samples' own histogram on the same bins (in this CTA's private counts, cleared
+      // again below): the floor is the lower edge of the bin where `want` samples are reached.
 #pragma unroll
       for (int q = 0; q < KPT; ++q)
-        if (!isnan(sv[q])) atomicAdd(&sample_hist(S)[value_bin(sv[q], gmin, sc) >> COARSE_SHIFT], 1u);
+        if (!isnan(sv[q])) atomicAdd(&S.hist[value_bin(sv[q], gmin, sc)], 1u);
       __syncthreads();
-      if (warp == 0) {
-        constexpr int CPL = NCOARSE / 32;  // coarse bins per lane, descending
-        uint32_t c[CPL];
-        uint32_t s = 0;
-#pragma unroll
-        for (int i = 0; i < CPL; ++i) {
-          c[i] = sample_hist(S)[NCOARSE - 1 - CPL * lane - i];
-          s += c[i];
-        }
-        uint32_t incl = s;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t t = __shfl_up_sync(FULL_MASK, incl, o);
-          if (lane >= o) incl += t;
-        }
-        const uint32_t excl = incl - s;
-        const unsigned hm = __ballot_sync(FULL_MASK, excl < want && incl >= want);
-        int fc = 0;
-        if (hm) {
-          const int src = __ffs(hm) - 1;
-          if (lane == src) {
-            uint32_t cum = excl;
-#pragma unroll
-            for (int i = 0; i < CPL; ++i) {
-              cum += c[i];
-              if (cum >= want) {
-                fc = NCOARSE - 1 - CPL * lane - i;
-                break;
-              }
-            }
-          }
-          fc = __shfl_sync(FULL_MASK, fc, src);
-        }
-        if (lane == 0) {
-          // any threshold works: bins above bin(t) are complete, bin(t) is partial
-          const float t = fc > 0 ? __fadd_rn(gmin, __fdiv_rn(float(fc << COARSE_SHIFT), sc)) : -INFINITY;
-          S.vthr = t;
-          S.fpart = fc > 0 ? value_bin(t, gmin, sc) : -1;
-        }
+      const int fb = suffix_cross<T>(S, S.hist, want);
+      if (tid == 0) {
+        // any threshold works: bins above bin(t) are complete, bin(t) is partial
+        const float t = fb > 0 ? __fadd_rn(gmin, __fdiv_rn(float(fb), sc)) : -INFINITY;
+        S.vthr = t;
+        S.fpart = fb > 0 ? value_bin(t, gmin, sc) : -1;
       }
+      for (int i = tid; i < NB; i += T) S.hist[i] = 0;
       __syncthreads();
       thr = S.vthr;
       fpart = S.fpart;
@@ -757,6 +856,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
         }
       }
     };
+    if (!(rounds == 1 && listed)) rounds += 10;  // diagnostics: collect read the share again
     if (rounds == 1 && listed) {
       const uint32_t n = S.list_n;
       for (uint32_t b0 = 0; b0 < n; b0 += T) {
@@ -861,57 +961,125 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   }
 
   // ---------------------------------------------------------------- rescue: cluster radix select
-  // Every score of the window takes part; positions outside the window are masked by position.
+  // Exact selection over the 32-bit order-preserving keys of every score of the window, one
+  // 8-bit digit per pass from the top.  Each pass counts the digits of the keys that still
+  // match the chosen prefix, pushes the counts (and the smallest / largest matching key) into
+  // every CTA, and fixes one digit of tau's key.  It stops early when the digits above the
+  // chosen one already account for exactly k keys, or when every matching key is the same
+  // (tie-heavy rows).  Positions outside the window are masked by position.
+  uint32_t* dloc = S.hist;  // this CTA's digit counts
+  auto dtot = [&](int buf) -> uint32_t* { return S.tot + 256 * buf; };
+  auto kslot = [&](int buf, int which) -> uint32_t* { return S.tot + 512 + 2 * buf + which; };
+  for (int i = tid; i < 512; i += T) S.tot[i] = 0;
+  if (tid == 0) {
+    *kslot(0, 0) = *kslot(1, 0) = 0xffffffffu;
+    *kslot(0, 1) = *kslot(1, 1) = 0u;
+  }
+  __syncthreads();
+  csync();  // every CTA's pushed totals start from zero
   uint32_t prefix = 0, pmask = 0, need = uint32_t(k);
+  uint32_t my_win = 0, my_eq = 0;  // this CTA's scores above tau / equal to tau
   bool ge = false;
   bool primed = rounds == 0;  // the first pass of a row that skipped the histogram is primed
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
     const int buf = pass & 1;
-    for (int i = tid; i < 256; i += T) digit_hist(S, buf)[i] = 0;
+    for (int i = tid; i < 256; i += T) dloc[i] = 0;
+    if (tid == 0) {
+      S.kmin_loc = 0xffffffffu;
+      S.kmax_loc = 0u;
+    }
     __syncthreads();
+    uint32_t tmin = 0xffffffffu, tmax = 0u;
     stream_pass(primed, [&](uint32_t slot, int32_t c0) {
       each_lane(slot, c0, [&](float e, int32_t, bool valid, int) {
         const uint32_t key = order_key(e);
         const bool pr = valid && (key & pmask) == prefix;
-        hist_add(digit_hist(S, buf), pr, (key >> shift) & 255u);
+        if (pr) {
+          tmin = min(tmin, key);
+          tmax = max(tmax, key);
+        }
+        hist_add(dloc, pr, (key >> shift) & 255u);
       });
     });
     primed = false;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      tmin = min(tmin, __shfl_xor_sync(FULL_MASK, tmin, o));
+      tmax = max(tmax, __shfl_xor_sync(FULL_MASK, tmax, o));
+    }
+    if (lane == 0) {
+      atomicMin(&S.kmin_loc, tmin);
+      atomicMax(&S.kmax_loc, tmax);
+    }
+    __syncthreads();
+    for (int d = tid; d < 256; d += T) {
+      const uint32_t v = dloc[d];
+      if (v) {
+        const uint32_t local = smem_u32(&dtot(buf)[d]);
+        for (uint32_t c = 0; c < cs; ++c) dsmem_red_add(dsmem_map(local, c), v);
+      }
+    }
+    if (tid == 0)
+      for (uint32_t c = 0; c < cs; ++c) {
+        dsmem_red_min(dsmem_map(smem_u32(kslot(buf, 0)), c), S.kmin_loc);
+        dsmem_red_max(dsmem_map(smem_u32(kslot(buf, 1)), c), S.kmax_loc);
+      }
     csync();
     report_timeout();
-    digit_cross<T>(S, buf, 0, cs, need);
-    const uint32_t d = S.dsel, ab = S.dabove, cnt = S.dcnt;
-    prefix |= d << shift;
+    const DigitCross dc = digit_scan<T>(S, dtot(buf), dloc, need);
+    const uint32_t kmin_all = *kslot(buf, 0), kmax_all = *kslot(buf, 1);
+    __syncthreads();  // every thread has read this pass's totals: reset them for pass + 2
+    for (int i = tid; i < 256; i += T) dtot(buf)[i] = 0;
+    if (tid == 0) {
+      *kslot(buf, 0) = 0xffffffffu;
+      *kslot(buf, 1) = 0u;
+    }
+    if (kmin_all == kmax_all) {  // every matching key is the same: they are all tied at tau
+      prefix = kmin_all;
+      pmask = 0xffffffffu;
+      my_eq = dc.my_all;
+      break;
+    }
+    prefix |= dc.digit << shift;
     pmask |= 0xFFu << shift;
-    need -= ab;
-    if (cnt == need) {
+    need -= dc.above;
+    my_win += dc.my_above;
+    my_eq = dc.my_at;
+    if (dc.cnt == need) {  // the keys with this prefix are exactly the remaining winners
       ge = true;
+      my_win += dc.my_at;
+      my_eq = 0;
       break;
     }
   }
+  // Emission: rank 0 hands this CTA a block of winner slots and a block of tie slots.
   const uint32_t nties = ge ? 0u : need;
   const uint32_t tie_base = uint32_t(k) - nties;
-  const uint32_t rwin = dsmem_map(smem_u32(&S.rc_win), 0);
-  const uint32_t rtie = dsmem_map(smem_u32(&S.rc_tie), 0);
-  stream_pass(false, [&](uint32_t slot, int32_t c0) {
-    each_lane(slot, c0, [&](float e, int32_t g, bool valid, int l) {
-      const uint32_t key = order_key(e);
-      const bool win = valid && (ge ? (key & pmask) >= prefix : key > prefix);
-      const bool tie = valid && !ge && key == prefix;
-      const int32_t jw = 4 * g + l - lead;
-      const uint32_t ws = warp_alloc_remote(rwin, win);
-      if (win && ws < tie_base) {
-        out[ws] = jw;
-        if (outv) outv[ws] = e;
-      }
-      const uint32_t ts = warp_alloc_remote(rtie, tie);
-      if (tie && ts < nties) {
-        out[tie_base + ts] = jw;
-        if (outv) outv[tie_base + ts] = e;
-      }
+  if (tid == 0) S.base_above = my_win ? dsmem_atom_add(dsmem_map(smem_u32(&S.rc_win), 0), my_win) : 0u;
+  if (tid == 32) S.base_cand = my_eq ? dsmem_atom_add(dsmem_map(smem_u32(&S.rc_tie), 0), my_eq) : 0u;
+  __syncthreads();
+  const uint32_t wbase = S.base_above, tbase = S.base_cand;
+  if (my_win > 0 || (my_eq > 0 && tbase < nties)) {
+    stream_pass(false, [&](uint32_t slot, int32_t c0) {
+      each_lane(slot, c0, [&](float e, int32_t g, bool valid, int l) {
+        const uint32_t key = order_key(e);
+        const bool win = valid && (ge ? (key & pmask) >= prefix : key > prefix);
+        const bool tie = valid && !ge && key == prefix;
+        const int32_t jw = 4 * g + l - lead;
+        const uint32_t ws = warp_alloc_local(&S.ctr_win, win);
+        if (win && wbase + ws < tie_base) {
+          out[wbase + ws] = jw;
+          if (outv) outv[wbase + ws] = e;
+        }
+        const uint32_t ts = warp_alloc_local(&S.ctr_cand, tie);
+        if (tie && tbase + ts < nties) {
+          out[tie_base + tbase + ts] = jw;
+          if (outv) outv[tie_base + tbase + ts] = e;
+        }
+      });
     });
-  });
+  }
   report_timeout();
   csync();  // rank 0's counters stay alive until every CTA is done with them
   if (rank == 0) {

@@ -24,16 +24,22 @@ struct DeviceState {
   std::once_flag once;
   cudaError_t err = cudaSuccess;
   int sms = 0;
+  int smem_per_sm = 0;     // shared memory per SM (bytes)
+  int smem_reserved = 0;   // shared memory the system reserves per CTA (bytes)
 };
+
+constexpr int kDefaultSmemPerSm = 228 * 1024;
+constexpr int kDefaultSmemReserved = 1024;
+constexpr int kMaxCtasPerSm = 7;  // registers: 128 threads x up to 72 registers
 DeviceState g_devices[kMaxDevices];
 
 cudaError_t set_attributes() {
   return cudaFuncSetAttribute(gvr::gvr_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              gvr::SMEM_BYTES);
+                              gvr::smem_bytes(gvr::MAX_STAGES));
 }
 
-// One-time per-device set-up: kernel attributes and the SM count.
-cudaError_t device_state(int* sms) {
+// One-time per-device set-up: kernel attributes, SM count and shared-memory capacity.
+cudaError_t device_state(int* sms, int* smem_per_sm, int* smem_reserved) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -41,10 +47,16 @@ cudaError_t device_state(int* sms) {
   DeviceState& st = g_devices[dev];
   std::call_once(st.once, [&st, dev]() {
     cudaError_t r = cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (r == cudaSuccess)
+      r = cudaDeviceGetAttribute(&st.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (r == cudaSuccess)
+      r = cudaDeviceGetAttribute(&st.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
     if (r == cudaSuccess) r = set_attributes();
     st.err = r;
   });
   *sms = st.sms;
+  *smem_per_sm = st.smem_per_sm;
+  *smem_reserved = st.smem_reserved;
   return st.err;
 }
 
@@ -63,47 +75,80 @@ gvr_status check_common(int64_t row_stride, int64_t num_rows, int32_t k, const g
   if (o) {
     if (o->reserved != 0) return GVR_ERR_ARG;
     if (o->cluster_size != 0 && !is_pow2_upto8(o->cluster_size)) return GVR_ERR_ARG;
-    if (o->reserved0 != 0) return GVR_ERR_ARG;
+    if (o->ring_stages != 0 && (o->ring_stages < gvr::MIN_STAGES || o->ring_stages > gvr::MAX_STAGES))
+      return GVR_ERR_ARG;
     if (o->flags & ~(GVR_FLAG_FORCE_RESCUE | GVR_FLAG_NO_FLOOR | GVR_FLAG_ZERO_CAP | GVR_FLAG_RADIX_REFINE))
       return GVR_ERR_ARG;
   }
   return GVR_OK;
 }
 
-// Launch geometry.  Each CTA streams its share of a row through a fixed shared-memory ring,
-// so any share length works; the cluster size only balances work.  A row is split so that a
-// CTA's share is about kShareVec float4 (8 CTAs cover a 131072-score row); few rows spread each
-// row over more CTAs (more SMs pulling one row), down to one ring stage per CTA.
-void plan_geometry(int64_t row_stride, int64_t num_rows, int sms, const gvr_options* o, int* cs_out) {
-  const int64_t need_vec = row_stride / 4;
+// Launch geometry.  Each CTA streams its share of a row through a shared-memory ring, so any
+// share length works; the cluster size only balances work.  A row is split so that a CTA's
+// share is about kShareVec float4 (8 CTAs cover a 131072-score row); few rows spread each row
+// over more CTAs (more SMs pulling one row), down to one ring stage per CTA.
+//
+// Ring depth: every cluster of the launch should be resident at once (a second wave would
+// wait for the whole latency chain of the first), so the ring is as deep as it can be while
+// rows x cluster_size CTAs still fit on the GPU, and no deeper than the CTA's share.
+struct Geometry {
   int cs;
+  int nstage;
+};
+
+int ctas_per_sm(int nstage, int smem_per_sm, int smem_reserved) {
+  const int by_smem = smem_per_sm / (gvr::smem_bytes(nstage) + smem_reserved);
+  return by_smem < kMaxCtasPerSm ? by_smem : kMaxCtasPerSm;
+}
+
+Geometry plan_geometry(int64_t row_stride, int64_t num_rows, int sms, int smem_per_sm, int smem_reserved,
+                       const gvr_options* o) {
+  const int64_t need_vec = row_stride / 4;
+  if (sms <= 0) sms = 148;
+  if (smem_per_sm <= 0) smem_per_sm = kDefaultSmemPerSm;
+  if (smem_reserved < 0) smem_reserved = kDefaultSmemReserved;
+  Geometry g{1, gvr::MIN_STAGES};
   if (o && o->cluster_size) {
-    cs = o->cluster_size;
+    g.cs = o->cluster_size;
   } else {
     int cs_min = pow2_ceil((need_vec + kShareVec - 1) / kShareVec);
     if (cs_min > kMaxCluster) cs_min = kMaxCluster;
     int cs_max = pow2_ceil((need_vec + gvr::STAGE_VEC - 1) / gvr::STAGE_VEC);
     if (cs_max > kMaxCluster) cs_max = kMaxCluster;
     if (cs_max < cs_min) cs_max = cs_min;
-    const int64_t slots = 7 * int64_t(sms > 0 ? sms : 148);  // seven 128-thread CTAs per SM
-    cs = cs_min;
-    while (cs < cs_max && num_rows * cs * 2 <= slots) cs *= 2;
+    const int64_t slots = int64_t(sms) * ctas_per_sm(gvr::MIN_STAGES, smem_per_sm, smem_reserved);
+    g.cs = cs_min;
+    while (g.cs < cs_max && num_rows * g.cs * 2 <= slots) g.cs *= 2;
   }
-  *cs_out = cs;
+  if (o && o->ring_stages) {
+    g.nstage = o->ring_stages;
+  } else {
+    const int64_t stages_per_cta = ((need_vec + gvr::STAGE_VEC - 1) / gvr::STAGE_VEC + g.cs - 1) / g.cs;
+    const int64_t ctas = num_rows * g.cs;
+    for (int d = gvr::MAX_STAGES; d > gvr::MIN_STAGES; --d) {
+      if (d > stages_per_cta) continue;
+      // clusters pack into GPCs, so leave a tenth of the slots as margin
+      if (ctas * 10 <= int64_t(sms) * ctas_per_sm(d, smem_per_sm, smem_reserved) * 9) {
+        g.nstage = d;
+        break;
+      }
+    }
+  }
+  return g;
 }
 
 gvr_status launch(const gvr::Params& prm, int64_t num_rows, const gvr_options* o, void* stream) {
-  int sms = 0;
-  if (device_state(&sms) != cudaSuccess) return GVR_ERR_LAUNCH;
-  int cs = 1;
-  plan_geometry(prm.row_stride, num_rows, sms, o, &cs);
+  int sms = 0, smem_per_sm = 0, smem_reserved = 0;
+  if (device_state(&sms, &smem_per_sm, &smem_reserved) != cudaSuccess) return GVR_ERR_LAUNCH;
+  const Geometry geo = plan_geometry(prm.row_stride, num_rows, sms, smem_per_sm, smem_reserved, o);
+  const int cs = geo.cs;
   const int64_t blocks = num_rows * cs;
   if (blocks > 0x7fffffffLL) return GVR_ERR_ARG;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(blocks), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = size_t(gvr::SMEM_BYTES);
+  cfg.dynamicSmemBytes = size_t(gvr::smem_bytes(geo.nstage));
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -113,7 +158,9 @@ gvr_status launch(const gvr::Params& prm, int64_t num_rows, const gvr_options* o
   cfg.attrs = attr;
   cfg.numAttrs = 1;
 
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel, prm);
+  gvr::Params q = prm;
+  q.nstage = geo.nstage;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel, q);
   return e == cudaSuccess ? GVR_OK : GVR_ERR_LAUNCH;
 }
 
@@ -202,23 +249,17 @@ const char* gvr_status_string(gvr_status status) {
 }
 
 gvr_status gvr_plan(int64_t row_stride, int64_t num_rows, int32_t k, const gvr_options* options,
-                    int32_t sm_count, int32_t* cluster_size, int32_t* stage_bytes, int32_t* threads,
+                    int32_t sm_count, int32_t* cluster_size, int32_t* ring_stages, int32_t* threads,
                     int32_t* smem_bytes) {
   gvr_status s = check_common(row_stride, num_rows, k, options);
   if (s != GVR_OK) return s;
-  int sms = sm_count;
-  if (sms <= 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return GVR_ERR_LAUNCH;
-  }
-  int cs = 1;
-  plan_geometry(row_stride, num_rows, sms, options, &cs);
-  if (cluster_size) *cluster_size = cs;
-  if (stage_bytes) *stage_bytes = int32_t(gvr::STAGE_VEC * 16);
+  int sms = sm_count, smem_per_sm = kDefaultSmemPerSm, smem_reserved = kDefaultSmemReserved;
+  if (sms <= 0 && device_state(&sms, &smem_per_sm, &smem_reserved) != cudaSuccess) return GVR_ERR_LAUNCH;
+  const Geometry geo = plan_geometry(row_stride, num_rows, sms, smem_per_sm, smem_reserved, options);
+  if (cluster_size) *cluster_size = geo.cs;
+  if (ring_stages) *ring_stages = geo.nstage;
   if (threads) *threads = kThreads;
-  if (smem_bytes) *smem_bytes = int32_t(gvr::SMEM_BYTES);
+  if (smem_bytes) *smem_bytes = int32_t(gvr::smem_bytes(geo.nstage));
   return GVR_OK;
 }
 

@@ -98,7 +98,7 @@ def test_prefill_argument_errors(lib):
 
 def test_option_errors(lib):
     import sparse_attention_indexer_exact_gb300 as gvr
-    for bad in (dict(cluster_size=3), dict(cluster_size=16), dict(reserved0=5), dict(reserved=1),
+    for bad in (dict(cluster_size=3), dict(cluster_size=16), dict(ring_stages=2), dict(ring_stages=17), dict(reserved=1),
                 dict(flags=64)):
         o = gvr.Options(**bad)
         st = lib.topk_decode_ex(ALIGNED, 1024, 4, ALIGNED, 1, 1, K, ALIGNED, None, None, ctypes.byref(o))
@@ -119,15 +119,18 @@ def test_plan_geometry(lib, stride, rows, k):
     if rows * 8 * 2 <= 7 * 152 and stride // 4 >= 8 * 256:
         assert cs == 8  # few rows: spread each row wide
     assert share_vec <= max(4096, -(-(stride // 4) // 8))  # balanced shares
-    assert p["threads"] == 128 and p["stage_bytes"] == 4096
-    assert 7 * (p["smem_bytes"] + 1024) <= 228 * 1024  # seven CTAs fit on an SM
+    assert p["threads"] == 128 and 3 <= p["ring_stages"] <= 16
+    per_sm = min(7, (228 * 1024) // (p["smem_bytes"] + 1024))
+    if p["ring_stages"] > 3:  # a deeper ring only while every cluster stays resident at once
+        assert rows * cs <= 152 * per_sm
+        assert p["ring_stages"] <= -(-share_vec // 256)
 
 
 def test_plan_respects_overrides(lib):
     import sparse_attention_indexer_exact_gb300 as gvr
-    o = gvr.Options(cluster_size=2)
+    o = gvr.Options(cluster_size=2, ring_stages=5)
     p = gvr.plan(131072, 1, 1024, o, sm_count=152)
-    assert p["cluster_size"] == 2
+    assert p["cluster_size"] == 2 and p["ring_stages"] == 5
 
 
 def test_product_path_has_no_oracle_dependency():

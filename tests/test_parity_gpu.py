@@ -143,6 +143,16 @@ def test_every_cluster_size(gvr, cs):
     assert_prefill_exact(gvr, pc, options=gvr.Options(cluster_size=cs))
 
 
+@pytest.mark.parametrize("stages", [3, 4, 5, 7, 16])
+def test_every_ring_depth(gvr, stages):
+    """Ring depths wrap the per-slot barrier phases differently; results must not change."""
+    case = workloads.decode_batch(seed=79, requests=5, next_n=2, cr=2, k=512, stride=65536, kv_lo=2000,
+                                  kv_hi=131072, boundary=False)
+    for cs in (1, 8):
+        assert_decode_exact(gvr, case, options=gvr.Options(cluster_size=cs, ring_stages=stages))
+        assert_decode_exact(gvr, case, options=gvr.Options(cluster_size=cs, ring_stages=stages, flags=1))
+
+
 @pytest.mark.parametrize("cs", [1, 2, 4])
 def test_stage_holding_only_the_partial_vector(gvr, cs):
     """Windows whose last ring stage holds nothing but the partial last vector (every lead)."""
