@@ -529,10 +529,9 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   }
 
   // ---------------------------------------------------------------- streaming ring
-  // The CTA's stages of every pass go through the ring in one sequence q = qbase + s: slot
-  // q % nst, mbarrier phase (q / nst) & 1.  Thread 0 refills a slot after all threads
-  // have left it.
-  uint32_t qbase = 0;
+  // The CTA's stages of every pass go through the ring in order; the ring position (slot,
+  // mbarrier phase) advances by one per stage.  Thread 0 refills a slot after all threads have
+  // left it.
   bool late = false;
   auto stage_full = [&](int32_t s) -> int32_t {  // whole vectors of stage s (bulk-copied)
     const int32_t c0 = stage_first(s);
@@ -541,10 +540,9 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     return fe > c0 ? fe - c0 : 0;
   };
   // Every stage completes exactly one phase of its slot's barrier, even a stage with no whole
-  // vector (only the partial tail), so slot phases stay in step with q.
-  auto issue_stage = [&](int32_t s) {  // thread 0 only
+  // vector (only the partial tail), so slot phases stay in step with the ring position.
+  auto issue_stage = [&](int32_t s, uint32_t slot) {  // thread 0 only
     const int32_t nfull = stage_full(s);
-    const uint32_t slot = (qbase + uint32_t(s)) % uint32_t(nst);
     if (nfull > 0) {
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(&S.bar[slot], uint32_t(nfull) * 16u);
@@ -556,27 +554,39 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   };
   // One pass over this CTA's stages: visit(slot, c0) once per stage, after the stage has landed
   // in ring slot `slot`; c0 is the row vector index of the stage's first vector.  All threads
-  // call visit the same number of times, so visitors may use warp collectives.
+  // call visit the same number of times, so visitors may use warp collectives.  The ring
+  // position (slot, phase) of the next stage to consume carries over from pass to pass.
   // A share that fits in the ring stays resident after its first pass: later passes reuse the
   // same slots (their barriers' phases are already complete) instead of copying it again.
   const bool ring_resident = nstages <= nst;
   bool loaded = false;
+  uint32_t rslot = 0, rphase = 0;
   auto stream_pass = [&](bool primed, auto&& visit) {
-    if (tid == 0 && !primed && !(ring_resident && loaded))
-      for (int32_t s = 0; s < nst && s < nstages; ++s) issue_stage(s);
+    if (tid == 0 && !primed && !(ring_resident && loaded)) {
+      uint32_t sl = rslot;
+      for (int32_t s = 0; s < nst && s < nstages; ++s) {
+        issue_stage(s, sl);
+        if (++sl == uint32_t(nst)) sl = 0;
+      }
+    }
+    uint32_t slot = rslot, ph = rphase;
     for (int32_t s = 0; s < nstages; ++s) {
-      const uint32_t q = qbase + uint32_t(s);
-      const uint32_t slot = q % uint32_t(nst);
-      const uint32_t ph = (q / uint32_t(nst)) & 1u;
       if (!mbar_wait_bounded(&S.bar[slot], ph, WAIT_LIMIT_NS)) {
         mbar_wait_bounded(&S.bar[slot], ph, WAIT_LIMIT_NS);  // let copies land
         late = true;
       }
       visit(slot, stage_first(s));
       __syncthreads();  // every thread is done with this slot
-      if (tid == 0 && s + nst < nstages) issue_stage(s + nst);
+      if (tid == 0 && s + nst < nstages) issue_stage(s + nst, slot);
+      if (++slot == uint32_t(nst)) {
+        slot = 0;
+        ph ^= 1u;
+      }
     }
-    if (!ring_resident) qbase += uint32_t(nstages);
+    if (!ring_resident) {
+      rslot = slot;
+      rphase = ph;
+    }
     loaded = true;
     if (__syncthreads_or(late) && tid == 0) S.tout = 1;
   };
@@ -621,7 +631,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   };
 
   if (tid == 0)
-    for (int32_t s = 0; s < nst && s < nstages; ++s) issue_stage(s);  // overlaps the sampling
+    for (int32_t s = 0; s < nst && s < nstages; ++s) issue_stage(s, uint32_t(s));  // overlaps sampling
 
   // ---------------------------------------------------------------- guess: block64 sample
   const uint32_t nblk = uint32_t(k) >> 6;
@@ -637,6 +647,13 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     const uint32_t s = __shfl_sync(FULL_MASK, run_start, blk & 31u);
     sv[q] = i < uint32_t(k) ? __ldg(rowp + a + s + (i & 63u)) : qnan;
   }
+  // Every later stage of this CTA is requested into L2 now (no shared memory needed), so HBM
+  // streams the whole row at once and the ring's refills are L2 hits.
+  if (warp == 1)
+    for (int32_t s = nst + lane; s < nstages; s += 32) {
+      const int32_t nfull = stage_full(s);
+      if (nfull > 0) bulk_prefetch_l2(base + 4 * size_t(stage_first(s)), uint32_t(nfull) * 16u);
+    }
   // Zero the counters while the samples are in flight (global loads are not waited for here).
   for (int i = tid; i < NB; i += T) S.hist[i] = S.tot[i] = 0;
   if (tid == 0) {
