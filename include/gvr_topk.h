@@ -117,8 +117,12 @@ enum {
   GVR_PATH_SHORT = 0,           /* nv <= k: identity and -1 pad */
   GVR_PATH_REFINE = 1,          /* histogram, crossing bin, candidates, exact refine */
   GVR_PATH_RESCUE_BRACKET = 2,  /* invalid sampled bracket: exact rescue */
-  GVR_PATH_RESCUE_OVERFLOW = 3, /* crossing bin exceeded the candidate buffer: exact rescue */
-  GVR_PATH_RESCUE_FORCED = 4    /* GVR_FLAG_FORCE_RESCUE */
+  GVR_PATH_RESCUE_OVERFLOW = 3, /* crossing bin exceeded the candidate buffer and some CTA's
+                                   list overflowed: exact digit passes over the row, seeded
+                                   with the crossing bin */
+  GVR_PATH_RESCUE_FORCED = 4,   /* GVR_FLAG_FORCE_RESCUE */
+  GVR_PATH_REFINE_CLUSTER = 5   /* crossing bin exceeded the candidate buffer, every CTA's list
+                                   held its counted scores: exact digit passes over the lists */
 };
 
 /* topk_decode with tuning/diagnostic options (NULL = automatic, identical to topk_decode). */

@@ -34,7 +34,8 @@ _lock = threading.Lock()
 _lib = None
 
 FLAG_FORCE_RESCUE, FLAG_NO_FLOOR, FLAG_ZERO_CAP, FLAG_RADIX_REFINE = 1, 2, 4, 8
-PATH_NAMES = {0: "short", 1: "refine", 2: "rescue_bracket", 3: "rescue_overflow", 4: "rescue_forced"}
+PATH_NAMES = {-1: "device_error", 0: "short", 1: "refine", 2: "rescue_bracket", 3: "rescue_overflow",
+              4: "rescue_forced", 5: "refine_cluster"}
 SUPPORTED_K = (512, 1024, 2048)
 EXPORTED_SYMBOLS = ("topk_decode", "topk_prefill", "topk_decode_ex", "topk_prefill_ex", "gvr_status_string",
                     "gvr_plan")

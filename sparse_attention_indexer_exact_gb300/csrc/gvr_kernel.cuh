@@ -69,7 +69,8 @@ enum : int32_t {
   PATH_REFINE = 1,
   PATH_RESCUE_BRACKET = 2,
   PATH_RESCUE_OVERFLOW = 3,
-  PATH_RESCUE_FORCED = 4
+  PATH_RESCUE_FORCED = 4,
+  PATH_REFINE_CLUSTER = 5
 };
 
 struct Params {
@@ -116,6 +117,7 @@ struct alignas(16) Smem {
   uint32_t dsel, dabove, dcnt, dmy_above, dmy_at;
   uint32_t kmin_loc, kmax_loc;     // rescue: smallest / largest key of this CTA's matching scores
   uint32_t list_n;                 // scores appended to the list (may exceed LIST_CAP)
+  uint32_t unlisted;               // CTAs of the cluster whose list overflowed (each pushes 1)
   uint32_t ctr_win, ctr_cand;      // this CTA's slot counters (refine path)
   uint32_t gctr_above, gctr_cand;  // rank 0: hands out each CTA's winner / candidate slot bases
   uint32_t base_above, base_cand;  // this CTA's slot bases
@@ -132,6 +134,11 @@ static_assert(offsetof(Smem, bar) % 8 == 0, "mbarriers must be 8-byte aligned");
 static_assert(2 * 256 + 4 <= NB, "the rescue's digit totals and key bounds live in tot");
 
 __device__ __forceinline__ uint32_t* digit_hist(Smem& S, int buf) { return S.tot + 256 * buf; }
+
+template <int N>
+struct IntC {
+  static constexpr int value = N;
+};
 
 // Dynamic shared memory: the fixed part, then the ring of nstage stages (bulk-copy
 // destinations, 128-byte aligned).
@@ -662,6 +669,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     S.gctr_above = S.gctr_cand = 0;
     S.rc_win = S.rc_tie = 0;
     S.tout = S.err = 0;
+    S.unlisted = 0;
     S.cross = Crossing{};
     S.dsel = S.dabove = S.dcnt = 0;
   }
@@ -816,12 +824,16 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       }
     };
     push(fpart > 0 ? fpart : 0, NB - 1);
+    if (tid == 0 && !listed)
+      for (uint32_t c = 0; c < cs; ++c) dsmem_red_add(dsmem_map(smem_u32(&S.unlisted), c), 1u);
     csync();
     report_timeout();
     cr = scan_crossing<T>(S, uint32_t(k));
-    if (fpart >= 0 && (cr.total < uint32_t(k) || cr.bin <= fpart)) {
-      // The crossing is in the partial floor bin or below: count the scores below the floor,
-      // push only these new counts, then scan the complete totals.
+    if (fpart >= 0 && cr.total < uint32_t(k)) {
+      // Fewer than k scores reached the floor: count the scores below it, push only these new
+      // counts, then scan the complete totals.  (When at least k scores reached the floor, tau
+      // is at or above it, and a crossing in the partial floor bin needs no second pass: its
+      // candidates are the counted scores, those >= thr.)
       rounds = 2;
       if (tid == 0) {
         S.saved = S.hist[fpart];
@@ -842,8 +854,14 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       cr = scan_crossing<T>(S, uint32_t(k));
     }
     const uint32_t cap = (p.flags & FLAG_ZERO_CAP) ? 0u : uint32_t(CAP);
-    if (cr.total < uint32_t(k) || cr.m > cap) path = PATH_RESCUE_OVERFLOW;  // < k: NaN in window
+    if (cr.total < uint32_t(k))
+      path = PATH_RESCUE_OVERFLOW;  // NaN in the window (out of contract)
+    else if (cr.m > cap)  // every list complete: the cluster selects among the listed scores
+      path = (rounds == 1 && S.unlisted == 0) ? PATH_REFINE_CLUSTER : PATH_RESCUE_OVERFLOW;
   }
+  // Candidates are the scores of the crossing bin that were counted: after one pass, the scores
+  // >= thr (this only matters when the crossing is the partial floor bin).
+  const float cthr = rounds == 1 ? thr : -INFINITY;
 
   if (path == PATH_REFINE) {
     // ------------------------------------------------------------ collect
@@ -890,7 +908,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       const float tb = S.vthr;  // scores >= tb are exactly those in bins >= b*
       stream_pass(false, [&](uint32_t slot, int32_t c0) {
         each_lane(slot, c0, [&](float e, int32_t g, bool valid, int l) {
-          const bool hit = valid && e >= tb;
+          const bool hit = valid && e >= tb && e >= cthr;
           if (__any_sync(FULL_MASK, hit)) place(e, 4 * g + l - lead, hit);
         });
       });
@@ -978,12 +996,19 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   }
 
   // ---------------------------------------------------------------- rescue: cluster radix select
-  // Exact selection over the 32-bit order-preserving keys of every score of the window, one
-  // 8-bit digit per pass from the top.  Each pass counts the digits of the keys that still
-  // match the chosen prefix, pushes the counts (and the smallest / largest matching key) into
-  // every CTA, and fixes one digit of tau's key.  It stops early when the digits above the
-  // chosen one already account for exactly k keys, or when every matching key is the same
-  // (tie-heavy rows).  Positions outside the window are masked by position.
+  // Exact selection over the 32-bit order-preserving keys, one 8-bit digit per pass from the
+  // top.  Each pass counts the digits of the keys that still match the chosen prefix, pushes
+  // the counts (and the smallest / largest matching key) into every CTA, and fixes one digit
+  // of tau's key.  It stops early when the digits above the chosen one already account for
+  // exactly the keys still needed, or when every matching key is the same (tie-heavy rows).
+  // Positions outside the window are masked by position.
+  // After a valid histogram the selection is seeded with it: only the counted scores of the
+  // crossing bin take part, k - above of them are needed, and every score of a higher bin is a
+  // winner.  When every CTA's list held its counted scores, the passes read the lists instead
+  // of the row.
+  const bool seeded = path == PATH_REFINE_CLUSTER || (path == PATH_RESCUE_OVERFLOW && cr.total >= uint32_t(k));
+  const bool from_lists = path == PATH_REFINE_CLUSTER;
+  const int bstar = cr.bin;
   uint32_t* dloc = S.hist;  // this CTA's digit counts
   auto dtot = [&](int buf) -> uint32_t* { return S.tot + 256 * buf; };
   auto kslot = [&](int buf, int which) -> uint32_t* { return S.tot + 512 + 2 * buf + which; };
@@ -994,10 +1019,19 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   }
   __syncthreads();
   csync();  // every CTA's pushed totals start from zero
-  uint32_t prefix = 0, pmask = 0, need = uint32_t(k);
-  uint32_t my_win = 0, my_eq = 0;  // this CTA's scores above tau / equal to tau
+  uint32_t prefix = 0, pmask = 0;
+  uint32_t need = seeded ? uint32_t(k) - cr.above : uint32_t(k);
+  uint32_t my_win = seeded ? cr.my_above : 0u;  // this CTA's scores above tau
+  uint32_t my_eq = 0;                             // this CTA's scores equal to tau
   bool ge = false;
   bool primed = rounds == 0;  // the first pass of a row that skipped the histogram is primed
+  // Bin class of a score for the seeded selection: 1 above the crossing bin, 0 a member of it,
+  // -1 below it (or not counted).  Unseeded, every score is a member.
+  auto bin_class = [&](float e) -> int {
+    if (!seeded) return 0;
+    const int b = value_bin(e, gmin, sc);
+    return b > bstar ? 1 : (b == bstar && e >= cthr ? 0 : -1);
+  };
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
     const int buf = pass & 1;
@@ -1008,23 +1042,63 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     }
     __syncthreads();
     uint32_t tmin = 0xffffffffu, tmax = 0u;
-    stream_pass(primed, [&](uint32_t slot, int32_t c0) {
-      each_lane(slot, c0, [&](float e, int32_t, bool valid, int) {
-        const uint32_t key = order_key(e);
-        const bool pr = valid && (key & pmask) == prefix;
-        if (pr) {
-          tmin = min(tmin, key);
-          tmax = max(tmax, key);
-        }
-        hist_add(dloc, pr, (key >> shift) & 255u);
-      });
-    });
-    primed = false;
+    // Count the digits of a thread's batch of N scores (bit j of vm: score j is in the window).
+    // Warp-collective.  A warp whose matching keys all share one digit adds them with one
+    // atomic (tie-heavy and narrow rows); otherwise one atomic per distinct digit per score slot.
+    auto digit_batch = [&](auto n_c, const float* e, uint32_t vm) {
+      constexpr int N = decltype(n_c)::value;
+      uint32_t keys[N];
+      uint32_t pm = 0, dmin = 0xffffffffu, dmax = 0u;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      tmin = min(tmin, __shfl_xor_sync(FULL_MASK, tmin, o));
-      tmax = max(tmax, __shfl_xor_sync(FULL_MASK, tmax, o));
+      for (int j = 0; j < N; ++j) {
+        keys[j] = order_key(e[j]);
+        const bool ok = ((vm >> j) & 1u) && (keys[j] & pmask) == prefix && bin_class(e[j]) == 0;
+        if (ok) {
+          pm |= 1u << j;
+          tmin = min(tmin, keys[j]);
+          tmax = max(tmax, keys[j]);
+          const uint32_t d = (keys[j] >> shift) & 255u;
+          dmin = min(dmin, d);
+          dmax = max(dmax, d);
+        }
+      }
+      dmin = __reduce_min_sync(FULL_MASK, dmin);
+      dmax = __reduce_max_sync(FULL_MASK, dmax);
+      if (dmin == dmax) {
+        const uint32_t c = __reduce_add_sync(FULL_MASK, uint32_t(__popc(pm)));
+        if (lane == 0) atomicAdd(&dloc[dmin], c);
+      } else if (dmin < dmax) {
+#pragma unroll
+        for (int j = 0; j < N; ++j) hist_add(dloc, (pm >> j) & 1u, (keys[j] >> shift) & 255u);
+      }
+    };
+    if (from_lists) {
+      const uint32_t n = S.list_n;  // <= LIST_CAP on this path
+      for (uint32_t b0 = 0; b0 < n; b0 += T) {
+        const uint32_t i = b0 + tid;
+        const float e[1] = {i < n ? S.list_v[i] : 0.f};
+        digit_batch(IntC<1>{}, e, i < n ? 1u : 0u);
+      }
+    } else {
+      stream_pass(primed, [&](uint32_t slot, int32_t c0) {
+        float e[4 * VPS];
+        uint32_t vm = 0;
+#pragma unroll
+        for (int i = 0; i < VPS; ++i) {
+          int32_t g;
+          float4 v;
+          vm |= stage_vec(slot, c0, i, g, v) << (4 * i);
+          e[4 * i + 0] = v.x;
+          e[4 * i + 1] = v.y;
+          e[4 * i + 2] = v.z;
+          e[4 * i + 3] = v.w;
+        }
+        digit_batch(IntC<4 * VPS>{}, e, vm);
+      });
     }
+    primed = false;
+    tmin = __reduce_min_sync(FULL_MASK, tmin);
+    tmax = __reduce_max_sync(FULL_MASK, tmax);
     if (lane == 0) {
       atomicMin(&S.kmin_loc, tmin);
       atomicMax(&S.kmax_loc, tmax);
@@ -1077,25 +1151,40 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   if (tid == 32) S.base_cand = my_eq ? dsmem_atom_add(dsmem_map(smem_u32(&S.rc_tie), 0), my_eq) : 0u;
   __syncthreads();
   const uint32_t wbase = S.base_above, tbase = S.base_cand;
-  if (my_win > 0 || (my_eq > 0 && tbase < nties)) {
-    stream_pass(false, [&](uint32_t slot, int32_t c0) {
-      each_lane(slot, c0, [&](float e, int32_t g, bool valid, int l) {
-        const uint32_t key = order_key(e);
-        const bool win = valid && (ge ? (key & pmask) >= prefix : key > prefix);
-        const bool tie = valid && !ge && key == prefix;
-        const int32_t jw = 4 * g + l - lead;
-        const uint32_t ws = warp_alloc_local(&S.ctr_win, win);
-        if (win && wbase + ws < tie_base) {
-          out[wbase + ws] = jw;
-          if (outv) outv[wbase + ws] = e;
-        }
-        const uint32_t ts = warp_alloc_local(&S.ctr_cand, tie);
-        if (tie && tbase + ts < nties) {
-          out[tie_base + tbase + ts] = jw;
-          if (outv) outv[tie_base + tbase + ts] = e;
-        }
+  // ties this CTA writes: its share of the nties slots, in the order the slots were handed out
+  const uint32_t my_ties = tbase < nties ? (my_eq < nties - tbase ? my_eq : nties - tbase) : 0u;
+  auto emit = [&](float e, int32_t jw, bool valid) {  // warp-collective
+    const uint32_t key = order_key(e);
+    const int bc = valid ? bin_class(e) : -1;
+    const bool win = bc == 1 || (bc == 0 && (ge ? (key & pmask) >= prefix : key > prefix));
+    const bool tie = bc == 0 && !ge && key == prefix;
+    const uint32_t ws = warp_alloc_local(&S.ctr_win, win);
+    if (win && wbase + ws < tie_base) {
+      out[wbase + ws] = jw;
+      if (outv) outv[wbase + ws] = e;
+    }
+    const uint32_t ts = warp_alloc_local(&S.ctr_cand, tie);
+    if (tie && tbase + ts < nties) {
+      out[tie_base + tbase + ts] = jw;
+      if (outv) outv[tie_base + tbase + ts] = e;
+    }
+  };
+  if (my_win > 0 || my_ties > 0) {
+    if (from_lists) {
+      const uint32_t n = S.list_n;
+      for (uint32_t b0 = 0; b0 < n; b0 += T) {
+        const uint32_t i = b0 + tid;
+        const bool in = i < n;
+        emit(in ? S.list_v[i] : 0.f, in ? S.list_j[i] : 0, in);
+      }
+    } else {
+      stream_pass(false, [&](uint32_t slot, int32_t c0) {
+        // the counters are settled at a stage boundary: stop visiting once this CTA's slots
+        // are all written (its remaining stages still land and are waited for)
+        if (S.ctr_win >= my_win && S.ctr_cand >= my_ties) return;
+        each_lane(slot, c0, [&](float e, int32_t g, bool valid, int l) { emit(e, 4 * g + l - lead, valid); });
       });
-    });
+    }
   }
   report_timeout();
   csync();  // rank 0's counters stay alive until every CTA is done with them
@@ -1107,7 +1196,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       stats[0] = failed ? PATH_DEVICE_ERROR : path;
       stats[1] = int32_t(cr.m);
       stats[2] = rounds;
-      stats[3] = 0;
+      stats[3] = seeded ? int32_t(cr.above) : 0;
     }
   }
 }

@@ -177,7 +177,7 @@ def test_stage_holding_only_the_partial_vector(gvr, cs):
     assert_prefill_exact(gvr, case, options=gvr.Options(cluster_size=cs, flags=1))
 
 
-@pytest.mark.parametrize("flags,expect", [(1, {4}), (4, {3}), (2, {1}), (8, {1}), (2 | 8, {1})])
+@pytest.mark.parametrize("flags,expect", [(1, {4}), (4, {3, 5}), (2, {1}), (8, {1}), (2 | 8, {1}), (2 | 4, {3, 5})])
 def test_forced_paths(gvr, flags, expect):
     case = workloads.decode_batch(seed=5, requests=8, next_n=2, cr=4, k=1024, stride=131072,
                                   boundary=False)
@@ -324,3 +324,59 @@ def test_signed_zero_and_inf_classes(gvr):
         case = workloads.adversarial_row(variant)
         for flags in (0, 1, 4):
             assert_decode_exact(gvr, case, options=gvr.Options(flags=flags))
+
+
+@pytest.mark.parametrize("cs", [0, 2, 8])
+def test_cluster_refine_over_lists(gvr, cs):
+    """Crossing bins larger than the candidate buffer whose members every CTA still listed.
+
+    Row families: a plateau of P equal scores on top (tau is the plateau), winners above a
+    plateau that holds tau, and a narrow band of distinct values around tau.  The selection then
+    runs the cluster's digit passes over the per-CTA lists (path 5), seeded with the crossing bin.
+    """
+    g = np.random.default_rng(500 + cs)
+    k, stride = 512, 65536
+    rows = []
+    for p in (600, 1000, 1500):
+        r = g.standard_normal(stride).astype(np.float32)
+        r[g.choice(stride, p, replace=False)] = 3.5
+        rows.append(r)
+    for above, plateau in ((300, 900), (100, 1200), (511, 700)):
+        r = g.standard_normal(stride).astype(np.float32)
+        pos = g.choice(stride, above + plateau, replace=False)
+        r[pos[:above]] = 5.0 + g.random(above).astype(np.float32)
+        r[pos[above:]] = 3.25
+        rows.append(r)
+    for width in (1e-3, 1e-5):
+        r = g.standard_normal(stride).astype(np.float32)
+        r[g.choice(stride, 1400, replace=False)] = (4.0 + width * g.random(1400)).astype(np.float32)
+        rows.append(r)
+    lg = np.stack(rows)
+    case = workloads.DecodeCase("plateau_lists", lg, np.full(len(rows), stride, np.int32), 1, 1, k)
+    st = assert_decode_exact(gvr, case, options=gvr.Options(cluster_size=cs), stats=True)
+    assert (st[:, 0] == 5).any(), st
+    assert (st[st[:, 0] == 5, 1] > 512).all(), st
+
+
+def test_crossing_in_the_floor_bin(gvr):
+    """tau inside the bin that holds the sampled floor: one counting pass, candidates >= the floor.
+
+    Each row has a few hundred scores far on top, then a dense class (one histogram bin wide)
+    that holds the K-th score and enough block64 samples to put the floor in its bin, and the
+    rest far below.
+    """
+    g = np.random.default_rng(71)
+    k, stride = 1024, 131072
+    rows = []
+    for top, dense, width in ((600, 1500, 0.0), (600, 3000, 1e-3), (300, 5000, 1e-4), (1000, 2500, 0.0)):
+        r = (g.standard_normal(stride) - 9.0).astype(np.float32)
+        pos = g.choice(stride, top + dense, replace=False)
+        r[pos[:top]] = 10.0 + g.random(top).astype(np.float32)
+        r[pos[top:]] = (2.0 + width * g.random(dense)).astype(np.float32)
+        rows.append(r)
+    lg = np.stack(rows)
+    case = workloads.DecodeCase("floor_bin", lg, np.full(len(rows), stride, np.int32), 1, 1, k)
+    for flags in (0, 8):
+        st = assert_decode_exact(gvr, case, options=gvr.Options(flags=flags), stats=True)
+        assert (st[:, 2] % 10 == 1).all(), st  # one counting pass per row
+        assert set(st[:, 0].tolist()) <= {1, 5}, st
