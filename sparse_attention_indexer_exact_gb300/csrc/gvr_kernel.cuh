@@ -55,6 +55,7 @@ constexpr int STAGE_VEC = THREADS * VPS;  // 256 float4 = 4 KB per stage
 constexpr int MIN_STAGES = 3;         // ring depth bounds (the host picks the depth per launch)
 constexpr int MAX_STAGES = 16;
 constexpr int LIST_CAP = 768;         // above-floor scores kept per CTA for the collect step
+constexpr int LIST_SEG = LIST_CAP / (THREADS / 32);  // each warp appends to its own segment
 constexpr int CAP = 512;              // candidate slots in cluster rank 0
 constexpr int RANK_REFINE_MAX = 256;  // m at or below: refine by pairwise ranking
 constexpr int SPARSE_MAX = 4;         // above-floor scores of a thread per stage before a warp aggregates
@@ -116,7 +117,7 @@ struct alignas(16) Smem {
   int32_t fpart;
   uint32_t dsel, dabove, dcnt, dmy_above, dmy_at;
   uint32_t kmin_loc, kmax_loc;     // rescue: smallest / largest key of this CTA's matching scores
-  uint32_t list_n;                 // scores appended to the list (may exceed LIST_CAP)
+  uint32_t list_n[THREADS / 32];   // scores each warp appended to its segment (may exceed LIST_SEG)
   uint32_t unlisted;               // CTAs of the cluster whose list overflowed (each pushes 1)
   uint32_t ctr_win, ctr_cand;      // this CTA's slot counters (refine path)
   uint32_t gctr_above, gctr_cand;  // rank 0: hands out each CTA's winner / candidate slot bases
@@ -551,7 +552,6 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   auto issue_stage = [&](int32_t s, uint32_t slot) {  // thread 0 only
     const int32_t nfull = stage_full(s);
     if (nfull > 0) {
-      fence_proxy_async_smem();
       mbar_arrive_expect_tx(&S.bar[slot], uint32_t(nfull) * 16u);
       bulk_copy_g2s(&ring[slot][0], base + 4 * size_t(stage_first(s)), uint32_t(nfull) * 16u,
                     &S.bar[slot]);
@@ -583,8 +583,10 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
         late = true;
       }
       visit(slot, stage_first(s));
-      __syncthreads();  // every thread is done with this slot
-      if (tid == 0 && s + nst < nstages) issue_stage(s + nst, slot);
+      if (s + nst < nstages) {  // refill this slot once every thread is done with it
+        __syncthreads();
+        if (tid == 0) issue_stage(s + nst, slot);
+      }
       if (++slot == uint32_t(nst)) {
         slot = 0;
         ph ^= 1u;
@@ -632,6 +634,23 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       for (int l = 0; l < 4; ++l) f(f4_get(v, l), g, ((lanes >> l) & 1u) != 0, l);
     }
   };
+  // Walk of this CTA's list (every warp segment): f(value, window index, valid), warp-collective
+  // with a CTA-uniform trip count.  Only valid once every segment held its scores.
+  auto each_listed = [&](auto&& f) {
+    uint32_t pre[NW + 1];  // segment starts in the concatenated list
+    pre[0] = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) pre[w + 1] = pre[w] + S.list_n[w];
+    for (uint32_t b0 = 0; b0 < pre[NW]; b0 += T) {
+      const uint32_t i = b0 + tid;
+      const bool in = i < pre[NW];
+      uint32_t at = i;  // slot of entry i: its segment's base plus its offset in the segment
+#pragma unroll
+      for (int w = 1; w < NW; ++w)
+        if (i >= pre[w]) at = uint32_t(w * LIST_SEG) + (i - pre[w]);
+      f(in ? S.list_v[at] : 0.f, in ? S.list_j[at] : 0, in);
+    }
+  };
   // After a cluster barrier: tell rank 0 that this CTA gave up waiting (rank 0 marks the row).
   auto report_timeout = [&]() {
     if (tid == 0 && S.tout) dsmem_st_u32(dsmem_map(smem_u32(&S.err), 0), 1u);
@@ -664,7 +683,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   // Zero the counters while the samples are in flight (global loads are not waited for here).
   for (int i = tid; i < NB; i += T) S.hist[i] = S.tot[i] = 0;
   if (tid == 0) {
-    S.list_n = 0;
+    for (int w = 0; w < NW; ++w) S.list_n[w] = 0;
     S.ctr_win = S.ctr_cand = S.ctr_rwin = S.ctr_rtie = 0;
     S.gctr_above = S.gctr_cand = 0;
     S.rc_win = S.rc_tie = 0;
@@ -762,55 +781,79 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     // ------------------------------------------------------------ verify: value histogram
     // Pass 1 counts (and lists) the scores >= thr; pass 2, only when the crossing falls in
     // the partial bin or below, counts the rest.
+    uint32_t wlist = 0;  // scores this warp has appended (warp-uniform; may exceed LIST_SEG)
+    float* const seg_v = S.list_v + warp * LIST_SEG;
+    int32_t* const seg_j = S.list_j + warp * LIST_SEG;
     stream_pass(true, [&](uint32_t slot, int32_t c0) {
+      float4 vv[VPS];
       uint32_t bits = 0;  // bit 4i+l: lane l of this thread's i-th vector is >= thr
 #pragma unroll
       for (int i = 0; i < VPS; ++i) {
         int32_t g;
-        float4 v;
-        const uint32_t lanes = stage_vec(slot, c0, i, g, v);
-        const uint32_t b = uint32_t(v.x >= thr) | (uint32_t(v.y >= thr) << 1) | (uint32_t(v.z >= thr) << 2) |
-                           (uint32_t(v.w >= thr) << 3);
+        const uint32_t lanes = stage_vec(slot, c0, i, g, vv[i]);
+        const uint32_t b = uint32_t(vv[i].x >= thr) | (uint32_t(vv[i].y >= thr) << 1) |
+                           (uint32_t(vv[i].z >= thr) << 2) | (uint32_t(vv[i].w >= thr) << 3);
         bits |= (b & lanes) << (4 * i);
       }
+      // The warp's exclusive prefix of hit counts from one ballot per bit of the count.
       const uint32_t nhit = __popc(bits);
-      if (!__any_sync(FULL_MASK, nhit > SPARSE_MAX)) {
-        // the usual case: a few scores per thread; list slots from one atomic per warp
-        uint32_t incl = nhit;
+      static_assert(4 * VPS < 16, "hit counts fit in 4 bits");
+      uint32_t excl = 0, wtot = 0;
+      const unsigned lt = lanemask_lt();
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t t = __shfl_up_sync(FULL_MASK, incl, o);
-          if (lane >= o) incl += t;
-        }
-        uint32_t wbase = 0;
-        if (lane == 31 && incl) wbase = atomicAdd(&S.list_n, incl);
-        uint32_t at = __shfl_sync(FULL_MASK, wbase, 31) + incl - nhit;
-        while (bits) {
-          const int j = __ffs(bits) - 1;
-          bits &= bits - 1;
-          const float e = stage_score(slot, c0, j);
-          atomicAdd(&S.hist[value_bin(e, gmin, sc)], 1u);
-          if (at < uint32_t(LIST_CAP)) {
-            S.list_v[at] = e;
-            S.list_j[at] = 4 * (c0 + (j >> 2) * T + tid) + (j & 3) - lead;
-          }
-          ++at;
-        }
-      } else {  // tie-heavy warp: aggregate per distinct bin and per warp
+      for (int q = 0; q < 4; ++q) {
+        const unsigned m = __ballot_sync(FULL_MASK, (nhit >> q) & 1u);
+        excl += uint32_t(__popc(m & lt)) << q;
+        wtot += uint32_t(__popc(m)) << q;
+      }
+      if (wtot == 0) return;  // nothing of this warp reaches the floor
+      uint32_t at = wlist + excl;
+      wlist += wtot;
+      // A warp with a few hits per thread counts them one by one; a dense warp (ties, a low
+      // floor) adds its hits with one atomic when they all share a bin, else one per distinct
+      // bin and score slot.
+      const bool dense = __any_sync(FULL_MASK, nhit > uint32_t(SPARSE_MAX));
+      uint32_t bmin = 0xffffffffu, bmax = 0u;
+      for (uint32_t rest = bits; rest;) {
+        const int j = __ffs(rest) - 1;
+        rest &= rest - 1;
+        float4 v = vv[0];
 #pragma unroll
-        for (int j = 0; j < 4 * VPS; ++j) {
-          const bool hit = (bits >> j) & 1u;
-          const float e = hit ? stage_score(slot, c0, j) : 0.f;
-          const uint32_t at = warp_alloc_local(&S.list_n, hit);
-          if (hit && at < uint32_t(LIST_CAP)) {
-            S.list_v[at] = e;
-            S.list_j[at] = 4 * (c0 + (j >> 2) * T + tid) + (j & 3) - lead;
+        for (int i = 1; i < VPS; ++i)
+          if ((j >> 2) == i) v = vv[i];
+        const float e = f4_get(v, j & 3);
+        const uint32_t b = uint32_t(value_bin(e, gmin, sc));
+        if (dense) {
+          bmin = min(bmin, b);
+          bmax = max(bmax, b);
+        } else {
+          atomicAdd(&S.hist[b], 1u);
+        }
+        if (at < uint32_t(LIST_SEG)) {
+          seg_v[at] = e;
+          seg_j[at] = 4 * (c0 + (j >> 2) * T + tid) + (j & 3) - lead;
+        }
+        ++at;
+      }
+      if (dense) {
+        bmin = __reduce_min_sync(FULL_MASK, bmin);
+        bmax = __reduce_max_sync(FULL_MASK, bmax);
+        if (bmin == bmax) {
+          if (lane == 0) atomicAdd(&S.hist[bmin], wtot);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4 * VPS; ++j) {
+            const bool hit = (bits >> j) & 1u;
+            hist_add(S.hist, hit, hit ? uint32_t(value_bin(stage_score(slot, c0, j), gmin, sc)) : 0u);
           }
-          hist_add(S.hist, hit, hit ? uint32_t(value_bin(e, gmin, sc)) : 0u);
         }
       }
     });
-    listed = S.list_n <= uint32_t(LIST_CAP);
+    if (lane == 0) S.list_n[warp] = wlist;
+    __syncthreads();
+    listed = true;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) listed = listed && S.list_n[w] <= uint32_t(LIST_SEG);
     rounds = 1;
     // Push this CTA's counts of bins [b0, b1] into every CTA's totals (fire-and-forget).
     auto push = [&](int b0, int b1) {
@@ -893,12 +936,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     };
     if (!(rounds == 1 && listed)) rounds += 10;  // diagnostics: collect read the share again
     if (rounds == 1 && listed) {
-      const uint32_t n = S.list_n;
-      for (uint32_t b0 = 0; b0 < n; b0 += T) {
-        const uint32_t i = b0 + tid;
-        const bool in = i < n;
-        place(in ? S.list_v[i] : 0.f, in ? S.list_j[i] : 0, in);
-      }
+      each_listed([&](float e, int32_t jw, bool in) { place(e, jw, in); });
     } else {  // the list overflowed or scores below the floor count: read the share again
       if (warp == 0) {
         const float t = bstar > 0 ? floor_value(bstar, gmin, sc) : -INFINITY;
@@ -1073,12 +1111,10 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       }
     };
     if (from_lists) {
-      const uint32_t n = S.list_n;  // <= LIST_CAP on this path
-      for (uint32_t b0 = 0; b0 < n; b0 += T) {
-        const uint32_t i = b0 + tid;
-        const float e[1] = {i < n ? S.list_v[i] : 0.f};
-        digit_batch(IntC<1>{}, e, i < n ? 1u : 0u);
-      }
+      each_listed([&](float v, int32_t, bool in) {
+        const float e[1] = {v};
+        digit_batch(IntC<1>{}, e, in ? 1u : 0u);
+      });
     } else {
       stream_pass(primed, [&](uint32_t slot, int32_t c0) {
         float e[4 * VPS];
@@ -1171,16 +1207,11 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   };
   if (my_win > 0 || my_ties > 0) {
     if (from_lists) {
-      const uint32_t n = S.list_n;
-      for (uint32_t b0 = 0; b0 < n; b0 += T) {
-        const uint32_t i = b0 + tid;
-        const bool in = i < n;
-        emit(in ? S.list_v[i] : 0.f, in ? S.list_j[i] : 0, in);
-      }
+      each_listed([&](float e, int32_t jw, bool in) { emit(e, jw, in); });
     } else {
       stream_pass(false, [&](uint32_t slot, int32_t c0) {
-        // the counters are settled at a stage boundary: stop visiting once this CTA's slots
-        // are all written (its remaining stages still land and are waited for)
+        // stop visiting once this CTA's slots are all handed out (the counters only grow, and a
+        // warp reads them together; the remaining stages still land and are waited for)
         if (S.ctr_win >= my_win && S.ctr_cand >= my_ties) return;
         each_lane(slot, c0, [&](float e, int32_t g, bool valid, int l) { emit(e, 4 * g + l - lead, valid); });
       });
