@@ -471,6 +471,15 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   const int32_t k = p.k;
   const float qnan = __int_as_float(0x7fffffff);
 
+  // The ring's barriers are initialized first: the fence that publishes them then overlaps the
+  // geometry load instead of delaying the first stage copies.
+  if (tid == 0) {
+#pragma unroll
+    for (int s = 0; s < MAX_STAGES; ++s)
+      if (s < nst) mbar_init(&S.bar[s], 1);
+    mbar_init_fence();
+  }
+
   // ---------------------------------------------------------------- row geometry
   // row_stride < 2^31 and every count below fits in 32 bits.
   const uint32_t stride = uint32_t(p.row_stride);
@@ -527,15 +536,6 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     return (int32_t(rank) + s * int32_t(cs)) * STAGE_VEC;
   };
 
-  // The ring's barriers are initialized before anything else so that its first stages can be
-  // in flight while the row is sampled.
-  if (tid == 0) {
-#pragma unroll
-    for (int s = 0; s < MAX_STAGES; ++s)
-      if (s < nst) mbar_init(&S.bar[s], 1);
-    mbar_init_fence();
-  }
-
   // ---------------------------------------------------------------- streaming ring
   // The CTA's stages of every pass go through the ring in order; the ring position (slot,
   // mbarrier phase) advances by one per stage.  Thread 0 refills a slot after all threads have
@@ -549,7 +549,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   };
   // Every stage completes exactly one phase of its slot's barrier, even a stage with no whole
   // vector (only the partial tail), so slot phases stay in step with the ring position.
-  auto issue_stage = [&](int32_t s, uint32_t slot) {  // thread 0 only
+  auto issue_stage = [&](int32_t s, uint32_t slot) {  // one thread per stage
     const int32_t nfull = stage_full(s);
     if (nfull > 0) {
       mbar_arrive_expect_tx(&S.bar[slot], uint32_t(nfull) * 16u);
@@ -569,13 +569,11 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   bool loaded = false;
   uint32_t rslot = 0, rphase = 0;
   auto stream_pass = [&](bool primed, auto&& visit) {
-    if (tid == 0 && !primed && !(ring_resident && loaded)) {
-      uint32_t sl = rslot;
-      for (int32_t s = 0; s < nst && s < nstages; ++s) {
-        issue_stage(s, sl);
-        if (++sl == uint32_t(nst)) sl = 0;
+    if (warp == 0 && !primed && !(ring_resident && loaded))
+      for (int32_t s = lane; s < nst && s < nstages; s += 32) {  // nst <= 16: one pass of lanes
+        const uint32_t sl = rslot + uint32_t(s);
+        issue_stage(s, sl < uint32_t(nst) ? sl : sl - uint32_t(nst));
       }
-    }
     uint32_t slot = rslot, ph = rphase;
     for (int32_t s = 0; s < nstages; ++s) {
       if (!mbar_wait_bounded(&S.bar[slot], ph, WAIT_LIMIT_NS)) {
@@ -656,9 +654,6 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     if (tid == 0 && S.tout) dsmem_st_u32(dsmem_map(smem_u32(&S.err), 0), 1u);
   };
 
-  if (tid == 0)
-    for (int32_t s = 0; s < nst && s < nstages; ++s) issue_stage(s, uint32_t(s));  // overlaps sampling
-
   // ---------------------------------------------------------------- guess: block64 sample
   const uint32_t nblk = uint32_t(k) >> 6;
   // Start of run b = floor(b (nv - 64) / (nblk - 1)), one run per lane (nblk <= 32), with no
@@ -673,6 +668,9 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     const uint32_t s = __shfl_sync(FULL_MASK, run_start, blk & 31u);
     sv[q] = i < uint32_t(k) ? __ldg(rowp + a + s + (i & 63u)) : qnan;
   }
+  // The first ring stages go in flight right behind the samples, one lane of warp 0 per stage.
+  if (warp == 0)
+    for (int32_t s = lane; s < nst && s < nstages; s += 32) issue_stage(s, uint32_t(s));
   // Every later stage of this CTA is requested into L2 now (no shared memory needed), so HBM
   // streams the whole row at once and the ring's refills are L2 hits.
   if (warp == 1)
@@ -786,25 +784,37 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     int32_t* const seg_j = S.list_j + warp * LIST_SEG;
     stream_pass(true, [&](uint32_t slot, int32_t c0) {
       float4 vv[VPS];
+      uint32_t lanes = 0xFFFFFFFFu;  // bit 4i+l: lane l of the i-th vector is in the window
+      if (c0 > 0 && c0 + STAGE_VEC <= ffull) {  // an interior stage: every lane is in the window
+#pragma unroll
+        for (int i = 0; i < VPS; ++i) vv[i] = ring[slot][i * T + tid];
+      } else {
+        lanes = 0;
+#pragma unroll
+        for (int i = 0; i < VPS; ++i) {
+          int32_t g;
+          lanes |= stage_vec(slot, c0, i, g, vv[i]) << (4 * i);
+        }
+      }
       uint32_t bits = 0;  // bit 4i+l: lane l of this thread's i-th vector is >= thr
 #pragma unroll
-      for (int i = 0; i < VPS; ++i) {
-        int32_t g;
-        const uint32_t lanes = stage_vec(slot, c0, i, g, vv[i]);
-        const uint32_t b = uint32_t(vv[i].x >= thr) | (uint32_t(vv[i].y >= thr) << 1) |
-                           (uint32_t(vv[i].z >= thr) << 2) | (uint32_t(vv[i].w >= thr) << 3);
-        bits |= (b & lanes) << (4 * i);
-      }
-      // The warp's exclusive prefix of hit counts from one ballot per bit of the count.
+      for (int i = 0; i < VPS; ++i)
+        bits |= (uint32_t(vv[i].x >= thr) | (uint32_t(vv[i].y >= thr) << 1) | (uint32_t(vv[i].z >= thr) << 2) |
+                 (uint32_t(vv[i].w >= thr) << 3))
+                << (4 * i);
+      bits &= lanes;
+      // The warp's exclusive prefix of hit counts from one ballot per bit of the count (the
+      // upper two bits only when some thread has 4 or more hits).
       const uint32_t nhit = __popc(bits);
       static_assert(4 * VPS < 16, "hit counts fit in 4 bits");
-      uint32_t excl = 0, wtot = 0;
       const unsigned lt = lanemask_lt();
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const unsigned m = __ballot_sync(FULL_MASK, (nhit >> q) & 1u);
-        excl += uint32_t(__popc(m & lt)) << q;
-        wtot += uint32_t(__popc(m)) << q;
+      const unsigned m0 = __ballot_sync(FULL_MASK, nhit & 1u), m1 = __ballot_sync(FULL_MASK, nhit & 2u);
+      uint32_t excl = uint32_t(__popc(m0 & lt)) + (uint32_t(__popc(m1 & lt)) << 1);
+      uint32_t wtot = uint32_t(__popc(m0)) + (uint32_t(__popc(m1)) << 1);
+      if (__any_sync(FULL_MASK, nhit >= 4u)) {
+        const unsigned m2 = __ballot_sync(FULL_MASK, nhit & 4u), m3 = __ballot_sync(FULL_MASK, nhit & 8u);
+        excl += (uint32_t(__popc(m2 & lt)) << 2) + (uint32_t(__popc(m3 & lt)) << 3);
+        wtot += (uint32_t(__popc(m2)) << 2) + (uint32_t(__popc(m3)) << 3);
       }
       if (wtot == 0) return;  // nothing of this warp reaches the floor
       uint32_t at = wlist + excl;
