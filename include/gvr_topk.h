@@ -96,7 +96,16 @@ enum {
   GVR_FLAG_FORCE_RESCUE = 1, /* skip the histogram: every long row takes the exact rescue */
   GVR_FLAG_NO_FLOOR = 2,     /* count every bin of the value histogram (no sampled floor) */
   GVR_FLAG_ZERO_CAP = 4,     /* candidate buffer of 0 slots: every long row overflows to rescue */
-  GVR_FLAG_RADIX_REFINE = 8  /* refine every candidate set by radix select (not by ranking) */
+  GVR_FLAG_RADIX_REFINE = 8, /* refine every candidate set by radix select (not by ranking) */
+  /* Deterministic mode ("Self-sampling GVR V2", the selection kernel's contract: exact
+   * membership with smallest-index deterministic ties, optional output sorting): of the scores
+   * equal to tau, the ones with the smallest window indices fill the remaining slots, so the
+   * selected set is the same on every run.  Output order stays unspecified. */
+  GVR_FLAG_DETERMINISTIC = 16,
+  /* Deterministic ties, and each long row's k indices ordered by (score descending, window
+   * index ascending), -0 equal to +0.  Rows with nv <= k keep the identity order 0..nv-1 and
+   * the -1 pad. */
+  GVR_FLAG_SORTED = 32
 };
 
 typedef struct gvr_options {

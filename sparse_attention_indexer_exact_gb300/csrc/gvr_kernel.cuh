@@ -63,7 +63,14 @@ constexpr int MAX_K = 2048;
 constexpr uint64_t WAIT_LIMIT_NS = 500000000ull;  // bound on any wait for staged data (0.5 s)
 
 enum : int32_t { MODE_DECODE = 0, MODE_PREFILL = 1 };
-enum : int32_t { FLAG_FORCE_RESCUE = 1, FLAG_NO_FLOOR = 2, FLAG_ZERO_CAP = 4, FLAG_RADIX_REFINE = 8 };
+enum : int32_t {
+  FLAG_FORCE_RESCUE = 1,
+  FLAG_NO_FLOOR = 2,
+  FLAG_ZERO_CAP = 4,
+  FLAG_RADIX_REFINE = 8,
+  FLAG_DETERMINISTIC = 16,
+  FLAG_SORTED = 32
+};
 enum : int32_t {
   PATH_DEVICE_ERROR = -1,
   PATH_SHORT = 0,
@@ -133,6 +140,7 @@ static_assert(offsetof(Smem, hist) % 16 == 0 && offsetof(Smem, tot) % 16 == 0,
               "histograms are read as 16-byte vectors");
 static_assert(offsetof(Smem, bar) % 8 == 0, "mbarriers must be 8-byte aligned");
 static_assert(2 * 256 + 4 <= NB, "the rescue's digit totals and key bounds live in tot");
+static_assert(offsetof(Smem, wsum) >= sizeof(uint64_t) * MAX_K, "sort keys fit below the scalars");
 
 __device__ __forceinline__ uint32_t* digit_hist(Smem& S, int buf) { return S.tot + 256 * buf; }
 
@@ -470,6 +478,8 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   const uint32_t row = cluster_id_x();
   const int32_t k = p.k;
   const float qnan = __int_as_float(0x7fffffff);
+  // ties at tau go to the smallest window indices (always so when the output is sorted)
+  const bool det = (p.flags & (FLAG_DETERMINISTIC | FLAG_SORTED)) != 0;
 
   // The ring's barriers are initialized first: the fence that publishes them then overlaps the
   // geometry load instead of delaying the first stage copies.
@@ -647,6 +657,38 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       for (int w = 1; w < NW; ++w)
         if (i >= pre[w]) at = uint32_t(w * LIST_SEG) + (i - pre[w]);
       f(in ? S.list_v[at] : 0.f, in ? S.list_j[at] : 0, in);
+    }
+  };
+  // Rank 0, block-collective: reorder out[0..k) (and the values) by (value desc, index asc), the
+  // order of the plain definition.  k is a power of two; the 64-bit sort keys (inverted order
+  // key, index) live in the histogram / list / candidate area, which no CTA uses any more.
+  auto sort_output = [&]() {
+    uint64_t* sk = reinterpret_cast<uint64_t*>(smem_raw);
+    __syncthreads();
+    for (int i = tid; i < k; i += T) {
+      const int32_t j = __ldcg(out + i);  // written by every CTA of the cluster
+      const float v = uint32_t(j) < nv ? __ldg(rowp + a + j) : -INFINITY;
+      sk[i] = (uint64_t(~order_key(v)) << 32) | uint32_t(j);
+    }
+    __syncthreads();
+    for (int kk = 2; kk <= k; kk <<= 1)  // bitonic network, ascending
+      for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+        for (int i = tid; i < k; i += T) {
+          const int l = i ^ jj;
+          if (l > i) {
+            const uint64_t x = sk[i], y = sk[l];
+            if ((x > y) == ((i & kk) == 0)) {
+              sk[i] = y;
+              sk[l] = x;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    for (int i = tid; i < k; i += T) {
+      const int32_t j = int32_t(uint32_t(sk[i]));
+      out[i] = j;
+      if (outv) outv[i] = uint32_t(j) < nv ? __ldg(rowp + a + j) : -FLT_MAX;
     }
   };
   // After a cluster barrier: tell rank 0 that this CTA gave up waiting (rank 0 marks the row).
@@ -968,7 +1010,8 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     // ------------------------------------------------------------ refine (rank 0)
     const uint32_t need = uint32_t(k) - cr.above;
     const uint32_t mm = cr.m < uint32_t(CAP) ? cr.m : uint32_t(CAP);
-    if (mm <= uint32_t(RANK_REFINE_MAX) && !(p.flags & FLAG_RADIX_REFINE)) {
+    if ((mm <= uint32_t(RANK_REFINE_MAX) && !(p.flags & FLAG_RADIX_REFINE)) || det) {
+      // (deterministic mode ranks every candidate set: ties by smallest index)
       // rank of candidate i = number of candidates ordered before it by (value desc, index asc)
       for (uint32_t i = tid; i < mm; i += T) {
         const float v = S.cand_v[i];
@@ -1034,6 +1077,8 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     const bool failed = S.err || S.tout;
     if (failed)
       for (int i = tid; i < k; i += T) out[i] = -2;
+    else if (p.flags & FLAG_SORTED)
+      sort_output();
     if (stats) {
       stats[0] = failed ? PATH_DEVICE_ERROR : PATH_REFINE;
       stats[1] = int32_t(cr.m);
@@ -1067,11 +1112,6 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   }
   __syncthreads();
   csync();  // every CTA's pushed totals start from zero
-  uint32_t prefix = 0, pmask = 0;
-  uint32_t need = seeded ? uint32_t(k) - cr.above : uint32_t(k);
-  uint32_t my_win = seeded ? cr.my_above : 0u;  // this CTA's scores above tau
-  uint32_t my_eq = 0;                             // this CTA's scores equal to tau
-  bool ge = false;
   bool primed = rounds == 0;  // the first pass of a row that skipped the histogram is primed
   // Bin class of a score for the seeded selection: 1 above the crossing bin, 0 a member of it,
   // -1 below it (or not counted).  Unseeded, every score is a member.
@@ -1080,118 +1120,165 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     const int b = value_bin(e, gmin, sc);
     return b > bstar ? 1 : (b == bstar && e >= cthr ? 0 : -1);
   };
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    const int buf = pass & 1;
-    for (int i = tid; i < 256; i += T) dloc[i] = 0;
-    if (tid == 0) {
-      S.kmin_loc = 0xffffffffu;
-      S.kmax_loc = 0u;
-    }
-    __syncthreads();
-    uint32_t tmin = 0xffffffffu, tmax = 0u;
-    // Count the digits of a thread's batch of N scores (bit j of vm: score j is in the window).
-    // Warp-collective.  A warp whose matching keys all share one digit adds them with one
-    // atomic (tie-heavy and narrow rows); otherwise one atomic per distinct digit per score slot.
-    auto digit_batch = [&](auto n_c, const float* e, uint32_t vm) {
-      constexpr int N = decltype(n_c)::value;
-      uint32_t keys[N];
-      uint32_t pm = 0, dmin = 0xffffffffu, dmax = 0u;
+  // One cluster radix selection: the `need` largest keys among the scores that sel(e, j, key)
+  // admits (it also computes the key), one 8-bit digit per pass from bit shift0 down, below the
+  // fixed key bits (prefix0 under pmask0).  The result is the selected keys' boundary: with ge
+  // the keys whose masked value is >= prefix are exactly the selected ones; without ge the keys
+  // above prefix are, plus `need` of the keys equal to prefix (pmask is then all ones).
+  // my_above / my_at: this CTA's admitted scores above / at the boundary.
+  struct Sel {
+    uint32_t prefix, pmask, need, my_above, my_at;
+    bool ge;
+  };
+  int rpass = 0;  // digit-total buffers alternate over the passes of every selection
+  auto radix_select = [&](auto&& sel, uint32_t need0, uint32_t fixed, int shift0) -> Sel {
+    Sel r{fixed, fixed, need0, 0u, 0u, false};
+    for (int shift = shift0; shift >= 0; shift -= 8) {
+      const int buf = rpass++ & 1;
+      for (int i = tid; i < 256; i += T) dloc[i] = 0;
+      if (tid == 0) {
+        S.kmin_loc = 0xffffffffu;
+        S.kmax_loc = 0u;
+      }
+      __syncthreads();
+      uint32_t tmin = 0xffffffffu, tmax = 0u;
+      // Count the digits of a thread's batch of N scores (bit j of vm: score j is in the
+      // window).  Warp-collective.  A warp whose admitted keys all share one digit adds them
+      // with one atomic (tie-heavy and narrow rows); otherwise one atomic per distinct digit per
+      // score slot.
+      auto digit_batch = [&](auto n_c, const float* e, const int32_t* jw, uint32_t vm) {
+        constexpr int N = decltype(n_c)::value;
+        uint32_t keys[N];
+        uint32_t pm = 0, dmin = 0xffffffffu, dmax = 0u;
 #pragma unroll
-      for (int j = 0; j < N; ++j) {
-        keys[j] = order_key(e[j]);
-        const bool ok = ((vm >> j) & 1u) && (keys[j] & pmask) == prefix && bin_class(e[j]) == 0;
-        if (ok) {
-          pm |= 1u << j;
-          tmin = min(tmin, keys[j]);
-          tmax = max(tmax, keys[j]);
-          const uint32_t d = (keys[j] >> shift) & 255u;
-          dmin = min(dmin, d);
-          dmax = max(dmax, d);
+        for (int j = 0; j < N; ++j) {
+          uint32_t key = 0;
+          const bool ok = ((vm >> j) & 1u) && sel(e[j], jw[j], key) && (key & r.pmask) == r.prefix;
+          keys[j] = key;
+          if (ok) {
+            pm |= 1u << j;
+            tmin = min(tmin, key);
+            tmax = max(tmax, key);
+            const uint32_t d = (key >> shift) & 255u;
+            dmin = min(dmin, d);
+            dmax = max(dmax, d);
+          }
+        }
+        dmin = __reduce_min_sync(FULL_MASK, dmin);
+        dmax = __reduce_max_sync(FULL_MASK, dmax);
+        if (dmin == dmax) {
+          const uint32_t c = __reduce_add_sync(FULL_MASK, uint32_t(__popc(pm)));
+          if (lane == 0) atomicAdd(&dloc[dmin], c);
+        } else if (dmin < dmax) {
+#pragma unroll
+          for (int j = 0; j < N; ++j) hist_add(dloc, (pm >> j) & 1u, (keys[j] >> shift) & 255u);
+        }
+      };
+      if (from_lists) {
+        each_listed([&](float v, int32_t j, bool in) {
+          const float e[1] = {v};
+          const int32_t jj[1] = {j};
+          digit_batch(IntC<1>{}, e, jj, in ? 1u : 0u);
+        });
+      } else {
+        stream_pass(primed, [&](uint32_t slot, int32_t c0) {
+          float e[4 * VPS];
+          int32_t jw[4 * VPS];
+          uint32_t vm = 0;
+#pragma unroll
+          for (int i = 0; i < VPS; ++i) {
+            int32_t g;
+            float4 v;
+            vm |= stage_vec(slot, c0, i, g, v) << (4 * i);
+#pragma unroll
+            for (int l = 0; l < 4; ++l) {
+              e[4 * i + l] = f4_get(v, l);
+              jw[4 * i + l] = 4 * g + l - lead;
+            }
+          }
+          digit_batch(IntC<4 * VPS>{}, e, jw, vm);
+        });
+      }
+      primed = false;
+      tmin = __reduce_min_sync(FULL_MASK, tmin);
+      tmax = __reduce_max_sync(FULL_MASK, tmax);
+      if (lane == 0) {
+        atomicMin(&S.kmin_loc, tmin);
+        atomicMax(&S.kmax_loc, tmax);
+      }
+      __syncthreads();
+      for (int d = tid; d < 256; d += T) {
+        const uint32_t v = dloc[d];
+        if (v) {
+          const uint32_t local = smem_u32(&dtot(buf)[d]);
+          for (uint32_t c = 0; c < cs; ++c) dsmem_red_add(dsmem_map(local, c), v);
         }
       }
-      dmin = __reduce_min_sync(FULL_MASK, dmin);
-      dmax = __reduce_max_sync(FULL_MASK, dmax);
-      if (dmin == dmax) {
-        const uint32_t c = __reduce_add_sync(FULL_MASK, uint32_t(__popc(pm)));
-        if (lane == 0) atomicAdd(&dloc[dmin], c);
-      } else if (dmin < dmax) {
-#pragma unroll
-        for (int j = 0; j < N; ++j) hist_add(dloc, (pm >> j) & 1u, (keys[j] >> shift) & 255u);
-      }
-    };
-    if (from_lists) {
-      each_listed([&](float v, int32_t, bool in) {
-        const float e[1] = {v};
-        digit_batch(IntC<1>{}, e, in ? 1u : 0u);
-      });
-    } else {
-      stream_pass(primed, [&](uint32_t slot, int32_t c0) {
-        float e[4 * VPS];
-        uint32_t vm = 0;
-#pragma unroll
-        for (int i = 0; i < VPS; ++i) {
-          int32_t g;
-          float4 v;
-          vm |= stage_vec(slot, c0, i, g, v) << (4 * i);
-          e[4 * i + 0] = v.x;
-          e[4 * i + 1] = v.y;
-          e[4 * i + 2] = v.z;
-          e[4 * i + 3] = v.w;
+      if (tid == 0)
+        for (uint32_t c = 0; c < cs; ++c) {
+          dsmem_red_min(dsmem_map(smem_u32(kslot(buf, 0)), c), S.kmin_loc);
+          dsmem_red_max(dsmem_map(smem_u32(kslot(buf, 1)), c), S.kmax_loc);
         }
-        digit_batch(IntC<4 * VPS>{}, e, vm);
-      });
-    }
-    primed = false;
-    tmin = __reduce_min_sync(FULL_MASK, tmin);
-    tmax = __reduce_max_sync(FULL_MASK, tmax);
-    if (lane == 0) {
-      atomicMin(&S.kmin_loc, tmin);
-      atomicMax(&S.kmax_loc, tmax);
-    }
-    __syncthreads();
-    for (int d = tid; d < 256; d += T) {
-      const uint32_t v = dloc[d];
-      if (v) {
-        const uint32_t local = smem_u32(&dtot(buf)[d]);
-        for (uint32_t c = 0; c < cs; ++c) dsmem_red_add(dsmem_map(local, c), v);
+      csync();
+      report_timeout();
+      const DigitCross dc = digit_scan<T>(S, dtot(buf), dloc, r.need);
+      const uint32_t kmin_all = *kslot(buf, 0), kmax_all = *kslot(buf, 1);
+      __syncthreads();  // every thread has read this pass's totals: reset them for two passes on
+      for (int i = tid; i < 256; i += T) dtot(buf)[i] = 0;
+      if (tid == 0) {
+        *kslot(buf, 0) = 0xffffffffu;
+        *kslot(buf, 1) = 0u;
+      }
+      if (kmin_all == kmax_all) {  // every admitted key with this prefix is the same
+        r.prefix = kmin_all;
+        r.pmask = 0xffffffffu;
+        r.my_at = dc.my_all;
+        break;
+      }
+      r.prefix |= dc.digit << shift;
+      r.pmask |= 0xFFu << shift;
+      r.need -= dc.above;
+      r.my_above += dc.my_above;
+      r.my_at = dc.my_at;
+      if (dc.cnt == r.need) {  // the keys with this prefix are exactly the remaining ones
+        r.ge = true;
+        r.my_above += dc.my_at;
+        r.my_at = 0;
+        break;
       }
     }
-    if (tid == 0)
-      for (uint32_t c = 0; c < cs; ++c) {
-        dsmem_red_min(dsmem_map(smem_u32(kslot(buf, 0)), c), S.kmin_loc);
-        dsmem_red_max(dsmem_map(smem_u32(kslot(buf, 1)), c), S.kmax_loc);
-      }
-    csync();
-    report_timeout();
-    const DigitCross dc = digit_scan<T>(S, dtot(buf), dloc, need);
-    const uint32_t kmin_all = *kslot(buf, 0), kmax_all = *kslot(buf, 1);
-    __syncthreads();  // every thread has read this pass's totals: reset them for pass + 2
-    for (int i = tid; i < 256; i += T) dtot(buf)[i] = 0;
-    if (tid == 0) {
-      *kslot(buf, 0) = 0xffffffffu;
-      *kslot(buf, 1) = 0u;
-    }
-    if (kmin_all == kmax_all) {  // every matching key is the same: they are all tied at tau
-      prefix = kmin_all;
-      pmask = 0xffffffffu;
-      my_eq = dc.my_all;
-      break;
-    }
-    prefix |= dc.digit << shift;
-    pmask |= 0xFFu << shift;
-    need -= dc.above;
-    my_win += dc.my_above;
-    my_eq = dc.my_at;
-    if (dc.cnt == need) {  // the keys with this prefix are exactly the remaining winners
-      ge = true;
-      my_win += dc.my_at;
-      my_eq = 0;
-      break;
-    }
+    return r;
+  };
+  // tau: the k - above largest order keys among the members
+  const Sel t = radix_select([&](float e, int32_t, uint32_t& key) {
+    key = order_key(e);
+    return bin_class(e) == 0;
+  }, seeded ? uint32_t(k) - cr.above : uint32_t(k), 0u, 24);
+  const uint32_t prefix = t.prefix, pmask = t.pmask;
+  const bool ge = t.ge;
+  const uint32_t my_win = (seeded ? cr.my_above : 0u) + t.my_above;  // this CTA's scores above tau
+  const uint32_t nties = ge ? 0u : t.need;                           // tie slots
+  // Deterministic mode: the tie slots go to the ties with the smallest window indices, the
+  // nties largest keys ~j among the scores equal to tau.  Keys of indices below 2^(8D) share
+  // their top 32 - 8D bits (all ones), so only D digit passes are needed.
+  bool by_index = false;
+  Sel ix{};
+  if (det && nties > 0) {
+    by_index = true;
+    const int digits = (32 - __clz(int(nv - 1u)) + 7) / 8;
+    const uint32_t fixed = digits < 4 ? (0xffffffffu << (8 * digits)) : 0u;
+    ix = radix_select([&](float e, int32_t jw, uint32_t& key) {
+      key = ~uint32_t(jw);
+      return bin_class(e) == 0 && order_key(e) == prefix;
+    }, nties, fixed, 8 * (digits - 1));
   }
+  auto index_selected = [&](int32_t jw) -> bool {
+    const uint32_t key = ~uint32_t(jw);
+    return ix.ge ? (key & ix.pmask) >= ix.prefix : key >= ix.prefix;
+  };
+  // this CTA's tie candidates for the slots: all its ties, or its index-selected ties
+  const uint32_t my_eq = by_index ? ix.my_above + (ix.ge ? 0u : ix.my_at) : t.my_at;
   // Emission: rank 0 hands this CTA a block of winner slots and a block of tie slots.
-  const uint32_t nties = ge ? 0u : need;
   const uint32_t tie_base = uint32_t(k) - nties;
   if (tid == 0) S.base_above = my_win ? dsmem_atom_add(dsmem_map(smem_u32(&S.rc_win), 0), my_win) : 0u;
   if (tid == 32) S.base_cand = my_eq ? dsmem_atom_add(dsmem_map(smem_u32(&S.rc_tie), 0), my_eq) : 0u;
@@ -1203,7 +1290,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     const uint32_t key = order_key(e);
     const int bc = valid ? bin_class(e) : -1;
     const bool win = bc == 1 || (bc == 0 && (ge ? (key & pmask) >= prefix : key > prefix));
-    const bool tie = bc == 0 && !ge && key == prefix;
+    const bool tie = bc == 0 && !ge && key == prefix && (!by_index || index_selected(jw));
     const uint32_t ws = warp_alloc_local(&S.ctr_win, win);
     if (win && wbase + ws < tie_base) {
       out[wbase + ws] = jw;
@@ -1233,6 +1320,8 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     const bool failed = S.err || S.tout;
     if (failed)
       for (int i = tid; i < k; i += T) out[i] = -2;
+    else if (p.flags & FLAG_SORTED)
+      sort_output();
     if (stats) {
       stats[0] = failed ? PATH_DEVICE_ERROR : path;
       stats[1] = int32_t(cr.m);

@@ -77,7 +77,8 @@ gvr_status check_common(int64_t row_stride, int64_t num_rows, int32_t k, const g
     if (o->cluster_size != 0 && !is_pow2_upto8(o->cluster_size)) return GVR_ERR_ARG;
     if (o->ring_stages != 0 && (o->ring_stages < gvr::MIN_STAGES || o->ring_stages > gvr::MAX_STAGES))
       return GVR_ERR_ARG;
-    if (o->flags & ~(GVR_FLAG_FORCE_RESCUE | GVR_FLAG_NO_FLOOR | GVR_FLAG_ZERO_CAP | GVR_FLAG_RADIX_REFINE))
+    if (o->flags & ~(GVR_FLAG_FORCE_RESCUE | GVR_FLAG_NO_FLOOR | GVR_FLAG_ZERO_CAP | GVR_FLAG_RADIX_REFINE |
+                     GVR_FLAG_DETERMINISTIC | GVR_FLAG_SORTED))
       return GVR_ERR_ARG;
   }
   return GVR_OK;

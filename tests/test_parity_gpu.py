@@ -381,3 +381,99 @@ def test_crossing_in_the_floor_bin(gvr):
         st = assert_decode_exact(gvr, case, options=gvr.Options(flags=flags), stats=True)
         assert (st[:, 2] % 10 == 1).all(), st  # one counting pass per row
         assert set(st[:, 0].tolist()) <= {1, 5}, st
+
+
+# ----------------------------------------------------------------------------- deterministic mode
+def _exact_vs_oracle(got, ref, n, k, ordered):
+    """Rows with nv <= k: the identity; long rows: the oracle's set (ordered: its sequence)."""
+    bad = []
+    for r in range(got.shape[0]):
+        if n[r] <= k or ordered:
+            ok = np.array_equal(got[r], ref[r])
+        else:
+            ok = np.array_equal(np.sort(got[r]), np.sort(ref[r]))
+        if not ok:
+            bad.append(r)
+    return bad
+
+
+def assert_decode_deterministic(gvr, case, flags, extra=0, **opt):
+    got, vals, st = run_decode(gvr, case, values=True, options=gvr.Options(flags=flags | extra, **opt),
+                               stats=True)
+    ref, _, _ = oracle.topk_decode(case.logits, case.kv_lens, case.next_n, case.compress_ratio, case.k)
+    n = case.row_lengths()
+    bad = _exact_vs_oracle(got, ref, n, case.k, ordered=bool(flags & gvr.FLAG_SORTED))
+    assert not bad, f"{case.name}: rows {bad[:8]} differ from the oracle (paths {st[bad[:8], 0]})"
+    # values stay the scores at the returned indices
+    nbad, why = compare_rows(decode_windows(case.logits, case.kv_lens, case.next_n, case.compress_ratio), case.k,
+                             got, ref, got_values=vals)
+    assert nbad == 0, why
+    return st
+
+
+def assert_prefill_deterministic(gvr, case, flags, extra=0, **opt):
+    got, _ = run_prefill(gvr, case, options=gvr.Options(flags=flags | extra, **opt))
+    ref, _ = oracle.topk_prefill(case.logits, case.row_starts, case.row_ends, case.k)
+    n = np.maximum(np.minimum(case.row_ends, case.logits.shape[1]) - np.maximum(case.row_starts, 0), 0)
+    bad = _exact_vs_oracle(got, ref, n, case.k, ordered=bool(flags & gvr.FLAG_SORTED))
+    assert not bad, f"{case.name}: rows {bad[:8]} differ from the oracle"
+
+
+DET_MODES = [16, 32]  # GVR_FLAG_DETERMINISTIC, GVR_FLAG_SORTED
+
+
+@pytest.mark.parametrize("flags", DET_MODES)
+def test_deterministic_workloads(gvr, flags):
+    assert_decode_deterministic(gvr, workloads.single_decode_row(), flags)
+    assert_decode_deterministic(gvr, workloads.decode_batch(), flags)
+    assert_decode_deterministic(gvr, workloads.decode_batch(requests=64, empty_request=True, stride=32768,
+                                                           kv_hi=131072), flags)
+    assert_prefill_deterministic(gvr, workloads.prefill_tile(), flags)
+
+
+@pytest.mark.parametrize("flags", DET_MODES)
+@pytest.mark.parametrize("variant", workloads.ADVERSARIAL_VARIANTS)
+def test_deterministic_ties(gvr, flags, variant):
+    """Tie classes at tau far larger than the free slots: the smallest indices must win."""
+    case = workloads.adversarial_row(variant)
+    for extra in (0, 1, 4):  # histogram path, forced rescue, overflow
+        assert_decode_deterministic(gvr, case, flags, extra)
+
+
+@pytest.mark.parametrize("flags", DET_MODES)
+@pytest.mark.parametrize("extra", [0, 1, 4, 8, 2 | 4])
+def test_deterministic_every_path(gvr, flags, extra):
+    g = np.random.default_rng(900 + extra)
+    rows, stride, k = 10, 65536, 1024
+    lg = np.round(g.standard_normal((rows, stride)) * (1.0 + np.arange(rows)[:, None])).astype(np.float32)
+    lg[0] = 1.0                      # one class
+    lg[1, ::3] = 7.0                 # a class of ~21845 on top
+    lg[2, g.choice(stride, 700, replace=False)] = 9.0
+    case = workloads.DecodeCase("det_paths", lg, np.full(rows, stride, np.int32), 1, 1, k)
+    assert_decode_deterministic(gvr, case, flags, extra)
+    assert_decode_deterministic(gvr, case, flags, extra, cluster_size=2)
+
+
+@pytest.mark.parametrize("flags", DET_MODES)
+def test_deterministic_list_refine_and_prefill_leads(gvr, flags):
+    g = np.random.default_rng(77)
+    k, stride = 512, 65536
+    rows = []
+    for p in (600, 1500):
+        r = g.standard_normal(stride).astype(np.float32)
+        r[g.choice(stride, p, replace=False)] = 3.5
+        rows.append(r)
+    case = workloads.DecodeCase("det_lists", np.stack(rows), np.full(2, stride, np.int32), 1, 1, k)
+    st = assert_decode_deterministic(gvr, case, flags)
+    assert (st[:, 0] == 5).all(), st
+    rows, ks, ke = [], [], []
+    for s in range(4):
+        row = workloads.PREFILL_POISON[np.arange(8192) % 4].copy()
+        w = np.round(g.standard_normal(7000)).astype(np.float32)
+        row[s:s + 7000] = w
+        rows.append(row)
+        ks.append(s)
+        ke.append(s + 7000)
+    pc = workloads.PrefillCase("det_prefill", np.stack(rows), np.array(ks, np.int32), np.array(ke, np.int32), 512)
+    for extra in (0, 1):
+        assert_prefill_deterministic(gvr, pc, flags, extra)
