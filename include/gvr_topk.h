@@ -145,6 +145,25 @@ gvr_status topk_prefill_ex(const float* logits, int64_t row_stride, int64_t num_
                            const int32_t* row_starts, const int32_t* row_ends, int32_t k,
                            int32_t* indices, void* stream, const gvr_options* options);
 
+/*
+ * Decode top-K with hinted sampling (the request-level temporal hint of "Block-skip fast path
+ * for self-sampling GVR top-K decode", PR #18122: the previous decode step's top-K indices of
+ * each request, taken as-is, with no offset).  Identical results to topk_decode_ex: the hints
+ * only choose the sampled positions that set the bracket and the first-pass floor.
+ *   pre_idx         int32 [ceil(num_rows / next_n)][pre_idx_stride], device; row q holds the
+ *                   window indices request q selected last step, shared by its next_n rows.
+ *                   Entries outside [0, n_r) (the -1 pad, stale or garbage values) are
+ *                   skipped; duplicates are allowed.  Only the first k entries of a row are read.
+ *   pre_idx_stride  >= k (GVR_ERR_ARG otherwise); pre_idx 4-byte aligned (GVR_ERR_ALIGN),
+ *                   non-NULL when num_rows > 0 (GVR_ERR_NULL).
+ * Every other argument, the ownership rules and the errors are those of topk_decode_ex.
+ */
+gvr_status topk_decode_hinted(const float* logits, int64_t row_stride, int64_t num_rows,
+                              const int32_t* kv_lens, int32_t next_n, int32_t compress_ratio,
+                              int32_t k, const int32_t* pre_idx, int64_t pre_idx_stride,
+                              int32_t* indices, float* values, void* stream,
+                              const gvr_options* options);
+
 /* Static English text for a status code; never NULL. */
 const char* gvr_status_string(gvr_status status);
 

@@ -24,7 +24,8 @@ import ctypes
 import os
 import threading
 
-__all__ = ["topk_decode", "topk_prefill", "topk_decode_raw", "topk_prefill_raw", "plan", "Options",
+__all__ = ["topk_decode", "topk_prefill", "topk_decode_raw", "topk_decode_hinted_raw", "topk_prefill_raw", "plan",
+           "Options",
            "GvrError", "library_path", "load_library", "FLAG_FORCE_RESCUE", "FLAG_NO_FLOOR", "FLAG_ZERO_CAP",
            "FLAG_RADIX_REFINE", "FLAG_DETERMINISTIC", "FLAG_SORTED", "PATH_NAMES", "SUPPORTED_K"]
 
@@ -65,10 +66,12 @@ def _declare(lib):
     i64, i32, p = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
     lib.topk_decode.argtypes = [p, i64, i64, p, i32, i32, i32, p, p, p]
     lib.topk_decode_ex.argtypes = [p, i64, i64, p, i32, i32, i32, p, p, p, ctypes.POINTER(Options)]
+    lib.topk_decode_hinted.argtypes = [p, i64, i64, p, i32, i32, i32, p, i64, p, p, p, ctypes.POINTER(Options)]
     lib.topk_prefill.argtypes = [p, i64, i64, p, p, i32, p, p]
     lib.topk_prefill_ex.argtypes = [p, i64, i64, p, p, i32, p, p, ctypes.POINTER(Options)]
     lib.gvr_plan.argtypes = [i64, i64, i32, ctypes.POINTER(Options), i32] + [ctypes.POINTER(i32)] * 4
-    for f in (lib.topk_decode, lib.topk_decode_ex, lib.topk_prefill, lib.topk_prefill_ex, lib.gvr_plan):
+    for f in (lib.topk_decode, lib.topk_decode_ex, lib.topk_decode_hinted, lib.topk_prefill, lib.topk_prefill_ex,
+              lib.gvr_plan):
         f.restype = ctypes.c_int
     lib.gvr_status_string.argtypes = [ctypes.c_int]
     lib.gvr_status_string.restype = ctypes.c_char_p
@@ -107,6 +110,17 @@ def topk_decode_raw(logits_ptr: int, row_stride: int, num_rows: int, kv_lens_ptr
     else:
         st = lib.topk_decode_ex(logits_ptr, row_stride, num_rows, kv_lens_ptr, next_n, compress_ratio, k,
                                 indices_ptr, values_ptr, stream, ctypes.byref(options))
+    _check(st)
+
+
+def topk_decode_hinted_raw(logits_ptr: int, row_stride: int, num_rows: int, kv_lens_ptr: int, next_n: int,
+                           compress_ratio: int, k: int, pre_idx_ptr: int, pre_idx_stride: int, indices_ptr: int,
+                           values_ptr: int | None, stream: int, options: Options | None = None) -> None:
+    """``topk_decode_hinted`` on raw device addresses (enqueue only)."""
+    lib = load_library()
+    st = lib.topk_decode_hinted(logits_ptr, row_stride, num_rows, kv_lens_ptr, next_n, compress_ratio, k,
+                                pre_idx_ptr, pre_idx_stride, indices_ptr, values_ptr, stream,
+                                ctypes.byref(options) if options is not None else None)
     _check(st)
 
 
@@ -176,10 +190,12 @@ def _out(t, rows, k, dtype, device, name):
 
 
 def topk_decode(logits, kv_lens, next_n: int, compress_ratio: int, k: int, indices=None, values=None, *,
-                want_values: bool = False, stream=None, options: Options | None = None):
+                want_values: bool = False, stream=None, options: Options | None = None, pre_idx=None):
     """Decode top-K of each row of ``logits`` [rows, >=n]; returns (indices, values or None).
 
     ``logits.stride(0)`` is the row stride.  ``kv_lens`` is int32 [ceil(rows / next_n)].
+    ``pre_idx`` (optional) is int32 [ceil(rows / next_n), >= k] with unit inner stride: each
+    request's previous selection, used only as sample positions (``topk_decode_hinted``).
     """
     rows, stride = _rows_2d(logits)
     _int32_vec(kv_lens, (rows + next_n - 1) // max(next_n, 1), "kv_lens")
@@ -188,9 +204,19 @@ def topk_decode(logits, kv_lens, next_n: int, compress_ratio: int, k: int, indic
         values = _out(None, rows, k, _torch().float32, logits.device, "values")
     elif values is not None:
         values = _out(values, rows, k, _torch().float32, logits.device, "values")
-    topk_decode_raw(logits.data_ptr(), stride, rows, kv_lens.data_ptr(), next_n, compress_ratio, k,
-                    indices.data_ptr(), values.data_ptr() if values is not None else None,
-                    _stream_handle(stream), options)
+    vptr = values.data_ptr() if values is not None else None
+    if pre_idx is not None:
+        torch = _torch()
+        reqs = (rows + next_n - 1) // max(next_n, 1)
+        if (pre_idx.dtype != torch.int32 or not pre_idx.is_cuda or pre_idx.dim() != 2 or pre_idx.shape[0] != reqs
+                or pre_idx.shape[1] < k or pre_idx.stride(1) != 1):
+            raise ValueError(f"pre_idx must be a CUDA int32 tensor [{reqs}, >= {k}] with unit inner stride")
+        topk_decode_hinted_raw(logits.data_ptr(), stride, rows, kv_lens.data_ptr(), next_n, compress_ratio, k,
+                               pre_idx.data_ptr(), pre_idx.stride(0), indices.data_ptr(), vptr,
+                               _stream_handle(stream), options)
+    else:
+        topk_decode_raw(logits.data_ptr(), stride, rows, kv_lens.data_ptr(), next_n, compress_ratio, k,
+                        indices.data_ptr(), vptr, _stream_handle(stream), options)
     return indices, values
 
 

@@ -87,6 +87,8 @@ struct Params {
   const int32_t* kv_lens;     // decode
   const int32_t* row_starts;  // prefill
   const int32_t* row_ends;    // prefill
+  const int32_t* pre_idx;     // decode, optional: sample positions per request
+  int64_t pre_stride;         // row stride of pre_idx (>= k)
   int32_t* indices;
   float* values;              // nullable
   int32_t* row_stats;         // nullable, [rows][4]
@@ -494,9 +496,11 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   // row_stride < 2^31 and every count below fits in 32 bits.
   const uint32_t stride = uint32_t(p.row_stride);
   uint32_t a = 0, nv = 0;
+  const int32_t* hints = nullptr;  // this row's sample positions (its request's hint row)
   if (p.mode == MODE_DECODE) {
     const uint32_t nn = uint32_t(p.next_n);
     const uint32_t req = row / nn;
+    if (p.pre_idx) hints = p.pre_idx + int64_t(req) * p.pre_stride;
     const int32_t kv = p.kv_lens[req];
     if (kv >= p.next_n) nv = (uint32_t(kv) - nn + (row - req * nn) + 1u) / uint32_t(p.compress_ratio);
     nv = nv < stride ? nv : stride;
@@ -703,12 +707,26 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   const uint32_t sq = (nv - 64u) / (nblk - 1u), sr = (nv - 64u) % (nblk - 1u);
   const uint32_t run_start = uint32_t(lane) * sq + (uint32_t(lane) * sr) / (nblk - 1u);
   float sv[KPT];
+  if (hints) {
+    // Hinted sampling: the k positions of the request's previous selection.  Any content is
+    // accepted: positions outside [0, nv) (the -1 pad, stale or garbage entries) are skipped,
+    // and duplicates only repeat a sample, so exactness never depends on the hints.
+    int32_t h[KPT];
 #pragma unroll
-  for (int q = 0; q < KPT; ++q) {  // the 64 samples of a run are 64 consecutive threads' slots
-    const uint32_t i = uint32_t(q * T + tid);
-    const uint32_t blk = i >> 6;
-    const uint32_t s = __shfl_sync(FULL_MASK, run_start, blk & 31u);
-    sv[q] = i < uint32_t(k) ? __ldg(rowp + a + s + (i & 63u)) : qnan;
+    for (int q = 0; q < KPT; ++q) {
+      const int i = q * T + tid;
+      h[q] = i < k ? __ldg(hints + i) : -1;
+    }
+#pragma unroll
+    for (int q = 0; q < KPT; ++q) sv[q] = uint32_t(h[q]) < nv ? __ldg(rowp + a + uint32_t(h[q])) : qnan;
+  } else {
+#pragma unroll
+    for (int q = 0; q < KPT; ++q) {  // the 64 samples of a run are 64 consecutive threads' slots
+      const uint32_t i = uint32_t(q * T + tid);
+      const uint32_t blk = i >> 6;
+      const uint32_t s = __shfl_sync(FULL_MASK, run_start, blk & 31u);
+      sv[q] = i < uint32_t(k) ? __ldg(rowp + a + s + (i & 63u)) : qnan;
+    }
   }
   // The first ring stages go in flight right behind the samples, one lane of warp 0 per stage.
   if (warp == 0)
@@ -789,7 +807,12 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   int fpart = -1;         // bin(thr): the one partially counted bin; -1 = no floor
   if (path == PATH_REFINE) {
     sc = __fdiv_rn(float(NB), __fsub_rn(gmax, gmin));
-    if (!(p.flags & FLAG_NO_FLOOR)) {
+    if (hints && !(p.flags & FLAG_NO_FLOOR)) {
+      // Hinted samples sit near the top of the row: the floor is the smallest of them, so the
+      // first pass counts every score that reaches the previous selection's lowest score.
+      thr = gmin;
+      fpart = 0;
+    } else if (!(p.flags & FLAG_NO_FLOOR)) {
       // mu = k*k/nv samples are expected above tau; keep mu + 3 sqrt(mu) + 6 above the floor
       const float mu = float(k) * float(k) / float(nv);
       const float want_f = mu + 3.0f * sqrtf(mu) + 6.0f;

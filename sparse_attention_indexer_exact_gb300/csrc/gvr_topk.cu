@@ -198,6 +198,39 @@ gvr_status topk_decode_ex(const float* logits, int64_t row_stride, int64_t num_r
   return launch(prm, num_rows, options, stream);
 }
 
+gvr_status topk_decode_hinted(const float* logits, int64_t row_stride, int64_t num_rows,
+                              const int32_t* kv_lens, int32_t next_n, int32_t compress_ratio,
+                              int32_t k, const int32_t* pre_idx, int64_t pre_idx_stride,
+                              int32_t* indices, float* values, void* stream,
+                              const gvr_options* options) {
+  gvr_status s = check_common(row_stride, num_rows, k, options);
+  if (s != GVR_OK) return s;
+  if (next_n < 1 || compress_ratio < 1 || pre_idx_stride < k) return GVR_ERR_ARG;
+  if (num_rows == 0) return GVR_OK;
+  if (!pre_idx) return GVR_ERR_NULL;
+  if (!aligned(pre_idx, 4)) return GVR_ERR_ALIGN;
+  // the plain decode checks, then the same launch with hinted sampling
+  if (!logits || !kv_lens || !indices) return GVR_ERR_NULL;
+  if (!aligned(logits, 16) || !aligned(indices, 4) || !aligned(kv_lens, 4) ||
+      (values && !aligned(values, 4)))
+    return GVR_ERR_ALIGN;
+  gvr::Params prm = {};
+  prm.logits = logits;
+  prm.row_stride = row_stride;
+  prm.kv_lens = kv_lens;
+  prm.pre_idx = pre_idx;
+  prm.pre_stride = pre_idx_stride;
+  prm.indices = indices;
+  prm.values = values;
+  prm.row_stats = options ? options->row_stats : nullptr;
+  prm.next_n = next_n;
+  prm.compress_ratio = compress_ratio;
+  prm.k = k;
+  prm.mode = gvr::MODE_DECODE;
+  prm.flags = options ? options->flags : 0;
+  return launch(prm, num_rows, options, stream);
+}
+
 gvr_status topk_decode(const float* logits, int64_t row_stride, int64_t num_rows,
                        const int32_t* kv_lens, int32_t next_n, int32_t compress_ratio, int32_t k,
                        int32_t* indices, float* values, void* stream) {

@@ -84,6 +84,28 @@ def test_decode_argument_errors(lib):
     assert call(num_rows=0, logits=None, indices=None, kv_lens=None) == 0  # empty batch: no-op
 
 
+def test_hinted_argument_errors(lib):
+    f = lib.topk_decode_hinted
+    ok = [ALIGNED, 1024, 4, ALIGNED, 1, 1, K, ALIGNED, K, ALIGNED, None, None, None]
+    names = ["logits", "row_stride", "num_rows", "kv_lens", "next_n", "cr", "k", "pre_idx", "pre_stride",
+             "indices", "values", "stream", "options"]
+
+    def call(**kw):
+        args = list(ok)
+        for key, v in kw.items():
+            args[names.index(key)] = v
+        return f(*args)
+
+    assert call(pre_idx=None) == 1
+    assert call(pre_idx=ALIGNED + 2) == 2
+    assert call(pre_stride=K - 1) == 5
+    assert call(logits=None) == 1
+    assert call(logits=ALIGNED + 4) == 2
+    assert call(k=300) == 4
+    assert call(next_n=0) == 5
+    assert call(num_rows=0, logits=None, indices=None, kv_lens=None, pre_idx=None) == 0
+
+
 def test_prefill_argument_errors(lib):
     f = lib.topk_prefill
     assert f(None, 1024, 4, ALIGNED, ALIGNED, K, ALIGNED, None) == 1
