@@ -119,6 +119,12 @@ struct alignas(16) Smem {
   int32_t cand_j[CAP];
   uint32_t wsum[2][8];
   float wmin[8];
+  float whmin[8], whmax[8];        // hinted sampling: smallest / largest finite hinted score per warp
+  uint32_t whcnt[8];               // hinted sampling: in-window hints per warp
+  float hpart_min, hpart_max;      // this CTA's share of the hints (read by the whole cluster)
+  uint32_t hpart_cnt;
+  float hagg_min, hagg_max;        // the cluster's hints
+  uint32_t hagg_cnt;
   float wmax[8];
   float4 tail;                     // the partial last vector of the window, NaN-padded
   Crossing cross;
@@ -492,15 +498,30 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     mbar_init_fence();
   }
 
+  // Hinted sampling: each CTA of the cluster reads its share of the request's hint row before
+  // anything else (it does not depend on the row's length), so the latency overlaps the
+  // geometry load; the cluster combines the shares after sampling.
+  const int32_t* hints = (p.mode == MODE_DECODE && p.pre_idx)
+                             ? p.pre_idx + int64_t(row / uint32_t(p.next_n)) * p.pre_stride
+                             : nullptr;
+  int32_t hpos[KPT];
+  if (hints) {
+    const int hs = (k + int(cs) - 1) / int(cs);  // hints per CTA
+#pragma unroll
+    for (int q = 0; q < KPT; ++q) {
+      const int f = q * T + tid;
+      const int i = int(rank) * hs + f;
+      hpos[q] = (f < hs && i < k) ? __ldg(hints + i) : -1;
+    }
+  }
+
   // ---------------------------------------------------------------- row geometry
   // row_stride < 2^31 and every count below fits in 32 bits.
   const uint32_t stride = uint32_t(p.row_stride);
   uint32_t a = 0, nv = 0;
-  const int32_t* hints = nullptr;  // this row's sample positions (its request's hint row)
   if (p.mode == MODE_DECODE) {
     const uint32_t nn = uint32_t(p.next_n);
     const uint32_t req = row / nn;
-    if (p.pre_idx) hints = p.pre_idx + int64_t(req) * p.pre_stride;
     const int32_t kv = p.kv_lens[req];
     if (kv >= p.next_n) nv = (uint32_t(kv) - nn + (row - req * nn) + 1u) / uint32_t(p.compress_ratio);
     nv = nv < stride ? nv : stride;
@@ -707,26 +728,20 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   const uint32_t sq = (nv - 64u) / (nblk - 1u), sr = (nv - 64u) % (nblk - 1u);
   const uint32_t run_start = uint32_t(lane) * sq + (uint32_t(lane) * sr) / (nblk - 1u);
   float sv[KPT];
+#pragma unroll
+  for (int q = 0; q < KPT; ++q) {  // the 64 samples of a run are 64 consecutive threads' slots
+    const uint32_t i = uint32_t(q * T + tid);
+    const uint32_t blk = i >> 6;
+    const uint32_t s = __shfl_sync(FULL_MASK, run_start, blk & 31u);
+    sv[q] = i < uint32_t(k) ? __ldg(rowp + a + s + (i & 63u)) : qnan;
+  }
+  // Hinted sampling adds the k scores at the request's previous selection.  Any content is
+  // accepted: positions outside [0, nv) (the -1 pad, stale or garbage entries) are skipped and
+  // duplicates only repeat a score, so exactness never depends on the hints.
+  float sh[KPT];
   if (hints) {
-    // Hinted sampling: the k positions of the request's previous selection.  Any content is
-    // accepted: positions outside [0, nv) (the -1 pad, stale or garbage entries) are skipped,
-    // and duplicates only repeat a sample, so exactness never depends on the hints.
-    int32_t h[KPT];
 #pragma unroll
-    for (int q = 0; q < KPT; ++q) {
-      const int i = q * T + tid;
-      h[q] = i < k ? __ldg(hints + i) : -1;
-    }
-#pragma unroll
-    for (int q = 0; q < KPT; ++q) sv[q] = uint32_t(h[q]) < nv ? __ldg(rowp + a + uint32_t(h[q])) : qnan;
-  } else {
-#pragma unroll
-    for (int q = 0; q < KPT; ++q) {  // the 64 samples of a run are 64 consecutive threads' slots
-      const uint32_t i = uint32_t(q * T + tid);
-      const uint32_t blk = i >> 6;
-      const uint32_t s = __shfl_sync(FULL_MASK, run_start, blk & 31u);
-      sv[q] = i < uint32_t(k) ? __ldg(rowp + a + s + (i & 63u)) : qnan;
-    }
+    for (int q = 0; q < KPT; ++q) sh[q] = uint32_t(hpos[q]) < nv ? __ldg(rowp + a + uint32_t(hpos[q])) : qnan;
   }
   // The first ring stages go in flight right behind the samples, one lane of warp 0 per stage.
   if (warp == 0)
@@ -770,11 +785,48 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     lmin = fminf(lmin, __shfl_xor_sync(FULL_MASK, lmin, o));
     lmax = fmaxf(lmax, __shfl_xor_sync(FULL_MASK, lmax, o));
   }
+  // Hinted: the largest finite hinted score widens GMAX (the hints hold the row's top), and the
+  // smallest hinted score with the count of in-window hints can raise the floor below.
+  if (hints) {
+    float hmin = INFINITY, hmax = -INFINITY;
+    uint32_t hcnt = 0;
+#pragma unroll
+    for (int q = 0; q < KPT; ++q) {
+      if (!isnan(sh[q])) {
+        hmin = fminf(hmin, sh[q]);
+        ++hcnt;
+      }
+      if (isfinite(sh[q])) hmax = fmaxf(hmax, sh[q]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      hmin = fminf(hmin, __shfl_xor_sync(FULL_MASK, hmin, o));
+      hmax = fmaxf(hmax, __shfl_xor_sync(FULL_MASK, hmax, o));
+      hcnt += __shfl_xor_sync(FULL_MASK, hcnt, o);
+    }
+    if (lane == 0) {
+      S.whmin[warp] = hmin;
+      S.whmax[warp] = hmax;
+      S.whcnt[warp] = hcnt;
+    }
+  }
   if (lane == 0) {
     S.wmin[warp] = lmin;
     S.wmax[warp] = lmax;
   }
   __syncthreads();
+  if (hints && tid == 0) {  // this CTA's share, published by the barrier below
+    float hmin = INFINITY, hmax = -INFINITY;
+    uint32_t hcnt = 0;
+    for (int w = 0; w < NW; ++w) {
+      hmin = fminf(hmin, S.whmin[w]);
+      hmax = fmaxf(hmax, S.whmax[w]);
+      hcnt += S.whcnt[w];
+    }
+    S.hpart_min = hmin;
+    S.hpart_max = hmax;
+    S.hpart_cnt = hcnt;
+  }
   // Every CTA's totals and rank 0's counters are now zero; no CTA of the cluster adds to them
   // before it has waited on this (split) barrier, right before its first remote update.
   cluster_arrive();
@@ -795,6 +847,31 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     gmin = fminf(gmin, S.wmin[w]);
     gmax = fmaxf(gmax, S.wmax[w]);
   }
+  if (hints) {  // every CTA's share of the hints, read from the cluster after the barrier
+    wait_init();
+    if (warp == 0) {
+      float hmin = INFINITY, hmax = -INFINITY;
+      uint32_t hcnt = 0;
+      if (uint32_t(lane) < cs) {
+        hmin = __uint_as_float(dsmem_ld_u32(dsmem_map(smem_u32(&S.hpart_min), uint32_t(lane))));
+        hmax = __uint_as_float(dsmem_ld_u32(dsmem_map(smem_u32(&S.hpart_max), uint32_t(lane))));
+        hcnt = dsmem_ld_u32(dsmem_map(smem_u32(&S.hpart_cnt), uint32_t(lane)));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        hmin = fminf(hmin, __shfl_xor_sync(FULL_MASK, hmin, o));
+        hmax = fmaxf(hmax, __shfl_xor_sync(FULL_MASK, hmax, o));
+        hcnt += __shfl_xor_sync(FULL_MASK, hcnt, o);
+      }
+      if (lane == 0) {
+        S.hagg_min = hmin;
+        S.hagg_max = hmax;
+        S.hagg_cnt = hcnt;
+      }
+    }
+    __syncthreads();
+    gmax = fmaxf(gmax, S.hagg_max);
+  }
   gmin = __fadd_rn(gmin, 0.0f);  // -0 -> +0, so every CTA holds the same bits
   const bool bracket_ok = isfinite(gmin) && isfinite(gmax) && gmin < gmax;
 
@@ -807,12 +884,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   int fpart = -1;         // bin(thr): the one partially counted bin; -1 = no floor
   if (path == PATH_REFINE) {
     sc = __fdiv_rn(float(NB), __fsub_rn(gmax, gmin));
-    if (hints && !(p.flags & FLAG_NO_FLOOR)) {
-      // Hinted samples sit near the top of the row: the floor is the smallest of them, so the
-      // first pass counts every score that reaches the previous selection's lowest score.
-      thr = gmin;
-      fpart = 0;
-    } else if (!(p.flags & FLAG_NO_FLOOR)) {
+    if (!(p.flags & FLAG_NO_FLOOR)) {
       // mu = k*k/nv samples are expected above tau; keep mu + 3 sqrt(mu) + 6 above the floor
       const float mu = float(k) * float(k) / float(nv);
       const float want_f = mu + 3.0f * sqrtf(mu) + 6.0f;
@@ -834,6 +906,17 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       __syncthreads();
       thr = S.vthr;
       fpart = S.fpart;
+      if (hints) {
+        // k in-window hints at k distinct positions put at least k scores at or above the
+        // smallest hinted score, so a floor there needs no second pass (with fewer distinct
+        // positions the second pass still makes the counts exact).
+        const float hm = __fadd_rn(S.hagg_min, 0.0f);  // -0 -> +0
+        const uint32_t hc = S.hagg_cnt;
+        if (hc == uint32_t(k) && hm > thr) {
+          thr = hm;
+          fpart = value_bin(hm, gmin, sc);
+        }
+      }
     }
   }
 
@@ -888,39 +971,42 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       // floor) adds its hits with one atomic when they all share a bin, else one per distinct
       // bin and score slot.
       const bool dense = __any_sync(FULL_MASK, nhit > uint32_t(SPARSE_MAX));
-      uint32_t bmin = 0xffffffffu, bmax = 0u;
-      for (uint32_t rest = bits; rest;) {
-        const int j = __ffs(rest) - 1;
-        rest &= rest - 1;
-        float4 v = vv[0];
-#pragma unroll
-        for (int i = 1; i < VPS; ++i)
-          if ((j >> 2) == i) v = vv[i];
-        const float e = f4_get(v, j & 3);
-        const uint32_t b = uint32_t(value_bin(e, gmin, sc));
-        if (dense) {
-          bmin = min(bmin, b);
-          bmax = max(bmax, b);
-        } else {
-          atomicAdd(&S.hist[b], 1u);
-        }
-        if (at < uint32_t(LIST_SEG)) {
-          seg_v[at] = e;
-          seg_j[at] = 4 * (c0 + (j >> 2) * T + tid) + (j & 3) - lead;
-        }
-        ++at;
-      }
       if (dense) {
+        uint32_t bj[4 * VPS];
+        uint32_t bmin = 0xffffffffu, bmax = 0u;
+#pragma unroll
+        for (int j = 0; j < 4 * VPS; ++j) {
+          bj[j] = uint32_t(value_bin(f4_get(vv[j >> 2], j & 3), gmin, sc));
+          if ((bits >> j) & 1u) {
+            bmin = min(bmin, bj[j]);
+            bmax = max(bmax, bj[j]);
+          }
+        }
         bmin = __reduce_min_sync(FULL_MASK, bmin);
         bmax = __reduce_max_sync(FULL_MASK, bmax);
         if (bmin == bmax) {
           if (lane == 0) atomicAdd(&S.hist[bmin], wtot);
         } else {
 #pragma unroll
-          for (int j = 0; j < 4 * VPS; ++j) {
-            const bool hit = (bits >> j) & 1u;
-            hist_add(S.hist, hit, hit ? uint32_t(value_bin(stage_score(slot, c0, j), gmin, sc)) : 0u);
+          for (int j = 0; j < 4 * VPS; ++j) hist_add(S.hist, (bits >> j) & 1u, bj[j]);
+        }
+      }
+      // List the hits (a dense warp only until its segment is full; the counts above are exact).
+      if (!dense || wlist - wtot < uint32_t(LIST_SEG)) {
+        for (uint32_t rest = bits; rest;) {
+          const int j = __ffs(rest) - 1;
+          rest &= rest - 1;
+          float4 v = vv[0];
+#pragma unroll
+          for (int i = 1; i < VPS; ++i)
+            if ((j >> 2) == i) v = vv[i];
+          const float e = f4_get(v, j & 3);
+          if (!dense) atomicAdd(&S.hist[value_bin(e, gmin, sc)], 1u);
+          if (at < uint32_t(LIST_SEG)) {
+            seg_v[at] = e;
+            seg_j[at] = 4 * (c0 + (j >> 2) * T + tid) + (j & 3) - lead;
           }
+          ++at;
         }
       }
     });
