@@ -214,6 +214,116 @@ def run_reference(args, case, ws, rank):
     return 0
 
 
+def prefill_algorithmic_bytes(case) -> int:
+    """Prefill: each score of a window that needs a selection read once, K indices written,
+    and the two window bounds read per row."""
+    n = case.window_lengths().astype(np.int64)
+    return int(np.where(n > case.k, 4 * n, 0).sum()) + case.rows * case.k * 4 + 8 * case.rows
+
+
+def run_sweep(args):
+    """Every sweep cell (BS x N x K, decode and prefill), cold and warm L2, one JSON line each;
+    then the tail check on the adversarial row and its variants."""
+    import torch
+    import workloads
+    import sparse_attention_indexer_exact_gb300 as gvr
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (no CPU fallback exists)")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    gvr.load_library()
+    stream = torch.cuda.current_stream()
+    scrub = torch.empty(512 << 20, dtype=torch.uint8, device=dev)  # > L2: evicts the scores
+    peak, _ = measured_peak_hbm()
+
+    def measure(launch, reps=32, warm_calls=100):
+        for _ in range(3):
+            launch(stream.cuda_stream)
+        torch.cuda.synchronize()
+        cold = []
+        for r in range(reps):
+            scrub.fill_(r & 255)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            launch(stream.cuda_stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            cold.append(e0.elapsed_time(e1) * 1e3)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            h = torch.cuda.current_stream().cuda_stream
+            for _ in range(warm_calls):
+                launch(h)
+        g.replay()
+        torch.cuda.synchronize()
+        warm = []
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            warm.append(e0.elapsed_time(e1) * 1e3 / warm_calls)
+        cold.sort()
+        return cold[len(cold) // 2], cold[min(len(cold) - 1, int(0.99 * len(cold)))], cold[-1], min(warm)
+
+    def emit(tag, case, nbytes, launch):
+        med, p99, mx, warm = measure(launch)
+        print(json.dumps({
+            "sweep": tag, "bs": case.rows, "n": int(case.meta.get("n", 0)), "k": case.k,
+            "cold_us": {"median": med, "p99": p99, "max": mx}, "warm_us": warm,
+            "rows_per_s_cold": case.rows / (med * 1e-6), "us_per_row_cold": med / case.rows,
+            "algorithmic_bytes": nbytes, "gbs_cold": nbytes / med / 1e3, "gbs_warm_effective": nbytes / warm / 1e3,
+            "frac_of_8tbs": nbytes / med / 1e3 / NOMINAL_HBM_GBS, "frac_of_measured": nbytes / med / 1e3 / peak,
+            "reachable_60pct": nbytes >= 36e6}), flush=True)
+        return med
+
+    for n in (16384, 32768, 65536, 131072):
+        for bs in (1, 4, 16, 64, 256):
+            dcase = workloads.sweep_decode(bs, n, 512)
+            lg = torch.from_numpy(dcase.logits).to(dev)
+            for k in (512, 1024, 2048):
+                dc = workloads.DecodeCase(dcase.name, dcase.logits, dcase.kv_lens, 1, 1, k, {"n": n})
+                kv = torch.from_numpy(dc.kv_lens).to(dev)
+                idx = torch.empty((bs, k), dtype=torch.int32, device=dev)
+                emit("decode", dc, algorithmic_bytes(dc, False),
+                     lambda h, lg=lg, kv=kv, idx=idx, k=k: gvr.topk_decode_raw(
+                         lg.data_ptr(), lg.stride(0), bs, kv.data_ptr(), 1, 1, k, idx.data_ptr(), None, h))
+                ks = torch.from_numpy((np.arange(bs) % 4).astype(np.int32)).to(dev)
+                ke = torch.full((bs,), n, dtype=torch.int32, device=dev)
+                pc = workloads.PrefillCase(dcase.name, dcase.logits, (np.arange(bs) % 4).astype(np.int32),
+                                           np.full(bs, n, np.int32), k, {"n": n})
+                emit("prefill", pc, prefill_algorithmic_bytes(pc),
+                     lambda h, lg=lg, ks=ks, ke=ke, idx=idx, k=k: gvr.topk_prefill_raw(
+                         lg.data_ptr(), lg.stride(0), bs, ks.data_ptr(), ke.data_ptr(), k, idx.data_ptr(), h))
+            del lg
+    # tail check: each adversarial variant against a row of the same shape drawn from N(0,1)
+    base = workloads.adversarial_row("base")
+    g = np.random.default_rng(1049)
+    plain = base.logits.copy()
+    n0 = int(base.row_lengths()[0])
+    plain[0, :n0] = g.standard_normal(n0).astype(np.float32)
+    ref_case = workloads.DecodeCase("adversarial_shape_normal", plain, base.kv_lens, 1, base.compress_ratio, base.k,
+                                    {"n": n0})
+
+    def adv_launch(case):
+        lg = torch.from_numpy(case.logits).to(dev)
+        kv = torch.from_numpy(case.kv_lens).to(dev)
+        idx = torch.empty((case.rows, case.k), dtype=torch.int32, device=dev)
+        return lambda h: gvr.topk_decode_raw(lg.data_ptr(), lg.stride(0), case.rows, kv.data_ptr(), case.next_n,
+                                             case.compress_ratio, case.k, idx.data_ptr(), None, h)
+
+    ref_med = emit("tail_reference_normal_row", ref_case, algorithmic_bytes(ref_case, False), adv_launch(ref_case))
+    for v in workloads.ADVERSARIAL_VARIANTS:
+        c = workloads.adversarial_row(v)
+        c.meta["n"] = n0
+        med = emit(f"tail_{v}", c, algorithmic_bytes(c, False), adv_launch(c))
+        print(json.dumps({"tail_check": v, "ratio_to_normal_row": med / ref_med, "within_2x": med <= 2 * ref_med}),
+              flush=True)
+    return 0
+
+
 def config_block(case, ws):
     return {"workload": f"decode batch: {case.meta['workload']}", "rows_per_gpu": case.rows,
             "global_rows": case.rows * ws, "k": case.k, "row_stride": case.row_stride,
@@ -233,8 +343,12 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--values", action="store_true", help="also write the fp32 values output")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the headline line: every sweep cell and the adversarial tail check")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.sweep:
+        return run_sweep(args)
 
     import workloads
     ws, rank, local = dist_env()

@@ -105,7 +105,10 @@ enum {
   /* Deterministic ties, and each long row's k indices ordered by (score descending, window
    * index ascending), -0 equal to +0.  Rows with nv <= k keep the identity order 0..nv-1 and
    * the -1 pad. */
-  GVR_FLAG_SORTED = 32
+  GVR_FLAG_SORTED = 32,
+  /* diagnostics: a crossing bin over the candidate buffer always takes the digit passes over
+   * the row (no selection over per-CTA lists) */
+  GVR_FLAG_STREAM_RESCUE = 64
 };
 
 typedef struct gvr_options {
@@ -130,8 +133,11 @@ enum {
                                    list overflowed: exact digit passes over the row, seeded
                                    with the crossing bin */
   GVR_PATH_RESCUE_FORCED = 4,   /* GVR_FLAG_FORCE_RESCUE */
-  GVR_PATH_REFINE_CLUSTER = 5   /* crossing bin exceeded the candidate buffer, every CTA's list
+  GVR_PATH_REFINE_CLUSTER = 5,  /* crossing bin exceeded the candidate buffer, every CTA's list
                                    held its counted scores: exact digit passes over the lists */
+  GVR_PATH_REFINE_RELIST = 6    /* crossing bin exceeded the candidate buffer and a first-pass
+                                   list overflowed: one more read of the row lists the crossing
+                                   bin and above per CTA, digit passes over those lists */
 };
 
 /* topk_decode with tuning/diagnostic options (NULL = automatic, identical to topk_decode). */

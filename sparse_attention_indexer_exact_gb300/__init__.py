@@ -27,7 +27,8 @@ import threading
 __all__ = ["topk_decode", "topk_prefill", "topk_decode_raw", "topk_decode_hinted_raw", "topk_prefill_raw", "plan",
            "Options",
            "GvrError", "library_path", "load_library", "FLAG_FORCE_RESCUE", "FLAG_NO_FLOOR", "FLAG_ZERO_CAP",
-           "FLAG_RADIX_REFINE", "FLAG_DETERMINISTIC", "FLAG_SORTED", "PATH_NAMES", "SUPPORTED_K"]
+           "FLAG_RADIX_REFINE", "FLAG_DETERMINISTIC", "FLAG_SORTED", "FLAG_STREAM_RESCUE", "PATH_NAMES",
+           "SUPPORTED_K"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libgvrtopk.so")
@@ -35,9 +36,9 @@ _lock = threading.Lock()
 _lib = None
 
 FLAG_FORCE_RESCUE, FLAG_NO_FLOOR, FLAG_ZERO_CAP, FLAG_RADIX_REFINE = 1, 2, 4, 8
-FLAG_DETERMINISTIC, FLAG_SORTED = 16, 32
+FLAG_DETERMINISTIC, FLAG_SORTED, FLAG_STREAM_RESCUE = 16, 32, 64
 PATH_NAMES = {-1: "device_error", 0: "short", 1: "refine", 2: "rescue_bracket", 3: "rescue_overflow",
-              4: "rescue_forced", 5: "refine_cluster"}
+              4: "rescue_forced", 5: "refine_cluster", 6: "refine_relist"}
 SUPPORTED_K = (512, 1024, 2048)
 EXPORTED_SYMBOLS = ("topk_decode", "topk_prefill", "topk_decode_ex", "topk_prefill_ex", "gvr_status_string",
                     "gvr_plan")

@@ -69,7 +69,8 @@ enum : int32_t {
   FLAG_ZERO_CAP = 4,
   FLAG_RADIX_REFINE = 8,
   FLAG_DETERMINISTIC = 16,
-  FLAG_SORTED = 32
+  FLAG_SORTED = 32,
+  FLAG_STREAM_RESCUE = 64
 };
 enum : int32_t {
   PATH_DEVICE_ERROR = -1,
@@ -78,7 +79,8 @@ enum : int32_t {
   PATH_RESCUE_BRACKET = 2,
   PATH_RESCUE_OVERFLOW = 3,
   PATH_RESCUE_FORCED = 4,
-  PATH_REFINE_CLUSTER = 5
+  PATH_REFINE_CLUSTER = 5,
+  PATH_REFINE_RELIST = 6
 };
 
 struct Params {
@@ -134,6 +136,9 @@ struct alignas(16) Smem {
   uint32_t kmin_loc, kmax_loc;     // rescue: smallest / largest key of this CTA's matching scores
   uint32_t list_n[THREADS / 32];   // scores each warp appended to its segment (may exceed LIST_SEG)
   uint32_t unlisted;               // CTAs of the cluster whose list overflowed (each pushes 1)
+  uint32_t relist_n;               // scores of the crossing bin and above listed again
+  uint32_t relist_bad;             // CTAs of the cluster whose second list overflowed
+  uint32_t klo, khi;               // order keys bounding the crossing bin's members
   uint32_t ctr_win, ctr_cand;      // this CTA's slot counters (refine path)
   uint32_t gctr_above, gctr_cand;  // rank 0: hands out each CTA's winner / candidate slot bases
   uint32_t base_above, base_cand;  // this CTA's slot bases
@@ -762,6 +767,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     S.rc_win = S.rc_tie = 0;
     S.tout = S.err = 0;
     S.unlisted = 0;
+    S.relist_n = S.relist_bad = 0;
     S.cross = Crossing{};
     S.dsel = S.dabove = S.dcnt = 0;
   }
@@ -1061,7 +1067,8 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     if (cr.total < uint32_t(k))
       path = PATH_RESCUE_OVERFLOW;  // NaN in the window (out of contract)
     else if (cr.m > cap)  // every list complete: the cluster selects among the listed scores
-      path = (rounds == 1 && S.unlisted == 0) ? PATH_REFINE_CLUSTER : PATH_RESCUE_OVERFLOW;
+      path = (rounds == 1 && S.unlisted == 0 && !(p.flags & FLAG_STREAM_RESCUE)) ? PATH_REFINE_CLUSTER
+                                                                                   : PATH_RESCUE_OVERFLOW;
   }
   // Candidates are the scores of the crossing bin that were counted: after one pass, the scores
   // >= thr (this only matters when the crossing is the partial floor bin).
@@ -1197,6 +1204,44 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     return;
   }
 
+  // ---------------------------------------------------------------- re-list
+  // The crossing bin holds more candidates than the buffer and some CTA's first-pass list
+  // overflowed: every CTA reads its share once more and lists only the scores of the crossing
+  // bin and above (one list per CTA).  When every such list fits, the selection below runs over
+  // the lists; otherwise it reads the row.
+  if (path == PATH_RESCUE_OVERFLOW && cr.total >= uint32_t(k) && !(p.flags & FLAG_STREAM_RESCUE)) {
+    if (warp == 0) {
+      const float t = cr.bin > 0 ? floor_value(cr.bin, gmin, sc) : -INFINITY;
+      if (lane == 0) S.vthr = t;
+    }
+    __syncthreads();
+    const float tb = fmaxf(S.vthr, cthr);  // scores >= tb: the crossing bin's members and above
+    stream_pass(false, [&](uint32_t slot, int32_t c0) {
+      each_lane(slot, c0, [&](float e, int32_t g, bool valid, int l) {
+        const bool hit = valid && e >= tb;
+        if (__any_sync(FULL_MASK, hit)) {
+          const uint32_t at = warp_alloc_local(&S.relist_n, hit);
+          if (hit && at < uint32_t(LIST_CAP)) {
+            S.list_v[at] = e;
+            S.list_j[at] = 4 * g + l - lead;
+          }
+        }
+      });
+    });
+    rounds += 10;  // diagnostics: the share was read again
+    if (tid == 0) {
+      const bool fits = S.relist_n <= uint32_t(LIST_CAP);
+#pragma unroll
+      for (int w = 0; w < NW; ++w) S.list_n[w] = 0;
+      S.list_n[0] = fits ? S.relist_n : 0u;  // one contiguous list
+      if (!fits)
+        for (uint32_t c = 0; c < cs; ++c) dsmem_red_add(dsmem_map(smem_u32(&S.relist_bad), c), 1u);
+    }
+    csync();
+    report_timeout();
+    if (S.relist_bad == 0) path = PATH_REFINE_RELIST;
+  }
+
   // ---------------------------------------------------------------- rescue: cluster radix select
   // Exact selection over the 32-bit order-preserving keys, one 8-bit digit per pass from the
   // top.  Each pass counts the digits of the keys that still match the chosen prefix, pushes
@@ -1208,8 +1253,8 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   // crossing bin take part, k - above of them are needed, and every score of a higher bin is a
   // winner.  When every CTA's list held its counted scores, the passes read the lists instead
   // of the row.
-  const bool seeded = path == PATH_REFINE_CLUSTER || (path == PATH_RESCUE_OVERFLOW && cr.total >= uint32_t(k));
-  const bool from_lists = path == PATH_REFINE_CLUSTER;
+  const bool from_lists = path == PATH_REFINE_CLUSTER || path == PATH_REFINE_RELIST;
+  const bool seeded = from_lists || (path == PATH_RESCUE_OVERFLOW && cr.total >= uint32_t(k));
   const int bstar = cr.bin;
   uint32_t* dloc = S.hist;  // this CTA's digit counts
   auto dtot = [&](int buf) -> uint32_t* { return S.tot + 256 * buf; };
@@ -1240,8 +1285,8 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     bool ge;
   };
   int rpass = 0;  // digit-total buffers alternate over the passes of every selection
-  auto radix_select = [&](auto&& sel, uint32_t need0, uint32_t fixed, int shift0) -> Sel {
-    Sel r{fixed, fixed, need0, 0u, 0u, false};
+  auto radix_select = [&](auto&& sel, uint32_t need0, uint32_t prefix0, uint32_t pmask0, int shift0) -> Sel {
+    Sel r{prefix0, pmask0, need0, 0u, 0u, false};
     for (int shift = shift0; shift >= 0; shift -= 8) {
       const int buf = rpass++ & 1;
       for (int i = tid; i < 256; i += T) dloc[i] = 0;
@@ -1358,11 +1403,33 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     }
     return r;
   };
+  // Seeded, every member's key lies in [klo, khi] (the crossing bin's value range, and >= cthr):
+  // the digits that klo and khi share are fixed before the first pass (at least one pass runs).
+  uint32_t tau_prefix = 0, tau_mask = 0;
+  int tau_shift = 24;
+  if (seeded) {
+    if (warp == 0) {
+      const float lo = bstar > 0 ? floor_value(bstar, gmin, sc) : -INFINITY;
+      const float hi = bstar < NB - 1 ? floor_value(bstar + 1, gmin, sc) : INFINITY;
+      if (lane == 0) {
+        S.klo = order_key(fmaxf(lo, cthr));
+        S.khi = bstar < NB - 1 ? order_key(hi) - 1u : 0xffffffffu;
+      }
+    }
+    __syncthreads();
+    const uint32_t klo = S.klo, khi = S.khi;
+    const int dfix = klo <= khi ? min(__clz(klo ^ khi) / 8, 3) : 0;
+    if (dfix > 0) {
+      tau_mask = 0xffffffffu << (32 - 8 * dfix);
+      tau_prefix = klo & tau_mask;
+      tau_shift = 24 - 8 * dfix;
+    }
+  }
   // tau: the k - above largest order keys among the members
   const Sel t = radix_select([&](float e, int32_t, uint32_t& key) {
     key = order_key(e);
     return bin_class(e) == 0;
-  }, seeded ? uint32_t(k) - cr.above : uint32_t(k), 0u, 24);
+  }, seeded ? uint32_t(k) - cr.above : uint32_t(k), tau_prefix, tau_mask, tau_shift);
   const uint32_t prefix = t.prefix, pmask = t.pmask;
   const bool ge = t.ge;
   const uint32_t my_win = (seeded ? cr.my_above : 0u) + t.my_above;  // this CTA's scores above tau
@@ -1379,7 +1446,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     ix = radix_select([&](float e, int32_t jw, uint32_t& key) {
       key = ~uint32_t(jw);
       return bin_class(e) == 0 && order_key(e) == prefix;
-    }, nties, fixed, 8 * (digits - 1));
+    }, nties, fixed, fixed, 8 * (digits - 1));
   }
   auto index_selected = [&](int32_t jw) -> bool {
     const uint32_t key = ~uint32_t(jw);

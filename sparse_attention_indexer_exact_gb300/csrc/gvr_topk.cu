@@ -78,7 +78,7 @@ gvr_status check_common(int64_t row_stride, int64_t num_rows, int32_t k, const g
     if (o->ring_stages != 0 && (o->ring_stages < gvr::MIN_STAGES || o->ring_stages > gvr::MAX_STAGES))
       return GVR_ERR_ARG;
     if (o->flags & ~(GVR_FLAG_FORCE_RESCUE | GVR_FLAG_NO_FLOOR | GVR_FLAG_ZERO_CAP | GVR_FLAG_RADIX_REFINE |
-                     GVR_FLAG_DETERMINISTIC | GVR_FLAG_SORTED))
+                     GVR_FLAG_DETERMINISTIC | GVR_FLAG_SORTED | GVR_FLAG_STREAM_RESCUE))
       return GVR_ERR_ARG;
   }
   return GVR_OK;

@@ -177,7 +177,8 @@ def test_stage_holding_only_the_partial_vector(gvr, cs):
     assert_prefill_exact(gvr, case, options=gvr.Options(cluster_size=cs, flags=1))
 
 
-@pytest.mark.parametrize("flags,expect", [(1, {4}), (4, {3, 5}), (2, {1}), (8, {1}), (2 | 8, {1}), (2 | 4, {3, 5})])
+@pytest.mark.parametrize("flags,expect", [(1, {4}), (4, {3, 5, 6}), (2, {1}), (8, {1}), (2 | 8, {1}),
+                                          (2 | 4, {3, 5, 6}), (4 | 64, {3}), (2 | 4 | 64, {3})])
 def test_forced_paths(gvr, flags, expect):
     case = workloads.decode_batch(seed=5, requests=8, next_n=2, cr=4, k=1024, stride=131072,
                                   boundary=False)
@@ -359,6 +360,18 @@ def test_cluster_refine_over_lists(gvr, cs):
     assert (st[st[:, 0] == 5, 1] > 512).all(), st
 
 
+def test_relist_after_list_overflow(gvr):
+    """No floor (every score listed, so long shares overflow their lists) and no candidate
+    buffer: overflowing rows read their share again and select over the re-built lists."""
+    case = workloads.decode_batch(seed=15, requests=16, next_n=2, cr=4, k=1024, stride=131072, boundary=False)
+    st = assert_decode_exact(gvr, case, options=gvr.Options(flags=2 | 4), stats=True)
+    long_rows = case.row_lengths() > case.k
+    assert (st[long_rows, 0] == 6).any(), st[:, 0]
+    assert ((st[st[:, 0] == 6, 2] // 10) >= 1).all(), st  # the share was read again
+    for flags in (16, 32):
+        assert_decode_deterministic(gvr, case, flags, 2 | 4)
+
+
 def test_crossing_in_the_floor_bin(gvr):
     """tau inside the bin that holds the sampled floor: one counting pass, candidates >= the floor.
 
@@ -380,7 +393,7 @@ def test_crossing_in_the_floor_bin(gvr):
     for flags in (0, 8):
         st = assert_decode_exact(gvr, case, options=gvr.Options(flags=flags), stats=True)
         assert (st[:, 2] % 10 == 1).all(), st  # one counting pass per row
-        assert set(st[:, 0].tolist()) <= {1, 5}, st
+        assert set(st[:, 0].tolist()) <= {1, 5, 6}, st
 
 
 # ----------------------------------------------------------------------------- deterministic mode
@@ -441,7 +454,7 @@ def test_deterministic_ties(gvr, flags, variant):
 
 
 @pytest.mark.parametrize("flags", DET_MODES)
-@pytest.mark.parametrize("extra", [0, 1, 4, 8, 2 | 4])
+@pytest.mark.parametrize("extra", [0, 1, 4, 8, 2 | 4, 4 | 64])
 def test_deterministic_every_path(gvr, flags, extra):
     g = np.random.default_rng(900 + extra)
     rows, stride, k = 10, 65536, 1024
