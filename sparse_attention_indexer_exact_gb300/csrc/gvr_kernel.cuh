@@ -1206,29 +1206,60 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
 
   // ---------------------------------------------------------------- re-list
   // The crossing bin holds more candidates than the buffer and some CTA's first-pass list
-  // overflowed: every CTA reads its share once more and lists only the scores of the crossing
-  // bin and above (one list per CTA).  When every such list fits, the selection below runs over
-  // the lists; otherwise it reads the row.
-  if (path == PATH_RESCUE_OVERFLOW && cr.total >= uint32_t(k) && !(p.flags & FLAG_STREAM_RESCUE)) {
+  // overflowed: every CTA lists only the scores of the crossing bin and above (one list per
+  // CTA) -- a CTA whose first-pass list is complete filters it in place, the others read their
+  // share once more.  When every such list fits, the selection below runs over the lists;
+  // otherwise it reads the row.  Rows whose crossing bin and above cannot fit in the cluster's
+  // lists (tie-heavy rows) go to the row-wide selection at once.
+  if (path == PATH_RESCUE_OVERFLOW && cr.total >= uint32_t(k) && !(p.flags & FLAG_STREAM_RESCUE) &&
+      uint64_t(cr.above) + cr.m <= uint64_t(cs) * LIST_CAP) {
     if (warp == 0) {
       const float t = cr.bin > 0 ? floor_value(cr.bin, gmin, sc) : -INFINITY;
       if (lane == 0) S.vthr = t;
     }
     __syncthreads();
     const float tb = fmaxf(S.vthr, cthr);  // scores >= tb: the crossing bin's members and above
-    stream_pass(false, [&](uint32_t slot, int32_t c0) {
-      each_lane(slot, c0, [&](float e, int32_t g, bool valid, int l) {
-        const bool hit = valid && e >= tb;
-        if (__any_sync(FULL_MASK, hit)) {
-          const uint32_t at = warp_alloc_local(&S.relist_n, hit);
-          if (hit && at < uint32_t(LIST_CAP)) {
-            S.list_v[at] = e;
-            S.list_j[at] = 4 * g + l - lead;
-          }
+    if (rounds == 1 && listed) {
+      // Compact the first-pass list (walk order, segments in turn) to the entries >= tb.  An
+      // entry is written below the walk index of every entry not read yet, so one barrier per
+      // round between the reads and the writes keeps unread entries intact.
+      uint32_t pre[NW + 1];
+      pre[0] = 0;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) pre[w + 1] = pre[w] + S.list_n[w];
+      for (uint32_t b0 = 0; b0 < pre[NW]; b0 += T) {
+        const uint32_t i = b0 + tid;
+        const bool in = i < pre[NW];
+        uint32_t at = i;
+#pragma unroll
+        for (int w = 1; w < NW; ++w)
+          if (i >= pre[w]) at = uint32_t(w * LIST_SEG) + (i - pre[w]);
+        const float v = in ? S.list_v[at] : 0.f;
+        const int32_t j = in ? S.list_j[at] : 0;
+        const bool hit = in && v >= tb;
+        __syncthreads();
+        const uint32_t slot = warp_alloc_local(&S.relist_n, hit);
+        if (hit) {
+          S.list_v[slot] = v;
+          S.list_j[slot] = j;
         }
+      }
+      __syncthreads();
+    } else {
+      stream_pass(false, [&](uint32_t slot, int32_t c0) {
+        each_lane(slot, c0, [&](float e, int32_t g, bool valid, int l) {
+          const bool hit = valid && e >= tb;
+          if (__any_sync(FULL_MASK, hit)) {
+            const uint32_t at = warp_alloc_local(&S.relist_n, hit);
+            if (hit && at < uint32_t(LIST_CAP)) {
+              S.list_v[at] = e;
+              S.list_j[at] = 4 * g + l - lead;
+            }
+          }
+        });
       });
-    });
-    rounds += 10;  // diagnostics: the share was read again
+      rounds += 10;  // diagnostics: the share was read again
+    }
     if (tid == 0) {
       const bool fits = S.relist_n <= uint32_t(LIST_CAP);
 #pragma unroll
