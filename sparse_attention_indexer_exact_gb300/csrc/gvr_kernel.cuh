@@ -891,9 +891,11 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   if (path == PATH_REFINE) {
     sc = __fdiv_rn(float(NB), __fsub_rn(gmax, gmin));
     if (!(p.flags & FLAG_NO_FLOOR)) {
-      // mu = k*k/nv samples are expected above tau; keep mu + 3 sqrt(mu) + 6 above the floor
+      // mu = k*k/nv samples are expected above tau (a Poisson count); keep mu + 2.5 sqrt(mu) + 4
+      // above the floor: 2.5 + 4 / sqrt(mu) standard deviations (3 or more while mu <= 64), so a
+      // second pass is rare while few scores beyond the k largest are counted
       const float mu = float(k) * float(k) / float(nv);
-      const float want_f = mu + 3.0f * sqrtf(mu) + 6.0f;
+      const float want_f = mu + 2.5f * sqrtf(mu) + 4.0f;
       const uint32_t want = want_f < float(k) ? uint32_t(want_f) : uint32_t(k);
       // The samples' own histogram on the same bins (in this CTA's private counts, cleared
       // again below): the floor is the lower edge of the bin where `want` samples are reached.
@@ -999,18 +1001,15 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       }
       // List the hits (a dense warp only until its segment is full; the counts above are exact).
       if (!dense || wlist - wtot < uint32_t(LIST_SEG)) {
+        const int32_t jbase = 4 * (c0 + tid) - lead;  // window index of this thread's lane 0
         for (uint32_t rest = bits; rest;) {
           const int j = __ffs(rest) - 1;
           rest &= rest - 1;
-          float4 v = vv[0];
-#pragma unroll
-          for (int i = 1; i < VPS; ++i)
-            if ((j >> 2) == i) v = vv[i];
-          const float e = f4_get(v, j & 3);
+          const float e = stage_score(slot, c0, j);
           if (!dense) atomicAdd(&S.hist[value_bin(e, gmin, sc)], 1u);
           if (at < uint32_t(LIST_SEG)) {
             seg_v[at] = e;
-            seg_j[at] = 4 * (c0 + (j >> 2) * T + tid) + (j & 3) - lead;
+            seg_j[at] = jbase + (j >> 2) * (4 * T) + (j & 3);
           }
           ++at;
         }
