@@ -891,11 +891,12 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   if (path == PATH_REFINE) {
     sc = __fdiv_rn(float(NB), __fsub_rn(gmax, gmin));
     if (!(p.flags & FLAG_NO_FLOOR)) {
-      // mu = k*k/nv samples are expected above tau (a Poisson count); keep mu + 2.5 sqrt(mu) + 4
-      // above the floor: 2.5 + 4 / sqrt(mu) standard deviations (3 or more while mu <= 64), so a
-      // second pass is rare while few scores beyond the k largest are counted
+      // mu = k*k/nv samples are expected above tau (a Poisson count); keep mu + 3 sqrt(mu) + 6
+      // above the floor.  A second pass is then rare enough per row (below 1e-4 for every mu of
+      // the workloads) that a batch of hundreds of rows seldom has one: the launch waits for its
+      // slowest row, so the margin is sized for the batch, not for the single row.
       const float mu = float(k) * float(k) / float(nv);
-      const float want_f = mu + 2.5f * sqrtf(mu) + 4.0f;
+      const float want_f = mu + 3.0f * sqrtf(mu) + 6.0f;
       const uint32_t want = want_f < float(k) ? uint32_t(want_f) : uint32_t(k);
       // The samples' own histogram on the same bins (in this CTA's private counts, cleared
       // again below): the floor is the lower edge of the bin where `want` samples are reached.

@@ -7,6 +7,7 @@
 // memory is read on the host and nothing synchronizes, so a call costs one launch.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 #include <mutex>
 
@@ -19,6 +20,8 @@ constexpr int kThreads = gvr::THREADS;
 constexpr int kMaxDevices = 64;
 constexpr int kMaxCluster = 8;
 constexpr int64_t kShareVec = 4096;  // target float4 per CTA when a row spans several CTAs
+constexpr int kListTarget = 480;       // expected first-pass list entries per CTA (of LIST_CAP)
+constexpr int64_t kCheapRereadStages = 4;
 
 struct DeviceState {
   std::once_flag once;
@@ -89,6 +92,14 @@ gvr_status check_common(int64_t row_stride, int64_t num_rows, int32_t k, const g
 // share is about kShareVec float4 (8 CTAs cover a 131072-score row); few rows spread each row
 // over more CTAs (more SMs pulling one row), down to one ring stage per CTA.
 //
+// List capacity: the first pass lists every score above the sampled floor, about
+// k + 3 sqrt(nv) + 6 nv / k of them for a row of nv scores (the floor keeps mu + 3 sqrt(mu) + 6
+// of the k samples above it, mu = k^2 / nv).  A CTA whose list overflows reads its share once
+// more, so the row is split at least so finely that a CTA expects to list at most
+// kListTarget scores -- unless the share is at most kCheapRereadStages stages, which are
+// read again cheaply, or the launch would exceed two waves of CTAs (there the extra CTAs'
+// fixed costs outweigh the rereads).
+//
 // Ring depth: every cluster of the launch should be resident at once (a second wave would
 // wait for the whole latency chain of the first), so the ring is as deep as it can be while
 // rows x cluster_size CTAs still fit on the GPU, and no deeper than the CTA's share.
@@ -102,8 +113,8 @@ int ctas_per_sm(int nstage, int smem_per_sm, int smem_reserved) {
   return by_smem < kMaxCtasPerSm ? by_smem : kMaxCtasPerSm;
 }
 
-Geometry plan_geometry(int64_t row_stride, int64_t num_rows, int sms, int smem_per_sm, int smem_reserved,
-                       const gvr_options* o) {
+Geometry plan_geometry(int64_t row_stride, int64_t num_rows, int32_t k, int sms, int smem_per_sm,
+                       int smem_reserved, const gvr_options* o) {
   const int64_t need_vec = row_stride / 4;
   if (sms <= 0) sms = 148;
   if (smem_per_sm <= 0) smem_per_sm = kDefaultSmemPerSm;
@@ -116,8 +127,15 @@ Geometry plan_geometry(int64_t row_stride, int64_t num_rows, int sms, int smem_p
     if (cs_min > kMaxCluster) cs_min = kMaxCluster;
     int cs_max = pow2_ceil((need_vec + gvr::STAGE_VEC - 1) / gvr::STAGE_VEC);
     if (cs_max > kMaxCluster) cs_max = kMaxCluster;
-    if (cs_max < cs_min) cs_max = cs_min;
     const int64_t slots = int64_t(sms) * ctas_per_sm(gvr::MIN_STAGES, smem_per_sm, smem_reserved);
+    const double nv = double(row_stride);
+    const double listed = k > 0 ? double(k) + 3.0 * std::sqrt(nv) + 6.0 * nv / double(k) : 0.0;
+    while (cs_min < kMaxCluster && listed > double(kListTarget) * cs_min &&
+           (need_vec + int64_t(cs_min) * gvr::STAGE_VEC - 1) / (int64_t(cs_min) * gvr::STAGE_VEC) >
+               kCheapRereadStages &&
+           num_rows * cs_min * 2 <= 2 * slots)
+      cs_min *= 2;
+    if (cs_max < cs_min) cs_max = cs_min;
     g.cs = cs_min;
     while (g.cs < cs_max && num_rows * g.cs * 2 <= slots) g.cs *= 2;
   }
@@ -141,7 +159,7 @@ Geometry plan_geometry(int64_t row_stride, int64_t num_rows, int sms, int smem_p
 gvr_status launch(const gvr::Params& prm, int64_t num_rows, const gvr_options* o, void* stream) {
   int sms = 0, smem_per_sm = 0, smem_reserved = 0;
   if (device_state(&sms, &smem_per_sm, &smem_reserved) != cudaSuccess) return GVR_ERR_LAUNCH;
-  const Geometry geo = plan_geometry(prm.row_stride, num_rows, sms, smem_per_sm, smem_reserved, o);
+  const Geometry geo = plan_geometry(prm.row_stride, num_rows, prm.k, sms, smem_per_sm, smem_reserved, o);
   const int cs = geo.cs;
   const int64_t blocks = num_rows * cs;
   if (blocks > 0x7fffffffLL) return GVR_ERR_ARG;
@@ -289,7 +307,7 @@ gvr_status gvr_plan(int64_t row_stride, int64_t num_rows, int32_t k, const gvr_o
   if (s != GVR_OK) return s;
   int sms = sm_count, smem_per_sm = kDefaultSmemPerSm, smem_reserved = kDefaultSmemReserved;
   if (sms <= 0 && device_state(&sms, &smem_per_sm, &smem_reserved) != cudaSuccess) return GVR_ERR_LAUNCH;
-  const Geometry geo = plan_geometry(row_stride, num_rows, sms, smem_per_sm, smem_reserved, options);
+  const Geometry geo = plan_geometry(row_stride, num_rows, k, sms, smem_per_sm, smem_reserved, options);
   if (cluster_size) *cluster_size = geo.cs;
   if (ring_stages) *ring_stages = geo.nstage;
   if (threads) *threads = kThreads;
