@@ -1300,10 +1300,37 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   bool primed = rounds == 0;  // the first pass of a row that skipped the histogram is primed
   // Bin class of a score for the seeded selection: 1 above the crossing bin, 0 a member of it,
   // -1 below it (or not counted).  Unseeded, every score is a member.
-  auto bin_class = [&](float e) -> int {
+  uint32_t klo = 0, khi = KEY_POS_INF;
+  // Seeded, every member's key lies in [klo, khi] (the crossing bin's value range, and >= cthr):
+  // the digits that klo and khi share are fixed before the first pass (at least one pass runs).
+  uint32_t tau_prefix = 0, tau_mask = 0;
+  int tau_shift = 24;
+  if (seeded) {
+    if (warp == 0) {
+      const float lo = bstar > 0 ? floor_value(bstar, gmin, sc) : -INFINITY;
+      const float hi = bstar < NB - 1 ? floor_value(bstar + 1, gmin, sc) : INFINITY;
+      if (lane == 0) {
+        S.klo = order_key(fmaxf(lo, cthr));
+        S.khi = bstar < NB - 1 ? order_key(hi) - 1u : KEY_POS_INF;
+      }
+    }
+    __syncthreads();
+    klo = S.klo;
+    khi = S.khi;
+    const int dfix = klo <= khi ? min(__clz(klo ^ khi) / 8, 3) : 0;
+    if (dfix > 0) {
+      tau_mask = 0xffffffffu << (32 - 8 * dfix);
+      tau_prefix = klo & tau_mask;
+      tau_shift = 24 - 8 * dfix;
+    }
+  }
+  // Class of a score by its order key, for the seeded selection: 1 above the crossing bin, 0 a
+  // member of it (a counted score of the bin: key in [klo, khi]), -1 below it, uncounted or NaN
+  // (whose keys lie beyond +inf's or below -inf's).  Unseeded, every score is a member.
+  auto key_class = [&](uint32_t key) -> int {
     if (!seeded) return 0;
-    const int b = value_bin(e, gmin, sc);
-    return b > bstar ? 1 : (b == bstar && e >= cthr ? 0 : -1);
+    if (key > KEY_POS_INF) return -1;
+    return key > khi ? 1 : (key >= klo ? 0 : -1);
   };
   // One cluster radix selection: the `need` largest keys among the scores that sel(e, j, key)
   // admits (it also computes the key), one 8-bit digit per pass from bit shift0 down, below the
@@ -1434,32 +1461,10 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     }
     return r;
   };
-  // Seeded, every member's key lies in [klo, khi] (the crossing bin's value range, and >= cthr):
-  // the digits that klo and khi share are fixed before the first pass (at least one pass runs).
-  uint32_t tau_prefix = 0, tau_mask = 0;
-  int tau_shift = 24;
-  if (seeded) {
-    if (warp == 0) {
-      const float lo = bstar > 0 ? floor_value(bstar, gmin, sc) : -INFINITY;
-      const float hi = bstar < NB - 1 ? floor_value(bstar + 1, gmin, sc) : INFINITY;
-      if (lane == 0) {
-        S.klo = order_key(fmaxf(lo, cthr));
-        S.khi = bstar < NB - 1 ? order_key(hi) - 1u : 0xffffffffu;
-      }
-    }
-    __syncthreads();
-    const uint32_t klo = S.klo, khi = S.khi;
-    const int dfix = klo <= khi ? min(__clz(klo ^ khi) / 8, 3) : 0;
-    if (dfix > 0) {
-      tau_mask = 0xffffffffu << (32 - 8 * dfix);
-      tau_prefix = klo & tau_mask;
-      tau_shift = 24 - 8 * dfix;
-    }
-  }
   // tau: the k - above largest order keys among the members
   const Sel t = radix_select([&](float e, int32_t, uint32_t& key) {
     key = order_key(e);
-    return bin_class(e) == 0;
+    return key_class(key) == 0;
   }, seeded ? uint32_t(k) - cr.above : uint32_t(k), tau_prefix, tau_mask, tau_shift);
   const uint32_t prefix = t.prefix, pmask = t.pmask;
   const bool ge = t.ge;
@@ -1476,7 +1481,8 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     const uint32_t fixed = digits < 4 ? (0xffffffffu << (8 * digits)) : 0u;
     ix = radix_select([&](float e, int32_t jw, uint32_t& key) {
       key = ~uint32_t(jw);
-      return bin_class(e) == 0 && order_key(e) == prefix;
+      const uint32_t kv = order_key(e);
+      return key_class(kv) == 0 && kv == prefix;
     }, nties, fixed, fixed, 8 * (digits - 1));
   }
   auto index_selected = [&](int32_t jw) -> bool {
@@ -1495,7 +1501,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   const uint32_t my_ties = tbase < nties ? (my_eq < nties - tbase ? my_eq : nties - tbase) : 0u;
   auto emit = [&](float e, int32_t jw, bool valid) {  // warp-collective
     const uint32_t key = order_key(e);
-    const int bc = valid ? bin_class(e) : -1;
+    const int bc = valid ? key_class(key) : -1;
     const bool win = bc == 1 || (bc == 0 && (ge ? (key & pmask) >= prefix : key > prefix));
     const bool tie = bc == 0 && !ge && key == prefix && (!by_index || index_selected(jw));
     const uint32_t ws = warp_alloc_local(&S.ctr_win, win);
