@@ -1396,16 +1396,29 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
         stream_pass(primed, [&](uint32_t slot, int32_t c0) {
           float e[4 * VPS];
           int32_t jw[4 * VPS];
-          uint32_t vm = 0;
+          uint32_t vm = 0xffffffffu;
+          if (c0 > 0 && c0 + STAGE_VEC <= ffull) {  // an interior stage: every lane is in the window
 #pragma unroll
-          for (int i = 0; i < VPS; ++i) {
-            int32_t g;
-            float4 v;
-            vm |= stage_vec(slot, c0, i, g, v) << (4 * i);
+            for (int i = 0; i < VPS; ++i) {
+              const float4 v = ring[slot][i * T + tid];
 #pragma unroll
-            for (int l = 0; l < 4; ++l) {
-              e[4 * i + l] = f4_get(v, l);
-              jw[4 * i + l] = 4 * g + l - lead;
+              for (int l = 0; l < 4; ++l) {
+                e[4 * i + l] = f4_get(v, l);
+                jw[4 * i + l] = 4 * (c0 + i * T + tid) + l - lead;
+              }
+            }
+          } else {
+            vm = 0;
+#pragma unroll
+            for (int i = 0; i < VPS; ++i) {
+              int32_t g;
+              float4 v;
+              vm |= stage_vec(slot, c0, i, g, v) << (4 * i);
+#pragma unroll
+              for (int l = 0; l < 4; ++l) {
+                e[4 * i + l] = f4_get(v, l);
+                jw[4 * i + l] = 4 * g + l - lead;
+              }
             }
           }
           digit_batch(IntC<4 * VPS>{}, e, jw, vm);
