@@ -325,6 +325,36 @@ def run_sweep(args):
                      lambda h, lg=lg, ks=ks, ke=ke, idx=idx, k=k: gvr.topk_prefill_raw(
                          lg.data_ptr(), lg.stride(0), bs, ks.data_ptr(), ke.data_ptr(), k, idx.data_ptr(), h))
             del lg
+    # block-skip: the same selection with exact block maxima given (decode rows)
+    def block_max_of(case):
+        nb = (case.row_stride + 31) // 32
+        out = np.full((case.rows, nb), -np.inf, np.float32)
+        n = case.row_lengths()
+        for r in range(case.rows):
+            if n[r]:
+                x = np.full(((n[r] + 31) // 32) * 32, -np.inf, np.float32)
+                x[:n[r]] = case.logits[r, :n[r]]
+                out[r, :x.size // 32] = x.reshape(-1, 32).max(axis=1)
+        return out
+
+    for case in (workloads.decode_batch(), workloads.sweep_decode(64, 131072, 1024),
+                 workloads.sweep_decode(256, 131072, 1024), workloads.sweep_decode(256, 65536, 512)):
+        lg = torch.from_numpy(case.logits).to(dev)
+        kv = torch.from_numpy(case.kv_lens).to(dev)
+        bm = torch.from_numpy(block_max_of(case)).to(dev)
+        idx = torch.empty((case.rows, case.k), dtype=torch.int32, device=dev)
+        case.meta.setdefault("n", int(case.row_lengths().max()))
+        for tag, fn in (("blockskip_off", None), ("blockskip_on", bm)):
+            if fn is None:
+                launch = (lambda h, lg=lg, kv=kv, idx=idx, case=case: gvr.topk_decode_raw(
+                    lg.data_ptr(), case.row_stride, case.rows, kv.data_ptr(), case.next_n, case.compress_ratio,
+                    case.k, idx.data_ptr(), None, h))
+            else:
+                launch = (lambda h, lg=lg, kv=kv, idx=idx, case=case, bm=bm: gvr.topk_decode_blockskip_raw(
+                    lg.data_ptr(), case.row_stride, case.rows, kv.data_ptr(), case.next_n, case.compress_ratio,
+                    case.k, bm.data_ptr(), bm.stride(0), idx.data_ptr(), None, h))
+            emit(f"{tag}:{case.name}", case, algorithmic_bytes(case, False), launch)
+        del lg, bm
     # tail check: each adversarial variant against a row of the same shape drawn from N(0,1)
     base = workloads.adversarial_row("base")
     g = np.random.default_rng(1049)

@@ -170,6 +170,29 @@ gvr_status topk_decode_hinted(const float* logits, int64_t row_stride, int64_t n
                               int32_t* indices, float* values, void* stream,
                               const gvr_options* options);
 
+/*
+ * Decode top-K with a block-maxima side tensor (the opt-in block-skip row pass of "Block-skip
+ * fast path for self-sampling GVR top-K decode", PR #18122, description and last commit): the
+ * first counting pass reads only the 32-score blocks whose bound reaches the sampled floor.
+ * Results are identical to topk_decode_ex for any valid bounds.
+ *   block_max         fp32 [num_rows][block_max_stride], device: block_max[r][b] must be >= every
+ *                     score of row r in columns [32 b, 32 b + 32) inside the row's window
+ *                     [0, n_r) (the block's maximum is the usual producer output; a larger bound
+ *                     only costs reads; NaN means "read the block").  Only blocks that meet the
+ *                     window are read.
+ *   block_max_stride  >= ceil(row_stride / 32) (GVR_ERR_ARG otherwise); block_max 4-byte
+ *                     aligned (GVR_ERR_ALIGN), non-NULL when num_rows > 0 (GVR_ERR_NULL).
+ * No gate is applied: the pages' shape gate (batch working set and row length) is left to the
+ * caller.  The later passes that need every score (the rare second pass below the floor, the
+ * row-wide selection) read whole shares as usual.  Every other argument, the ownership rules
+ * and the errors are those of topk_decode_ex.
+ */
+gvr_status topk_decode_blockskip(const float* logits, int64_t row_stride, int64_t num_rows,
+                                 const int32_t* kv_lens, int32_t next_n, int32_t compress_ratio,
+                                 int32_t k, const float* block_max, int64_t block_max_stride,
+                                 int32_t* indices, float* values, void* stream,
+                                 const gvr_options* options);
+
 /* Static English text for a status code; never NULL. */
 const char* gvr_status_string(gvr_status status);
 

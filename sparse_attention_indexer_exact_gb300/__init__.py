@@ -24,7 +24,8 @@ import ctypes
 import os
 import threading
 
-__all__ = ["topk_decode", "topk_prefill", "topk_decode_raw", "topk_decode_hinted_raw", "topk_prefill_raw", "plan",
+__all__ = ["topk_decode", "topk_prefill", "topk_decode_raw", "topk_decode_hinted_raw", "topk_decode_blockskip_raw",
+           "topk_prefill_raw", "plan",
            "Options",
            "GvrError", "library_path", "load_library", "FLAG_FORCE_RESCUE", "FLAG_NO_FLOOR", "FLAG_ZERO_CAP",
            "FLAG_RADIX_REFINE", "FLAG_DETERMINISTIC", "FLAG_SORTED", "FLAG_STREAM_RESCUE", "PATH_NAMES",
@@ -68,11 +69,12 @@ def _declare(lib):
     lib.topk_decode.argtypes = [p, i64, i64, p, i32, i32, i32, p, p, p]
     lib.topk_decode_ex.argtypes = [p, i64, i64, p, i32, i32, i32, p, p, p, ctypes.POINTER(Options)]
     lib.topk_decode_hinted.argtypes = [p, i64, i64, p, i32, i32, i32, p, i64, p, p, p, ctypes.POINTER(Options)]
+    lib.topk_decode_blockskip.argtypes = [p, i64, i64, p, i32, i32, i32, p, i64, p, p, p, ctypes.POINTER(Options)]
     lib.topk_prefill.argtypes = [p, i64, i64, p, p, i32, p, p]
     lib.topk_prefill_ex.argtypes = [p, i64, i64, p, p, i32, p, p, ctypes.POINTER(Options)]
     lib.gvr_plan.argtypes = [i64, i64, i32, ctypes.POINTER(Options), i32] + [ctypes.POINTER(i32)] * 4
-    for f in (lib.topk_decode, lib.topk_decode_ex, lib.topk_decode_hinted, lib.topk_prefill, lib.topk_prefill_ex,
-              lib.gvr_plan):
+    for f in (lib.topk_decode, lib.topk_decode_ex, lib.topk_decode_hinted, lib.topk_decode_blockskip,
+              lib.topk_prefill, lib.topk_prefill_ex, lib.gvr_plan):
         f.restype = ctypes.c_int
     lib.gvr_status_string.argtypes = [ctypes.c_int]
     lib.gvr_status_string.restype = ctypes.c_char_p
@@ -122,6 +124,18 @@ def topk_decode_hinted_raw(logits_ptr: int, row_stride: int, num_rows: int, kv_l
     st = lib.topk_decode_hinted(logits_ptr, row_stride, num_rows, kv_lens_ptr, next_n, compress_ratio, k,
                                 pre_idx_ptr, pre_idx_stride, indices_ptr, values_ptr, stream,
                                 ctypes.byref(options) if options is not None else None)
+    _check(st)
+
+
+def topk_decode_blockskip_raw(logits_ptr: int, row_stride: int, num_rows: int, kv_lens_ptr: int, next_n: int,
+                              compress_ratio: int, k: int, block_max_ptr: int, block_max_stride: int,
+                              indices_ptr: int, values_ptr: int | None, stream: int,
+                              options: Options | None = None) -> None:
+    """``topk_decode_blockskip`` on raw device addresses (enqueue only)."""
+    lib = load_library()
+    st = lib.topk_decode_blockskip(logits_ptr, row_stride, num_rows, kv_lens_ptr, next_n, compress_ratio, k,
+                                   block_max_ptr, block_max_stride, indices_ptr, values_ptr, stream,
+                                   ctypes.byref(options) if options is not None else None)
     _check(st)
 
 
@@ -191,12 +205,15 @@ def _out(t, rows, k, dtype, device, name):
 
 
 def topk_decode(logits, kv_lens, next_n: int, compress_ratio: int, k: int, indices=None, values=None, *,
-                want_values: bool = False, stream=None, options: Options | None = None, pre_idx=None):
+                want_values: bool = False, stream=None, options: Options | None = None, pre_idx=None,
+                block_max=None):
     """Decode top-K of each row of ``logits`` [rows, >=n]; returns (indices, values or None).
 
     ``logits.stride(0)`` is the row stride.  ``kv_lens`` is int32 [ceil(rows / next_n)].
     ``pre_idx`` (optional) is int32 [ceil(rows / next_n), >= k] with unit inner stride: each
     request's previous selection, used only as sample positions (``topk_decode_hinted``).
+    ``block_max`` (optional) is fp32 [rows, >= ceil(row_stride / 32)] with unit inner stride: an
+    upper bound of every 32-score block of each row's window (``topk_decode_blockskip``).
     """
     rows, stride = _rows_2d(logits)
     _int32_vec(kv_lens, (rows + next_n - 1) // max(next_n, 1), "kv_lens")
@@ -206,7 +223,18 @@ def topk_decode(logits, kv_lens, next_n: int, compress_ratio: int, k: int, indic
     elif values is not None:
         values = _out(values, rows, k, _torch().float32, logits.device, "values")
     vptr = values.data_ptr() if values is not None else None
-    if pre_idx is not None:
+    if pre_idx is not None and block_max is not None:
+        raise ValueError("pre_idx and block_max select different entry points; pass one of them")
+    if block_max is not None:
+        torch = _torch()
+        if (block_max.dtype != torch.float32 or not block_max.is_cuda or block_max.dim() != 2
+                or block_max.shape[0] != rows or block_max.shape[1] < (stride + 31) // 32 or block_max.stride(1) != 1):
+            raise ValueError(f"block_max must be a CUDA fp32 tensor [{rows}, >= {(stride + 31) // 32}] "
+                             "with unit inner stride")
+        topk_decode_blockskip_raw(logits.data_ptr(), stride, rows, kv_lens.data_ptr(), next_n, compress_ratio, k,
+                                  block_max.data_ptr(), block_max.stride(0), indices.data_ptr(), vptr,
+                                  _stream_handle(stream), options)
+    elif pre_idx is not None:
         torch = _torch()
         reqs = (rows + next_n - 1) // max(next_n, 1)
         if (pre_idx.dtype != torch.int32 or not pre_idx.is_cuda or pre_idx.dim() != 2 or pre_idx.shape[0] != reqs

@@ -91,6 +91,8 @@ struct Params {
   const int32_t* row_ends;    // prefill
   const int32_t* pre_idx;     // decode, optional: sample positions per request
   int64_t pre_stride;         // row stride of pre_idx (>= k)
+  const float* block_max;     // decode, optional: an upper bound of every 32-score block
+  int64_t bmax_stride;        // row stride of block_max (>= ceil(row_stride / 32))
   int32_t* indices;
   float* values;              // nullable
   int32_t* row_stats;         // nullable, [rows][4]
@@ -748,12 +750,16 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
 #pragma unroll
     for (int q = 0; q < KPT; ++q) sh[q] = uint32_t(hpos[q]) < nv ? __ldg(rowp + a + uint32_t(hpos[q])) : qnan;
   }
+  // Block-skip rows (block maxima given) read only the blocks that can reach the floor in the
+  // first pass, so nothing is staged ahead for them.
+  const float* bmax_row =
+      (p.mode == MODE_DECODE && p.block_max) ? p.block_max + int64_t(row) * p.bmax_stride : nullptr;
   // The first ring stages go in flight right behind the samples, one lane of warp 0 per stage.
-  if (warp == 0)
+  if (warp == 0 && !bmax_row)
     for (int32_t s = lane; s < nst && s < nstages; s += 32) issue_stage(s, uint32_t(s));
   // Every later stage of this CTA is requested into L2 now (no shared memory needed), so HBM
   // streams the whole row at once and the ring's refills are L2 hits.
-  if (warp == 1)
+  if (warp == 1 && !bmax_row)
     for (int32_t s = nst + lane; s < nstages; s += 32) {
       const int32_t nfull = stage_full(s);
       if (nfull > 0) bulk_prefetch_l2(base + 4 * size_t(stage_first(s)), uint32_t(nfull) * 16u);
@@ -939,83 +945,132 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     uint32_t wlist = 0;  // scores this warp has appended (warp-uniform; may exceed LIST_SEG)
     float* const seg_v = S.list_v + warp * LIST_SEG;
     int32_t* const seg_j = S.list_j + warp * LIST_SEG;
-    stream_pass(true, [&](uint32_t slot, int32_t c0) {
-      float4 vv[VPS];
-      uint32_t lanes = 0xFFFFFFFFu;  // bit 4i+l: lane l of the i-th vector is in the window
-      if (c0 > 0 && c0 + STAGE_VEC <= ffull) {  // an interior stage: every lane is in the window
+    if (bmax_row) {
+      // ---------------------------------------------------------- block-skip first pass
+      // ("Block-skip fast path for self-sampling GVR top-K decode", opt-in row pass): a block
+      // of 32 scores whose bound is below the floor holds no score the first pass counts, so
+      // only the surviving blocks are read, with plain coalesced loads (one block per warp
+      // load, up to 8 in flight per warp).  The counts and lists equal those of the full pass.
+      const int64_t wend = int64_t(a) + nv;  // decode: a = 0, the window is [0, nv)
+      for (int32_t s = warp; s < nstages; s += NW) {  // this CTA's stages, one warp each
+        const int64_t colst = 4 * int64_t(stage_first(s));  // first column (a multiple of 1024)
+        const int64_t bi = (colst >> 5) + lane;              // this lane's block
+        const bool inwin = bi * 32 < wend;
+        const float bm = inwin ? __ldg(bmax_row + bi) : -INFINITY;
+        unsigned surv = __ballot_sync(FULL_MASK, inwin && !(bm < thr));  // NaN bounds survive
+        while (surv) {
+          int32_t blk[8];
+          float v[8];
 #pragma unroll
-        for (int i = 0; i < VPS; ++i) vv[i] = ring[slot][i * T + tid];
-      } else {
-        lanes = 0;
+          for (int q = 0; q < 8; ++q) {
+            blk[q] = surv ? __ffs(surv) - 1 : -1;
+            surv &= surv - 1u;
+          }
 #pragma unroll
-        for (int i = 0; i < VPS; ++i) {
-          int32_t g;
-          lanes |= stage_vec(slot, c0, i, g, vv[i]) << (4 * i);
-        }
-      }
-      uint32_t bits = 0;  // bit 4i+l: lane l of this thread's i-th vector is >= thr
+          for (int q = 0; q < 8; ++q) {
+            const int64_t col = colst + 32 * blk[q] + lane;
+            v[q] = (blk[q] >= 0 && col < wend) ? __ldg(rowp + col) : -INFINITY;
+          }
 #pragma unroll
-      for (int i = 0; i < VPS; ++i)
-        bits |= (uint32_t(vv[i].x >= thr) | (uint32_t(vv[i].y >= thr) << 1) | (uint32_t(vv[i].z >= thr) << 2) |
-                 (uint32_t(vv[i].w >= thr) << 3))
-                << (4 * i);
-      bits &= lanes;
-      // The warp's exclusive prefix of hit counts from one ballot per bit of the count (the
-      // upper two bits only when some thread has 4 or more hits).
-      const uint32_t nhit = __popc(bits);
-      static_assert(4 * VPS < 16, "hit counts fit in 4 bits");
-      const unsigned lt = lanemask_lt();
-      const unsigned m0 = __ballot_sync(FULL_MASK, nhit & 1u), m1 = __ballot_sync(FULL_MASK, nhit & 2u);
-      uint32_t excl = uint32_t(__popc(m0 & lt)) + (uint32_t(__popc(m1 & lt)) << 1);
-      uint32_t wtot = uint32_t(__popc(m0)) + (uint32_t(__popc(m1)) << 1);
-      if (__any_sync(FULL_MASK, nhit >= 4u)) {
-        const unsigned m2 = __ballot_sync(FULL_MASK, nhit & 4u), m3 = __ballot_sync(FULL_MASK, nhit & 8u);
-        excl += (uint32_t(__popc(m2 & lt)) << 2) + (uint32_t(__popc(m3 & lt)) << 3);
-        wtot += (uint32_t(__popc(m2)) << 2) + (uint32_t(__popc(m3)) << 3);
-      }
-      if (wtot == 0) return;  // nothing of this warp reaches the floor
-      uint32_t at = wlist + excl;
-      wlist += wtot;
-      // A warp with a few hits per thread counts them one by one; a dense warp (ties, a low
-      // floor) adds its hits with one atomic when they all share a bin, else one per distinct
-      // bin and score slot.
-      const bool dense = __any_sync(FULL_MASK, nhit > uint32_t(SPARSE_MAX));
-      if (dense) {
-        uint32_t bj[4 * VPS];
-        uint32_t bmin = 0xffffffffu, bmax = 0u;
-#pragma unroll
-        for (int j = 0; j < 4 * VPS; ++j) {
-          bj[j] = uint32_t(value_bin(f4_get(vv[j >> 2], j & 3), gmin, sc));
-          if ((bits >> j) & 1u) {
-            bmin = min(bmin, bj[j]);
-            bmax = max(bmax, bj[j]);
+          for (int q = 0; q < 8; ++q) {
+            if (blk[q] < 0) break;  // warp-uniform
+            const int64_t col = colst + 32 * blk[q] + lane;
+            const bool hit = col < wend && v[q] >= thr;
+            const unsigned hm = __ballot_sync(FULL_MASK, hit);
+            if (!hm) continue;
+            const uint32_t at = wlist + uint32_t(__popc(hm & lanemask_lt()));
+            wlist += uint32_t(__popc(hm));
+            const uint32_t b = hit ? uint32_t(value_bin(v[q], gmin, sc)) : 0u;
+            if (__popc(hm) > 8)
+              hist_add(S.hist, hit, b);  // tie-heavy blocks: one atomic per distinct bin
+            else if (hit)
+              atomicAdd(&S.hist[b], 1u);
+            if (hit && at < uint32_t(LIST_SEG)) {
+              seg_v[at] = v[q];
+              seg_j[at] = int32_t(col - a);
+            }
           }
         }
-        bmin = __reduce_min_sync(FULL_MASK, bmin);
-        bmax = __reduce_max_sync(FULL_MASK, bmax);
-        if (bmin == bmax) {
-          if (lane == 0) atomicAdd(&S.hist[bmin], wtot);
+      }
+    } else {
+      stream_pass(true, [&](uint32_t slot, int32_t c0) {
+        float4 vv[VPS];
+        uint32_t lanes = 0xFFFFFFFFu;  // bit 4i+l: lane l of the i-th vector is in the window
+        if (c0 > 0 && c0 + STAGE_VEC <= ffull) {  // an interior stage: every lane is in the window
+  #pragma unroll
+          for (int i = 0; i < VPS; ++i) vv[i] = ring[slot][i * T + tid];
         } else {
-#pragma unroll
-          for (int j = 0; j < 4 * VPS; ++j) hist_add(S.hist, (bits >> j) & 1u, bj[j]);
-        }
-      }
-      // List the hits (a dense warp only until its segment is full; the counts above are exact).
-      if (!dense || wlist - wtot < uint32_t(LIST_SEG)) {
-        const int32_t jbase = 4 * (c0 + tid) - lead;  // window index of this thread's lane 0
-        for (uint32_t rest = bits; rest;) {
-          const int j = __ffs(rest) - 1;
-          rest &= rest - 1;
-          const float e = stage_score(slot, c0, j);
-          if (!dense) atomicAdd(&S.hist[value_bin(e, gmin, sc)], 1u);
-          if (at < uint32_t(LIST_SEG)) {
-            seg_v[at] = e;
-            seg_j[at] = jbase + (j >> 2) * (4 * T) + (j & 3);
+          lanes = 0;
+  #pragma unroll
+          for (int i = 0; i < VPS; ++i) {
+            int32_t g;
+            lanes |= stage_vec(slot, c0, i, g, vv[i]) << (4 * i);
           }
-          ++at;
         }
-      }
-    });
+        uint32_t bits = 0;  // bit 4i+l: lane l of this thread's i-th vector is >= thr
+  #pragma unroll
+        for (int i = 0; i < VPS; ++i)
+          bits |= (uint32_t(vv[i].x >= thr) | (uint32_t(vv[i].y >= thr) << 1) | (uint32_t(vv[i].z >= thr) << 2) |
+                   (uint32_t(vv[i].w >= thr) << 3))
+                  << (4 * i);
+        bits &= lanes;
+        // The warp's exclusive prefix of hit counts from one ballot per bit of the count (the
+        // upper two bits only when some thread has 4 or more hits).
+        const uint32_t nhit = __popc(bits);
+        static_assert(4 * VPS < 16, "hit counts fit in 4 bits");
+        const unsigned lt = lanemask_lt();
+        const unsigned m0 = __ballot_sync(FULL_MASK, nhit & 1u), m1 = __ballot_sync(FULL_MASK, nhit & 2u);
+        uint32_t excl = uint32_t(__popc(m0 & lt)) + (uint32_t(__popc(m1 & lt)) << 1);
+        uint32_t wtot = uint32_t(__popc(m0)) + (uint32_t(__popc(m1)) << 1);
+        if (__any_sync(FULL_MASK, nhit >= 4u)) {
+          const unsigned m2 = __ballot_sync(FULL_MASK, nhit & 4u), m3 = __ballot_sync(FULL_MASK, nhit & 8u);
+          excl += (uint32_t(__popc(m2 & lt)) << 2) + (uint32_t(__popc(m3 & lt)) << 3);
+          wtot += (uint32_t(__popc(m2)) << 2) + (uint32_t(__popc(m3)) << 3);
+        }
+        if (wtot == 0) return;  // nothing of this warp reaches the floor
+        uint32_t at = wlist + excl;
+        wlist += wtot;
+        // A warp with a few hits per thread counts them one by one; a dense warp (ties, a low
+        // floor) adds its hits with one atomic when they all share a bin, else one per distinct
+        // bin and score slot.
+        const bool dense = __any_sync(FULL_MASK, nhit > uint32_t(SPARSE_MAX));
+        if (dense) {
+          uint32_t bj[4 * VPS];
+          uint32_t bmin = 0xffffffffu, bmax = 0u;
+  #pragma unroll
+          for (int j = 0; j < 4 * VPS; ++j) {
+            bj[j] = uint32_t(value_bin(f4_get(vv[j >> 2], j & 3), gmin, sc));
+            if ((bits >> j) & 1u) {
+              bmin = min(bmin, bj[j]);
+              bmax = max(bmax, bj[j]);
+            }
+          }
+          bmin = __reduce_min_sync(FULL_MASK, bmin);
+          bmax = __reduce_max_sync(FULL_MASK, bmax);
+          if (bmin == bmax) {
+            if (lane == 0) atomicAdd(&S.hist[bmin], wtot);
+          } else {
+  #pragma unroll
+            for (int j = 0; j < 4 * VPS; ++j) hist_add(S.hist, (bits >> j) & 1u, bj[j]);
+          }
+        }
+        // List the hits (a dense warp only until its segment is full; the counts above are exact).
+        if (!dense || wlist - wtot < uint32_t(LIST_SEG)) {
+          const int32_t jbase = 4 * (c0 + tid) - lead;  // window index of this thread's lane 0
+          for (uint32_t rest = bits; rest;) {
+            const int j = __ffs(rest) - 1;
+            rest &= rest - 1;
+            const float e = stage_score(slot, c0, j);
+            if (!dense) atomicAdd(&S.hist[value_bin(e, gmin, sc)], 1u);
+            if (at < uint32_t(LIST_SEG)) {
+              seg_v[at] = e;
+              seg_j[at] = jbase + (j >> 2) * (4 * T) + (j & 3);
+            }
+            ++at;
+          }
+        }
+      });
+    }
     if (lane == 0) S.list_n[warp] = wlist;
     __syncthreads();
     listed = true;
@@ -1297,7 +1352,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   }
   __syncthreads();
   csync();  // every CTA's pushed totals start from zero
-  bool primed = rounds == 0;  // the first pass of a row that skipped the histogram is primed
+  bool primed = rounds == 0 && !bmax_row;  // the head primed the ring for a row without a first pass
   // Bin class of a score for the seeded selection: 1 above the crossing bin, 0 a member of it,
   // -1 below it (or not counted).  Unseeded, every score is a member.
   uint32_t klo = 0, khi = KEY_POS_INF;

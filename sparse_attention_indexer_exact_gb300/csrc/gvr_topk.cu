@@ -249,6 +249,36 @@ gvr_status topk_decode_hinted(const float* logits, int64_t row_stride, int64_t n
   return launch(prm, num_rows, options, stream);
 }
 
+gvr_status topk_decode_blockskip(const float* logits, int64_t row_stride, int64_t num_rows,
+                                 const int32_t* kv_lens, int32_t next_n, int32_t compress_ratio,
+                                 int32_t k, const float* block_max, int64_t block_max_stride,
+                                 int32_t* indices, float* values, void* stream,
+                                 const gvr_options* options) {
+  gvr_status s = check_common(row_stride, num_rows, k, options);
+  if (s != GVR_OK) return s;
+  if (next_n < 1 || compress_ratio < 1 || block_max_stride < (row_stride + 31) / 32) return GVR_ERR_ARG;
+  if (num_rows == 0) return GVR_OK;
+  if (!block_max || !logits || !kv_lens || !indices) return GVR_ERR_NULL;
+  if (!aligned(block_max, 4) || !aligned(logits, 16) || !aligned(indices, 4) || !aligned(kv_lens, 4) ||
+      (values && !aligned(values, 4)))
+    return GVR_ERR_ALIGN;
+  gvr::Params prm = {};
+  prm.logits = logits;
+  prm.row_stride = row_stride;
+  prm.kv_lens = kv_lens;
+  prm.block_max = block_max;
+  prm.bmax_stride = block_max_stride;
+  prm.indices = indices;
+  prm.values = values;
+  prm.row_stats = options ? options->row_stats : nullptr;
+  prm.next_n = next_n;
+  prm.compress_ratio = compress_ratio;
+  prm.k = k;
+  prm.mode = gvr::MODE_DECODE;
+  prm.flags = options ? options->flags : 0;
+  return launch(prm, num_rows, options, stream);
+}
+
 gvr_status topk_decode(const float* logits, int64_t row_stride, int64_t num_rows,
                        const int32_t* kv_lens, int32_t next_n, int32_t compress_ratio, int32_t k,
                        int32_t* indices, float* values, void* stream) {

@@ -106,6 +106,28 @@ def test_hinted_argument_errors(lib):
     assert call(num_rows=0, logits=None, indices=None, kv_lens=None, pre_idx=None) == 0
 
 
+def test_blockskip_argument_errors(lib):
+    f = lib.topk_decode_blockskip
+    ok = [ALIGNED, 1024, 4, ALIGNED, 1, 1, K, ALIGNED, 32, ALIGNED, None, None, None]
+    names = ["logits", "row_stride", "num_rows", "kv_lens", "next_n", "cr", "k", "bmax", "bmax_stride",
+             "indices", "values", "stream", "options"]
+
+    def call(**kw):
+        args = list(ok)
+        for key, v in kw.items():
+            args[names.index(key)] = v
+        return f(*args)
+
+    assert call(bmax=None) == 1
+    assert call(bmax=ALIGNED + 1) == 2
+    assert call(bmax_stride=31) == 5
+    assert call(row_stride=1028, bmax_stride=32) == 5  # ceil(1028 / 32) = 33 blocks
+    assert call(row_stride=1028, bmax_stride=33) != 5
+    assert call(logits=None) == 1
+    assert call(k=300) == 4
+    assert call(num_rows=0, logits=None, indices=None, kv_lens=None, bmax=None) == 0
+
+
 def test_prefill_argument_errors(lib):
     f = lib.topk_prefill
     assert f(None, 1024, 4, ALIGNED, ALIGNED, K, ALIGNED, None) == 1

@@ -1,0 +1,118 @@
+"""Block-skip first pass (topk_decode_blockskip) against the oracle.
+
+The block-maxima side tensor bounds every 32-score block of a row's window ("Block-skip fast
+path for self-sampling GVR top-K decode", opt-in row pass); the first counting pass reads
+only the blocks whose bound reaches the sampled floor.  For any valid bounds the selection is
+the exact one: exact maxima, loose bounds, +inf (nothing skipped) and NaN bounds (read), on
+every workload, every forced path and in deterministic / sorted mode.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from tiecheck import compare_rows, decode_windows
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def gvr():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_attention_indexer_exact_gb300 import _build
+    _build.build_library()
+    import sparse_attention_indexer_exact_gb300 as mod
+    mod.load_library()
+    torch.cuda.set_device(0)
+    return mod
+
+
+def block_bounds(case, kind, seed=0):
+    """fp32 [rows, ceil(stride / 32) + 2]: per 32-column block, a bound of the window's scores."""
+    nb = (case.row_stride + 31) // 32
+    out = np.full((case.rows, nb + 2), -np.inf, np.float32)
+    n = case.row_lengths()
+    g = np.random.default_rng(seed)
+    for r in range(case.rows):
+        if n[r] == 0:
+            continue
+        x = np.full(((n[r] + 31) // 32) * 32, -np.inf, np.float32)
+        x[:n[r]] = case.logits[r, :n[r]]
+        m = x.reshape(-1, 32).max(axis=1)
+        if kind == "loose":
+            m = m + np.abs(g.standard_normal(m.size)).astype(np.float32)
+        elif kind == "inf":
+            m[:] = np.inf
+        elif kind == "nan":
+            m[g.random(m.size) < 0.1] = np.nan
+        out[r, :m.size] = m
+    return out
+
+
+def assert_blockskip_exact(gvr, case, kind="exact", flags=0, seed=0):
+    bm = block_bounds(case, kind, seed)
+    lg = torch.from_numpy(case.logits).to(DEV)
+    kv = torch.from_numpy(case.kv_lens).to(DEV)
+    st = torch.full((case.rows, 4), -7, dtype=torch.int32, device=DEV)
+    opts = gvr.Options(flags=flags)
+    opts.row_stats = st.data_ptr()
+    idx, vals = gvr.topk_decode(lg, kv, case.next_n, case.compress_ratio, case.k, want_values=True, options=opts,
+                                block_max=torch.from_numpy(bm).to(DEV))
+    torch.cuda.synchronize()
+    got, gv = idx.cpu().numpy(), vals.cpu().numpy()
+    ref, _, _ = oracle.topk_decode(case.logits, case.kv_lens, case.next_n, case.compress_ratio, case.k)
+    bad, why = compare_rows(decode_windows(case.logits, case.kv_lens, case.next_n, case.compress_ratio), case.k,
+                            got, ref, got_values=gv)
+    assert bad == 0, f"{case.name}/{kind}/{flags}: {bad} inexact rows: {why}"
+    if flags & 32:
+        assert np.array_equal(got, ref)
+    return st.cpu().numpy()
+
+
+@pytest.mark.parametrize("kind", ["exact", "loose", "inf", "nan"])
+def test_blockskip_decode_batch(gvr, kind):
+    assert_blockskip_exact(gvr, workloads.decode_batch(), kind, seed=3)
+
+
+@pytest.mark.parametrize("variant", workloads.ADVERSARIAL_VARIANTS)
+def test_blockskip_adversarial(gvr, variant):
+    case = workloads.adversarial_row(variant)
+    for kind in ("exact", "loose"):
+        assert_blockskip_exact(gvr, case, kind, seed=4)
+
+
+@pytest.mark.parametrize("flags", [1, 2, 4, 8, 16, 32, 2 | 4, 4 | 64])
+def test_blockskip_forced_paths_and_modes(gvr, flags):
+    case = workloads.decode_batch(seed=6, requests=10, next_n=3, cr=4, k=512, stride=65536, boundary=True)
+    assert_blockskip_exact(gvr, case, "exact", flags)
+
+
+@pytest.mark.parametrize("bs,n,k", [(4, 131072, 512), (16, 65536, 2048), (1, 16384, 1024), (8, 100003, 1024)])
+def test_blockskip_sweep_cells(gvr, bs, n, k):
+    if n % 64:  # a window that ends inside a block and inside a vector
+        case = workloads.sweep_decode(bs, 131072, k)
+        case = workloads.DecodeCase("odd_n", case.logits, np.full(bs, n, np.int32), 1, 1, k)
+        lg = case.logits
+        for r in range(bs):
+            lg[r, n:] = workloads.DECODE_POISON[np.arange(n, lg.shape[1]) % 3]
+    else:
+        case = workloads.sweep_decode(bs, n, k)
+    assert_blockskip_exact(gvr, case, "exact")
+    assert_blockskip_exact(gvr, case, "loose", seed=5)
+
+
+def test_blockskip_rejects_bad_bounds(gvr):
+    case = workloads.single_decode_row()
+    lg = torch.from_numpy(case.logits).to(DEV)
+    kv = torch.from_numpy(case.kv_lens).to(DEV)
+    with pytest.raises(ValueError):
+        gvr.topk_decode(lg, kv, 1, 1, case.k, block_max=torch.zeros((1, 3), dtype=torch.float32, device=DEV))
+    with pytest.raises(ValueError):
+        gvr.topk_decode(lg, kv, 1, 1, case.k, block_max=torch.zeros((1, 256), dtype=torch.float32, device=DEV),
+                        pre_idx=torch.zeros((1, 512), dtype=torch.int32, device=DEV))
