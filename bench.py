@@ -337,7 +337,7 @@ def run_sweep(args):
                 out[r, :x.size // 32] = x.reshape(-1, 32).max(axis=1)
         return out
 
-    for case in (workloads.decode_batch(), workloads.sweep_decode(64, 131072, 1024),
+    for case in (workloads.decode_batch(), workloads.peaky_decode_batch(), workloads.sweep_decode(64, 131072, 1024),
                  workloads.sweep_decode(256, 131072, 1024), workloads.sweep_decode(256, 65536, 512)):
         lg = torch.from_numpy(case.logits).to(dev)
         kv = torch.from_numpy(case.kv_lens).to(dev)

@@ -80,6 +80,13 @@ def test_blockskip_decode_batch(gvr, kind):
     assert_blockskip_exact(gvr, workloads.decode_batch(), kind, seed=3)
 
 
+@pytest.mark.parametrize("kind", ["exact", "loose"])
+def test_blockskip_peaky_batch(gvr, kind):
+    """Block-concentrated rows, where most blocks fall below the floor and are never read."""
+    assert_blockskip_exact(gvr, workloads.peaky_decode_batch(), kind, seed=8)
+    assert_blockskip_exact(gvr, workloads.peaky_decode_batch(requests=8, next_n=3, hot_frac=0.002), kind, 32)
+
+
 @pytest.mark.parametrize("variant", workloads.ADVERSARIAL_VARIANTS)
 def test_blockskip_adversarial(gvr, variant):
     case = workloads.adversarial_row(variant)

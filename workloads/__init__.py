@@ -153,6 +153,37 @@ def decode_batch(seed: int = 1002, requests: int = 64, next_n: int = 2, cr: int 
                                    f"stride={stride} kv_lens~U[{kv_lo},{kv_hi}]"})
 
 
+def peaky_decode_batch(seed: int = 1006, requests: int = 64, next_n: int = 2, cr: int = 4, k: int = 1024,
+                       stride: int = 131072, kv_lo: int = 16384, kv_hi: int = 524288,
+                       hot_frac: float = 0.015) -> DecodeCase:
+    """The decode batch's geometry with block-concentrated scores, a stand-in for captured
+    attention rows (the block-skip pass targets them): a low N(0,1) - 4 background, the first
+    and last 128 positions (sink and recent tokens) and a random hot_frac of the 32-score
+    blocks raised by +5.  Pad columns j >= n are poisoned.
+    """
+    g0 = _rng(seed, 0)
+    kv = g0.integers(kv_lo, kv_hi, size=requests, endpoint=True).astype(np.int32)
+    rows = requests * next_n
+    n = _decode_lengths(kv, next_n, cr, rows, stride)
+    logits = np.empty((rows, stride), np.float32)
+    for r in range(rows):
+        g = _rng(seed, r + 1)
+        nr = int(n[r])
+        if not nr:
+            continue
+        x = g.standard_normal(nr, dtype=np.float32) - 4.0
+        nb = (nr + 31) // 32
+        hot = g.random(nb) < hot_frac
+        boost = np.repeat(hot, 32)[:nr].astype(np.float32) * 5.0
+        boost[:128] = 5.0
+        boost[-128:] = 5.0
+        logits[r, :nr] = x + boost
+    _poison_decode(logits, n)
+    return DecodeCase("peaky_decode_batch", logits, kv, next_n, cr, k,
+                      {"workload": f"peaky decode requests={requests} next_n={next_n} rows={rows} cr={cr} K={k} "
+                                   f"stride={stride} hot blocks {hot_frac}"})
+
+
 # --------------------------------------------------------------------------- workload 3
 def prefill_tile(seed: int = 1003, rows: int = 4096, k: int = 2048,
                  lengths=(512, 1536, 4096, 8192)) -> PrefillCase:
