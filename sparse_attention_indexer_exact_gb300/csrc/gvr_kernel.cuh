@@ -479,6 +479,10 @@ __device__ __forceinline__ void digit_cross(Smem& S, int buf, uint32_t c0, uint3
   __syncthreads();
 }
 
+// EXT: the extended modes (deterministic ties and sorting, hinted sampling, block skipping) are
+// compiled in.  The plain instantiation leaves them out, which keeps the common path's code
+// smaller (measured ~3 % faster).
+template <bool EXT>
 __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   constexpr int T = THREADS;
   constexpr int NW = T / 32;
@@ -494,7 +498,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   const int32_t k = p.k;
   const float qnan = __int_as_float(0x7fffffff);
   // ties at tau go to the smallest window indices (always so when the output is sorted)
-  const bool det = (p.flags & (FLAG_DETERMINISTIC | FLAG_SORTED)) != 0;
+  const bool det = EXT && (p.flags & (FLAG_DETERMINISTIC | FLAG_SORTED)) != 0;
 
   // The ring's barriers are initialized first: the fence that publishes them then overlaps the
   // geometry load instead of delaying the first stage copies.
@@ -508,7 +512,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   // Hinted sampling: each CTA of the cluster reads its share of the request's hint row before
   // anything else (it does not depend on the row's length), so the latency overlaps the
   // geometry load; the cluster combines the shares after sampling.
-  const int32_t* hints = (p.mode == MODE_DECODE && p.pre_idx)
+  const int32_t* hints = (EXT && p.mode == MODE_DECODE && p.pre_idx)
                              ? p.pre_idx + int64_t(row / uint32_t(p.next_n)) * p.pre_stride
                              : nullptr;
   int32_t hpos[KPT];
@@ -753,7 +757,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   // Block-skip rows (block maxima given) read only the blocks that can reach the floor in the
   // first pass, so nothing is staged ahead for them.
   const float* bmax_row =
-      (p.mode == MODE_DECODE && p.block_max) ? p.block_max + int64_t(row) * p.bmax_stride : nullptr;
+      (EXT && p.mode == MODE_DECODE && p.block_max) ? p.block_max + int64_t(row) * p.bmax_stride : nullptr;
   // The first ring stages go in flight right behind the samples, one lane of warp 0 per stage.
   if (warp == 0 && !bmax_row)
     for (int32_t s = lane; s < nst && s < nstages; s += 32) issue_stage(s, uint32_t(s));
@@ -1248,7 +1252,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     const bool failed = S.err || S.tout;
     if (failed)
       for (int i = tid; i < k; i += T) out[i] = -2;
-    else if (p.flags & FLAG_SORTED)
+    else if (EXT && (p.flags & FLAG_SORTED))
       sort_output();
     if (stats) {
       stats[0] = failed ? PATH_DEVICE_ERROR : PATH_REFINE;
@@ -1601,7 +1605,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     const bool failed = S.err || S.tout;
     if (failed)
       for (int i = tid; i < k; i += T) out[i] = -2;
-    else if (p.flags & FLAG_SORTED)
+    else if (EXT && (p.flags & FLAG_SORTED))
       sort_output();
     if (stats) {
       stats[0] = failed ? PATH_DEVICE_ERROR : path;

@@ -37,8 +37,12 @@ constexpr int kMaxCtasPerSm = 7;  // registers: 128 threads x up to 72 registers
 DeviceState g_devices[kMaxDevices];
 
 cudaError_t set_attributes() {
-  return cudaFuncSetAttribute(gvr::gvr_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              gvr::smem_bytes(gvr::MAX_STAGES));
+  cudaError_t e = cudaFuncSetAttribute(gvr::gvr_topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       gvr::smem_bytes(gvr::MAX_STAGES));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gvr::gvr_topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             gvr::smem_bytes(gvr::MAX_STAGES));
+  return e;
 }
 
 // One-time per-device set-up: kernel attributes, SM count and shared-memory capacity.
@@ -179,7 +183,10 @@ gvr_status launch(const gvr::Params& prm, int64_t num_rows, const gvr_options* o
 
   gvr::Params q = prm;
   q.nstage = geo.nstage;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel, q);
+  // the extended instantiation only when a call uses one of its modes
+  const bool ext = (q.flags & (gvr::FLAG_DETERMINISTIC | gvr::FLAG_SORTED)) || q.pre_idx || q.block_max;
+  const cudaError_t e = ext ? cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<true>, q)
+                            : cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<false>, q);
   return e == cudaSuccess ? GVR_OK : GVR_ERR_LAUNCH;
 }
 
