@@ -187,7 +187,7 @@ def time_oracle(case, nthreads: int, repeats: int):
     return statistics.median(times), cores
 
 
-REFERENCE_BUDGET_S = 120.0  # the reference arm's timed steps take about this long in all
+REFERENCE_BUDGET_S = 90.0  # the reference arm's timed steps take about this long in all
 
 
 def run_reference(args, case, ws, rank):
