@@ -55,15 +55,6 @@ __device__ __forceinline__ uint32_t dsmem_ld_u32(uint32_t addr) {
   return v;
 }
 
-__device__ __forceinline__ uint4 dsmem_ld_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-
 __device__ __forceinline__ void dsmem_st_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
@@ -72,15 +63,6 @@ __device__ __forceinline__ uint32_t dsmem_atom_add(uint32_t addr, uint32_t v) {
   uint32_t old;
   asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
   return old;
-}
-
-// 16-byte load of data read exactly once: read-only path, no L1 allocation.
-__device__ __forceinline__ float4 ld_stream_v4(const float* p) {
-  float4 v;
-  asm("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
-      : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-      : "l"(p));
-  return v;
 }
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
@@ -173,11 +155,6 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
           smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
-}
-
-// Orders this thread's earlier generic-proxy shared-memory accesses before later bulk copies.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 }  // namespace gvr

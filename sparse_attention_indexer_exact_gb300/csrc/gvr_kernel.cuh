@@ -15,23 +15,27 @@
 //           b* that crosses the K-th largest value tau ("Why the GLM row overflows").
 //   Refine  scores in bins above b* are winners and are written at once; the m members of
 //           b* go to a bounded candidate buffer in cluster rank 0, which picks the remaining
-//           need = K - above winners exactly.
-//   Rescue  an invalid bracket (no finite sample, or GMIN == GMAX) or m above the buffer
-//           capacity sends the row to an exact radix select over the 32-bit order-preserving
-//           keys of every score, four 8-bit digit passes whose digit histograms are summed
-//           over all CTAs of the cluster through distributed shared memory -- the parallel
-//           rescue of PR #20998, in the same launch, with no host synchronization.
+//           need = K - above winners exactly.  When m exceeds the buffer, the same exact
+//           selection as the rescue runs over the CTAs' lists of counted scores instead of
+//           the row (re-built by one more read when a list overflowed).
+//   Rescue  an invalid bracket (no finite sample, or GMIN == GMAX) or a crossing bin that no
+//           list can hold sends the row to an exact radix select over the 32-bit
+//           order-preserving keys, 8-bit digit passes whose digit histograms are summed over
+//           all CTAs of the cluster through distributed shared memory -- the parallel rescue of
+//           PR #20998, in the same launch, with no host synchronization.  After a valid
+//           histogram only the crossing bin's members take part.
 //
 // Implementation choices that keep the per-score work to about one compare:
-//  * sampled histogram floor: the samples also give a floor t below which, by the sample
-//    quantile, the crossing should not lie; only scores >= t are counted, and they are kept in
-//    a small shared-memory list for the collect step (no second read of the row).  Bins above
-//    bin(t) are then complete, bin(t) itself is partial.  If the crossing lands in bin(t) or
-//    below, the scores below t are counted in a second pass, so the result never depends on
-//    the floor.
-//  * warp-aggregated shared-memory atomics (__match_any_sync) for every histogram update and
-//    ballot-aggregated slot allocation for list, winner and candidate slots, so tie-heavy rows
-//    cost one atomic per distinct bin per warp instruction.
+//  * sampled histogram floor: the samples also give a floor t with a Poisson margin above the
+//    expected K-th sample; only scores >= t are counted, and they are kept in per-warp
+//    shared-memory lists for the collect step (no second read of the row).  Bins above bin(t)
+//    are then complete, bin(t) itself is partial.  Only when fewer than K scores reach t are
+//    the scores below it counted in a second pass, so the result never depends on the floor.
+//  * ballot-built prefixes for list slots; a warp whose hits share one bin adds them with one
+//    atomic, other dense warps aggregate with __match_any_sync, so tie-heavy rows cost one
+//    atomic per distinct bin per warp instruction.
+//  * extended modes in a second instantiation (EXT): deterministic ties by smallest index and
+//    sorted output, hinted sampling, and the block-skip first pass.
 //
 // The bin function is monotone non-decreasing in the score (IEEE round-to-nearest subtract and
 // multiply by a positive scale, clamp, truncate), which is all the crossing-bin logic needs;
@@ -215,18 +219,6 @@ __device__ __forceinline__ uint32_t warp_alloc_local(uint32_t* ctr, bool want) {
   if (mask) {
     const int leader = __ffs(mask) - 1;
     if ((threadIdx.x & 31) == leader) base = atomicAdd(ctr, uint32_t(__popc(mask)));
-    base = __shfl_sync(FULL_MASK, base, leader);
-  }
-  return base + __popc(mask & lanemask_lt());
-}
-
-// Same, on a counter in another CTA's shared memory (DSMEM address).  Warp-collective.
-__device__ __forceinline__ uint32_t warp_alloc_remote(uint32_t ctr_addr, bool want) {
-  const unsigned mask = __ballot_sync(FULL_MASK, want);
-  uint32_t base = 0;
-  if (mask) {
-    const int leader = __ffs(mask) - 1;
-    if ((threadIdx.x & 31) == leader) base = dsmem_atom_add(ctr_addr, uint32_t(__popc(mask)));
     base = __shfl_sync(FULL_MASK, base, leader);
   }
   return base + __popc(mask & lanemask_lt());
