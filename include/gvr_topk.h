@@ -112,7 +112,9 @@ enum {
 };
 
 typedef struct gvr_options {
-  int32_t cluster_size;       /* CTAs per row: 0 = automatic, else 1, 2, 4 or 8 */
+  int32_t cluster_size;       /* CTAs per row: 0 = automatic, else 1, 2, 4, 8 or 16 (16 is a
+                                 non-portable cluster size: the launch fails where the device
+                                 cannot schedule it; automatic use checks first) */
   int32_t ring_stages;        /* shared-memory ring stages of 4 KB per CTA: 0 = automatic,
                                  else 3..16 */
   int32_t flags;              /* GVR_FLAG_* bits; results stay exact under every flag */

@@ -18,7 +18,7 @@ namespace {
 
 constexpr int kThreads = gvr::THREADS;
 constexpr int kMaxDevices = 64;
-constexpr int kMaxCluster = 8;
+constexpr int kMaxCluster = 16;  // 16 is a non-portable cluster size (checked per ring depth)
 constexpr int64_t kShareVec = 4096;  // target float4 per CTA when a row spans several CTAs
 constexpr int kListTarget = 480;       // expected first-pass list entries per CTA (of LIST_CAP)
 constexpr int64_t kCheapRereadStages = 4;
@@ -29,6 +29,7 @@ struct DeviceState {
   int sms = 0;
   int smem_per_sm = 0;     // shared memory per SM (bytes)
   int smem_reserved = 0;   // shared memory the system reserves per CTA (bytes)
+  int fits16[gvr::MAX_STAGES + 1] = {};  // a 16-CTA cluster can be scheduled: 0 unknown, 1 yes, 2 no
 };
 
 constexpr int kDefaultSmemPerSm = 228 * 1024;
@@ -42,6 +43,10 @@ cudaError_t set_attributes() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(gvr::gvr_topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              gvr::smem_bytes(gvr::MAX_STAGES));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gvr::gvr_topk_kernel<false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gvr::gvr_topk_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   return e;
 }
 
@@ -67,7 +72,7 @@ cudaError_t device_state(int* sms, int* smem_per_sm, int* smem_reserved) {
   return st.err;
 }
 
-bool is_pow2_upto8(int v) { return v == 1 || v == 2 || v == 4 || v == 8; }
+bool is_cluster_size(int v) { return v == 1 || v == 2 || v == 4 || v == 8 || v == 16; }
 
 int pow2_ceil(int64_t v) {
   int p = 1;
@@ -81,7 +86,7 @@ gvr_status check_common(int64_t row_stride, int64_t num_rows, int32_t k, const g
   if (k != 512 && k != 1024 && k != 2048) return GVR_ERR_K;
   if (o) {
     if (o->reserved != 0) return GVR_ERR_ARG;
-    if (o->cluster_size != 0 && !is_pow2_upto8(o->cluster_size)) return GVR_ERR_ARG;
+    if (o->cluster_size != 0 && !is_cluster_size(o->cluster_size)) return GVR_ERR_ARG;
     if (o->ring_stages != 0 && (o->ring_stages < gvr::MIN_STAGES || o->ring_stages > gvr::MAX_STAGES))
       return GVR_ERR_ARG;
     if (o->flags & ~(GVR_FLAG_FORCE_RESCUE | GVR_FLAG_NO_FLOOR | GVR_FLAG_ZERO_CAP | GVR_FLAG_RADIX_REFINE |
@@ -163,7 +168,35 @@ Geometry plan_geometry(int64_t row_stride, int64_t num_rows, int32_t k, int sms,
 gvr_status launch(const gvr::Params& prm, int64_t num_rows, const gvr_options* o, void* stream) {
   int sms = 0, smem_per_sm = 0, smem_reserved = 0;
   if (device_state(&sms, &smem_per_sm, &smem_reserved) != cudaSuccess) return GVR_ERR_LAUNCH;
-  const Geometry geo = plan_geometry(prm.row_stride, num_rows, prm.k, sms, smem_per_sm, smem_reserved, o);
+  Geometry geo = plan_geometry(prm.row_stride, num_rows, prm.k, sms, smem_per_sm, smem_reserved, o);
+  if (geo.cs == 16 && !(o && o->cluster_size == 16)) {
+    // A 16-CTA cluster needs 16 SMs of one GPC with room for it: checked once per ring depth,
+    // else the row goes to 8 CTAs.
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int& f = g_devices[dev].fits16[geo.nstage];
+    if (f == 0) {
+      cudaLaunchConfig_t qc = {};
+      qc.gridDim = dim3(16, 1, 1);
+      qc.blockDim = dim3(kThreads, 1, 1);
+      qc.dynamicSmemBytes = size_t(gvr::smem_bytes(geo.nstage));
+      cudaLaunchAttribute qa[1];
+      qa[0].id = cudaLaunchAttributeClusterDimension;
+      qa[0].val.clusterDim.x = 16;
+      qa[0].val.clusterDim.y = 1;
+      qa[0].val.clusterDim.z = 1;
+      qc.attrs = qa;
+      qc.numAttrs = 1;
+      int n = 0;
+      f = (cudaOccupancyMaxActiveClusters(&n, gvr::gvr_topk_kernel<false>, &qc) == cudaSuccess && n > 0) ? 1 : 2;
+      cudaGetLastError();  // a refused query leaves no sticky error
+    }
+    if (f != 1) {
+      gvr_options o8 = o ? *o : gvr_options{};
+      o8.cluster_size = 8;
+      geo = plan_geometry(prm.row_stride, num_rows, prm.k, sms, smem_per_sm, smem_reserved, &o8);
+    }
+  }
   const int cs = geo.cs;
   const int64_t blocks = num_rows * cs;
   if (blocks > 0x7fffffffLL) return GVR_ERR_ARG;

@@ -142,7 +142,7 @@ def test_prefill_argument_errors(lib):
 
 def test_option_errors(lib):
     import sparse_attention_indexer_exact_gb300 as gvr
-    for bad in (dict(cluster_size=3), dict(cluster_size=16), dict(ring_stages=2), dict(ring_stages=17), dict(reserved=1),
+    for bad in (dict(cluster_size=3), dict(cluster_size=32), dict(ring_stages=2), dict(ring_stages=17), dict(reserved=1),
                 dict(flags=128)):
         o = gvr.Options(**bad)
         st = lib.topk_decode_ex(ALIGNED, 1024, 4, ALIGNED, 1, 1, K, ALIGNED, None, None, ctypes.byref(o))
@@ -156,13 +156,15 @@ def test_plan_geometry(lib, stride, rows, k):
     import sparse_attention_indexer_exact_gb300 as gvr
     p = gvr.plan(stride, rows, k, sm_count=152)
     cs = p["cluster_size"]
-    assert cs in (1, 2, 4, 8)
+    assert cs in (1, 2, 4, 8, 16)
     share_vec = -(-(stride // 4) // cs)
     if stride // 4 >= 8 * 4096:
-        assert cs == 8  # long rows always spread over a full cluster
+        assert cs >= 8  # long rows always spread over a full cluster
     if rows * 8 * 2 <= 7 * 152 and stride // 4 >= 8 * 256:
-        assert cs == 8  # few rows: spread each row wide
-    assert share_vec <= max(4096, -(-(stride // 4) // 8))  # balanced shares
+        assert cs >= 8  # few rows: spread each row wide
+    if rows * 16 * 2 <= 7 * 152 and stride // 4 >= 16 * 256:
+        assert cs == 16  # very few long rows: sixteen CTAs each
+    assert share_vec <= max(4096, -(-(stride // 4) // 16))  # balanced shares
     assert p["threads"] == 128 and 3 <= p["ring_stages"] <= 16
     per_sm = min(7, (228 * 1024) // (p["smem_bytes"] + 1024))
     if p["ring_stages"] > 3:  # a deeper ring only while every cluster stays resident at once

@@ -133,7 +133,7 @@ def test_sweep_cells_prefill(gvr, bs, n, k):
 
 
 # ----------------------------------------------------------------------------- geometry and paths
-@pytest.mark.parametrize("cs", [1, 2, 4, 8])
+@pytest.mark.parametrize("cs", [1, 2, 4, 8, 16])
 def test_every_cluster_size(gvr, cs):
     """Every cluster size: shares from a fraction of one ring stage to many stages."""
     case = workloads.decode_batch(seed=77, requests=6, next_n=2, cr=1, k=1024, stride=40960, kv_lo=900,
@@ -148,7 +148,7 @@ def test_every_ring_depth(gvr, stages):
     """Ring depths wrap the per-slot barrier phases differently; results must not change."""
     case = workloads.decode_batch(seed=79, requests=5, next_n=2, cr=2, k=512, stride=65536, kv_lo=2000,
                                   kv_hi=131072, boundary=False)
-    for cs in (1, 8):
+    for cs in (1, 8, 16):
         assert_decode_exact(gvr, case, options=gvr.Options(cluster_size=cs, ring_stages=stages))
         assert_decode_exact(gvr, case, options=gvr.Options(cluster_size=cs, ring_stages=stages, flags=1))
 
