@@ -146,7 +146,9 @@ Geometry plan_geometry(int64_t row_stride, int64_t num_rows, int32_t k, int sms,
       cs_min *= 2;
     if (cs_max < cs_min) cs_max = cs_min;
     g.cs = cs_min;
-    while (g.cs < cs_max && num_rows * g.cs * 2 <= slots) g.cs *= 2;
+    // widen while the wider launch fills at most half the slots (a quarter for the step to 16,
+    // whose CTAs would otherwise share SMs and shallow rings without adding throughput)
+    while (g.cs < cs_max && num_rows * g.cs * 2 * (g.cs >= 8 ? 2 : 1) <= slots) g.cs *= 2;
   }
   if (o && o->ring_stages) {
     g.nstage = o->ring_stages;
