@@ -61,6 +61,7 @@ constexpr int MAX_STAGES = 16;
 constexpr int LIST_CAP = 768;         // above-floor scores kept per CTA for the collect step
 constexpr int LIST_SEG = LIST_CAP / (THREADS / 32);  // each warp appends to its own segment
 constexpr int CAP = 512;              // candidate slots in cluster rank 0
+constexpr int BIG_CAP = MIN_STAGES * STAGE_VEC * 16 / 8;  // candidates rank 0's idle ring can hold
 constexpr int RANK_REFINE_MAX = 256;  // m at or below: refine by pairwise ranking
 constexpr int SPARSE_MAX = 4;         // above-floor scores of a thread per stage before a warp aggregates
 constexpr int MAX_K = 2048;
@@ -160,6 +161,7 @@ static_assert(offsetof(Smem, hist) % 16 == 0 && offsetof(Smem, tot) % 16 == 0,
 static_assert(offsetof(Smem, bar) % 8 == 0, "mbarriers must be 8-byte aligned");
 static_assert(2 * 256 + 4 <= NB, "the rescue's digit totals and key bounds live in tot");
 static_assert(offsetof(Smem, wsum) >= sizeof(uint64_t) * MAX_K, "sort keys fit below the scalars");
+static_assert(BIG_CAP > CAP, "the ring holds more candidates than the buffer");
 
 __device__ __forceinline__ uint32_t* digit_hist(Smem& S, int buf) { return S.tot + 256 * buf; }
 
@@ -1117,9 +1119,13 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     const uint32_t cap = (p.flags & FLAG_ZERO_CAP) ? 0u : uint32_t(CAP);
     if (cr.total < uint32_t(k))
       path = PATH_RESCUE_OVERFLOW;  // NaN in the window (out of contract)
-    else if (cr.m > cap)  // every list complete: the cluster selects among the listed scores
+    else if (cr.m > cap && (p.flags & FLAG_ZERO_CAP || det || rounds != 1 || S.unlisted != 0 ||
+                            cr.m > uint32_t(BIG_CAP)))
+      // every list complete: the cluster selects among the listed scores
       path = (rounds == 1 && S.unlisted == 0 && !(p.flags & FLAG_STREAM_RESCUE)) ? PATH_REFINE_CLUSTER
                                                                                    : PATH_RESCUE_OVERFLOW;
+    // else CAP < m <= BIG_CAP with every list complete: rank 0 collects the candidates in its
+    // ring, idle since no CTA reads the row again, and refines them alone
   }
   // Candidates are the scores of the crossing bin that were counted: after one pass, the scores
   // >= thr (this only matters when the crossing is the partial floor bin).
@@ -1132,8 +1138,12 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     if (tid == 32) S.base_cand = dsmem_atom_add(dsmem_map(smem_u32(&S.gctr_cand), 0), cr.my_cand);
     __syncthreads();
     const int bstar = cr.bin;
-    const uint32_t rv = dsmem_map(smem_u32(&S.cand_v[0]), 0);
-    const uint32_t rj = dsmem_map(smem_u32(&S.cand_j[0]), 0);
+    const bool big = cr.m > uint32_t(CAP);
+    float* const cand_v = big ? reinterpret_cast<float*>(&ring[0][0]) : S.cand_v;
+    int32_t* const cand_j = big ? reinterpret_cast<int32_t*>(&ring[0][0]) + BIG_CAP : S.cand_j;
+    const uint32_t cand_cap = big ? uint32_t(BIG_CAP) : uint32_t(CAP);
+    const uint32_t rv = dsmem_map(smem_u32(cand_v), 0);
+    const uint32_t rj = dsmem_map(smem_u32(cand_j), 0);
     auto place = [&](float e, int32_t jw, bool valid) {  // warp-collective
       const int b = valid ? value_bin(e, gmin, sc) : -1;
       const uint32_t ws = warp_alloc_local(&S.ctr_win, b > bstar);
@@ -1147,7 +1157,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       const uint32_t cslot = warp_alloc_local(&S.ctr_cand, b == bstar);
       if (b == bstar) {
         const uint32_t c = S.base_cand + cslot;
-        if (c < uint32_t(CAP)) {  // always true: m <= CAP on this path
+        if (c < cand_cap) {  // always true: m fits the buffer on this path
           dsmem_st_u32(rv + 4u * c, __float_as_uint(e));
           dsmem_st_u32(rj + 4u * c, uint32_t(jw));
         }
@@ -1176,17 +1186,17 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
 
     // ------------------------------------------------------------ refine (rank 0)
     const uint32_t need = uint32_t(k) - cr.above;
-    const uint32_t mm = cr.m < uint32_t(CAP) ? cr.m : uint32_t(CAP);
+    const uint32_t mm = cr.m < cand_cap ? cr.m : cand_cap;
     if ((mm <= uint32_t(RANK_REFINE_MAX) && !(p.flags & FLAG_RADIX_REFINE)) || det) {
       // (deterministic mode ranks every candidate set: ties by smallest index)
       // rank of candidate i = number of candidates ordered before it by (value desc, index asc)
       for (uint32_t i = tid; i < mm; i += T) {
-        const float v = S.cand_v[i];
-        const int32_t j = S.cand_j[i];
+        const float v = cand_v[i];
+        const int32_t j = cand_j[i];
         uint32_t r = 0;
         for (uint32_t q = 0; q < mm; ++q) {
-          const float w = S.cand_v[q];
-          const int32_t jj = S.cand_j[q];
+          const float w = cand_v[q];
+          const int32_t jj = cand_j[q];
           r += (w > v) || (w == v && jj < j);
         }
         if (r < need && cr.above + r < uint32_t(k)) {
@@ -1204,7 +1214,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
         for (uint32_t b0 = 0; b0 < mm; b0 += T) {
           const uint32_t i = b0 + tid;
           const bool in = i < mm;
-          const uint32_t key = in ? order_key(S.cand_v[i]) : 0u;
+          const uint32_t key = in ? order_key(cand_v[i]) : 0u;
           const bool pr = in && (key & pmask) == prefix;
           hist_add(digit_hist(S, 0), pr, (key >> shift) & 255u);
         }
@@ -1225,18 +1235,18 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       for (uint32_t b0 = 0; b0 < mm; b0 += T) {
         const uint32_t i = b0 + tid;
         const bool in = i < mm;
-        const uint32_t key = in ? order_key(S.cand_v[i]) : 0u;
+        const uint32_t key = in ? order_key(cand_v[i]) : 0u;
         const bool win = in && (ge ? (key & pmask) >= prefix : key > prefix);
         const bool tie = in && !ge && key == prefix;
         const uint32_t ws = warp_alloc_local(&S.ctr_rwin, win);
         if (win && win_base + ws < tie_base) {
-          out[win_base + ws] = S.cand_j[i];
-          if (outv) outv[win_base + ws] = S.cand_v[i];
+          out[win_base + ws] = cand_j[i];
+          if (outv) outv[win_base + ws] = cand_v[i];
         }
         const uint32_t ts = warp_alloc_local(&S.ctr_rtie, tie);
         if (tie && ts < nties) {
-          out[tie_base + ts] = S.cand_j[i];
-          if (outv) outv[tie_base + ts] = S.cand_v[i];
+          out[tie_base + ts] = cand_j[i];
+          if (outv) outv[tie_base + ts] = cand_v[i];
         }
       }
     }

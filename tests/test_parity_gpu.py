@@ -328,21 +328,23 @@ def test_signed_zero_and_inf_classes(gvr):
 
 
 @pytest.mark.parametrize("cs", [0, 2, 8])
-def test_cluster_refine_over_lists(gvr, cs):
+def test_large_crossing_bins(gvr, cs):
     """Crossing bins larger than the candidate buffer whose members every CTA still listed.
 
     Row families: a plateau of P equal scores on top (tau is the plateau), winners above a
-    plateau that holds tau, and a narrow band of distinct values around tau.  The selection then
-    runs the cluster's digit passes over the per-CTA lists (path 5), seeded with the crossing bin.
+    plateau that holds tau, and a narrow band of distinct values around tau.  Up to BIG_CAP
+    (1536) members, rank 0 collects them in its idle ring and refines them alone (path 1 with
+    m > 512); beyond, the cluster's digit passes run over the per-CTA lists (path 5), seeded
+    with the crossing bin.
     """
     g = np.random.default_rng(500 + cs)
     k, stride = 512, 65536
     rows = []
-    for p in (600, 1000, 1500):
+    for p in (600, 1000, 1500, 2500, 3500):
         r = g.standard_normal(stride).astype(np.float32)
         r[g.choice(stride, p, replace=False)] = 3.5
         rows.append(r)
-    for above, plateau in ((300, 900), (100, 1200), (511, 700)):
+    for above, plateau in ((300, 900), (100, 1200), (511, 700), (200, 2600)):
         r = g.standard_normal(stride).astype(np.float32)
         pos = g.choice(stride, above + plateau, replace=False)
         r[pos[:above]] = 5.0 + g.random(above).astype(np.float32)
@@ -356,7 +358,8 @@ def test_cluster_refine_over_lists(gvr, cs):
     case = workloads.DecodeCase("plateau_lists", lg, np.full(len(rows), stride, np.int32), 1, 1, k)
     st = assert_decode_exact(gvr, case, options=gvr.Options(cluster_size=cs), stats=True)
     if cs != 2:  # two CTAs per row: the lists hold too few of the ~2K above-floor scores
-        assert (st[:, 0] == 5).any(), st
+        assert ((st[:, 0] == 1) & (st[:, 1] > 512)).any(), st  # rank 0 refined a large bin
+        assert (st[:, 0] == 5).any(), st  # the cluster refined a larger one over the lists
     assert (st[st[:, 0] == 5, 1] > 512).all(), st
 
 
