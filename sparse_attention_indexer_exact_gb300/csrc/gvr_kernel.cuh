@@ -6,10 +6,11 @@
 // is read from HBM once and each CTA needs little shared memory: several CTAs -- several rows
 // -- are resident on every SM at a time.  Per row:
 //
-//   Guess   uniform block64 sampling: K scores in K/64 runs of 64 consecutive scores whose
-//           starts spread evenly over the window, first run at 0, last run ending at nv.
-//           GMIN / GMAX are the smallest / largest finite sample ("GVR K=2048 reg_clus with
-//           block64 sampling and parallel rescue", TensorRT-LLM PR #20998, "What changes").
+//   Guess   uniform block64 sampling: runs of 64 consecutive scores whose starts spread
+//           evenly over the window, first run at 0, last run ending at nv -- K/64 runs, as in
+//           "GVR K=2048 reg_clus with block64 sampling and parallel rescue" (TensorRT-LLM PR
+//           #20998, "What changes"), or more when K is small against nv (at most 32).
+//           GMIN / GMAX are the smallest / largest finite sample.
 //   Verify  a value histogram of NB bins over [GMIN, GMAX] (values above GMAX saturate into
 //           the top bin, below GMIN into bin 0); its cluster-wide suffix sums locate the bin
 //           b* that crosses the K-th largest value tau ("Why the GLM row overflows").
@@ -65,6 +66,19 @@ constexpr int BIG_CAP = MIN_STAGES * STAGE_VEC * 16 / 8;  // candidates rank 0's
 constexpr int RANK_REFINE_MAX = 256;  // m at or below: refine by pairwise ranking
 constexpr int SPARSE_MAX = 4;         // above-floor scores of a thread per stage before a warp aggregates
 constexpr int MAX_K = 2048;
+constexpr int MAX_SAMPLES = 2048;     // block64 samples per row at most (32 runs, one per lane)
+
+// Samples of a long row (nv > k): k (the k / 64 runs of uniform block64 sampling), or more
+// when k is small against nv -- enough runs, up to MAX_SAMPLES, that about 8 samples are
+// expected above the K-th score (k * samples / nv >= 8).  The floor keeps a margin of a few
+// samples over that expectation, so with fewer samples it would count and list several times
+// K scores.
+__host__ __device__ constexpr uint32_t sample_count(uint32_t k, uint32_t nv) {
+  const uint32_t runs = (nv + 8u * k - 1u) / (8u * k);  // ceil(nv / 8k): nv < 2^31, k <= 2048
+  const uint32_t n = 64u * runs;
+  return n <= k ? k : (n >= uint32_t(MAX_SAMPLES) ? uint32_t(MAX_SAMPLES) : n);
+}
+
 constexpr uint64_t WAIT_LIMIT_NS = 500000000ull;  // bound on any wait for staged data (0.5 s)
 
 enum : int32_t { MODE_DECODE = 0, MODE_PREFILL = 1 };
@@ -727,7 +741,8 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   };
 
   // ---------------------------------------------------------------- guess: block64 sample
-  const uint32_t nblk = uint32_t(k) >> 6;
+  const uint32_t nsamp = sample_count(uint32_t(k), nv);
+  const uint32_t nblk = nsamp >> 6;
   // Start of run b = floor(b (nv - 64) / (nblk - 1)), one run per lane (nblk <= 32), with no
   // 64-bit arithmetic: b (nv - 64) = b sq (nblk - 1) + b sr.
   const uint32_t sq = (nv - 64u) / (nblk - 1u), sr = (nv - 64u) % (nblk - 1u);
@@ -738,7 +753,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     const uint32_t i = uint32_t(q * T + tid);
     const uint32_t blk = i >> 6;
     const uint32_t s = __shfl_sync(FULL_MASK, run_start, blk & 31u);
-    sv[q] = i < uint32_t(k) ? __ldg(rowp + a + s + (i & 63u)) : qnan;
+    sv[q] = i < nsamp ? __ldg(rowp + a + s + (i & 63u)) : qnan;
   }
   // Hinted sampling adds the k scores at the request's previous selection.  Any content is
   // accepted: positions outside [0, nv) (the -1 pad, stale or garbage entries) are skipped and
@@ -895,13 +910,13 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   if (path == PATH_REFINE) {
     sc = __fdiv_rn(float(NB), __fsub_rn(gmax, gmin));
     if (!(p.flags & FLAG_NO_FLOOR)) {
-      // mu = k*k/nv samples are expected above tau (a Poisson count); keep mu + 3 sqrt(mu) + 6
-      // above the floor.  A second pass is then rare enough per row (below 1e-4 for every mu of
-      // the workloads) that a batch of hundreds of rows seldom has one: the launch waits for its
-      // slowest row, so the margin is sized for the batch, not for the single row.
-      const float mu = float(k) * float(k) / float(nv);
+      // mu = k*nsamp/nv samples are expected above tau (a Poisson count); keep mu + 3 sqrt(mu)
+      // + 6 above the floor.  A second pass is then rare enough per row (below 1e-4 for every mu
+      // of the workloads) that a batch of hundreds of rows seldom has one: the launch waits for
+      // its slowest row, so the margin is sized for the batch, not for the single row.
+      const float mu = float(k) * float(nsamp) / float(nv);
       const float want_f = mu + 3.0f * sqrtf(mu) + 6.0f;
-      const uint32_t want = want_f < float(k) ? uint32_t(want_f) : uint32_t(k);
+      const uint32_t want = want_f < float(nsamp) ? uint32_t(want_f) : nsamp;
       // The samples' own histogram on the same bins (in this CTA's private counts, cleared
       // again below): the floor is the lower edge of the bin where `want` samples are reached.
 #pragma unroll

@@ -138,7 +138,9 @@ Geometry plan_geometry(int64_t row_stride, int64_t num_rows, int32_t k, int sms,
     if (cs_max > kMaxCluster) cs_max = kMaxCluster;
     const int64_t slots = int64_t(sms) * ctas_per_sm(gvr::MIN_STAGES, smem_per_sm, smem_reserved);
     const double nv = double(row_stride);
-    const double listed = k > 0 ? double(k) + 3.0 * std::sqrt(nv) + 6.0 * nv / double(k) : 0.0;
+    // scores expected above the sampled floor: (mu + 3 sqrt(mu) + 6) nv / samples, mu = k samples / nv
+    const double ns = double(gvr::sample_count(uint32_t(k > 0 ? k : 0), uint32_t(row_stride)));
+    const double listed = k > 0 ? double(k) + 3.0 * std::sqrt(double(k) * nv / ns) + 6.0 * nv / ns : 0.0;
     while (cs_min < kMaxCluster && listed > double(kListTarget) * cs_min &&
            (need_vec + int64_t(cs_min) * gvr::STAGE_VEC - 1) / (int64_t(cs_min) * gvr::STAGE_VEC) >
                kCheapRereadStages &&
