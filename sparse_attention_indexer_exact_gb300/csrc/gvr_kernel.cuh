@@ -1120,8 +1120,10 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       csync();  // every CTA has finished reading its totals before new counts arrive
       stream_pass(false, [&](uint32_t slot, int32_t c0) {
         each_lane(slot, c0, [&](float e, int32_t, bool valid, int) {
+          // most scores hit here, with bins that differ: plain atomics (the hardware merges
+          // lanes that share an address) beat aggregating them first
           const bool hit = valid && e < thr;
-          if (__any_sync(FULL_MASK, hit)) hist_add(S.hist, hit, uint32_t(value_bin(e, gmin, sc)));
+          if (hit) atomicAdd(&S.hist[value_bin(e, gmin, sc)], 1u);
         });
       });
       push(0, fpart);
@@ -1231,7 +1233,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
           const bool in = i < mm;
           const uint32_t key = in ? order_key(cand_v[i]) : 0u;
           const bool pr = in && (key & pmask) == prefix;
-          hist_add(digit_hist(S, 0), pr, (key >> shift) & 255u);
+          if (pr) atomicAdd(&digit_hist(S, 0)[(key >> shift) & 255u], 1u);
         }
         __syncthreads();
         digit_cross<T>(S, 0, rank, 1, rneed);
@@ -1457,9 +1459,10 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
         if (dmin == dmax) {
           const uint32_t c = __reduce_add_sync(FULL_MASK, uint32_t(__popc(pm)));
           if (lane == 0) atomicAdd(&dloc[dmin], c);
-        } else if (dmin < dmax) {
+        } else if (dmin < dmax) {  // plain atomics: the hardware merges lanes on one digit
 #pragma unroll
-          for (int j = 0; j < N; ++j) hist_add(dloc, (pm >> j) & 1u, (keys[j] >> shift) & 255u);
+          for (int j = 0; j < N; ++j)
+            if ((pm >> j) & 1u) atomicAdd(&dloc[(keys[j] >> shift) & 255u], 1u);
         }
       };
       if (from_lists) {
