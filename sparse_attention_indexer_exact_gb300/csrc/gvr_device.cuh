@@ -192,10 +192,4 @@ __device__ __forceinline__ void dsmem_red_max(uint32_t addr, uint32_t v) {
 
 namespace gvr {
 
-// Ask the TMA unit to bring [src, src + bytes) into L2 (no completion, no shared memory).
-// src 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 }  // namespace gvr

@@ -770,13 +770,6 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   // The first ring stages go in flight right behind the samples, one lane of warp 0 per stage.
   if (warp == 0 && !bmax_row)
     for (int32_t s = lane; s < nst && s < nstages; s += 32) issue_stage(s, uint32_t(s));
-  // Every later stage of this CTA is requested into L2 now (no shared memory needed), so HBM
-  // streams the whole row at once and the ring's refills are L2 hits.
-  if (warp == 1 && !bmax_row)
-    for (int32_t s = nst + lane; s < nstages; s += 32) {
-      const int32_t nfull = stage_full(s);
-      if (nfull > 0) bulk_prefetch_l2(base + 4 * size_t(stage_first(s)), uint32_t(nfull) * 16u);
-    }
   // Zero the counters while the samples are in flight (global loads are not waited for here).
   for (int i = tid; i < NB; i += T) S.hist[i] = S.tot[i] = 0;
   if (tid == 0) {
