@@ -122,7 +122,7 @@ def test_adversarial_row(gvr, variant):
 
 
 @pytest.mark.parametrize("bs,n,k", [(1, 16384, 512), (4, 32768, 1024), (16, 65536, 2048), (4, 131072, 512),
-                                    (1, 131072, 2048), (64, 16384, 1024)])
+                                    (1, 131072, 2048), (64, 16384, 1024), (64, 131072, 512), (16, 65536, 512)])
 def test_sweep_cells_decode(gvr, bs, n, k):
     assert_decode_exact(gvr, workloads.sweep_decode(bs, n, k))
 
@@ -373,6 +373,37 @@ def test_relist_after_list_overflow(gvr):
     assert ((st[st[:, 0] == 6, 2] // 10) >= 1).any(), st  # some shares were read again
     for flags in (16, 32):
         assert_decode_deterministic(gvr, case, flags, 2 | 4)
+
+
+def test_second_pass_block_concentrated(gvr):
+    """Sink, recent tokens and hot blocks: the block64 runs at both row ends over-represent the
+    top, the sampled floor is too high and the rows need the second counting pass (scores below
+    the floor), then the collect reads the share again."""
+    case = workloads.peaky_decode_batch(requests=24)
+    st = assert_decode_exact(gvr, case, stats=True)
+    long_rows = case.row_lengths() > case.k
+    assert ((st[long_rows, 2] % 10) == 2).sum() >= long_rows.sum() // 2, st
+    assert_decode_deterministic(gvr, case, 16)
+
+
+def test_second_pass_ties_below_floor(gvr):
+    """Half of K scores at 10.0 exactly where the block64 runs fall, every other score 0.0: the
+    floor sits at 10.0, fewer than K scores reach it, and the second pass counts a warp of equal
+    scores at a time (tau = 0.0, a tie class of about n - K/2 members)."""
+    k, nv, rows = 1024, 131072, 4
+    lg = np.zeros((rows, nv), np.float32)
+    nblk = k // 64  # 1024 samples on these rows: k * samples / nv = 8
+    for b in range(nblk):
+        st0 = b * (nv - 64) // (nblk - 1)
+        lg[:, st0:st0 + 32] = 10.0
+    lg[1, 5] = -1.0   # a few distinct scores below the tie class
+    lg[2, 77777] = 3.0  # one more winner above it
+    case = workloads.DecodeCase("ties_below_floor", lg, np.full(rows, nv, np.int32), 1, 1, k)
+    for flags in (0, 8):
+        st = assert_decode_exact(gvr, case, options=gvr.Options(flags=flags), stats=True)
+        assert ((st[:, 2] % 10) == 2).all(), st
+    for flags in (16, 32):
+        assert_decode_deterministic(gvr, case, flags)
 
 
 def test_crossing_in_the_floor_bin(gvr):
