@@ -161,6 +161,23 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
 
 namespace gvr {
 
+// Orders this thread's earlier generic-proxy shared-memory writes before later bulk (async
+// proxy) reads of the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Bulk add of `bytes` of u32 counters from this CTA's shared memory (src) into the counters at
+// cluster address dst, counting the bytes on the mbarrier at cluster address bar (the
+// destination CTA's).  src, dst 16-byte aligned; bytes a multiple of 16.  The source must stay
+// unchanged until the destination's barrier phase has completed.
+__device__ __forceinline__ void bulk_reduce_add_u32(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.reduce.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes.add.u32 [%0], [%1], %2, [%3];"
+      ::"r"(dst), "r"(smem_u32(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // Fire-and-forget add into another CTA's shared memory (DSMEM address).
 __device__ __forceinline__ void dsmem_red_add(uint32_t addr, uint32_t v) {
   asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
@@ -190,6 +207,3 @@ __device__ __forceinline__ void dsmem_red_max(uint32_t addr, uint32_t v) {
 
 }  // namespace gvr
 
-namespace gvr {
-
-}  // namespace gvr

@@ -63,6 +63,7 @@ constexpr int LIST_CAP = 768;         // above-floor scores kept per CTA for the
 constexpr int LIST_SEG = LIST_CAP / (THREADS / 32);  // each warp appends to its own segment
 constexpr int CAP = 512;              // candidate slots in cluster rank 0
 constexpr int BIG_CAP = MIN_STAGES * STAGE_VEC * 16 / 8;  // candidates rank 0's idle ring can hold
+constexpr int BULK_BINS = 512;       // first-pass counts of at most this many bins go as bulk adds
 constexpr int RANK_REFINE_MAX = 256;  // m at or below: refine by pairwise ranking
 constexpr int SPARSE_MAX = 4;         // above-floor scores of a thread per stage before a warp aggregates
 constexpr int MAX_K = 2048;
@@ -133,9 +134,11 @@ struct Crossing {
 };
 
 struct alignas(16) Smem {
-  uint32_t hist[NB];               // this CTA's counts (groups of 4 bins read as 16-byte vectors)
-  uint32_t tot[NB];                // cluster-wide counts, pushed here by every CTA of the cluster;
-                                   // the rescue's two 256-bin digit histograms reuse it
+  uint32_t hist[NB + 4];           // this CTA's counts (groups of 4 bins read as 16-byte vectors);
+                                   // hist[NB]: 1 when this CTA's list overflowed in pass 1
+  uint32_t tot[NB + 4];            // cluster-wide counts, added here by every CTA of the cluster
+                                   // (tot[NB]: CTAs whose list overflowed); the rescue's two
+                                   // 256-bin digit histograms reuse it
   float list_v[LIST_CAP];
   int32_t list_j[LIST_CAP];
   float cand_v[CAP];
@@ -169,6 +172,7 @@ struct alignas(16) Smem {
   uint32_t tout;                   // this CTA gave up waiting for staged data
   uint32_t err;                    // rank 0: some CTA of the cluster gave up
   uint64_t bar[MAX_STAGES];        // one mbarrier per ring stage
+  uint64_t hbar;                   // completes once every CTA's first-pass counts have landed in tot
 };
 static_assert(offsetof(Smem, hist) % 16 == 0 && offsetof(Smem, tot) % 16 == 0,
               "histograms are read as 16-byte vectors");
@@ -514,6 +518,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
 #pragma unroll
     for (int s = 0; s < MAX_STAGES; ++s)
       if (s < nst) mbar_init(&S.bar[s], 1);
+    mbar_init(&S.hbar, 1);
     mbar_init_fence();
   }
 
@@ -771,7 +776,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   if (warp == 0 && !bmax_row)
     for (int32_t s = lane; s < nst && s < nstages; s += 32) issue_stage(s, uint32_t(s));
   // Zero the counters while the samples are in flight (global loads are not waited for here).
-  for (int i = tid; i < NB; i += T) S.hist[i] = S.tot[i] = 0;
+  for (int i = tid; i < NB + 4; i += T) S.hist[i] = S.tot[i] = 0;
   if (tid == 0) {
     for (int w = 0; w < NW; ++w) S.list_n[w] = 0;
     S.ctr_win = S.ctr_cand = S.ctr_rwin = S.ctr_rtie = 0;
@@ -846,7 +851,10 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     S.hpart_cnt = hcnt;
   }
   // Every CTA's totals and rank 0's counters are now zero; no CTA of the cluster adds to them
-  // before it has waited on this (split) barrier, right before its first remote update.
+  // before it has waited on this (split) barrier, right before its first remote update.  The
+  // bulk adds that land in the totals go through the async proxy, so the zeros are fenced
+  // for it first.
+  fence_proxy_async_smem();
   cluster_arrive();
   bool init_waited = false;
   auto wait_init = [&]() {
@@ -1094,10 +1102,35 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
         }
       }
     };
-    push(fpart > 0 ? fpart : 0, NB - 1);
-    if (tid == 0 && !listed)
-      for (uint32_t c = 0; c < cs; ++c) dsmem_red_add(dsmem_map(smem_u32(&S.unlisted), c), 1u);
-    csync();
+    // The counts of bins >= the floor's bin go to every CTA of the cluster.  A narrow range
+    // (the usual case: the floor a few hundred bins below the sampled maximum) goes as bulk
+    // adds, one per destination from a 16-byte boundary (the bins below the floor are zero
+    // here), with the list flag in hist[NB]; each CTA's barrier counts the bytes of all of them
+    // (the floor is cluster-uniform, so every CTA expects the same count) and no cluster
+    // barrier is needed.  A wide range -- a far outlier stretched the bins, few of them are
+    // occupied -- goes bin by bin, only the occupied ones, then a cluster barrier.
+    const int fb0 = (fpart > 0 ? fpart : 0) & ~3;
+    if (NB - fb0 <= BULK_BINS) {
+      const uint32_t pbytes = uint32_t(NB + 4 - fb0) * 4u;
+      if (tid == 0) S.hist[NB] = listed ? 0u : 1u;
+      fence_proxy_async_smem();  // the counts, written by this CTA's threads, are read by the bulk copies
+      wait_init();               // every CTA's totals are zero and its barrier initialized
+      __syncthreads();
+      if (tid == 0) {
+        for (uint32_t c = 0; c < cs; ++c)
+          bulk_reduce_add_u32(dsmem_map(smem_u32(&S.tot[fb0]), c), &S.hist[fb0], pbytes,
+                              dsmem_map(smem_u32(&S.hbar), c));
+        mbar_arrive_expect_tx(&S.hbar, cs * pbytes);
+      }
+      if (!mbar_wait_bounded(&S.hbar, 0, WAIT_LIMIT_NS)) late = true;
+      if (__syncthreads_or(late) && tid == 0) S.tout = 1;
+      if (tid == 0) S.unlisted = S.tot[NB];
+    } else {
+      push(fpart > 0 ? fpart : 0, NB - 1);
+      if (tid == 0 && !listed)
+        for (uint32_t c = 0; c < cs; ++c) dsmem_red_add(dsmem_map(smem_u32(&S.unlisted), c), 1u);
+      csync();
+    }
     report_timeout();
     cr = scan_crossing<T>(S, uint32_t(k));
     if (fpart >= 0 && cr.total < uint32_t(k)) {
@@ -1106,11 +1139,14 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       // is at or above it, and a crossing in the partial floor bin needs no second pass: its
       // candidates are the counted scores, those >= thr.)
       rounds = 2;
+      // every CTA has finished reading its totals before new counts arrive, and every bulk add
+      // of the first counts (reading hist) has landed
+      csync();
       if (tid == 0) {
         S.saved = S.hist[fpart];
         S.hist[fpart] = 0;
       }
-      csync();  // every CTA has finished reading its totals before new counts arrive
+      __syncthreads();
       stream_pass(false, [&](uint32_t slot, int32_t c0) {
         each_lane(slot, c0, [&](float e, int32_t, bool valid, int) {
           // most scores hit here, with bins that differ: plain atomics (the hardware merges
