@@ -62,9 +62,10 @@ constexpr int MAX_STAGES = 16;
 constexpr int LIST_CAP = 768;         // above-floor scores kept per CTA for the collect step
 constexpr int LIST_SEG = LIST_CAP / (THREADS / 32);  // each warp appends to its own segment
 constexpr int CAP = 512;              // candidate slots in cluster rank 0
-constexpr int BIG_CAP = MIN_STAGES * STAGE_VEC * 16 / 8;  // candidates rank 0's idle ring can hold
+constexpr int RING_CAND = STAGE_VEC * 16 / 8;  // (score, index) candidates one idle ring stage holds
 constexpr int BULK_BINS = 512;       // first-pass counts of at most this many bins go as bulk adds
-constexpr int RANK_REFINE_MAX = 256;  // m at or below: refine by pairwise ranking
+constexpr int RANK_REFINE_MAX = 256;
+constexpr uint32_t UNLISTED_RANK0 = 1u << 16;  // marks rank 0's overflowed list in the count  // m at or below: refine by pairwise ranking
 constexpr int SPARSE_MAX = 4;         // above-floor scores of a thread per stage before a warp aggregates
 constexpr int MAX_K = 2048;
 constexpr int MAX_SAMPLES = 2048;     // block64 samples per row at most (32 runs, one per lane)
@@ -159,7 +160,8 @@ struct alignas(16) Smem {
   uint32_t dsel, dabove, dcnt, dmy_above, dmy_at;
   uint32_t kmin_loc, kmax_loc;     // rescue: smallest / largest key of this CTA's matching scores
   uint32_t list_n[THREADS / 32];   // scores each warp appended to its segment (may exceed LIST_SEG)
-  uint32_t unlisted;               // CTAs of the cluster whose list overflowed (each pushes 1)
+  uint32_t unlisted;               // CTAs of the cluster whose list overflowed (each adds 1; rank 0
+                                   // adds 1 + UNLISTED_RANK0)
   uint32_t relist_n;               // scores of the crossing bin and above listed again
   uint32_t relist_bad;             // CTAs of the cluster whose second list overflowed
   uint32_t klo, khi;               // order keys bounding the crossing bin's members
@@ -179,7 +181,7 @@ static_assert(offsetof(Smem, hist) % 16 == 0 && offsetof(Smem, tot) % 16 == 0,
 static_assert(offsetof(Smem, bar) % 8 == 0, "mbarriers must be 8-byte aligned");
 static_assert(2 * 256 + 4 <= NB, "the rescue's digit totals and key bounds live in tot");
 static_assert(offsetof(Smem, wsum) >= sizeof(uint64_t) * MAX_K, "sort keys fit below the scalars");
-static_assert(BIG_CAP > CAP, "the ring holds more candidates than the buffer");
+static_assert(MIN_STAGES * RING_CAND > CAP, "the ring holds more candidates than the buffer");
 
 __device__ __forceinline__ uint32_t* digit_hist(Smem& S, int buf) { return S.tot + 256 * buf; }
 
@@ -1112,7 +1114,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     const int fb0 = (fpart > 0 ? fpart : 0) & ~3;
     if (NB - fb0 <= BULK_BINS) {
       const uint32_t pbytes = uint32_t(NB + 4 - fb0) * 4u;
-      if (tid == 0) S.hist[NB] = listed ? 0u : 1u;
+      if (tid == 0) S.hist[NB] = listed ? 0u : (rank == 0 ? 1u + UNLISTED_RANK0 : 1u);
       fence_proxy_async_smem();  // the counts, written by this CTA's threads, are read by the bulk copies
       wait_init();               // every CTA's totals are zero and its barrier initialized
       __syncthreads();
@@ -1128,7 +1130,8 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     } else {
       push(fpart > 0 ? fpart : 0, NB - 1);
       if (tid == 0 && !listed)
-        for (uint32_t c = 0; c < cs; ++c) dsmem_red_add(dsmem_map(smem_u32(&S.unlisted), c), 1u);
+        for (uint32_t c = 0; c < cs; ++c)
+          dsmem_red_add(dsmem_map(smem_u32(&S.unlisted), c), rank == 0 ? 1u + UNLISTED_RANK0 : 1u);
       csync();
     }
     report_timeout();
@@ -1165,13 +1168,14 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     const uint32_t cap = (p.flags & FLAG_ZERO_CAP) ? 0u : uint32_t(CAP);
     if (cr.total < uint32_t(k))
       path = PATH_RESCUE_OVERFLOW;  // NaN in the window (out of contract)
-    else if (cr.m > cap && (p.flags & FLAG_ZERO_CAP || det || rounds != 1 || S.unlisted != 0 ||
-                            cr.m > uint32_t(BIG_CAP)))
+    else if (cr.m > cap && (p.flags & FLAG_ZERO_CAP || det || rounds != 1 || S.unlisted >= UNLISTED_RANK0 ||
+                            cr.m > uint32_t(nst) * RING_CAND))
       // every list complete: the cluster selects among the listed scores
       path = (rounds == 1 && S.unlisted == 0 && !(p.flags & FLAG_STREAM_RESCUE)) ? PATH_REFINE_CLUSTER
                                                                                    : PATH_RESCUE_OVERFLOW;
-    // else CAP < m <= BIG_CAP with every list complete: rank 0 collects the candidates in its
-    // ring, idle since no CTA reads the row again, and refines them alone
+    // else CAP < m <= (ring stages) * RING_CAND after one pass with rank 0's list complete: rank
+    // 0 collects the candidates in its ring, idle since rank 0 does not read the row again (CTAs
+    // whose list overflowed read their own share through their own ring), and refines alone
   }
   // Candidates are the scores of the crossing bin that were counted: after one pass, the scores
   // >= thr (this only matters when the crossing is the partial floor bin).
@@ -1185,9 +1189,10 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     __syncthreads();
     const int bstar = cr.bin;
     const bool big = cr.m > uint32_t(CAP);
+    const uint32_t ring_cap = uint32_t(nst) * RING_CAND;  // scores first, then their indices
     float* const cand_v = big ? reinterpret_cast<float*>(&ring[0][0]) : S.cand_v;
-    int32_t* const cand_j = big ? reinterpret_cast<int32_t*>(&ring[0][0]) + BIG_CAP : S.cand_j;
-    const uint32_t cand_cap = big ? uint32_t(BIG_CAP) : uint32_t(CAP);
+    int32_t* const cand_j = big ? reinterpret_cast<int32_t*>(&ring[0][0]) + ring_cap : S.cand_j;
+    const uint32_t cand_cap = big ? ring_cap : uint32_t(CAP);
     const uint32_t rv = dsmem_map(smem_u32(cand_v), 0);
     const uint32_t rj = dsmem_map(smem_u32(cand_j), 0);
     auto place = [&](float e, int32_t jw, bool valid) {  // warp-collective

@@ -332,10 +332,11 @@ def test_large_crossing_bins(gvr, cs):
     """Crossing bins larger than the candidate buffer whose members every CTA still listed.
 
     Row families: a plateau of P equal scores on top (tau is the plateau), winners above a
-    plateau that holds tau, and a narrow band of distinct values around tau.  Up to BIG_CAP
-    (1536) members, rank 0 collects them in its idle ring and refines them alone (path 1 with
-    m > 512); beyond, the cluster's digit passes run over the per-CTA lists (path 5), seeded
-    with the crossing bin.
+    plateau that holds tau, and a narrow band of distinct values around tau.  Up to 512 members
+    per ring stage (1536 with the 3-stage ring forced here), rank 0 collects them in its idle
+    ring and refines them alone (path 1 with m > 512); beyond, the cluster's digit passes run
+    over the per-CTA lists (path 5), seeded with the crossing bin.  With the automatic ring
+    depth the same rows are exact, and a deeper ring takes larger bins on rank 0.
     """
     g = np.random.default_rng(500 + cs)
     k, stride = 512, 65536
@@ -356,11 +357,35 @@ def test_large_crossing_bins(gvr, cs):
         rows.append(r)
     lg = np.stack(rows)
     case = workloads.DecodeCase("plateau_lists", lg, np.full(len(rows), stride, np.int32), 1, 1, k)
-    st = assert_decode_exact(gvr, case, options=gvr.Options(cluster_size=cs), stats=True)
+    st = assert_decode_exact(gvr, case, options=gvr.Options(cluster_size=cs, ring_stages=3), stats=True)
     if cs != 2:  # two CTAs per row: the lists hold too few of the ~2K above-floor scores
         assert ((st[:, 0] == 1) & (st[:, 1] > 512)).any(), st  # rank 0 refined a large bin
         assert (st[:, 0] == 5).any(), st  # the cluster refined a larger one over the lists
     assert (st[st[:, 0] == 5, 1] > 512).all(), st
+    assert (st[(st[:, 0] == 1) & (st[:, 2] == 1), 1] <= 3 * 512).all(), st
+    nst = gvr.plan(stride, len(rows), k, gvr.Options(cluster_size=cs))["ring_stages"]
+    st = assert_decode_exact(gvr, case, options=gvr.Options(cluster_size=cs), stats=True)
+    assert (st[(st[:, 0] == 1) & (st[:, 2] == 1), 1] <= nst * 512).all(), (nst, st)
+
+
+def test_big_collect_with_an_overflowed_list(gvr):
+    """A crossing bin of ~1K equal scores that all sit in rank 1's first stage: rank 1's list
+    overflows, rank 0's does not, so rank 0 still collects the bin in its ring (path 1) while
+    rank 1 reads its share again for the collect."""
+    g = np.random.default_rng(77)
+    k, stride, cs = 512, 65536, 4
+    rows = []
+    for plateau in (3.0, 3.0, 2.75):
+        r = g.standard_normal(stride).astype(np.float32)
+        r[1024:2048] = plateau  # stage 1: rank 1 of 4
+        r[g.choice(np.arange(4096, stride), 300, replace=False)] = (5.0 + g.random(300)).astype(np.float32)
+        rows.append(r)
+    lg = np.stack(rows)
+    case = workloads.DecodeCase("plateau_in_one_share", lg, np.full(len(rows), stride, np.int32), 1, 1, k)
+    st = assert_decode_exact(gvr, case, options=gvr.Options(cluster_size=cs, ring_stages=3), stats=True)
+    assert ((st[:, 0] == 1) & (st[:, 1] > 512)).all(), st
+    for flags in (16, 32):
+        assert_decode_deterministic(gvr, case, flags, cluster_size=cs, ring_stages=3)
 
 
 def test_relist_after_list_overflow(gvr):
