@@ -926,7 +926,28 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       for (int q = 0; q < KPT; ++q)
         if (!isnan(sv[q])) atomicAdd(&S.hist[value_bin(sv[q], gmin, sc)], 1u);
       __syncthreads();
-      const int fb = suffix_cross<T>(S, S.hist, want);
+      int fb = suffix_cross<T>(S, S.hist, want);
+      // A far outlier sample stretches every bin, and with them the floor's bin (more scores
+      // listed) and the crossing bin (more candidates).  When mu is large enough that the r-th
+      // largest sample, r = mu - 4 sqrt(mu), lies above tau all but surely, the bins end at the
+      // top of that sample's bin instead: the scores above it clamp into the top bin, which then
+      // holds about (1 - 4 / sqrt(mu)) k of them, all winners, and the floor is found again on
+      // the narrower bins.  Only when the floor and that sample sit in the lower half of the
+      // bins (a handful of far samples stretched them).  The samples, and so the scale, are the
+      // same in every CTA.
+      const float rf = mu - 4.0f * sqrtf(mu);
+      const int hb = (rf >= 2.0f && fb < NB / 2) ? suffix_cross<T>(S, S.hist, uint32_t(rf)) : -1;
+      if (hb >= 0 && hb < NB / 2) {
+        const float hi = __fadd_rn(gmin, __fdiv_rn(float(hb + 1), sc));
+        sc = __fdiv_rn(float(NB), __fsub_rn(hi, gmin));
+        for (int i = tid; i < NB; i += T) S.hist[i] = 0;
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < KPT; ++q)
+          if (!isnan(sv[q])) atomicAdd(&S.hist[value_bin(sv[q], gmin, sc)], 1u);
+        __syncthreads();
+        fb = suffix_cross<T>(S, S.hist, want);
+      }
       if (tid == 0) {
         // any threshold works: bins above bin(t) are complete, bin(t) is partial
         const float t = fb > 0 ? __fadd_rn(gmin, __fdiv_rn(float(fb), sc)) : -INFINITY;
