@@ -19,7 +19,7 @@ namespace {
 constexpr int kThreads = gvr::THREADS;
 constexpr int kMaxDevices = 64;
 constexpr int kMaxCluster = 16;  // 16 is a non-portable cluster size (checked per ring depth)
-constexpr int64_t kShareVec = 4096;  // target float4 per CTA when a row spans several CTAs
+constexpr int64_t kShareVec = 8192;  // largest float4 share per CTA before rows are split further
 constexpr int kListTarget = 480;       // expected first-pass list entries per CTA (of LIST_CAP)
 constexpr int64_t kCheapRereadStages = 4;
 
@@ -98,12 +98,13 @@ gvr_status check_common(int64_t row_stride, int64_t num_rows, int32_t k, const g
 
 // Launch geometry.  Each CTA streams its share of a row through a shared-memory ring, so any
 // share length works; the cluster size only balances work.  A row is split so that a CTA's
-// share is about kShareVec float4 (8 CTAs cover a 131072-score row); few rows spread each row
-// over more CTAs (more SMs pulling one row), down to one ring stage per CTA.
+// share is at most kShareVec float4 (4 CTAs cover a 131072-score row: big batches stay one wave
+// of CTAs, whose fixed costs a second wave would repeat); few rows spread each row over more
+// CTAs (more SMs pulling one row), down to one ring stage per CTA.
 //
 // List capacity: the first pass lists every score above the sampled floor, about
-// k + 3 sqrt(nv) + 6 nv / k of them for a row of nv scores (the floor keeps mu + 3 sqrt(mu) + 6
-// of the k samples above it, mu = k^2 / nv).  A CTA whose list overflows reads its share once
+// k + 3 sqrt(k nv / s) + 6 nv / s of them for a row of nv scores and s samples (the floor keeps
+// mu + 3 sqrt(mu) + 6 samples above it, mu = k s / nv).  A CTA whose list overflows reads its share once
 // more, so the row is split at least so finely that a CTA expects to list at most
 // kListTarget scores -- unless the share is at most kCheapRereadStages stages, which are
 // read again cheaply, or the launch would exceed two waves of CTAs (there the extra CTAs'
