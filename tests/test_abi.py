@@ -158,13 +158,13 @@ def test_plan_geometry(lib, stride, rows, k):
     cs = p["cluster_size"]
     assert cs in (1, 2, 4, 8, 16)
     share_vec = -(-(stride // 4) // cs)
-    if stride // 4 >= 8 * 4096:
-        assert cs >= 8  # long rows always spread over a full cluster
+    if stride // 4 >= 8 * 8192:
+        assert cs >= 8  # long rows always spread over a full cluster (shares of at most 8192 float4)
     if rows * 8 * 2 <= 7 * 152 and stride // 4 >= 8 * 256:
         assert cs >= 8  # few rows: spread each row wide
     if rows * 16 * 2 <= 7 * 152 and stride // 4 >= 16 * 256:
         assert cs == 16  # very few long rows: sixteen CTAs each
-    assert share_vec <= max(4096, -(-(stride // 4) // 16))  # balanced shares
+    assert share_vec <= max(8192, -(-(stride // 4) // 16))  # balanced shares
     assert p["threads"] == 128 and 3 <= p["ring_stages"] <= 16
     per_sm = min(7, (228 * 1024) // (p["smem_bytes"] + 1024))
     if p["ring_stages"] > 3:  # a deeper ring only while every cluster stays resident at once
