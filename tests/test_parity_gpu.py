@@ -400,6 +400,29 @@ def test_relist_after_list_overflow(gvr):
         assert_decode_deterministic(gvr, case, flags, 2 | 4)
 
 
+def test_far_outlier_samples_trim_the_bins(gvr):
+    """Heavy-tailed rows whose samples include a far spike (Pareto tail up to ~10^3 sigma): the
+    bins end at a robust sample rank instead of the sampled maximum, so the crossing bin stays
+    small (no list refine, no rescue); the spikes above it clamp into the top bin as winners."""
+    case = workloads.sweep_decode(64, 32768, 2048)
+    st = assert_decode_exact(gvr, case, stats=True)
+    assert (st[:, 0] == 1).all() and (st[:, 1] <= 512).all(), st
+    g = np.random.default_rng(91)
+    k, n = 2048, 32768
+    lg = g.standard_normal((4, n)).astype(np.float32)
+    nblk = 2048 // 64  # 2048 samples on these rows
+    for r in range(4):  # a spike inside a sampled run, plus unsampled spikes elsewhere
+        st0 = (5 + r) * (n - 64) // (nblk - 1)
+        lg[r, st0 + 7] = 1e3 * (r + 1)
+        lg[r, g.choice(n, 50, replace=False)] = (20.0 + 100.0 * g.random(50)).astype(np.float32)
+    case = workloads.DecodeCase("sampled_spike", lg, np.full(4, n, np.int32), 1, 1, k)
+    for flags in (0, 8):
+        st = assert_decode_exact(gvr, case, options=gvr.Options(flags=flags), stats=True)
+        assert (st[:, 0] == 1).all() and (st[:, 1] <= 512).all(), st
+    for flags in (16, 32):
+        assert_decode_deterministic(gvr, case, flags)
+
+
 def test_second_pass_block_concentrated(gvr):
     """Sink, recent tokens and hot blocks: the block64 runs at both row ends over-represent the
     top, the sampled floor is too high and the rows need the second counting pass (scores below
