@@ -108,7 +108,11 @@ enum {
   GVR_FLAG_SORTED = 32,
   /* diagnostics: a crossing bin over the candidate buffer always takes the digit passes over
    * the row (no selection over per-CTA lists) */
-  GVR_FLAG_STREAM_RESCUE = 64
+  GVR_FLAG_STREAM_RESCUE = 64,
+  /* the compact first-pass lists (1024 entries of score and 16-bit share position per CTA, 16
+   * samples expected above tau) on every launch; by default the host picks them only where
+   * they let a two-wave launch run as one wave with half the CTAs per row */
+  GVR_FLAG_COMPACT_LISTS = 128
 };
 
 typedef struct gvr_options {

@@ -28,7 +28,7 @@ __all__ = ["topk_decode", "topk_prefill", "topk_decode_raw", "topk_decode_hinted
            "topk_prefill_raw", "plan",
            "Options",
            "GvrError", "library_path", "load_library", "FLAG_FORCE_RESCUE", "FLAG_NO_FLOOR", "FLAG_ZERO_CAP",
-           "FLAG_RADIX_REFINE", "FLAG_DETERMINISTIC", "FLAG_SORTED", "FLAG_STREAM_RESCUE", "PATH_NAMES",
+           "FLAG_RADIX_REFINE", "FLAG_DETERMINISTIC", "FLAG_SORTED", "FLAG_STREAM_RESCUE", "FLAG_COMPACT_LISTS", "PATH_NAMES",
            "SUPPORTED_K"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -37,7 +37,7 @@ _lock = threading.Lock()
 _lib = None
 
 FLAG_FORCE_RESCUE, FLAG_NO_FLOOR, FLAG_ZERO_CAP, FLAG_RADIX_REFINE = 1, 2, 4, 8
-FLAG_DETERMINISTIC, FLAG_SORTED, FLAG_STREAM_RESCUE = 16, 32, 64
+FLAG_DETERMINISTIC, FLAG_SORTED, FLAG_STREAM_RESCUE, FLAG_COMPACT_LISTS = 16, 32, 64, 128
 PATH_NAMES = {-1: "device_error", 0: "short", 1: "refine", 2: "rescue_bracket", 3: "rescue_overflow",
               4: "rescue_forced", 5: "refine_cluster", 6: "refine_relist"}
 SUPPORTED_K = (512, 1024, 2048)

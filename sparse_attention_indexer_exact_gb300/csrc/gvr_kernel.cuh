@@ -59,8 +59,13 @@ constexpr int VPS = 2;                // float4 per thread per stage
 constexpr int STAGE_VEC = THREADS * VPS;  // 256 float4 = 4 KB per stage
 constexpr int MIN_STAGES = 3;         // ring depth bounds (the host picks the depth per launch)
 constexpr int MAX_STAGES = 16;
-constexpr int LIST_CAP = 768;         // above-floor scores kept per CTA for the collect step
-constexpr int LIST_SEG = LIST_CAP / (THREADS / 32);  // each warp appends to its own segment
+constexpr int LIST_BYTES = 6144;      // the per-CTA list of above-floor scores kept for the collect
+// Two list formats in the same bytes: (score, 32-bit window index) -- 768 entries -- or
+// (score, 16-bit position in the CTA's share) -- 1024 entries, for shares of at most
+// LIST_MAX_STAGES stages (the compact format, chosen by the host for long shares).
+constexpr int LIST_CAP = LIST_BYTES / 8;
+constexpr int LIST_CAP16 = LIST_BYTES / 6;
+constexpr int LIST_MAX_STAGES = 64;
 constexpr int CAP = 512;              // candidate slots in cluster rank 0
 constexpr int RING_CAND = STAGE_VEC * 16 / 8;  // (score, index) candidates one idle ring stage holds
 constexpr int BULK_BINS = 512;       // first-pass counts of at most this many bins go as bulk adds
@@ -71,12 +76,13 @@ constexpr int MAX_K = 2048;
 constexpr int MAX_SAMPLES = 2048;     // block64 samples per row at most (32 runs, one per lane)
 
 // Samples of a long row (nv > k): k (the k / 64 runs of uniform block64 sampling), or more
-// when k is small against nv -- enough runs, up to MAX_SAMPLES, that about 8 samples are
-// expected above the K-th score (k * samples / nv >= 8).  The floor keeps a margin of a few
+// when k is small against nv -- enough runs, up to MAX_SAMPLES, that about mu_target (8, or 16
+// for the compact lists' long shares) samples are expected above the K-th score.  The floor keeps a margin of a few
 // samples over that expectation, so with fewer samples it would count and list several times
 // K scores.
-__host__ __device__ constexpr uint32_t sample_count(uint32_t k, uint32_t nv) {
-  const uint32_t runs = (nv + 8u * k - 1u) / (8u * k);  // ceil(nv / 8k): nv < 2^31, k <= 2048
+__host__ __device__ constexpr uint32_t sample_count(uint32_t k, uint32_t nv, uint32_t mu_target = 8) {
+  const uint32_t per = 64u * k / mu_target;              // row scores per run for that target
+  const uint32_t runs = (nv + per - 1u) / per;           // nv < 2^31, per <= 16384
   const uint32_t n = 64u * runs;
   return n <= k ? k : (n >= uint32_t(MAX_SAMPLES) ? uint32_t(MAX_SAMPLES) : n);
 }
@@ -91,7 +97,8 @@ enum : int32_t {
   FLAG_RADIX_REFINE = 8,
   FLAG_DETERMINISTIC = 16,
   FLAG_SORTED = 32,
-  FLAG_STREAM_RESCUE = 64
+  FLAG_STREAM_RESCUE = 64,
+  FLAG_COMPACT_LISTS = 128
 };
 enum : int32_t {
   PATH_DEVICE_ERROR = -1,
@@ -140,8 +147,16 @@ struct alignas(16) Smem {
   uint32_t tot[NB + 4];            // cluster-wide counts, added here by every CTA of the cluster
                                    // (tot[NB]: CTAs whose list overflowed); the rescue's two
                                    // 256-bin digit histograms reuse it
-  float list_v[LIST_CAP];
-  int32_t list_j[LIST_CAP];
+  union {  // the first-pass list, in one of its two formats
+    struct {
+      float list_v[LIST_CAP];
+      int32_t list_j[LIST_CAP];
+    };
+    struct {
+      float list_v16[LIST_CAP16];
+      uint16_t list_p16[LIST_CAP16];  // stage of the share * 1024 + offset in the stage
+    };
+  };
   float cand_v[CAP];
   int32_t cand_j[CAP];
   uint32_t wsum[2][8];
@@ -159,7 +174,7 @@ struct alignas(16) Smem {
   int32_t fpart;
   uint32_t dsel, dabove, dcnt, dmy_above, dmy_at;
   uint32_t kmin_loc, kmax_loc;     // rescue: smallest / largest key of this CTA's matching scores
-  uint32_t list_n[THREADS / 32];   // scores each warp appended to its segment (may exceed LIST_SEG)
+  uint32_t list_n[THREADS / 32];   // scores each warp appended to its segment (may exceed it)
   uint32_t unlisted;               // CTAs of the cluster whose list overflowed (each adds 1; rank 0
                                    // adds 1 + UNLISTED_RANK0)
   uint32_t relist_n;               // scores of the crossing bin and above listed again
@@ -496,7 +511,7 @@ __device__ __forceinline__ void digit_cross(Smem& S, int buf, uint32_t c0, uint3
 // EXT: the extended modes (deterministic ties and sorting, hinted sampling, block skipping) are
 // compiled in.  The plain instantiation leaves them out, which keeps the common path's code
 // smaller (measured ~3 % faster).
-template <bool EXT>
+template <bool EXT, bool L16>
 __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   constexpr int T = THREADS;
   constexpr int NW = T / 32;
@@ -693,6 +708,42 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       for (int l = 0; l < 4; ++l) f(f4_get(v, l), g, ((lanes >> l) & 1u) != 0, l);
     }
   };
+  // The list: LCAP scores, then their window indices (int32) or, compact, their positions in
+  // this CTA's share (16 bits: stage of the share * 1024 + offset in the stage).
+  constexpr int LCAP = L16 ? LIST_CAP16 : LIST_CAP;
+  constexpr int LSEG = LCAP / NW;  // each warp appends to its own segment
+  const int lcs = __ffs(int(cs)) - 1;  // cs is a power of two
+  auto share_to_window = [&](uint32_t sp) -> int32_t {
+    return (int32_t(rank) + (int32_t(sp >> 10) << lcs)) * (4 * STAGE_VEC) + int32_t(sp & 1023u) - lead;
+  };
+  // Index field of the entry for the score at row vector g, lane l (g inside this CTA's share).
+  auto list_key = [&](int32_t g, int l) -> uint32_t {
+    if constexpr (L16)
+      return (uint32_t((g / STAGE_VEC - int32_t(rank)) >> lcs) << 10) + uint32_t(g % STAGE_VEC) * 4u + uint32_t(l);
+    else
+      return uint32_t(4 * g + l - lead);
+  };
+  auto list_val = [&](uint32_t at) -> float {
+    if constexpr (L16) return S.list_v16[at];
+    else return S.list_v[at];
+  };
+  auto list_put = [&](uint32_t at, float v, uint32_t key) {
+    if constexpr (L16) {
+      S.list_v16[at] = v;
+      S.list_p16[at] = uint16_t(key);
+    } else {
+      S.list_v[at] = v;
+      S.list_j[at] = int32_t(key);
+    }
+  };
+  auto list_keyat = [&](uint32_t at) -> uint32_t {
+    if constexpr (L16) return S.list_p16[at];
+    else return uint32_t(S.list_j[at]);
+  };
+  auto list_window = [&](uint32_t at) -> int32_t {
+    if constexpr (L16) return share_to_window(S.list_p16[at]);
+    else return S.list_j[at];
+  };
   // Walk of this CTA's list (every warp segment): f(value, window index, valid), warp-collective
   // with a CTA-uniform trip count.  Only valid once every segment held its scores.
   auto each_listed = [&](auto&& f) {
@@ -706,8 +757,8 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       uint32_t at = i;  // slot of entry i: its segment's base plus its offset in the segment
 #pragma unroll
       for (int w = 1; w < NW; ++w)
-        if (i >= pre[w]) at = uint32_t(w * LIST_SEG) + (i - pre[w]);
-      f(in ? S.list_v[at] : 0.f, in ? S.list_j[at] : 0, in);
+        if (i >= pre[w]) at = uint32_t(w * LSEG) + (i - pre[w]);
+      f(in ? list_val(at) : 0.f, in ? list_window(at) : 0, in);
     }
   };
   // Rank 0, block-collective: reorder out[0..k) (and the values) by (value desc, index asc), the
@@ -748,7 +799,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   };
 
   // ---------------------------------------------------------------- guess: block64 sample
-  const uint32_t nsamp = sample_count(uint32_t(k), nv);
+  const uint32_t nsamp = sample_count(uint32_t(k), nv, L16 ? 16u : 8u);
   const uint32_t nblk = nsamp >> 6;
   // Start of run b = floor(b (nv - 64) / (nblk - 1)), one run per lane (nblk <= 32), with no
   // 64-bit arithmetic: b (nv - 64) = b sq (nblk - 1) + b sr.
@@ -979,9 +1030,10 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     // ------------------------------------------------------------ verify: value histogram
     // Pass 1 counts (and lists) the scores >= thr; pass 2, only when the crossing falls in
     // the partial bin or below, counts the rest.
-    uint32_t wlist = 0;  // scores this warp has appended (warp-uniform; may exceed LIST_SEG)
-    float* const seg_v = S.list_v + warp * LIST_SEG;
-    int32_t* const seg_j = S.list_j + warp * LIST_SEG;
+    uint32_t wlist = 0;  // scores this warp has appended (warp-uniform; may exceed LSEG)
+    float* const seg_v = (L16 ? S.list_v16 : S.list_v) + warp * LSEG;  // this warp's segment
+    int32_t* const seg_j = S.list_j + warp * LSEG;
+    uint16_t* const seg_p = S.list_p16 + warp * LSEG;
     if (bmax_row) {
       // ---------------------------------------------------------- block-skip first pass
       // ("Block-skip fast path for self-sampling GVR top-K decode", opt-in row pass): a block
@@ -1022,9 +1074,10 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
               hist_add(S.hist, hit, b);  // tie-heavy blocks: one atomic per distinct bin
             else if (hit)
               atomicAdd(&S.hist[b], 1u);
-            if (hit && at < uint32_t(LIST_SEG)) {
+            if (hit && at < uint32_t(LSEG)) {
               seg_v[at] = v[q];
-              seg_j[at] = int32_t(col - a);
+              if constexpr (L16) seg_p[at] = uint16_t(s * 1024 + 32 * blk[q] + lane);
+              else seg_j[at] = int32_t(col - a);
             }
           }
         }
@@ -1092,16 +1145,18 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
           }
         }
         // List the hits (a dense warp only until its segment is full; the counts above are exact).
-        if (!dense || wlist - wtot < uint32_t(LIST_SEG)) {
-          const int32_t jbase = 4 * (c0 + tid) - lead;  // window index of this thread's lane 0
+        if (!dense || wlist - wtot < uint32_t(LSEG)) {
+          const uint32_t kbase = list_key(c0 + tid, 0);  // index field of this thread's lane 0
+          const int32_t jbase = 4 * (c0 + tid) - lead;   // window index of this thread's lane 0
           for (uint32_t rest = bits; rest;) {
             const int j = __ffs(rest) - 1;
             rest &= rest - 1;
             const float e = stage_score(slot, c0, j);
             if (!dense) atomicAdd(&S.hist[value_bin(e, gmin, sc)], 1u);
-            if (at < uint32_t(LIST_SEG)) {
+            if (at < uint32_t(LSEG)) {
               seg_v[at] = e;
-              seg_j[at] = jbase + (j >> 2) * (4 * T) + (j & 3);
+              if constexpr (L16) seg_p[at] = uint16_t(kbase + uint32_t(j >> 2) * (4 * T) + uint32_t(j & 3));
+              else seg_j[at] = jbase + (j >> 2) * (4 * T) + (j & 3);
             }
             ++at;
           }
@@ -1112,7 +1167,8 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     __syncthreads();
     listed = true;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) listed = listed && S.list_n[w] <= uint32_t(LIST_SEG);
+    for (int w = 0; w < NW; ++w) listed = listed && S.list_n[w] <= uint32_t(LSEG);
+    if (L16) listed = listed && nstages <= LIST_MAX_STAGES;  // positions fit 16 bits
     rounds = 1;
     // Push this CTA's counts of bins [b0, b1] into every CTA's totals (fire-and-forget).
     auto push = [&](int b0, int b1) {
@@ -1345,7 +1401,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   // otherwise it reads the row.  Rows whose crossing bin and above cannot fit in the cluster's
   // lists (tie-heavy rows) go to the row-wide selection at once.
   if (path == PATH_RESCUE_OVERFLOW && cr.total >= uint32_t(k) && !(p.flags & FLAG_STREAM_RESCUE) &&
-      uint64_t(cr.above) + cr.m <= uint64_t(cs) * LIST_CAP) {
+      uint64_t(cr.above) + cr.m <= uint64_t(cs) * LCAP) {
     if (warp == 0) {
       const float t = cr.bin > 0 ? floor_value(cr.bin, gmin, sc) : -INFINITY;
       if (lane == 0) S.vthr = t;
@@ -1366,16 +1422,13 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
         uint32_t at = i;
 #pragma unroll
         for (int w = 1; w < NW; ++w)
-          if (i >= pre[w]) at = uint32_t(w * LIST_SEG) + (i - pre[w]);
-        const float v = in ? S.list_v[at] : 0.f;
-        const int32_t j = in ? S.list_j[at] : 0;
+          if (i >= pre[w]) at = uint32_t(w * LSEG) + (i - pre[w]);
+        const float v = in ? list_val(at) : 0.f;
+        const uint32_t key = in ? list_keyat(at) : 0u;
         const bool hit = in && v >= tb;
         __syncthreads();
         const uint32_t slot = warp_alloc_local(&S.relist_n, hit);
-        if (hit) {
-          S.list_v[slot] = v;
-          S.list_j[slot] = j;
-        }
+        if (hit) list_put(slot, v, key);
       }
       __syncthreads();
     } else {
@@ -1384,17 +1437,14 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
           const bool hit = valid && e >= tb;
           if (__any_sync(FULL_MASK, hit)) {
             const uint32_t at = warp_alloc_local(&S.relist_n, hit);
-            if (hit && at < uint32_t(LIST_CAP)) {
-              S.list_v[at] = e;
-              S.list_j[at] = 4 * g + l - lead;
-            }
+            if (hit && at < uint32_t(LCAP)) list_put(at, e, list_key(g, l));
           }
         });
       });
       rounds += 10;  // diagnostics: the share was read again
     }
     if (tid == 0) {
-      const bool fits = S.relist_n <= uint32_t(LIST_CAP);
+      const bool fits = S.relist_n <= uint32_t(LCAP) && (!L16 || nstages <= LIST_MAX_STAGES);
 #pragma unroll
       for (int w = 0; w < NW; ++w) S.list_n[w] = 0;
       S.list_n[0] = fits ? S.relist_n : 0u;  // one contiguous list

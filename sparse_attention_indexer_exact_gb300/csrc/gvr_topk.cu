@@ -21,6 +21,7 @@ constexpr int kMaxDevices = 64;
 constexpr int kMaxCluster = 16;  // 16 is a non-portable cluster size (checked per ring depth)
 constexpr int64_t kShareVec = 8192;  // largest float4 share per CTA before rows are split further
 constexpr int kListTarget = 480;       // expected first-pass list entries per CTA (of LIST_CAP)
+constexpr int kListTarget16 = 640;     // the same for the compact lists (of LIST_CAP16)
 constexpr int64_t kCheapRereadStages = 4;
 
 struct DeviceState {
@@ -37,16 +38,20 @@ constexpr int kDefaultSmemReserved = 1024;
 constexpr int kMaxCtasPerSm = 7;  // registers: 128 threads x up to 72 registers
 DeviceState g_devices[kMaxDevices];
 
-cudaError_t set_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(gvr::gvr_topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <bool EXT, bool L16>
+cudaError_t set_attributes_of() {
+  cudaError_t e = cudaFuncSetAttribute(gvr::gvr_topk_kernel<EXT, L16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        gvr::smem_bytes(gvr::MAX_STAGES));
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gvr::gvr_topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             gvr::smem_bytes(gvr::MAX_STAGES));
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gvr::gvr_topk_kernel<false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gvr::gvr_topk_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(gvr::gvr_topk_kernel<EXT, L16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
+}
+
+cudaError_t set_attributes() {
+  cudaError_t e = set_attributes_of<false, false>();
+  if (e == cudaSuccess) e = set_attributes_of<true, false>();
+  if (e == cudaSuccess) e = set_attributes_of<false, true>();
+  if (e == cudaSuccess) e = set_attributes_of<true, true>();
   return e;
 }
 
@@ -90,7 +95,7 @@ gvr_status check_common(int64_t row_stride, int64_t num_rows, int32_t k, const g
     if (o->ring_stages != 0 && (o->ring_stages < gvr::MIN_STAGES || o->ring_stages > gvr::MAX_STAGES))
       return GVR_ERR_ARG;
     if (o->flags & ~(GVR_FLAG_FORCE_RESCUE | GVR_FLAG_NO_FLOOR | GVR_FLAG_ZERO_CAP | GVR_FLAG_RADIX_REFINE |
-                     GVR_FLAG_DETERMINISTIC | GVR_FLAG_SORTED | GVR_FLAG_STREAM_RESCUE))
+                     GVR_FLAG_DETERMINISTIC | GVR_FLAG_SORTED | GVR_FLAG_STREAM_RESCUE | GVR_FLAG_COMPACT_LISTS))
       return GVR_ERR_ARG;
   }
   return GVR_OK;
@@ -116,6 +121,7 @@ gvr_status check_common(int64_t row_stride, int64_t num_rows, int32_t k, const g
 struct Geometry {
   int cs;
   int nstage;
+  bool l16 = false;  // compact lists (and mu_target 16)
 };
 
 int ctas_per_sm(int nstage, int smem_per_sm, int smem_reserved) {
@@ -152,7 +158,23 @@ Geometry plan_geometry(int64_t row_stride, int64_t num_rows, int32_t k, int sms,
     // widen while the wider launch fills at most half the slots (a quarter for the step to 16,
     // whose CTAs would otherwise share SMs and shallow rings without adding throughput)
     while (g.cs < cs_max && num_rows * g.cs * 2 * (g.cs >= 8 ? 2 : 1) <= slots) g.cs *= 2;
+    // Compact lists: when the launch takes two waves of CTAs and half the cluster would fit in
+    // one, the 1024-entry lists with 16 samples expected above tau (fewer listed scores) may
+    // let half as many CTAs hold each row's list; a second wave would repeat every CTA's
+    // fixed latency chain.
+    if (g.cs >= 2 && num_rows * g.cs > slots && num_rows * (g.cs / 2) <= slots) {
+      const int cs2 = g.cs / 2;
+      const double ns16 = double(gvr::sample_count(uint32_t(k > 0 ? k : 0), uint32_t(row_stride), 16u));
+      const double listed16 =
+          k > 0 ? double(k) + 3.0 * std::sqrt(double(k) * nv / ns16) + 6.0 * nv / ns16 : 0.0;
+      const int64_t stages2 = (need_vec + int64_t(cs2) * gvr::STAGE_VEC - 1) / (int64_t(cs2) * gvr::STAGE_VEC);
+      if (listed16 <= double(kListTarget16) * cs2 && stages2 <= gvr::LIST_MAX_STAGES) {
+        g.cs = cs2;
+        g.l16 = true;
+      }
+    }
   }
+  if (o && (o->flags & GVR_FLAG_COMPACT_LISTS)) g.l16 = true;
   if (o && o->ring_stages) {
     g.nstage = o->ring_stages;
   } else {
@@ -193,7 +215,8 @@ gvr_status launch(const gvr::Params& prm, int64_t num_rows, const gvr_options* o
       qc.attrs = qa;
       qc.numAttrs = 1;
       int n = 0;
-      f = (cudaOccupancyMaxActiveClusters(&n, gvr::gvr_topk_kernel<false>, &qc) == cudaSuccess && n > 0) ? 1 : 2;
+      f = (cudaOccupancyMaxActiveClusters(&n, gvr::gvr_topk_kernel<false, false>, &qc) == cudaSuccess && n > 0) ? 1
+                                                                                                            : 2;
       cudaGetLastError();  // a refused query leaves no sticky error
     }
     if (f != 1) {
@@ -223,8 +246,13 @@ gvr_status launch(const gvr::Params& prm, int64_t num_rows, const gvr_options* o
   q.nstage = geo.nstage;
   // the extended instantiation only when a call uses one of its modes
   const bool ext = (q.flags & (gvr::FLAG_DETERMINISTIC | gvr::FLAG_SORTED)) || q.pre_idx || q.block_max;
-  const cudaError_t e = ext ? cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<true>, q)
-                            : cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<false>, q);
+  cudaError_t e;
+  if (geo.l16)
+    e = ext ? cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<true, true>, q)
+            : cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<false, true>, q);
+  else
+    e = ext ? cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<true, false>, q)
+            : cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<false, false>, q);
   return e == cudaSuccess ? GVR_OK : GVR_ERR_LAUNCH;
 }
 

@@ -143,7 +143,7 @@ def test_prefill_argument_errors(lib):
 def test_option_errors(lib):
     import sparse_attention_indexer_exact_gb300 as gvr
     for bad in (dict(cluster_size=3), dict(cluster_size=32), dict(ring_stages=2), dict(ring_stages=17), dict(reserved=1),
-                dict(flags=128)):
+                dict(flags=256)):
         o = gvr.Options(**bad)
         st = lib.topk_decode_ex(ALIGNED, 1024, 4, ALIGNED, 1, 1, K, ALIGNED, None, None, ctypes.byref(o))
         assert st == 5, bad

@@ -572,3 +572,67 @@ def test_deterministic_list_refine_and_prefill_leads(gvr, flags):
     pc = workloads.PrefillCase("det_prefill", np.stack(rows), np.array(ks, np.int32), np.array(ke, np.int32), 512)
     for extra in (0, 1):
         assert_prefill_deterministic(gvr, pc, flags, extra)
+
+
+# ----------------------------------------------------------------------------- compact lists
+CL = 128  # GVR_FLAG_COMPACT_LISTS: (score, 16-bit share position) lists, 16 samples above tau
+
+
+def test_compact_lists_chosen_for_two_wave_launches(gvr):
+    """256 rows of 64K scores at K=1024 would take two waves of 8-CTA clusters; the host halves
+    the cluster and takes the compact lists (their instantiation runs by default here)."""
+    case = workloads.sweep_decode(256, 65536, 1024)
+    st = assert_decode_exact(gvr, case, stats=True)
+    assert (st[:, 0] == 1).all() and (st[:, 2] % 10 == 1).all(), st
+    assert gvr.plan(case.row_stride, case.rows, case.k)["cluster_size"] == 4
+
+
+@pytest.mark.parametrize("flags,expect", [(4, {3, 5, 6}), (2, {1}), (8, {1}), (2 | 4, {3, 5, 6}), (0, {1})])
+def test_compact_lists_forced_paths(gvr, flags, expect):
+    case = workloads.decode_batch(seed=5, requests=8, next_n=2, cr=4, k=1024, stride=131072,
+                                  boundary=False)
+    st = assert_decode_exact(gvr, case, options=gvr.Options(flags=flags | CL), stats=True)
+    long_rows = case.row_lengths() > case.k
+    assert set(np.unique(st[long_rows, 0]).tolist()) <= expect, st[:, 0]
+    assert_decode_exact(gvr, workloads.adversarial_row("base"), options=gvr.Options(flags=flags | CL))
+    pc = workloads.prefill_tile(seed=9, rows=32, k=512, lengths=(600, 1800, 3000, 6000))
+    assert_prefill_exact(gvr, pc, options=gvr.Options(flags=flags | CL))
+
+
+@pytest.mark.parametrize("cs", [1, 4, 16])
+def test_compact_lists_workloads(gvr, cs):
+    """The compact format through every list consumer: collect, rank-0 ring collect, the
+    cluster selection over lists, the relist, deterministic ties and sorting, prefill windows
+    with lead lanes, and shares longer than 64 stages (no 16-bit positions: read again)."""
+    o = dict(flags=CL, cluster_size=cs)
+    assert_decode_exact(gvr, workloads.decode_batch(requests=16), options=gvr.Options(**o))
+    assert_decode_exact(gvr, workloads.single_decode_row(), options=gvr.Options(**o))
+    for bs, n, k in ((16, 65536, 512), (4, 131072, 2048), (8, 32768, 1024)):
+        assert_decode_exact(gvr, workloads.sweep_decode(bs, n, k), options=gvr.Options(**o))
+        assert_prefill_exact(gvr, workloads.sweep_prefill(bs, n, k), options=gvr.Options(**o))
+    assert_prefill_exact(gvr, workloads.prefill_tile(seed=11, rows=64, k=2048), options=gvr.Options(**o))
+    relist = workloads.decode_batch(seed=15, requests=8, next_n=2, cr=4, k=1024, stride=131072, boundary=False)
+    assert_decode_exact(gvr, relist, options=gvr.Options(flags=CL | 2 | 4, cluster_size=cs))
+    for flags in (16, 32):
+        assert_decode_deterministic(gvr, workloads.decode_batch(requests=8), flags, CL, cluster_size=cs)
+        assert_decode_deterministic(gvr, relist, flags, CL | 2 | 4, cluster_size=cs)
+
+
+def test_compact_lists_large_bins_and_long_shares(gvr):
+    """Large crossing bins (rank-0 ring collect, cluster selection over lists) with compact
+    lists, and one CTA per 512K-score row: 128 stages, beyond 16-bit positions, so the lists
+    are not used and the collect reads the share again."""
+    g = np.random.default_rng(123)
+    k, stride = 512, 65536
+    rows = []
+    for p in (600, 1500, 3500):
+        r = g.standard_normal(stride).astype(np.float32)
+        r[g.choice(stride, p, replace=False)] = 3.5
+        rows.append(r)
+    case = workloads.DecodeCase("plateau_compact", np.stack(rows), np.full(3, stride, np.int32), 1, 1, k)
+    st = assert_decode_exact(gvr, case, options=gvr.Options(flags=CL, cluster_size=4, ring_stages=3), stats=True)
+    assert (st[:, 1] > 512).all(), st
+    big = workloads.sweep_decode(2, 1 << 19, 1024)
+    st = assert_decode_exact(gvr, big, options=gvr.Options(flags=CL, cluster_size=1), stats=True)
+    # no list is used: the collect reads the share again, or an overflowing bin goes to the rescue
+    assert ((st[:, 0] == 3) | ((st[:, 0] == 1) & (st[:, 2] >= 10))).all(), st
