@@ -21,7 +21,7 @@ constexpr int kMaxDevices = 64;
 constexpr int kMaxCluster = 16;  // 16 is a non-portable cluster size (checked per ring depth)
 constexpr int64_t kShareVec = 8192;  // largest float4 share per CTA before rows are split further
 constexpr int kListTarget = 480;       // expected first-pass list entries per CTA (of LIST_CAP)
-constexpr int kListTarget16 = 640;     // the same for the compact lists (of LIST_CAP16)
+constexpr int kListTarget16 = 680;     // the same for the compact lists (of LIST_CAP16)
 constexpr int64_t kCheapRereadStages = 4;
 
 struct DeviceState {
