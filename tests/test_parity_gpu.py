@@ -581,10 +581,11 @@ CL = 128  # GVR_FLAG_COMPACT_LISTS: (score, 16-bit share position) lists, 16 sam
 def test_compact_lists_chosen_for_two_wave_launches(gvr):
     """256 rows of 64K scores at K=1024 would take two waves of 8-CTA clusters; the host halves
     the cluster and takes the compact lists (their instantiation runs by default here)."""
-    case = workloads.sweep_decode(256, 65536, 1024)
-    st = assert_decode_exact(gvr, case, stats=True)
-    assert (st[:, 0] == 1).all() and (st[:, 2] % 10 == 1).all(), st
-    assert gvr.plan(case.row_stride, case.rows, case.k)["cluster_size"] == 4
+    for bs, n, k in ((256, 65536, 1024), (256, 32768, 2048)):
+        case = workloads.sweep_decode(bs, n, k)
+        st = assert_decode_exact(gvr, case, stats=True)
+        assert (st[:, 0] == 1).all() and (st[:, 2] % 10 == 1).all(), st
+        assert gvr.plan(case.row_stride, case.rows, case.k)["cluster_size"] == 4
 
 
 @pytest.mark.parametrize("flags,expect", [(4, {3, 5, 6}), (2, {1}), (8, {1}), (2 | 4, {3, 5, 6}), (0, {1})])
