@@ -94,8 +94,8 @@ def test_blockskip_adversarial(gvr, variant):
         assert_blockskip_exact(gvr, case, kind, seed=4)
 
 
-@pytest.mark.parametrize("flags", [1, 2, 4, 8, 16, 32, 2 | 4, 4 | 64])
-def test_blockskip_forced_paths_and_modes(gvr, flags):
+@pytest.mark.parametrize("flags", [1, 2, 4, 8, 16, 32, 2 | 4, 4 | 64, 128, 128 | 4, 128 | 32])
+def test_blockskip_forced_paths_and_modes(gvr, flags):  # 128: the compact lists
     case = workloads.decode_batch(seed=6, requests=10, next_n=3, cr=4, k=512, stride=65536, boundary=True)
     assert_blockskip_exact(gvr, case, "exact", flags)
 

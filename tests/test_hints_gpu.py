@@ -108,8 +108,8 @@ def test_hinted_single_and_adversarial(gvr, kind):
 
 
 @pytest.mark.parametrize("kind", ["previous", "zero", "neg_pad"])
-@pytest.mark.parametrize("flags", [16, 32, 1, 4])
-def test_hinted_modes_and_forced_paths(gvr, kind, flags):
+@pytest.mark.parametrize("flags", [16, 32, 1, 4, 128, 128 | 32])
+def test_hinted_modes_and_forced_paths(gvr, kind, flags):  # 128: the compact lists
     case = workloads.decode_batch(seed=5, requests=12, next_n=3, cr=4, k=512, stride=65536, boundary=True)
     assert_hinted_exact(gvr, case, kind, flags, seed=14)
 
