@@ -12,7 +12,8 @@
 //           #20998, "What changes"), or more when K is small against nv (at most 32).
 //           GMIN / GMAX are the smallest / largest finite sample.
 //   Verify  a value histogram of NB bins over [GMIN, GMAX] (values above GMAX saturate into
-//           the top bin, below GMIN into bin 0); its cluster-wide suffix sums locate the bin
+//           the top bin, below GMIN into bin 0; when a few far samples stretch the bins, they
+//           end lower, at a robust sample rank); its cluster-wide suffix sums locate the bin
 //           b* that crosses the K-th largest value tau ("Why the GLM row overflows").
 //   Refine  scores in bins above b* are winners and are written at once; the m members of
 //           b* go to a bounded candidate buffer in cluster rank 0, which picks the remaining
@@ -35,8 +36,12 @@
 //  * ballot-built prefixes for list slots; a warp whose hits share one bin adds them with one
 //    atomic, other dense warps aggregate with __match_any_sync, so tie-heavy rows cost one
 //    atomic per distinct bin per warp instruction.
-//  * extended modes in a second instantiation (EXT): deterministic ties by smallest index and
-//    sorted output, hinted sampling, and the block-skip first pass.
+//  * the first pass's histogram reaches every CTA of the cluster as TMA bulk reductions into
+//    shared memory, counted on an mbarrier (no cluster barrier).
+//  * four instantiations: the extended modes (EXT: deterministic ties by smallest index and
+//    sorted output, hinted sampling, the block-skip first pass) or not, and the compact lists
+//    (L16: 1024 entries of score and 16-bit share position instead of 768 of score and index,
+//    chosen by the host where they let half as many CTAs hold a row's list) or not.
 //
 // The bin function is monotone non-decreasing in the score (IEEE round-to-nearest subtract and
 // multiply by a positive scale, clamp, truncate), which is all the crossing-bin logic needs;
