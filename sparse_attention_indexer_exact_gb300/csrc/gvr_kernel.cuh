@@ -324,15 +324,16 @@ __device__ __forceinline__ Crossing scan_crossing(Smem& S, uint32_t k) {
   const uint32_t el = wl + il - sl;  // this CTA's count there
   if (et < k && et + st >= k) {
     uint32_t cum = et, cl = el;
+    bool found = false;  // predicated, not break: the loop stays unrolled, the arrays in registers
 #pragma unroll
     for (int j = 0; j < BPT; ++j) {
-      if (cum + tot[j] >= k) {
+      if (!found && cum + tot[j] >= k) {
         S.cross.bin = lo_bin + BPT - 1 - j;
         S.cross.above = cum;
         S.cross.m = tot[j];
         S.cross.my_above = cl;
         S.cross.my_cand = loc[j];
-        break;
+        found = true;
       }
       cum += tot[j];
       cl += loc[j];
@@ -379,12 +380,13 @@ __device__ __forceinline__ int suffix_cross(Smem& S, const uint32_t* arr, uint32
   const uint32_t ex = before + it - st;
   if (ex < want && ex + st >= want) {
     uint32_t cum = ex;
+    bool found = false;
 #pragma unroll
     for (int j = 0; j < BPT; ++j) {
       cum += c[j];
-      if (cum >= want) {
+      if (!found && cum >= want) {
         S.dsel = uint32_t(lo_bin + BPT - 1 - j);
-        break;
+        found = true;
       }
     }
   }
@@ -450,15 +452,16 @@ __device__ __forceinline__ DigitCross digit_scan(Smem& S, const uint32_t* dtot, 
   const uint32_t et = wt + it - st, el = wl + il - sl;
   if (et < need && et + st >= need) {
     uint32_t cum = et, cl = el;
+    bool found = false;
 #pragma unroll
     for (int j = 0; j < DPT; ++j) {
-      if (cum + tot[j] >= need) {
+      if (!found && cum + tot[j] >= need) {
         S.dsel = uint32_t(255 - DPT * tid - j);
         S.dabove = cum;
         S.dcnt = tot[j];
         S.dmy_above = cl;
         S.dmy_at = loc[j];
-        break;
+        found = true;
       }
       cum += tot[j];
       cl += loc[j];
@@ -499,13 +502,14 @@ __device__ __forceinline__ void digit_cross(Smem& S, int buf, uint32_t c0, uint3
     if (w < warp) before += S.wsum[0][w];
   uint32_t excl = before + incl - st;
   if (excl < need && excl + st >= need) {
+    bool found = false;
 #pragma unroll
     for (int j = 0; j < DPT; ++j) {
-      if (excl + cnt[j] >= need) {
+      if (!found && excl + cnt[j] >= need) {
         S.dsel = uint32_t(255 - DPT * tid - j);
         S.dabove = excl;
         S.dcnt = cnt[j];
-        break;
+        found = true;
       }
       excl += cnt[j];
     }
@@ -1546,7 +1550,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       // window).  Warp-collective.  A warp whose admitted keys all share one digit adds them
       // with one atomic (tie-heavy and narrow rows); otherwise one atomic per distinct digit per
       // score slot.
-      auto digit_batch = [&](auto n_c, const float* e, const int32_t* jw, uint32_t vm) {
+      auto digit_batch = [&](auto n_c, const auto& e, const auto& jw, uint32_t vm) {  // arrays of N, by reference
         constexpr int N = decltype(n_c)::value;
         uint32_t keys[N];
         uint32_t pm = 0, dmin = 0xffffffffu, dmax = 0u;
