@@ -124,7 +124,8 @@ typedef struct gvr_options {
   int32_t flags;              /* GVR_FLAG_* bits; results stay exact under every flag */
   int32_t reserved;           /* must be 0 */
   int32_t* row_stats;         /* optional device int32 [num_rows][4]: path (GVR_PATH_*),
-                                 candidate count m, histogram rounds, winners above the
+                                 candidate count m, histogram rounds (+10 when the row was
+                                 read again to list the crossing bin), winners above the
                                  crossing bin */
 } gvr_options;
 

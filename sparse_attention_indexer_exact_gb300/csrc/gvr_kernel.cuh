@@ -266,6 +266,25 @@ __device__ __forceinline__ uint32_t warp_alloc_local(uint32_t* ctr, bool want) {
   return base + __popc(mask & lanemask_lt());
 }
 
+// Warp-aggregated allocation of n < 16 consecutive slots per lane from *ctr (shared memory of
+// this CTA): returns the lane's first slot.  Warp-collective.
+__device__ __forceinline__ uint32_t warp_alloc_n(uint32_t* ctr, uint32_t n) {
+  const unsigned lt = lanemask_lt();
+  uint32_t excl = 0, tot = 0;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const unsigned m = __ballot_sync(FULL_MASK, (n >> b) & 1u);
+    excl += uint32_t(__popc(m & lt)) << b;
+    tot += uint32_t(__popc(m)) << b;
+  }
+  uint32_t base = 0;
+  if (tot) {  // warp-uniform
+    if ((threadIdx.x & 31) == 0) base = atomicAdd(ctr, tot);
+    base = __shfl_sync(FULL_MASK, base, 0);
+  }
+  return base + excl;
+}
+
 // Find the crossing bin in the cluster-wide totals S.tot: the highest b with
 // sum_{bins >= b} tot >= k, with this CTA's own counts above and at b (from S.hist).  Thread t
 // owns the NB/T bins NB-1-(NB/T)t down to NB-(NB/T)(t+1), so thread order is descending order.
@@ -1725,11 +1744,33 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     if (from_lists) {
       each_listed([&](float e, int32_t jw, bool in) { emit(e, jw, in); });
     } else {
+      static_assert(4 * VPS < 16, "a thread's slot count per stage fits in 4 bits");
       stream_pass(false, [&](uint32_t slot, int32_t c0) {
         // stop visiting once this CTA's slots are all handed out (the counters only grow, and a
         // warp reads them together; the remaining stages still land and are waited for)
         if (S.ctr_win >= my_win && S.ctr_cand >= my_ties) return;
-        each_lane(slot, c0, [&](float e, int32_t g, bool valid, int l) { emit(e, 4 * g + l - lead, valid); });
+        // Each thread marks its winners and ties of the stage (bit 4i + l), the warp takes its
+        // slots of each kind with one atomic, and each thread writes its own in turn.
+        uint32_t wm = 0, tm = 0;
+        each_lane(slot, c0, [&](float e, int32_t g, bool valid, int l) {
+          const uint32_t key = order_key(e);
+          const int bc = valid ? key_class(key) : -1;
+          const bool win = bc == 1 || (bc == 0 && (ge ? (key & pmask) >= prefix : key > prefix));
+          const bool tie = bc == 0 && !ge && key == prefix && (!by_index || index_selected(4 * g + l - lead));
+          const int j = 4 * ((g - c0) / T) + l;
+          wm |= uint32_t(win) << j;
+          tm |= uint32_t(tie) << j;
+        });
+        uint32_t ws = warp_alloc_n(&S.ctr_win, __popc(wm));
+        uint32_t ts = warp_alloc_n(&S.ctr_cand, __popc(tm));
+        auto put = [&](int j, uint32_t at) {
+          out[at] = 4 * (c0 + (j >> 2) * T + tid) + (j & 3) - lead;
+          if (outv) outv[at] = stage_score(slot, c0, j);
+        };
+        for (uint32_t rest = wm; rest; rest &= rest - 1, ++ws)
+          if (wbase + ws < tie_base) put(__ffs(rest) - 1, wbase + ws);
+        for (uint32_t rest = tm; rest; rest &= rest - 1, ++ts)
+          if (tbase + ts < nties) put(__ffs(rest) - 1, tie_base + tbase + ts);
       });
     }
   }

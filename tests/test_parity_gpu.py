@@ -368,6 +368,43 @@ def test_large_crossing_bins(gvr, cs):
     assert (st[(st[:, 0] == 1) & (st[:, 2] == 1), 1] <= nst * 512).all(), (nst, st)
 
 
+@pytest.mark.parametrize("cs", [0, 4, 16])
+def test_tie_class_fills_the_crossing_bin(gvr, cs):
+    """A tie class too large for the lists fills the crossing bin: alone, below a few hundred
+    winners, and with a few scores one ulp above it in the same bin (early in a share, where
+    they are listed, or late, where the lists are full).  Rows with fewer than K finite scores
+    (tau = -inf), and a -inf class that shares its top key digit with finite scores near
+    -FLT_MAX."""
+    g = np.random.default_rng(601 + cs)
+    k, n = 512, 131072
+    up = np.nextafter(np.float32(2.0), np.float32(3.0))
+    rows = []
+    r = np.where(g.random(n) < 0.5, 1.0, 2.0).astype(np.float32)  # two-valued
+    rows.append(r)
+    r = (0.3 * g.standard_normal(n)).astype(np.float32)  # below 1.6: no score in 2.0's bin
+    pos = g.choice(n, n // 2 + 300, replace=False)
+    r[pos[:n // 2]] = 2.0
+    r[pos[n // 2:]] = (5.0 + g.random(300)).astype(np.float32)  # winners above the tie class
+    rows.append(r)
+    for where in (slice(n - 8, n - 3), slice(3, 8)):  # one more key in the bin: late, then early
+        r = np.where(g.random(n) < 0.5, 1.0, 2.0).astype(np.float32)
+        r[where] = up
+        rows.append(r)
+    r = np.full(n, -np.inf, np.float32)  # tau = -inf
+    r[g.choice(n, k - 100, replace=False)] = g.standard_normal(k - 100).astype(np.float32)
+    rows.append(r)
+    r = np.full(n, -np.inf, np.float32)  # -inf shares its top digit with scores near -FLT_MAX
+    pos = g.choice(n, k + 50, replace=False)
+    r[pos[:k - 60]] = g.standard_normal(k - 60).astype(np.float32)
+    r[pos[k - 60:]] = np.float32(-3.0e38) * (1.0 + g.random(110).astype(np.float32) * 0.1)
+    rows.append(r)
+    lg = np.stack(rows)
+    case = workloads.DecodeCase("tie_class_bins", lg, np.full(len(rows), n, np.int32), 1, 1, k)
+    assert_decode_exact(gvr, case, options=gvr.Options(cluster_size=cs))
+    for flags in (16, 32):
+        assert_decode_deterministic(gvr, case, flags, cluster_size=cs)
+
+
 def test_big_collect_with_an_overflowed_list(gvr):
     """A crossing bin of ~1K equal scores that all sit in rank 1's first stage: rank 1's list
     overflows, rank 0's does not, so rank 0 still collects the bin in its ring (path 1) while
