@@ -34,8 +34,8 @@
 //    are then complete, bin(t) itself is partial.  Only when fewer than K scores reach t are
 //    the scores below it counted in a second pass, so the result never depends on the floor.
 //  * ballot-built prefixes for list slots; a warp whose hits share one bin adds them with one
-//    atomic, other dense warps aggregate with __match_any_sync, so tie-heavy rows cost one
-//    atomic per distinct bin per warp instruction.
+//    atomic, other warps with one plain shared atomic per hit (the hardware merges the lanes
+//    of one instruction that share a bin).
 //  * the first pass's histogram reaches every CTA of the cluster as TMA bulk reductions into
 //    shared memory, counted on an mbarrier (no cluster barrier).
 //  * four instantiations: the extended modes (EXT: deterministic ties by smallest index and
@@ -241,16 +241,6 @@ __device__ __forceinline__ float floor_value(int fbin, float gmin, float sc) {
     hi = nhi;
   }
   return key_to_float(hi);
-}
-
-// hist[b] += 1 for every lane with pr set, one shared-memory atomic per distinct b per warp.
-// Warp-collective.
-__device__ __forceinline__ void hist_add(uint32_t* hist, bool pr, uint32_t b) {
-  const unsigned act = __ballot_sync(FULL_MASK, pr);
-  if (pr) {
-    const unsigned peers = __match_any_sync(act, b);
-    if ((peers & lanemask_lt()) == 0) atomicAdd(&hist[b], uint32_t(__popc(peers)));
-  }
 }
 
 // Warp-aggregated slot allocation: lanes with `want` set get consecutive values of *ctr
@@ -1097,11 +1087,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
             if (!hm) continue;
             const uint32_t at = wlist + uint32_t(__popc(hm & lanemask_lt()));
             wlist += uint32_t(__popc(hm));
-            const uint32_t b = hit ? uint32_t(value_bin(v[q], gmin, sc)) : 0u;
-            if (__popc(hm) > 8)
-              hist_add(S.hist, hit, b);  // tie-heavy blocks: one atomic per distinct bin
-            else if (hit)
-              atomicAdd(&S.hist[b], 1u);
+            if (hit) atomicAdd(&S.hist[value_bin(v[q], gmin, sc)], 1u);
             if (hit && at < uint32_t(LSEG)) {
               seg_v[at] = v[q];
               if constexpr (L16) seg_p[at] = uint16_t(s * 1024 + 32 * blk[q] + lane);
@@ -1149,8 +1135,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
         uint32_t at = wlist + excl;
         wlist += wtot;
         // A warp with a few hits per thread counts them one by one; a dense warp (ties, a low
-        // floor) adds its hits with one atomic when they all share a bin, else one per distinct
-        // bin and score slot.
+        // floor) adds its hits with one atomic when they all share a bin, else one per score.
         const bool dense = __any_sync(FULL_MASK, nhit > uint32_t(SPARSE_MAX));
         if (dense) {
           uint32_t bj[4 * VPS];
@@ -1167,9 +1152,10 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
           bmax = __reduce_max_sync(FULL_MASK, bmax);
           if (bmin == bmax) {
             if (lane == 0) atomicAdd(&S.hist[bmin], wtot);
-          } else {
+          } else {  // plain atomics: the hardware merges the lanes that share a bin
   #pragma unroll
-            for (int j = 0; j < 4 * VPS; ++j) hist_add(S.hist, (bits >> j) & 1u, bj[j]);
+            for (int j = 0; j < 4 * VPS; ++j)
+              if ((bits >> j) & 1u) atomicAdd(&S.hist[bj[j]], 1u);
           }
         }
         // List the hits (a dense warp only until its segment is full; the counts above are exact).
