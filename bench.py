@@ -174,17 +174,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def time_oracle(case, nthreads: int, repeats: int):
-    """Median wall time of the oracle over the whole batch; returns (seconds, cores)."""
+def time_oracle(case, nthreads: int, repeats: int, min_seconds: float = 0.0, max_runs: int = 1000):
+    """Median wall time of one oracle run over the whole batch, over at least `repeats` runs and
+    at least `min_seconds` of runs in all (at most `max_runs`); returns (seconds, cores, runs,
+    total seconds)."""
     import oracle
     oracle.build()
     cores = oracle.thread_count(nthreads)
     times = []
-    for _ in range(repeats):
+    while len(times) < max_runs and (len(times) < repeats or sum(times) < min_seconds):
         t0 = time.perf_counter()
         oracle.topk_decode(case.logits, case.kv_lens, case.next_n, case.compress_ratio, case.k, nthreads=nthreads)
         times.append(time.perf_counter() - t0)
-    return statistics.median(times), cores
+    return statistics.median(times), cores, len(times), sum(times)
+
+
+CPU_BASELINE_S = 10.0  # the cpu_baseline leg's runs take about this long in all
 
 
 REFERENCE_BUDGET_S = 90.0  # the reference arm's timed steps take about this long in all
@@ -540,14 +545,16 @@ def main():
         warm_per = warm_s / args.steps
         cpu = None
         if not args.no_cpu_baseline:
-            secs, cores = time_oracle(case, 0, 5)
+            secs, cores, runs, total = time_oracle(case, 0, 5, CPU_BASELINE_S)
             sub = workloads.DecodeCase(case.name, case.logits[:16], case.kv_lens[:16 // case.next_n], case.next_n,
                                        case.compress_ratio, case.k)
-            secs1, _ = time_oracle(sub, 1, 5)
+            secs1, _, runs1, total1 = time_oracle(sub, 1, 5, CPU_BASELINE_S / 4)
             cpu = {"value": rows / secs, "unit": "rows/s", "cores": cores, "kind": "oracle",
-                   "sample": f"all {rows} rows of the batch (one step), full sort per row, median of 5 runs",
+                   "sample": f"all {rows} rows of the batch per run (one step), full sort per row, median of "
+                             f"{runs} runs ({total:.1f} s)",
                    "single_thread": {"value": sub.rows / secs1, "unit": "rows/s", "cores": 1,
-                                     "sample": "the batch's first 16 rows, one thread, median of 5 runs"}}
+                                     "sample": f"the batch's first 16 rows per run, one thread, median of {runs1} "
+                                               f"runs ({total1:.1f} s)"}}
         clocks = clk.summary()
         line = {
             "metric": METRIC,

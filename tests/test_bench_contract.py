@@ -65,3 +65,15 @@ def test_gpu_modes_refuse_without_a_gpu(flags):
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *flags], capture_output=True, text=True,
                        cwd=ROOT, timeout=600)
     assert r.returncode != 0 and "no CPU fallback" in (r.stdout + r.stderr)
+
+
+def test_cpu_baseline_sample_is_bounded_by_time_and_runs():
+    import bench
+    import workloads
+    case = workloads.decode_batch()
+    sub = workloads.DecodeCase(case.name, case.logits[:4], case.kv_lens[:4 // case.next_n], case.next_n,
+                               case.compress_ratio, case.k)
+    secs, cores, runs, total = bench.time_oracle(sub, 1, 3, 0.2)
+    assert cores == 1 and secs > 0 and runs >= 3 and total >= 0.2
+    secs, cores, runs, total = bench.time_oracle(sub, 1, 2, 1e9, max_runs=4)
+    assert runs == 4
