@@ -23,6 +23,8 @@ from __future__ import annotations
 import itertools
 import math
 import os
+import subprocess
+import sys
 import tempfile
 
 import numpy as np
@@ -68,17 +70,27 @@ def _parse_golden_topk():
         yield row, ks, ke, int(k), [int(x) for x in exp.split()], float(tau)
 
 
+GOLDEN_POISON = 100.0  # larger than every golden score: selected whenever a window leaks onto it
+
+
 def pin_golden_tiny_topk(lib):
     for row, ks, ke, k, exp, tau in _parse_golden_topk():
         stride = ((row.size + 3) // 4) * 4
-        logits = np.full((1, stride), np.nan, np.float32)
-        logits[0, :row.size] = row
-        idx, t = oracle.topk_prefill(logits, [ks], [ke], k, lib=lib)
-        assert idx[0].tolist() == exp, f"{row.tolist()} [{ks},{ke}) k={k}: {idx[0].tolist()} != {exp}"
+        # The golden row sits between two poison rows on each side, with NaN padding after its
+        # values: a window that ignores the row's bounds (a dropped clamp) reads poison or NaN in
+        # the same allocation and its result changes, instead of reading outside the buffer.
+        assert -2 * stride <= ks and ke <= 3 * stride, "golden windows stay within the poison rows"
+        logits = np.full((5, stride), GOLDEN_POISON, np.float32)
+        logits[2, :] = np.nan
+        logits[2, :row.size] = row
+        starts = np.array([0, 0, ks, 0, 0], np.int32)
+        ends = np.array([0, 0, ke, 0, 0], np.int32)
+        idx, t = oracle.topk_prefill(logits, starts, ends, k, lib=lib)
+        assert idx[2].tolist() == exp, f"{row.tolist()} [{ks},{ke}) k={k}: {idx[2].tolist()} != {exp}"
         if math.isnan(tau):
-            assert math.isnan(t[0])
+            assert math.isnan(t[2])
         else:
-            assert t[0] == np.float32(tau) and not (t[0] == 0 and np.signbit(t[0])), (t[0], tau)
+            assert t[2] == np.float32(tau) and not (t[2] == 0 and np.signbit(t[2])), (t[2], tau)
 
 
 def _tiny_rows(seed=7, count=160):
@@ -228,6 +240,22 @@ def pin_prefill_translation(lib):
             # and the decode form of the same aligned window agrees
             didx, _, _ = oracle.topk_decode(aligned, np.array([nv], np.int32), 1, 1, k, lib=lib)
             assert didx[0].tolist() == ref[0].tolist()
+        # windows that end exactly at the row stride, or claim to end past it (clamped to the
+        # stride), equal the same scores copied to an aligned window; the row sits between poison
+        # rows, so a window that runs past the stride would read poison instead
+        for nv, over in ((300, 0), (300, 7), (64, 1), (1001, 5)):
+            stride = 2048
+            w = np.round(g.standard_normal(nv) * 3).astype(np.float32)
+            rows = np.full((3, stride), GOLDEN_POISON, np.float32)
+            ks = stride - nv
+            rows[1, :ks] = np.inf
+            rows[1, ks:] = w
+            idx, tau = oracle.topk_prefill(rows, [0, ks, 0], [0, stride + over, 0], k, lib=lib)
+            aligned = np.full((1, stride), -np.inf, np.float32)
+            aligned[0, :nv] = w
+            ref, rtau = oracle.topk_prefill(aligned, [0], [nv], k, lib=lib)
+            assert idx[1].tolist() == ref[0].tolist(), (s, nv, over)
+            assert (math.isnan(tau[1]) and math.isnan(rtau[0])) or tau[1] == rtau[0]
 
 
 ALL_PINS = [pin_golden_decode_row_len, pin_golden_tiny_topk, pin_brute_force_tiny, pin_invariant_random,
@@ -276,6 +304,8 @@ MUTANTS = {
     "prefill_global_frame": ("logits + r * row_stride + a, nv", "logits + r * row_stride, nv"),
     "tau_off_by_one": ("*tau = scratch[k - 1].v;", "*tau = scratch[k].v;"),
     "values_from_sorted_slot": ("vals[i] = w[scratch[i].j];", "vals[i] = w[i];"),
+    "no_ks_clamp": ("if (ks < 0) ks = 0;", ""),
+    "no_ke_clamp": ("if (ke > row_stride) ke = row_stride;", ""),
 }
 
 
@@ -298,6 +328,14 @@ def test_pins_catch_planted_mistakes(name):
         path = os.path.join(d, "mutant.c")
         open(path, "w").write(src.replace(old, new))
         so = oracle.compile_oracle(path, os.path.join(d, "libmutant.so"))
-        lib = oracle.load(so)
-        failed = _pins_fail(lib)
+        # The pins run in a child process: a mutant that drops a bound may write past its own
+        # scratch buffer, and a crash of the child counts as a caught mistake.
+        code = ("import sys; sys.path[:0] = sys.argv[2:4]; import oracle, test_oracle_pins as t; "
+                "print('FAILED=' + ','.join(t._pins_fail(oracle.load(sys.argv[1]))))")
+        here = os.path.dirname(os.path.abspath(__file__))
+        r = subprocess.run([sys.executable, "-c", code, so, os.path.dirname(here), here],
+                           capture_output=True, text=True, timeout=900)
+        out = [ln for ln in r.stdout.splitlines() if ln.startswith("FAILED=")]
+        failed = ["(child process crashed)"] if r.returncode != 0 or not out else \
+            [x for x in out[-1][len("FAILED="):].split(",") if x]
     assert failed, f"planted mistake {name} passed every pin"
