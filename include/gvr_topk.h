@@ -37,7 +37,13 @@
  *   - k must be 512, 1024 or 2048.
  *   - num_rows == 0 is a no-op that returns GVR_OK.
  *   - Errors are returned, never raised on the device: argument errors are detected on the
- *     host before anything is enqueued; GVR_ERR_LAUNCH reports a failed launch.
+ *     host before anything is enqueued; GVR_ERR_LAUNCH is returned when cudaLaunchKernelEx
+ *     returns an error for the one launch (no device, bad configuration, ...).
+ *   - Device-side failure marker: every wait of the kernel for its staged scores is bounded
+ *     (0.5 s).  A row whose wait gave up -- not expected to happen on a healthy GPU -- gets -2
+ *     in every index slot instead of a selection (values are then unspecified).  -2 is never a
+ *     valid index or pad: a caller that gathers with the indices must treat it as invalid.  The
+ *     *_ex entry points also report it per row as GVR_PATH_DEVICE_ERROR in row_stats.
  *   - Calls may run concurrently on different streams: no state is shared between calls.
  */
 #ifndef GVR_TOPK_H
@@ -68,7 +74,8 @@ typedef enum gvr_status {
  * "run_varlen"): kv_lens holds each request's total uncompressed cache length, and the
  * empty-row rule is from its commit "engine/reference convention alignment".
  *   kv_lens  int32 [ceil(num_rows / next_n)], device, read on the device only.
- *   indices  int32 [num_rows][k]: window indices (= column indices for decode), -1 pads.
+ *   indices  int32 [num_rows][k]: window indices (= column indices for decode), -1 pads; -2 in
+ *            every slot of a row whose bounded wait gave up (see the conventions above).
  *   values   optional fp32 [num_rows][k]: the score at each returned index, bit-exact copied
  *            from logits; -FLT_MAX in -1 slots ("values output" commit of PR #18122).
  */
@@ -85,7 +92,8 @@ gvr_status topk_decode(const float* logits, int64_t row_stride, int64_t num_rows
  * is treated as 0, an end beyond row_stride as row_stride, and an end at or before the start
  * as an empty window.
  *   row_starts, row_ends  int32 [num_rows], device.
- *   indices               int32 [num_rows][k].
+ *   indices               int32 [num_rows][k]; -2 in every slot of a row whose bounded wait gave
+ *                         up (see the conventions above).
  */
 gvr_status topk_prefill(const float* logits, int64_t row_stride, int64_t num_rows,
                         const int32_t* row_starts, const int32_t* row_ends, int32_t k,

@@ -41,8 +41,8 @@ FLAG_DETERMINISTIC, FLAG_SORTED, FLAG_STREAM_RESCUE, FLAG_COMPACT_LISTS = 16, 32
 PATH_NAMES = {-1: "device_error", 0: "short", 1: "refine", 2: "rescue_bracket", 3: "rescue_overflow",
               4: "rescue_forced", 5: "refine_cluster", 6: "refine_relist"}
 SUPPORTED_K = (512, 1024, 2048)
-EXPORTED_SYMBOLS = ("topk_decode", "topk_prefill", "topk_decode_ex", "topk_prefill_ex", "gvr_status_string",
-                    "gvr_plan")
+EXPORTED_SYMBOLS = ("topk_decode", "topk_prefill", "topk_decode_ex", "topk_prefill_ex", "topk_decode_hinted",
+                    "topk_decode_blockskip", "gvr_status_string", "gvr_plan")
 
 
 class GvrError(RuntimeError):
@@ -169,14 +169,27 @@ def _torch():
     return torch
 
 
-def _stream_handle(stream) -> int:
+def _stream_handle(stream, device) -> int:
+    """The CUDA stream handle to launch on: ``stream`` if given, else the current stream of
+    ``device`` (the tensors' device, not whichever device happens to be current)."""
     torch = _torch()
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def _same_device(device, **tensors):
+    """Every given tensor must live on ``device``: the library launches on one device with
+    pointers that must all belong to it."""
+    for name, t in tensors.items():
+        if t is not None and t.device != device:
+            raise ValueError(f"{name} is on {t.device}, logits on {device}: all tensors must share one device")
+
+
 def _rows_2d(logits):
+    """(rows, row stride) of a 2-D fp32 CUDA tensor.  The row stride passed to the library is the
+    row length: windows are clamped to it, so a narrowed view (stride(0) > shape[1]) is refused
+    rather than read past its columns."""
     torch = _torch()
     if not isinstance(logits, torch.Tensor) or not logits.is_cuda:
         raise TypeError("logits must be a CUDA tensor")
@@ -184,7 +197,10 @@ def _rows_2d(logits):
         raise TypeError("logits must be float32")
     if logits.dim() != 2 or logits.stride(1) != 1:
         raise ValueError("logits must be 2-D with unit inner stride")
-    return logits.shape[0], logits.stride(0)
+    if logits.shape[0] > 1 and logits.stride(0) != logits.shape[1]:
+        raise ValueError("logits rows must be packed (stride(0) == shape[1]); pass .contiguous() for a "
+                         "narrowed view")
+    return logits.shape[0], logits.shape[1]
 
 
 def _int32_vec(t, n, name):
@@ -217,6 +233,15 @@ def topk_decode(logits, kv_lens, next_n: int, compress_ratio: int, k: int, indic
     """
     rows, stride = _rows_2d(logits)
     _int32_vec(kv_lens, (rows + next_n - 1) // max(next_n, 1), "kv_lens")
+    _same_device(logits.device, kv_lens=kv_lens, indices=indices, values=values, pre_idx=pre_idx,
+                 block_max=block_max)
+    with _torch().cuda.device(logits.device):
+        return _topk_decode_on_device(logits, rows, stride, kv_lens, next_n, compress_ratio, k, indices, values,
+                                      want_values, stream, options, pre_idx, block_max)
+
+
+def _topk_decode_on_device(logits, rows, stride, kv_lens, next_n, compress_ratio, k, indices, values, want_values,
+                           stream, options, pre_idx, block_max):
     indices = _out(indices, rows, k, _torch().int32, logits.device, "indices")
     if values is None and want_values:
         values = _out(None, rows, k, _torch().float32, logits.device, "values")
@@ -233,7 +258,7 @@ def topk_decode(logits, kv_lens, next_n: int, compress_ratio: int, k: int, indic
                              "with unit inner stride")
         topk_decode_blockskip_raw(logits.data_ptr(), stride, rows, kv_lens.data_ptr(), next_n, compress_ratio, k,
                                   block_max.data_ptr(), block_max.stride(0), indices.data_ptr(), vptr,
-                                  _stream_handle(stream), options)
+                                  _stream_handle(stream, logits.device), options)
     elif pre_idx is not None:
         torch = _torch()
         reqs = (rows + next_n - 1) // max(next_n, 1)
@@ -242,10 +267,10 @@ def topk_decode(logits, kv_lens, next_n: int, compress_ratio: int, k: int, indic
             raise ValueError(f"pre_idx must be a CUDA int32 tensor [{reqs}, >= {k}] with unit inner stride")
         topk_decode_hinted_raw(logits.data_ptr(), stride, rows, kv_lens.data_ptr(), next_n, compress_ratio, k,
                                pre_idx.data_ptr(), pre_idx.stride(0), indices.data_ptr(), vptr,
-                               _stream_handle(stream), options)
+                               _stream_handle(stream, logits.device), options)
     else:
         topk_decode_raw(logits.data_ptr(), stride, rows, kv_lens.data_ptr(), next_n, compress_ratio, k,
-                        indices.data_ptr(), vptr, _stream_handle(stream), options)
+                        indices.data_ptr(), vptr, _stream_handle(stream, logits.device), options)
     return indices, values
 
 
@@ -255,7 +280,9 @@ def topk_prefill(logits, row_starts, row_ends, k: int, indices=None, *, stream=N
     rows, stride = _rows_2d(logits)
     _int32_vec(row_starts, rows, "row_starts")
     _int32_vec(row_ends, rows, "row_ends")
-    indices = _out(indices, rows, k, _torch().int32, logits.device, "indices")
-    topk_prefill_raw(logits.data_ptr(), stride, rows, row_starts.data_ptr(), row_ends.data_ptr(), k,
-                     indices.data_ptr(), _stream_handle(stream), options)
+    _same_device(logits.device, row_starts=row_starts, row_ends=row_ends, indices=indices)
+    with _torch().cuda.device(logits.device):
+        indices = _out(indices, rows, k, _torch().int32, logits.device, "indices")
+        topk_prefill_raw(logits.data_ptr(), stride, rows, row_starts.data_ptr(), row_ends.data_ptr(), k,
+                         indices.data_ptr(), _stream_handle(stream, logits.device), options)
     return indices

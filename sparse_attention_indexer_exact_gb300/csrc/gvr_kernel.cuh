@@ -662,7 +662,12 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   const bool ring_resident = nstages <= nst;
   bool loaded = false;
   uint32_t rslot = 0, rphase = 0;
+  // A CTA whose wait gave up (S.tout, set once every thread has seen it) visits no more stages:
+  // its row's indices become -2 at the end, and every later pass returns at once.  At the moment
+  // it gives up it issues no more refills and waits (bounded) for the copies already in flight,
+  // so none is still writing into its shared memory when it moves on or exits.
   auto stream_pass = [&](bool primed, auto&& visit) {
+    if (S.tout) return;  // CTA-uniform: written before a barrier that every thread has passed
     if (warp == 0 && !primed && !(ring_resident && loaded))
       for (int32_t s = lane; s < nst && s < nstages; s += 32) {  // nst <= 16: one pass of lanes
         const uint32_t sl = rslot + uint32_t(s);
@@ -675,10 +680,23 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
         late = true;
       }
       visit(slot, stage_first(s));
-      if (s + nst < nstages) {  // refill this slot once every thread is done with it
-        __syncthreads();
-        if (tid == 0) issue_stage(s + nst, slot);
+      // refill this slot once every thread is done with it, unless some thread gave up waiting
+      const bool refill = s + nst < nstages;
+      if (refill ? __syncthreads_or(late) : false) {
+        // drain: the stages after this one that are already in flight (no refill was issued
+        // for this slot), each waited for once, with the same bound
+        uint32_t dsl = slot, dph = ph;
+        for (int32_t d = s + 1; d < nstages && d < s + nst; ++d) {
+          if (++dsl == uint32_t(nst)) {
+            dsl = 0;
+            dph ^= 1u;
+          }
+          mbar_wait_bounded(&S.bar[dsl], dph, WAIT_LIMIT_NS);
+        }
+        late = true;
+        break;
       }
+      if (refill && tid == 0) issue_stage(s + nst, slot);
       if (++slot == uint32_t(nst)) {
         slot = 0;
         ph ^= 1u;
@@ -690,6 +708,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     }
     loaded = true;
     if (__syncthreads_or(late) && tid == 0) S.tout = 1;
+    __syncthreads();  // S.tout is read by the next pass
   };
   // The i-th vector of this thread in the stage at (slot, c0): its share index g, its values
   // and the 4-bit mask of its in-window lanes (0 past the share).

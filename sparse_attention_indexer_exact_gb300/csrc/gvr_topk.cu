@@ -7,6 +7,7 @@
 // memory is read on the host and nothing synchronizes, so a call costs one launch.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -30,7 +31,9 @@ struct DeviceState {
   int sms = 0;
   int smem_per_sm = 0;     // shared memory per SM (bytes)
   int smem_reserved = 0;   // shared memory the system reserves per CTA (bytes)
-  int fits16[gvr::MAX_STAGES + 1] = {};  // a 16-CTA cluster can be scheduled: 0 unknown, 1 yes, 2 no
+  // a 16-CTA cluster can be scheduled at this ring depth: 0 unknown, 1 yes, 2 no (written by any
+  // host thread that launches first, so atomic)
+  std::atomic<int> fits16[gvr::MAX_STAGES + 1] = {};
 };
 
 constexpr int kDefaultSmemPerSm = 228 * 1024;
@@ -201,7 +204,8 @@ gvr_status launch(const gvr::Params& prm, int64_t num_rows, const gvr_options* o
     // else the row goes to 8 CTAs.
     int dev = 0;
     cudaGetDevice(&dev);
-    int& f = g_devices[dev].fits16[geo.nstage];
+    std::atomic<int>& fits = g_devices[dev].fits16[geo.nstage];
+    int f = fits.load(std::memory_order_relaxed);
     if (f == 0) {
       cudaLaunchConfig_t qc = {};
       qc.gridDim = dim3(16, 1, 1);
@@ -215,9 +219,11 @@ gvr_status launch(const gvr::Params& prm, int64_t num_rows, const gvr_options* o
       qc.attrs = qa;
       qc.numAttrs = 1;
       int n = 0;
-      f = (cudaOccupancyMaxActiveClusters(&n, gvr::gvr_topk_kernel<false, false>, &qc) == cudaSuccess && n > 0) ? 1
-                                                                                                            : 2;
-      cudaGetLastError();  // a refused query leaves no sticky error
+      const cudaError_t qe = cudaOccupancyMaxActiveClusters(&n, gvr::gvr_topk_kernel<false, false>, &qc);
+      // a refused query leaves its error in the thread's last-error slot: clear that one only
+      if (qe != cudaSuccess) cudaGetLastError();
+      f = (qe == cudaSuccess && n > 0) ? 1 : 2;
+      fits.store(f, std::memory_order_relaxed);
     }
     if (f != 1) {
       gvr_options o8 = o ? *o : gvr_options{};

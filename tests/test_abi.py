@@ -191,3 +191,19 @@ def test_product_path_has_no_oracle_dependency():
         if fn.endswith((".py", ".c")):
             text = open(os.path.join(ROOT, "oracle", fn)).read()
             assert "sparse_attention_indexer_exact_gb300" not in text and "gvr_topk.h" not in text
+
+
+def test_binding_refuses_tensors_on_different_devices():
+    # The binding launches on logits' device with every pointer it is given; a tensor on another
+    # device must be refused on the host before anything is enqueued.
+    import types
+
+    import torch
+
+    import sparse_attention_indexer_exact_gb300 as gvr
+    d0, d1 = torch.device("cuda", 0), torch.device("cuda", 1)
+    on = lambda d: types.SimpleNamespace(device=d)  # noqa: E731 - only .device is looked at
+    gvr._same_device(d0, kv_lens=on(d0), indices=on(d0), values=None)
+    for name in ("kv_lens", "indices", "values", "pre_idx", "block_max", "row_starts", "row_ends"):
+        with pytest.raises(ValueError, match=name):
+            gvr._same_device(d0, **{name: on(d1)})

@@ -674,3 +674,15 @@ def test_compact_lists_large_bins_and_long_shares(gvr):
     st = assert_decode_exact(gvr, big, options=gvr.Options(flags=CL, cluster_size=1), stats=True)
     # no list is used: the collect reads the share again, or an overflowing bin goes to the rescue
     assert ((st[:, 0] == 3) | ((st[:, 0] == 1) & (st[:, 2] >= 10))).all(), st
+
+
+def test_binding_refuses_narrowed_views(gvr):
+    # The row stride passed to the library bounds every window; a narrowed view would let a
+    # window run past the view's columns, so the binding refuses it.
+    buf = torch.zeros((4, 2048), dtype=torch.float32, device=DEV)
+    kv = torch.full((4,), 2048, dtype=torch.int32, device=DEV)
+    with pytest.raises(ValueError, match="packed"):
+        gvr.topk_decode(buf[:, :1024], kv, 1, 1, 512)
+    ks = torch.zeros((4,), dtype=torch.int32, device=DEV)
+    with pytest.raises(ValueError, match="packed"):
+        gvr.topk_prefill(buf[:, :1024], ks, kv, 512)
