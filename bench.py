@@ -7,12 +7,19 @@ K = 1024, row stride 131072 fp32, scores N(0,1) plus a position-linear bias,
 poisoned padding, and three requests at n = K-1, K, K+1.  Synthetic and seeded
 (workloads.decode_batch).
 
-One step = one topk_decode call over the whole batch (one kernel launch).
+One step = one topk_decode_ws call over the whole batch (one kernel launch: the
+balanced kernel, which splits the batch's valid scores evenly over the GPU).
 
 * value (cold L2): the timed region replays a CUDA graph that runs the step on
   R distinct device copies of the batch in turn, R * 64 MiB >> L2 (129 MB), so
   no step finds its scores in L2.  Timed with CUDA events on the launching
   stream, a barrier and torch.cuda.synchronize() on both sides, max over ranks.
+  The --steps window is repeated until --min-seconds have passed; the line
+  reports the median window (clocks are sampled over all of them).
+* extra keys (the target configurations, cold/warm, outside the timed region):
+  sweep_big (the >= 36 MB sweep cells, decode and prefill), tail (each
+  adversarial variant against a normal row of the same shape), single_row
+  (one 8192-score row, K = 512) and prefill_tile (4096 rows, K = 2048).
 * warm_l2: the same graph over one copy (scores L2-resident after the first).
 * e2e: the public API with host buffers: every step copies the batch from
   pinned host memory to the device, selects, and copies the indices back.
@@ -31,7 +38,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -45,7 +51,7 @@ sys.path.insert(0, ROOT)
 METRIC = "rows/s and µs/row top-K (cold/warm L2); HBM GB/s vs ~8 TB/s at 1 GB300"
 NOMINAL_HBM_GBS = 8000.0
 KERNEL_NAME = "gvr_topk_kernel"
-PROFILE_NOTE = os.path.join(ROOT, "profiles", "gvr_topk_kernel_decode_batch.md")
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
 
 
 def dist_env():
@@ -101,17 +107,18 @@ def source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """dram bytes per launch from the committed ncu summary, if it matches the current kernel."""
+def profiled_traffic(kernel: str):
+    """DRAM bytes (read + write) per launch of ``kernel`` on the headline workload, from the ncu
+    capture recorded in profiles/traffic.json -- only while the kernel sources still match the
+    digest recorded with it (a changed kernel has no measured traffic until it is captured again)."""
     try:
-        text = open(PROFILE_NOTE).read()
-    except OSError:
+        with open(TRAFFIC_JSON) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    src = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
-    tb = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not src or not tb or src.group(1) != source_digest():
+    if rec.get("source_sha256") != source_digest() or rec.get("kernel") != kernel:
         return None
-    return float(tb.group(1))
+    return float(rec["dram_bytes_per_launch"])
 
 
 def measured_peak_hbm():
@@ -248,27 +255,40 @@ def prefill_algorithmic_bytes(case) -> int:
     return int(np.where(n > case.k, 4 * n, 0).sum()) + case.rows * case.k * 4 + 8 * case.rows
 
 
-def run_sweep(args):
-    """Every sweep cell (BS x N x K, decode and prefill), cold and warm L2, one JSON line each;
-    then the tail check on the adversarial row and its variants.
+class ColdWarm:
+    """Cold- and warm-L2 timing of one call on the current stream.
 
-    cold: a 512 MiB scrub write before each call; per call CUDA events (median / p99 / max of
-    32) and, at finer resolution, the mean over graphs of (scrub + call) minus (scrub) -- the
-    rates use the graph mean.  warm: a graph of 100 back-to-back calls on one input."""
-    import torch
-    import workloads
-    import sparse_attention_indexer_exact_gb300 as gvr
+    cold: a 512 MiB scrub write before each call (the call then finds none of its inputs in L2);
+    per call CUDA events (median / p99 / max of ``reps``; the event clock ticks in ~2 us steps on
+    this GPU) and, at finer resolution, the mean over graphs of (scrub + call) minus (scrub) --
+    rates use that graph mean.  warm: a graph of ``warm_calls`` back-to-back calls on one input."""
 
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py needs a CUDA GPU (no CPU fallback exists)")
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    gvr.load_library()
-    stream = torch.cuda.current_stream()
-    scrub = torch.empty(512 << 20, dtype=torch.uint8, device=dev)  # > L2: evicts the scores
-    peak, _ = measured_peak_hbm()
+    def __init__(self, torch, dev):
+        self.torch = torch
+        self.stream = torch.cuda.current_stream()
+        self.scrub = torch.empty(512 << 20, dtype=torch.uint8, device=dev)  # > L2 (129 MB)
 
-    def measure(launch, reps=32, warm_calls=100):
+    def _graph_us(self, body, calls):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            h = torch.cuda.current_stream().cuda_stream
+            for i in range(calls):
+                body(i, h)
+        g.replay()
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(self.stream)
+            g.replay()
+            e1.record(self.stream)
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1) * 1e3)
+        return best / calls
+
+    def __call__(self, launch, reps=32, warm_calls=100):
+        torch, stream, scrub = self.torch, self.stream, self.scrub
         for _ in range(3):
             launch(stream.cuda_stream)
         torch.cuda.synchronize()
@@ -281,77 +301,148 @@ def run_sweep(args):
             e1.record(stream)
             torch.cuda.synchronize()
             cold.append(e0.elapsed_time(e1) * 1e3)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            h = torch.cuda.current_stream().cuda_stream
-            for _ in range(warm_calls):
-                launch(h)
-        g.replay()
-        torch.cuda.synchronize()
-        warm = []
-        for _ in range(3):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            g.replay()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            warm.append(e0.elapsed_time(e1) * 1e3 / warm_calls)
-        # the event clock ticks in ~2 us steps here, so the cold mean is also taken from graphs:
-        # (scrub + call) x R minus (scrub) x R, over R calls
-        def graph_of(with_call, r=16):
-            gg = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gg):
-                h = torch.cuda.current_stream().cuda_stream
-                for i in range(r):
-                    scrub.fill_(i & 255)
-                    if with_call:
-                        launch(h)
-            gg.replay()
-            torch.cuda.synchronize()
-            best = float("inf")
-            for _ in range(3):
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                gg.replay()
-                e1.record(stream)
-                torch.cuda.synchronize()
-                best = min(best, e0.elapsed_time(e1) * 1e3)
-            return best / r
-        cold_mean = graph_of(True) - graph_of(False)
-        cold.sort()
-        return (cold[len(cold) // 2], cold[min(len(cold) - 1, int(0.99 * len(cold)))], cold[-1], min(warm),
-                cold_mean)
+        warm = self._graph_us(lambda i, h: launch(h), warm_calls)
 
-    def emit(tag, case, nbytes, launch):
-        med, p99, mx, warm, cmean = measure(launch)
-        print(json.dumps({
-            "sweep": tag, "bs": case.rows, "n": int(case.meta.get("n", 0)), "k": case.k,
-            "cold_us": {"median": med, "p99": p99, "max": mx, "graph_mean": cmean}, "warm_us": warm,
-            "rows_per_s_cold": case.rows / (cmean * 1e-6), "us_per_row_cold": cmean / case.rows,
-            "algorithmic_bytes": nbytes, "gbs_cold": nbytes / cmean / 1e3, "gbs_warm_effective": nbytes / warm / 1e3,
-            "frac_of_8tbs": nbytes / cmean / 1e3 / NOMINAL_HBM_GBS, "frac_of_measured": nbytes / cmean / 1e3 / peak,
-            "reachable_60pct": nbytes >= 36e6}), flush=True)
-        return cmean
+        def scrub_then(with_call):
+            def body(i, h):
+                scrub.fill_(i & 255)
+                if with_call:
+                    launch(h)
+            return body
+        cold_mean = self._graph_us(scrub_then(True), 16) - self._graph_us(scrub_then(False), 16)
+        cold.sort()
+        return {"median": cold[len(cold) // 2], "p99": cold[min(len(cold) - 1, int(0.99 * len(cold)))],
+                "max": cold[-1], "graph_mean": cold_mean, "warm": warm}
+
+
+def _launchers(torch, gvr, dev, wsb):
+    """Callables that run one decode / prefill call of a case through the *_ws entry points
+    (the default dispatch: the balanced kernel where it fits, else the cluster kernel)."""
+
+    def decode(case, flags=0):
+        lg = torch.from_numpy(case.logits).to(dev)
+        kv = torch.from_numpy(case.kv_lens).to(dev)
+        idx = torch.empty((case.rows, case.k), dtype=torch.int32, device=dev)
+        o = gvr.Options(flags=flags) if flags else None
+        return lambda h: gvr.topk_decode_ws_raw(lg.data_ptr(), lg.shape[1], case.rows, kv.data_ptr(), case.next_n,
+                                                case.compress_ratio, case.k, idx.data_ptr(), None, wsb.data_ptr(),
+                                                wsb.numel(), h, o)
+
+    def prefill(case, flags=0):
+        lg = torch.from_numpy(case.logits).to(dev)
+        ks = torch.from_numpy(case.row_starts).to(dev)
+        ke = torch.from_numpy(case.row_ends).to(dev)
+        idx = torch.empty((case.rows, case.k), dtype=torch.int32, device=dev)
+        o = gvr.Options(flags=flags) if flags else None
+        return lambda h: gvr.topk_prefill_ws_raw(lg.data_ptr(), lg.shape[1], case.rows, ks.data_ptr(), ke.data_ptr(),
+                                                 case.k, idx.data_ptr(), wsb.data_ptr(), wsb.numel(), h, o)
+    return decode, prefill
+
+
+def _cell(tag, case, nbytes, t, peak):
+    cm = t["graph_mean"]
+    return {"cell": tag, "bs": case.rows, "n": int(case.meta.get("n", 0)), "k": case.k,
+            "cold_us": {k: round(v, 2) for k, v in t.items() if k != "warm"}, "warm_us": round(t["warm"], 2),
+            "rows_per_s_cold": case.rows / (cm * 1e-6), "us_per_row_cold": cm / case.rows,
+            "algorithmic_bytes": nbytes, "gbs_cold": nbytes / cm / 1e3,
+            "frac_of_measured": nbytes / cm / 1e3 / peak, "frac_of_8tbs": nbytes / cm / 1e3 / NOMINAL_HBM_GBS,
+            "reachable_60pct": nbytes >= 36e6}
+
+
+def tail_check(torch, gvr, dev, wsb, timer, peak, emit=None):
+    """Each adversarial variant's cold graph-mean time over that of a row of the same shape drawn
+    from N(0,1) (the benchmark spec's bound: no rescue-induced tail beyond 2x)."""
+    import workloads
+    decode, _ = _launchers(torch, gvr, dev, wsb)
+    base = workloads.adversarial_row("base")
+    g = np.random.default_rng(1049)
+    plain = base.logits.copy()
+    n0 = int(base.row_lengths()[0])
+    plain[0, :n0] = g.standard_normal(n0).astype(np.float32)
+    ref_case = workloads.DecodeCase("adversarial_shape_normal", plain, base.kv_lens, 1, base.compress_ratio, base.k,
+                                    {"n": n0})
+    t_ref = timer(decode(ref_case))
+    if emit:
+        emit(_cell("tail_reference_normal_row", ref_case, algorithmic_bytes(ref_case, False), t_ref, peak))
+    ratios = {}
+    for v in workloads.ADVERSARIAL_VARIANTS:
+        c = workloads.adversarial_row(v)
+        c.meta["n"] = n0
+        t = timer(decode(c))
+        if emit:
+            emit(_cell(f"tail_{v}", c, algorithmic_bytes(c, False), t, peak))
+        ratios[v] = round(t["graph_mean"] / t_ref["graph_mean"], 3)
+    return {"normal_row_us": round(t_ref["graph_mean"], 2), "ratio_to_normal_row": ratios,
+            "within_2x": all(r <= 2.0 for r in ratios.values())}
+
+
+SWEEP_BIG = [(256, 131072, 512), (256, 131072, 1024), (256, 131072, 2048), (256, 65536, 512)]
+
+
+def extras(torch, gvr, dev, wsb, peak):
+    """The target configurations beside the headline, one call each at a time, cold and warm:
+    the >= 36 MB sweep cells (decode and prefill), the tail check, the single decode row and
+    the 4096-row prefill tile."""
+    import workloads
+    timer = ColdWarm(torch, dev)
+    decode, prefill = _launchers(torch, gvr, dev, wsb)
+    out = {}
+    cells = []
+    for bs, n, k in SWEEP_BIG:
+        dc = workloads.sweep_decode(bs, n, k)
+        cells.append(_cell("decode", dc, algorithmic_bytes(dc, False), timer(decode(dc), reps=8), peak))
+        pc = workloads.sweep_prefill(bs, n, k)
+        cells.append(_cell("prefill", pc, prefill_algorithmic_bytes(pc), timer(prefill(pc), reps=8), peak))
+        del dc, pc
+        torch.cuda.empty_cache()
+    out["sweep_big"] = cells
+    out["tail"] = tail_check(torch, gvr, dev, wsb, timer, peak)
+    sr = workloads.single_decode_row()
+    t = timer(decode(sr))
+    out["single_row"] = {"workload": sr.meta["workload"], "cold_us": round(t["graph_mean"], 2),
+                         "cold_event_us": {"median": t["median"], "p99": t["p99"], "max": t["max"]},
+                         "warm_us": round(t["warm"], 2)}
+    pt = workloads.prefill_tile()
+    t = timer(prefill(pt), reps=8)
+    nb = prefill_algorithmic_bytes(pt)
+    out["prefill_tile"] = {"workload": pt.meta.get("workload", "prefill tile"), "rows": pt.rows,
+                           "cold_us": round(t["graph_mean"], 2), "warm_us": round(t["warm"], 2),
+                           "rows_per_s_cold": pt.rows / (t["graph_mean"] * 1e-6),
+                           "us_per_row_cold": t["graph_mean"] / pt.rows, "algorithmic_bytes": nb,
+                           "frac_of_measured": nb / t["graph_mean"] / 1e3 / peak}
+    return out
+
+
+def run_sweep(args):
+    """Every sweep cell (BS x N x K, decode and prefill), cold and warm L2, one JSON line each;
+    the block-skip cells; then the tail check on the adversarial row and its variants."""
+    import torch
+    import workloads
+    import sparse_attention_indexer_exact_gb300 as gvr
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (no CPU fallback exists)")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    gvr.load_library()
+    wsb = torch.zeros(gvr.workspace_size(), dtype=torch.uint8, device=dev)
+    peak, _ = measured_peak_hbm()
+    timer = ColdWarm(torch, dev)
+    decode, prefill = _launchers(torch, gvr, dev, wsb)
+
+    def emit(d):
+        print(json.dumps(d), flush=True)
 
     for n in (16384, 32768, 65536, 131072):
         for bs in (1, 4, 16, 64, 256):
-            dcase = workloads.sweep_decode(bs, n, 512)
-            lg = torch.from_numpy(dcase.logits).to(dev)
             for k in (512, 1024, 2048):
-                dc = workloads.DecodeCase(dcase.name, dcase.logits, dcase.kv_lens, 1, 1, k, {"n": n})
-                kv = torch.from_numpy(dc.kv_lens).to(dev)
-                idx = torch.empty((bs, k), dtype=torch.int32, device=dev)
-                emit("decode", dc, algorithmic_bytes(dc, False),
-                     lambda h, lg=lg, kv=kv, idx=idx, k=k: gvr.topk_decode_raw(
-                         lg.data_ptr(), lg.stride(0), bs, kv.data_ptr(), 1, 1, k, idx.data_ptr(), None, h))
-                ks = torch.from_numpy((np.arange(bs) % 4).astype(np.int32)).to(dev)
-                ke = torch.full((bs,), n, dtype=torch.int32, device=dev)
-                pc = workloads.PrefillCase(dcase.name, dcase.logits, (np.arange(bs) % 4).astype(np.int32),
-                                           np.full(bs, n, np.int32), k, {"n": n})
-                emit("prefill", pc, prefill_algorithmic_bytes(pc),
-                     lambda h, lg=lg, ks=ks, ke=ke, idx=idx, k=k: gvr.topk_prefill_raw(
-                         lg.data_ptr(), lg.stride(0), bs, ks.data_ptr(), ke.data_ptr(), k, idx.data_ptr(), h))
-            del lg
+                dc = workloads.sweep_decode(bs, n, k)
+                emit(_cell("decode", dc, algorithmic_bytes(dc, False), timer(decode(dc)), peak))
+                pc = workloads.sweep_prefill(bs, n, k)
+                emit(_cell("prefill", pc, prefill_algorithmic_bytes(pc), timer(prefill(pc)), peak))
+                del dc, pc
+            torch.cuda.empty_cache()
+
     # block-skip: the same selection with exact block maxima given (decode rows)
     def block_max_of(case):
         nb = (case.row_stride + 31) // 32
@@ -371,40 +462,18 @@ def run_sweep(args):
         bm = torch.from_numpy(block_max_of(case)).to(dev)
         idx = torch.empty((case.rows, case.k), dtype=torch.int32, device=dev)
         case.meta.setdefault("n", int(case.row_lengths().max()))
-        for tag, fn in (("blockskip_off", None), ("blockskip_on", bm)):
-            if fn is None:
-                launch = (lambda h, lg=lg, kv=kv, idx=idx, case=case: gvr.topk_decode_raw(
+        runs = (("cluster", lambda h, lg=lg, kv=kv, idx=idx, case=case: gvr.topk_decode_raw(
                     lg.data_ptr(), case.row_stride, case.rows, kv.data_ptr(), case.next_n, case.compress_ratio,
-                    case.k, idx.data_ptr(), None, h))
-            else:
-                launch = (lambda h, lg=lg, kv=kv, idx=idx, case=case, bm=bm: gvr.topk_decode_blockskip_raw(
+                    case.k, idx.data_ptr(), None, h)),
+                ("balanced", decode(case)),
+                ("blockskip_on", lambda h, lg=lg, kv=kv, idx=idx, case=case, bm=bm: gvr.topk_decode_blockskip_raw(
                     lg.data_ptr(), case.row_stride, case.rows, kv.data_ptr(), case.next_n, case.compress_ratio,
-                    case.k, bm.data_ptr(), bm.stride(0), idx.data_ptr(), None, h))
-            emit(f"{tag}:{case.name}", case, algorithmic_bytes(case, False), launch)
+                    case.k, bm.data_ptr(), bm.stride(0), idx.data_ptr(), None, h)))
+        for tag, launch in runs:
+            emit(_cell(f"{tag}:{case.name}", case, algorithmic_bytes(case, False), timer(launch), peak))
         del lg, bm
-    # tail check: each adversarial variant against a row of the same shape drawn from N(0,1)
-    base = workloads.adversarial_row("base")
-    g = np.random.default_rng(1049)
-    plain = base.logits.copy()
-    n0 = int(base.row_lengths()[0])
-    plain[0, :n0] = g.standard_normal(n0).astype(np.float32)
-    ref_case = workloads.DecodeCase("adversarial_shape_normal", plain, base.kv_lens, 1, base.compress_ratio, base.k,
-                                    {"n": n0})
-
-    def adv_launch(case):
-        lg = torch.from_numpy(case.logits).to(dev)
-        kv = torch.from_numpy(case.kv_lens).to(dev)
-        idx = torch.empty((case.rows, case.k), dtype=torch.int32, device=dev)
-        return lambda h: gvr.topk_decode_raw(lg.data_ptr(), lg.stride(0), case.rows, kv.data_ptr(), case.next_n,
-                                             case.compress_ratio, case.k, idx.data_ptr(), None, h)
-
-    ref_med = emit("tail_reference_normal_row", ref_case, algorithmic_bytes(ref_case, False), adv_launch(ref_case))
-    for v in workloads.ADVERSARIAL_VARIANTS:
-        c = workloads.adversarial_row(v)
-        c.meta["n"] = n0
-        med = emit(f"tail_{v}", c, algorithmic_bytes(c, False), adv_launch(c))
-        print(json.dumps({"tail_check": v, "ratio_to_normal_row": med / ref_med, "within_2x": med <= 2 * ref_med}),
-              flush=True)
+    t = tail_check(torch, gvr, dev, wsb, timer, peak, emit)
+    emit({"tail_check": t})
     return 0
 
 
@@ -420,13 +489,16 @@ def config_block(case, ws):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["gvr", "reference"], default="gvr")
     ap.add_argument("--copies", type=int, default=16, help="distinct device copies of the batch (cold L2)")
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="repeat the --steps window until this much time has passed; report the median window")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--values", action="store_true", help="also write the fp32 values output")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the sweep_big / tail / single_row / prefill_tile keys")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the headline line: every sweep cell and the adversarial tail check")
     args = ap.parse_args()
@@ -461,15 +533,21 @@ def main():
     idx = torch.empty((rows, k), dtype=torch.int32, device=dev)
     vals = torch.empty((rows, k), dtype=torch.float32, device=dev) if args.values else None
     vptr = vals.data_ptr() if vals is not None else None
+    # the workspace of the balanced kernel (zero-filled once; every call leaves it zero-filled)
+    wsb = torch.zeros(gvr.workspace_size(), dtype=torch.uint8, device=dev)
 
-    def launch(buf, stream_handle):
-        gvr.topk_decode_raw(buf.data_ptr(), stride, rows, kv.data_ptr(), case.next_n, case.compress_ratio, k,
-                            idx.data_ptr(), vptr, stream_handle)
+    def launch(buf, stream_handle, options=None):
+        gvr.topk_decode_ws_raw(buf.data_ptr(), stride, rows, kv.data_ptr(), case.next_n, case.compress_ratio, k,
+                               idx.data_ptr(), vptr, wsb.data_ptr(), wsb.numel(), stream_handle, options)
 
     stream = torch.cuda.current_stream()
     for i in range(args.warmup):  # eager warm-up also performs the one-time device set-up
         launch(bufs[i % copies], stream.cuda_stream)
+    # which kernel the library chose for this call: its per-row path codes (untimed call)
+    st = torch.full((rows, 4), -1, dtype=torch.int32, device=dev)
+    launch(bufs[0], stream.cuda_stream, gvr.Options(row_stats=st.data_ptr()))
     torch.cuda.synchronize()
+    kernel = "gvr_split_kernel" if bool(((st[:, 0] == 7) | (st[:, 0] == 8)).any()) else "gvr_topk_kernel"
 
     def make_graph(buffers):
         g = torch.cuda.CUDAGraph()
@@ -481,12 +559,14 @@ def main():
 
     cold_graph = make_graph(bufs)
     warm_graph = make_graph([bufs[0]] * copies)
+    cold_graph.replay()  # graph upload
+    warm_graph.replay()
     torch.cuda.synchronize()
 
-    def timed(graph, steps):
+    def window(graph, steps):
+        """Exactly `steps` steps, bracketed by a barrier and a synchronize on both sides; device
+        seconds from CUDA events on the launching stream, and wall seconds."""
         reps, rem = divmod(steps, copies)
-        graph.replay()  # one untimed replay: graph upload
-        torch.cuda.synchronize()
         barrier()
         torch.cuda.synchronize()
         t_wall = time.perf_counter()
@@ -502,9 +582,22 @@ def main():
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / 1e3, time.perf_counter() - t_wall
 
+    def windows(graph):
+        """Repeat the window until --min-seconds of wall time (the same count on every rank);
+        returns the median window's device seconds, the window count and the wall seconds."""
+        first, wall0 = window(graph, args.steps)
+        n = max(3, int(np.ceil(args.min_seconds / max(wall0, 1e-6))))
+        n = int(max_over_ranks(float(n), dev))
+        times, wall = [first], wall0
+        for _ in range(n - 1):
+            t, w = window(graph, args.steps)
+            times.append(t)
+            wall += w
+        return statistics.median(times), len(times), wall
+
     with ClockSampler(local) as clk:
-        cold_s, cold_wall = timed(cold_graph, args.steps)
-    warm_s, _ = timed(warm_graph, args.steps)
+        cold_s, n_windows, cold_wall = windows(cold_graph)
+    warm_s, _, _ = windows(warm_graph)
 
     # end to end through the public API with host buffers
     pinned = host.pin_memory()
@@ -543,6 +636,9 @@ def main():
         achieved = nbytes / per_launch / 1e9
         peak, peak_kind = measured_peak_hbm()
         warm_per = warm_s / args.steps
+        del bufs
+        torch.cuda.empty_cache()
+        extra = None if args.no_extras else extras(torch, gvr, dev, wsb, peak)
         cpu = None
         if not args.no_cpu_baseline:
             secs, cores, runs, total = time_oracle(case, 0, 5, CPU_BASELINE_S)
@@ -571,6 +667,8 @@ def main():
             "dtype": "f32",
             "data": "synthetic",
             "config": config_block(case, ws),
+            "timing": {"windows": n_windows, "steps_per_window": args.steps, "window_s": "median",
+                       "wall_s": round(cold_wall, 3)},
             "warm_l2": {"value": total_rows * args.steps / warm_max, "unit": "rows/s",
                         "us_per_call": 1e6 * warm_per, "us_per_row": 1e6 * warm_per / rows,
                         "effective_gbs": nbytes / warm_per / 1e9},
@@ -578,17 +676,19 @@ def main():
                                    "frac": achieved / NOMINAL_HBM_GBS},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
-                         "traffic": profiled_traffic(), "algorithmic_bytes_per_launch": nbytes,
-                         "us_per_launch": 1e6 * per_launch, "kernel": KERNEL_NAME},
+                         "traffic": profiled_traffic(kernel), "algorithmic_bytes_per_launch": nbytes,
+                         "us_per_launch": 1e6 * per_launch, "kernel": kernel},
             "e2e": {"value": total_rows * e2e_steps / e2e_max, "unit": "rows/s",
                     "h2d_bytes_per_step": int(pinned.numel() * 4 + kv_host.numel() * 4),
                     "d2h_bytes_per_step": int(idx_host.numel() * 4)},
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * n_windows,
             "cpu_baseline": cpu,
             "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                        "reasons": clocks["reasons"], "samples": clocks["samples"],
                        "window_s": round(cold_wall, 3)},
         }
+        if extra:
+            line.update(extra)
         print(json.dumps(line))
     if ws > 1:
         dist.destroy_process_group()

@@ -49,6 +49,7 @@
 #ifndef GVR_TOPK_H
 #define GVR_TOPK_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -62,7 +63,9 @@ typedef enum gvr_status {
   GVR_ERR_STRIDE = 3, /* row_stride is not a multiple of 4, below 4, or not below 2^31 */
   GVR_ERR_K = 4,      /* k is not 512, 1024 or 2048 */
   GVR_ERR_ARG = 5,    /* a negative row count, next_n < 1, compress_ratio < 1, bad options */
-  GVR_ERR_LAUNCH = 6  /* the kernel launch failed (no device, bad configuration, ...) */
+  GVR_ERR_LAUNCH = 6,   /* the kernel launch failed (no device, bad configuration, ...) */
+  GVR_ERR_WORKSPACE = 7 /* the workspace is NULL, not 16-byte aligned or smaller than
+                           gvr_workspace_size reports */
 } gvr_status;
 
 /*
@@ -120,7 +123,14 @@ enum {
   /* the compact first-pass lists (1024 entries of score and 16-bit share position per CTA, 16
    * samples expected above tau) on every launch; by default the host picks them only where
    * they let a two-wave launch run as one wave with half the CTAs per row */
-  GVR_FLAG_COMPACT_LISTS = 128
+  GVR_FLAG_COMPACT_LISTS = 128,
+  /* *_ws entry points: always the cluster kernel (the workspace is then not touched) */
+  GVR_FLAG_CLUSTER_KERNEL = 256,
+  /* diagnostics, *_ws entry points: the balanced kernel's last CTA of every long row selects the
+   * row alone (the exact path it takes when the published scores cannot decide the row) */
+  GVR_FLAG_SPLIT_ALONE = 512,
+  /* *_ws entry points: the balanced kernel whenever the call fits it */
+  GVR_FLAG_SPLIT_KERNEL = 1024
 };
 
 typedef struct gvr_options {
@@ -150,9 +160,11 @@ enum {
   GVR_PATH_RESCUE_FORCED = 4,   /* GVR_FLAG_FORCE_RESCUE */
   GVR_PATH_REFINE_CLUSTER = 5,  /* crossing bin exceeded the candidate buffer, every CTA's list
                                    held its counted scores: exact digit passes over the lists */
-  GVR_PATH_REFINE_RELIST = 6    /* crossing bin exceeded the candidate buffer and a first-pass
+  GVR_PATH_REFINE_RELIST = 6,   /* crossing bin exceeded the candidate buffer and a first-pass
                                    list overflowed: one more read of the row lists the crossing
                                    bin and above per CTA, digit passes over those lists */
+  GVR_PATH_SPLIT = 7,           /* balanced kernel: selected from the row's published scores */
+  GVR_PATH_SPLIT_ALONE = 8      /* balanced kernel: the row's last CTA selected it alone */
 };
 
 /* topk_decode with tuning/diagnostic options (NULL = automatic, identical to topk_decode). */
@@ -207,6 +219,44 @@ gvr_status topk_decode_blockskip(const float* logits, int64_t row_stride, int64_
                                  int32_t k, const float* block_max, int64_t block_max_stride,
                                  int32_t* indices, float* values, void* stream,
                                  const gvr_options* options);
+
+/*
+ * Balanced entry points with a workspace.  A decode batch's rows can differ widely in length
+ * (n_r from kv_lens, known only on the device), and the cluster kernel above sizes every row's
+ * cluster from row_stride, so its longest rows set the time.  These entry points may instead
+ * run the balanced kernel: every CTA reads all rows' lengths on the device, the batch's valid
+ * scores are cut into chunks of one size, one CTA per chunk, and each chunk publishes the scores
+ * at or above its row's sampled floor to the workspace; the last chunk of a row to finish
+ * selects the row from them (histogram over the sampled bracket, crossing bin, exact refine), or
+ * -- when they cannot decide it (fewer than k reached the floor, a chunk's slot overflowed, an
+ * invalid bracket) -- selects the row alone by an exact radix select over the whole window.
+ * Same method ("GVR K=2048 reg_clus with block64 sampling and parallel rescue", PR #20998,
+ * "What changes"), same results: exact, tie-interchangeable, identical conventions.
+ *
+ * The balanced kernel runs when options->flags asks for it (GVR_FLAG_SPLIT_KERNEL or
+ * GVR_FLAG_SPLIT_ALONE, and no other flag), num_rows <= 512 and num_rows is at most half its
+ * grid (the device's SM count x 8 CTAs); otherwise the call is exactly topk_decode_ex /
+ * topk_prefill_ex and the workspace is not touched (GVR_FLAG_CLUSTER_KERNEL forces that).
+ *
+ * The workspace is device memory the caller owns, at least gvr_workspace_size bytes, 16-byte
+ * aligned, and ZERO-FILLED before its first use (cudaMemset once); every call that completes
+ * leaves it zero-filled again.  Calls that can overlap on the GPU (different streams without an
+ * ordering between them) must use different workspaces.  Every other argument, the ownership
+ * rules and the errors are those of topk_decode_ex / topk_prefill_ex, plus GVR_ERR_WORKSPACE.
+ */
+/* Bytes of workspace the *_ws entry points need on the current device (sm_count <= 0) or on a
+ * GB300-class device with sm_count SMs; the size does not depend on the call's shape. */
+gvr_status gvr_workspace_size(int32_t sm_count, size_t* bytes);
+
+gvr_status topk_decode_ws(const float* logits, int64_t row_stride, int64_t num_rows,
+                          const int32_t* kv_lens, int32_t next_n, int32_t compress_ratio,
+                          int32_t k, int32_t* indices, float* values, void* workspace,
+                          size_t workspace_bytes, void* stream, const gvr_options* options);
+
+gvr_status topk_prefill_ws(const float* logits, int64_t row_stride, int64_t num_rows,
+                           const int32_t* row_starts, const int32_t* row_ends, int32_t k,
+                           int32_t* indices, void* workspace, size_t workspace_bytes, void* stream,
+                           const gvr_options* options);
 
 /* Static English text for a status code; never NULL. */
 const char* gvr_status_string(gvr_status status);

@@ -25,7 +25,7 @@ import os
 import threading
 
 __all__ = ["topk_decode", "topk_prefill", "topk_decode_raw", "topk_decode_hinted_raw", "topk_decode_blockskip_raw",
-           "topk_prefill_raw", "plan",
+           "topk_prefill_raw", "topk_decode_ws_raw", "topk_prefill_ws_raw", "workspace_size", "workspace", "plan",
            "Options",
            "GvrError", "library_path", "load_library", "FLAG_FORCE_RESCUE", "FLAG_NO_FLOOR", "FLAG_ZERO_CAP",
            "FLAG_RADIX_REFINE", "FLAG_DETERMINISTIC", "FLAG_SORTED", "FLAG_STREAM_RESCUE", "FLAG_COMPACT_LISTS", "PATH_NAMES",
@@ -38,11 +38,13 @@ _lib = None
 
 FLAG_FORCE_RESCUE, FLAG_NO_FLOOR, FLAG_ZERO_CAP, FLAG_RADIX_REFINE = 1, 2, 4, 8
 FLAG_DETERMINISTIC, FLAG_SORTED, FLAG_STREAM_RESCUE, FLAG_COMPACT_LISTS = 16, 32, 64, 128
+FLAG_CLUSTER_KERNEL, FLAG_SPLIT_ALONE, FLAG_SPLIT_KERNEL = 256, 512, 1024
 PATH_NAMES = {-1: "device_error", 0: "short", 1: "refine", 2: "rescue_bracket", 3: "rescue_overflow",
-              4: "rescue_forced", 5: "refine_cluster", 6: "refine_relist"}
+              4: "rescue_forced", 5: "refine_cluster", 6: "refine_relist", 7: "split", 8: "split_alone"}
 SUPPORTED_K = (512, 1024, 2048)
 EXPORTED_SYMBOLS = ("topk_decode", "topk_prefill", "topk_decode_ex", "topk_prefill_ex", "topk_decode_hinted",
-                    "topk_decode_blockskip", "gvr_status_string", "gvr_plan")
+                    "topk_decode_blockskip", "topk_decode_ws", "topk_prefill_ws", "gvr_workspace_size",
+                    "gvr_status_string", "gvr_plan")
 
 
 class GvrError(RuntimeError):
@@ -73,8 +75,13 @@ def _declare(lib):
     lib.topk_prefill.argtypes = [p, i64, i64, p, p, i32, p, p]
     lib.topk_prefill_ex.argtypes = [p, i64, i64, p, p, i32, p, p, ctypes.POINTER(Options)]
     lib.gvr_plan.argtypes = [i64, i64, i32, ctypes.POINTER(Options), i32] + [ctypes.POINTER(i32)] * 4
+    sz = ctypes.c_size_t
+    lib.topk_decode_ws.argtypes = [p, i64, i64, p, i32, i32, i32, p, p, p, sz, p, ctypes.POINTER(Options)]
+    lib.topk_prefill_ws.argtypes = [p, i64, i64, p, p, i32, p, p, sz, p, ctypes.POINTER(Options)]
+    lib.gvr_workspace_size.argtypes = [i32, ctypes.POINTER(sz)]
     for f in (lib.topk_decode, lib.topk_decode_ex, lib.topk_decode_hinted, lib.topk_decode_blockskip,
-              lib.topk_prefill, lib.topk_prefill_ex, lib.gvr_plan):
+              lib.topk_prefill, lib.topk_prefill_ex, lib.gvr_plan, lib.topk_decode_ws, lib.topk_prefill_ws,
+              lib.gvr_workspace_size):
         f.restype = ctypes.c_int
     lib.gvr_status_string.argtypes = [ctypes.c_int]
     lib.gvr_status_string.restype = ctypes.c_char_p
@@ -150,6 +157,53 @@ def topk_prefill_raw(logits_ptr: int, row_stride: int, num_rows: int, row_starts
         st = lib.topk_prefill_ex(logits_ptr, row_stride, num_rows, row_starts_ptr, row_ends_ptr, k, indices_ptr,
                                  stream, ctypes.byref(options))
     _check(st)
+
+
+def topk_decode_ws_raw(logits_ptr: int, row_stride: int, num_rows: int, kv_lens_ptr: int, next_n: int,
+                       compress_ratio: int, k: int, indices_ptr: int, values_ptr: int | None, workspace_ptr: int,
+                       workspace_bytes: int, stream: int, options: Options | None = None) -> None:
+    """``topk_decode_ws`` on raw device addresses (enqueue only)."""
+    lib = load_library()
+    st = lib.topk_decode_ws(logits_ptr, row_stride, num_rows, kv_lens_ptr, next_n, compress_ratio, k, indices_ptr,
+                            values_ptr, workspace_ptr, workspace_bytes, stream,
+                            ctypes.byref(options) if options is not None else None)
+    _check(st)
+
+
+def topk_prefill_ws_raw(logits_ptr: int, row_stride: int, num_rows: int, row_starts_ptr: int, row_ends_ptr: int,
+                        k: int, indices_ptr: int, workspace_ptr: int, workspace_bytes: int, stream: int,
+                        options: Options | None = None) -> None:
+    """``topk_prefill_ws`` on raw device addresses (enqueue only)."""
+    lib = load_library()
+    st = lib.topk_prefill_ws(logits_ptr, row_stride, num_rows, row_starts_ptr, row_ends_ptr, k, indices_ptr,
+                             workspace_ptr, workspace_bytes, stream,
+                             ctypes.byref(options) if options is not None else None)
+    _check(st)
+
+
+def workspace_size(sm_count: int = 0) -> int:
+    """Bytes of workspace the *_ws entry points need (current device, or a device of sm_count SMs)."""
+    lib = load_library()
+    out = ctypes.c_size_t(0)
+    _check(lib.gvr_workspace_size(sm_count, ctypes.byref(out)))
+    return int(out.value)
+
+
+_workspaces: dict = {}
+
+
+def workspace(device, stream_handle: int):
+    """The zero-filled workspace this binding keeps per (device, stream): calls on one stream are
+    ordered, so they may share it; calls on different streams get different ones.  It is
+    allocated (torch.zeros) on the first call for that pair, so make that call before capturing
+    a CUDA graph that replays it."""
+    torch = _torch()
+    key = (device.index, int(stream_handle))
+    ws = _workspaces.get(key)
+    if ws is None:
+        ws = torch.zeros(workspace_size(), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
 
 
 def plan(row_stride: int, num_rows: int, k: int, options: Options | None = None, sm_count: int = 0) -> dict:
@@ -269,8 +323,10 @@ def _topk_decode_on_device(logits, rows, stride, kv_lens, next_n, compress_ratio
                                pre_idx.data_ptr(), pre_idx.stride(0), indices.data_ptr(), vptr,
                                _stream_handle(stream, logits.device), options)
     else:
-        topk_decode_raw(logits.data_ptr(), stride, rows, kv_lens.data_ptr(), next_n, compress_ratio, k,
-                        indices.data_ptr(), vptr, _stream_handle(stream, logits.device), options)
+        h = _stream_handle(stream, logits.device)
+        ws = workspace(logits.device, h)
+        topk_decode_ws_raw(logits.data_ptr(), stride, rows, kv_lens.data_ptr(), next_n, compress_ratio, k,
+                           indices.data_ptr(), vptr, ws.data_ptr(), ws.numel(), h, options)
     return indices, values
 
 
@@ -283,6 +339,8 @@ def topk_prefill(logits, row_starts, row_ends, k: int, indices=None, *, stream=N
     _same_device(logits.device, row_starts=row_starts, row_ends=row_ends, indices=indices)
     with _torch().cuda.device(logits.device):
         indices = _out(indices, rows, k, _torch().int32, logits.device, "indices")
-        topk_prefill_raw(logits.data_ptr(), stride, rows, row_starts.data_ptr(), row_ends.data_ptr(), k,
-                         indices.data_ptr(), _stream_handle(stream, logits.device), options)
+        h = _stream_handle(stream, logits.device)
+        ws = workspace(logits.device, h)
+        topk_prefill_ws_raw(logits.data_ptr(), stride, rows, row_starts.data_ptr(), row_ends.data_ptr(), k,
+                            indices.data_ptr(), ws.data_ptr(), ws.numel(), h, options)
     return indices

@@ -278,8 +278,8 @@ __device__ __forceinline__ uint32_t warp_alloc_n(uint32_t* ctr, uint32_t n) {
 // Find the crossing bin in the cluster-wide totals S.tot: the highest b with
 // sum_{bins >= b} tot >= k, with this CTA's own counts above and at b (from S.hist).  Thread t
 // owns the NB/T bins NB-1-(NB/T)t down to NB-(NB/T)(t+1), so thread order is descending order.
-template <int T>
-__device__ __forceinline__ Crossing scan_crossing(Smem& S, uint32_t k) {
+template <int T, class SM>
+__device__ __forceinline__ Crossing scan_crossing(SM& S, uint32_t k) {
   constexpr int BPT = NB / T;
   constexpr int NW = T / 32;
   static_assert(BPT % 4 == 0 && NW <= 8, "bins per thread must be a multiple of 4");
@@ -360,8 +360,8 @@ __device__ __forceinline__ Crossing scan_crossing(Smem& S, uint32_t k) {
 // 255 - DPT t down to 256 - DPT (t + 1).
 // The highest bin b of arr[0..NB) with sum_{bins >= b} arr >= want, or -1 when the total is
 // below want.  Block-collective; thread t owns bins NB-1-(NB/T)t down to NB-(NB/T)(t+1).
-template <int T>
-__device__ __forceinline__ int suffix_cross(Smem& S, const uint32_t* arr, uint32_t want) {
+template <int T, class SM>
+__device__ __forceinline__ int suffix_cross(SM& S, const uint32_t* arr, uint32_t want) {
   constexpr int BPT = NB / T;
   constexpr int NW = T / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -417,8 +417,8 @@ struct DigitCross {
 // Digit crossing over pushed cluster-wide digit counts dtot (local) and this CTA's own counts
 // dloc: the digit d (scanning from 255 down) where the running cluster count reaches `need`.
 // Thread t owns digits 255 - DPT t down to 256 - DPT (t + 1).
-template <int T>
-__device__ __forceinline__ DigitCross digit_scan(Smem& S, const uint32_t* dtot, const uint32_t* dloc,
+template <int T, class SM>
+__device__ __forceinline__ DigitCross digit_scan(SM& S, const uint32_t* dtot, const uint32_t* dloc,
                                                  uint32_t need) {
   constexpr int DPT = 256 / T;
   constexpr int NW = T / 32;

@@ -1,0 +1,725 @@
+// gvr_split.cuh -- the balanced GVR top-K kernel: rows of uneven length split into equal chunks.
+//
+// The cluster kernel (gvr_kernel.cuh) gives every row the same number of CTAs, chosen on the
+// host from the row stride, because the real row lengths (from kv_lens or the window bounds)
+// live on the device.  In a decode batch whose lengths spread from a few thousand to the full
+// stride, the CTAs of the longest rows then set the launch time while the others idle.  This
+// kernel decides the split on the device instead: every CTA reads all rows' lengths, cuts the
+// batch's valid scores into chunks of one common size (rounded to whole 4 KB stages), and takes
+// the chunk whose number is its block index.  Per chunk, the GVR steps of "GVR K=2048 reg_clus
+// with block64 sampling and parallel rescue" (TensorRT-LLM PR #20998, "What changes") run as:
+//
+//   Guess   the row's uniform block64 samples (the same positions and count as the cluster
+//           kernel) give GMIN / GMAX and the sampled floor t, identically in every chunk of the
+//           row (same samples, same arithmetic);
+//   Verify  the chunk streams through a shared-memory ring filled by bulk copies; every score
+//           >= t (a few per cent of the row) is published to the chunk's slot of the workspace;
+//   Refine  the last chunk of the row to finish (a per-row arrival counter) reads the row's
+//           published scores from L2, histograms them over the value bins of [GMIN, GMAX],
+//           finds the bin that crosses the K-th largest score ("Why the GLM row overflows"),
+//           writes the winners above it and refines the crossing bin's members exactly.
+//
+// Exactness: every score of the row that is >= t was published, so when at least K were, the
+// K largest of the row are the K largest of the published ones.  When fewer than K reached t, a
+// chunk overflowed its slot, or the crossing bin holds more members than the idle ring can take,
+// the last CTA selects the row alone by an exact radix select over the order keys of the whole
+// window (4 digit passes at most, reading the row from global memory) -- correct in every case,
+// slow for long rows, and rare: the floor's margin makes it a per-row event of about 1e-4 on the
+// workloads' score distributions.
+//
+// The workspace (caller-owned, zero-filled before its first use) holds per chunk the published
+// scores and window indices and their count, and per row the arrival counter; the last chunk of
+// a row resets that counter, so every call leaves the workspace as it found it.
+#pragma once
+
+#include "gvr_kernel.cuh"
+
+namespace gvr {
+
+constexpr int SPLIT_NST = 4;                 // ring stages (4 KB each) per CTA
+constexpr int SPLIT_CTAS_PER_SM = 8;         // occupancy the launch bound and shared memory allow
+constexpr int SPLIT_UNIT_CAP = 4096;         // scores one chunk can publish
+constexpr int32_t SPLIT_MIN_CHUNK_VEC = 1024;  // 4096 scores: the smallest chunk
+constexpr int SPLIT_MAX_ROWS = 512;          // rows a split launch can schedule
+constexpr uint32_t SPLIT_RING_CAND = SPLIT_NST * STAGE_VEC * 16 / 8;  // (score, index) pairs the ring holds
+constexpr int PATH_SPLIT = 7;                // row_stats: selected from the published scores
+constexpr int PATH_SPLIT_ALONE = 8;          // row_stats: the last CTA selected the row alone
+
+enum : int32_t { FLAG_SPLIT_ALONE = 512 };   // diagnostics: every long row takes the lone path
+
+struct SplitParams {
+  const float* logits;
+  int64_t row_stride;
+  const int32_t* kv_lens;     // decode
+  const int32_t* row_starts;  // prefill
+  const int32_t* row_ends;    // prefill
+  int32_t* indices;
+  float* values;              // nullable
+  int32_t* row_stats;         // nullable, [rows][4]
+  float* surv_v;              // workspace: [grid][SPLIT_UNIT_CAP] published scores
+  int32_t* surv_j;            // workspace: [grid][SPLIT_UNIT_CAP] their window indices
+  uint32_t* surv_n;           // workspace: [grid] scores each chunk found >= t (may exceed the cap)
+  uint32_t* arrive;           // workspace: [rows] chunks of the row done (zero between calls)
+  int32_t num_rows;
+  int32_t next_n;
+  int32_t compress_ratio;
+  int32_t k;
+  int32_t mode;
+  int32_t flags;
+};
+
+struct alignas(16) SplitSmem {
+  uint32_t hist[NB + 4];  // the samples' histogram (floor)
+  union {
+    uint32_t tot[NB + 4];  // the last CTA: histogram of the row's published scores
+    struct {               // the schedule: every row's window
+      uint32_t nv[SPLIT_MAX_ROWS];
+      uint32_t a[SPLIT_MAX_ROWS];
+    } rows;
+  };
+  uint32_t wsum[2][8];
+  float wmin[8], wmax[8];
+  Crossing cross;
+  float vthr;
+  int32_t fpart;
+  uint32_t dsel, dabove, dcnt, dmy_above, dmy_at;
+  uint32_t kmin_loc, kmax_loc;
+  uint32_t nsurv;                    // scores of this chunk >= t (may exceed SPLIT_UNIT_CAP)
+  uint32_t ctr_win, ctr_cand, ctr_rwin, ctr_rtie;
+  uint32_t red_n, red_over;          // the last CTA: published scores of the row, overflow flag
+  int32_t sched[7];                  // row, chunk, chunks of the row, first chunk, all chunks, a, nv
+  uint32_t is_last;
+  uint32_t tout;
+  float4 tail;
+  uint64_t bar[SPLIT_NST];
+};
+static_assert(offsetof(SplitSmem, hist) % 16 == 0 && offsetof(SplitSmem, tot) % 16 == 0,
+              "histograms are read as 16-byte vectors");
+static_assert(offsetof(SplitSmem, bar) % 8 == 0, "mbarriers must be 8-byte aligned");
+static_assert(2 * SPLIT_MAX_ROWS <= NB + 4, "the schedule fits the histogram it shares memory with");
+
+constexpr int SPLIT_SMEM_FIXED = int((sizeof(SplitSmem) + 127) / 128 * 128);
+__host__ __device__ constexpr int split_smem_bytes() { return SPLIT_SMEM_FIXED + SPLIT_NST * STAGE_VEC * 16; }
+
+// Window [a, a + nv) of row r (the same geometry as the cluster kernel's head) from its inputs:
+// decode x = kv_lens[r / next_n]; prefill x = row_starts[r], y = row_ends[r].
+__device__ __forceinline__ void split_row_window(const SplitParams& p, uint32_t r, int32_t x, int32_t y, uint32_t& a,
+                                                 uint32_t& nv) {
+  const uint32_t stride = uint32_t(p.row_stride);
+  a = 0;
+  nv = 0;
+  if (p.mode == MODE_DECODE) {
+    const uint32_t nn = uint32_t(p.next_n);
+    const uint32_t req = r / nn;
+    const int32_t kv = x;
+    if (kv >= p.next_n) nv = (uint32_t(kv) - nn + (r - req * nn) + 1u) / uint32_t(p.compress_ratio);
+    nv = nv < stride ? nv : stride;
+  } else {
+    const int32_t ks = x;
+    const int32_t ke = y;
+    const uint32_t s = ks > 0 ? uint32_t(ks) : 0u;
+    const uint32_t e = ke > 0 ? (uint32_t(ke) < stride ? uint32_t(ke) : stride) : 0u;
+    a = s < stride ? s : stride;
+    nv = e > a ? e - a : 0u;
+  }
+}
+
+// Chunks of a row: one for a short row (it writes the identity), else its vectors over the
+// chunk size.
+__device__ __forceinline__ uint32_t split_units(uint32_t a, uint32_t nv, uint32_t k, uint32_t chv) {
+  if (nv <= k) return 1u;
+  const uint32_t nvec = ((a & 3u) + nv + 3u) >> 2;
+  return (nvec + chv - 1u) / chv;
+}
+
+template <bool UNUSED>
+__global__ void __launch_bounds__(THREADS, SPLIT_CTAS_PER_SM) gvr_split_kernel(const SplitParams p) {
+  constexpr int T = THREADS;
+  constexpr int NW = T / 32;
+  constexpr int KPT = (MAX_K + T - 1) / T;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  SplitSmem& S = *reinterpret_cast<SplitSmem*>(smem_raw);
+  float4 (*ring)[STAGE_VEC] = reinterpret_cast<float4 (*)[STAGE_VEC]>(smem_raw + SPLIT_SMEM_FIXED);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int32_t k = p.k;
+  const int32_t R = p.num_rows;
+  const uint32_t unit = blockIdx.x;
+  const float qnan = __int_as_float(0x7fffffff);
+
+  if (tid == 0) {
+#pragma unroll
+    for (int s = 0; s < SPLIT_NST; ++s) mbar_init(&S.bar[s], 1);
+    mbar_init_fence();
+  }
+
+  // ---------------------------------------------------------------- schedule (warp 0)
+  // Every CTA computes the same split: rows' windows, the chunk size (the long rows' vectors
+  // over the grid minus one chunk per row for rounding, whole stages, at least
+  // SPLIT_MIN_CHUNK_VEC), the chunks of each row in row order, and which chunk is this block's.
+  if (warp == 0) {
+    uint64_t fsum = 0;
+    for (int32_t r0 = 0; r0 < R; r0 += 4 * 32) {  // four rows per lane in flight at once
+      int32_t x[4], y[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int32_t r = r0 + 32 * q + lane;
+        x[q] = y[q] = 0;
+        if (r < R) {
+          if (p.mode == MODE_DECODE) {
+            x[q] = __ldg(p.kv_lens + uint32_t(r) / uint32_t(p.next_n));
+          } else {
+            x[q] = __ldg(p.row_starts + r);
+            y[q] = __ldg(p.row_ends + r);
+          }
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int32_t r = r0 + 32 * q + lane;
+        if (r < R) {
+          uint32_t a, nv;
+          split_row_window(p, uint32_t(r), x[q], y[q], a, nv);
+          S.rows.a[r] = a;
+          S.rows.nv[r] = nv;
+          if (nv > uint32_t(k)) fsum += ((a & 3u) + nv + 3u) >> 2;
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) fsum += __shfl_xor_sync(FULL_MASK, fsum, o);
+    __syncwarp();
+    const uint64_t denom = uint64_t(gridDim.x) - uint64_t(R);  // the host keeps the grid >= 2 rows
+    uint64_t chv = (fsum + denom - 1u) / denom;
+    chv = (chv + STAGE_VEC - 1) / STAGE_VEC * STAGE_VEC;
+    if (chv < uint64_t(SPLIT_MIN_CHUNK_VEC)) chv = SPLIT_MIN_CHUNK_VEC;
+    const uint32_t cv = uint32_t(chv);  // <= the longest row's vectors rounded up: < 2^30
+    const int32_t per = (R + 31) / 32;  // rows [lane * per, lane * per + per) in row order
+    const int32_t r0 = lane * per, r1 = min(R, r0 + per);
+    uint32_t mine = 0;
+    for (int32_t r = r0; r < r1; ++r) mine += split_units(S.rows.a[r], S.rows.nv[r], uint32_t(k), cv);
+    uint32_t incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_up_sync(FULL_MASK, incl, o);
+      if (lane >= o) incl += x;
+    }
+    const uint32_t total = __shfl_sync(FULL_MASK, incl, 31);  // <= gridDim.x by the chunk size
+    uint32_t base = incl - mine;
+    if (unit >= base && unit < incl) {
+      for (int32_t r = r0; r < r1; ++r) {
+        const uint32_t nu = split_units(S.rows.a[r], S.rows.nv[r], uint32_t(k), cv);
+        if (unit < base + nu) {
+          S.sched[0] = r;
+          S.sched[1] = int32_t(unit - base);
+          S.sched[2] = int32_t(nu);
+          S.sched[3] = int32_t(base);
+          S.sched[5] = int32_t(S.rows.a[r]);
+          S.sched[6] = int32_t(S.rows.nv[r]);
+          break;
+        }
+        base += nu;
+      }
+    }
+    if (lane == 0) {
+      S.sched[4] = int32_t(total);
+      S.vthr = __uint_as_float(cv);  // the chunk size, passed through shared memory
+    }
+  }
+  __syncthreads();
+  if (unit >= uint32_t(S.sched[4])) return;  // no chunk left for this block
+  const uint32_t row = uint32_t(S.sched[0]);
+  const int32_t chunk = S.sched[1];
+  const int32_t nunits = S.sched[2];
+  const uint32_t unit0 = uint32_t(S.sched[3]);
+  const uint32_t a = uint32_t(S.sched[5]);
+  const uint32_t nv = uint32_t(S.sched[6]);
+  const int32_t chv = int32_t(__float_as_uint(S.vthr));
+  const float* rowp = p.logits + int64_t(row) * p.row_stride;
+  int32_t* out = p.indices + int64_t(row) * k;
+  float* outv = p.values ? p.values + int64_t(row) * k : nullptr;
+
+  // ---------------------------------------------------------------- short row: identity
+  if (nv <= uint32_t(k)) {
+    for (int i = tid; i < k; i += T) {
+      out[i] = uint32_t(i) < nv ? i : -1;
+      if (outv) outv[i] = uint32_t(i) < nv ? rowp[a + i] : -FLT_MAX;
+    }
+    if (p.row_stats && tid == 0) {
+      int32_t* st = p.row_stats + 4 * int64_t(row);
+      st[0] = PATH_SHORT;
+      st[1] = st[2] = st[3] = 0;
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------------- this chunk's vectors
+  // Vectors are 16-byte aligned float4s from the aligned column at or below the window start
+  // (vector g holds window positions 4g - lead .. 4g + 3 - lead); the chunk is vectors
+  // [v0, v1) of the window, streamed in stages of STAGE_VEC vectors.
+  const int32_t lead = int32_t(a & 3u);
+  const float* base = rowp + (a - uint32_t(lead));
+  const int32_t span = lead + int32_t(nv);
+  const int32_t ffull = span >> 2;
+  const int32_t tailn = span & 3;
+  const int32_t nvec = ffull + (tailn ? 1 : 0);
+  const int32_t v0 = chunk * chv;
+  const int32_t v1 = min(nvec, v0 + chv);
+  const int32_t nst = (v1 - v0 + STAGE_VEC - 1) / STAGE_VEC;
+  auto issue_stage = [&](int32_t s, uint32_t slot) {  // one thread
+    const int32_t c0 = v0 + s * STAGE_VEC;
+    const int32_t c1 = min(min(c0 + STAGE_VEC, v1), ffull);
+    if (c1 > c0) {
+      mbar_arrive_expect_tx(&S.bar[slot], uint32_t(c1 - c0) * 16u);
+      bulk_copy_g2s(&ring[slot][0], base + 4 * size_t(c0), uint32_t(c1 - c0) * 16u, &S.bar[slot]);
+    } else {
+      mbar_arrive(&S.bar[slot]);  // a stage holding only the partial last vector
+    }
+  };
+
+  // ---------------------------------------------------------------- guess: block64 sample
+  const uint32_t nsamp = sample_count(uint32_t(k), nv, 8u);
+  const uint32_t nblk = nsamp >> 6;
+  const uint32_t sq = (nv - 64u) / (nblk - 1u), sr = (nv - 64u) % (nblk - 1u);
+  const uint32_t run_start = uint32_t(lane) * sq + (uint32_t(lane) * sr) / (nblk - 1u);
+  float sv[KPT];
+#pragma unroll
+  for (int q = 0; q < KPT; ++q) {
+    const uint32_t i = uint32_t(q * T + tid);
+    const uint32_t s = __shfl_sync(FULL_MASK, run_start, (i >> 6) & 31u);
+    sv[q] = i < nsamp ? __ldg(rowp + a + s + (i & 63u)) : qnan;
+  }
+  // the chunk's first stages go in flight right behind the samples
+  if (warp == 0 && lane < SPLIT_NST && lane < nst) issue_stage(lane, uint32_t(lane));
+  for (int i = tid; i < NB + 4; i += T) S.hist[i] = 0;
+  if (tid == 0) {
+    S.nsurv = 0;
+    S.tout = 0;
+  }
+  if (tid == 32) {  // the partial last vector, read with scalar loads, never past the window
+    S.tail = make_float4(qnan, qnan, qnan, qnan);
+    if (tailn && ffull >= v0 && ffull < v1) {
+      const float* q = base + 4 * size_t(ffull);
+      S.tail = make_float4(q[0], tailn > 1 ? q[1] : qnan, tailn > 2 ? q[2] : qnan, qnan);
+    }
+  }
+  float lmin = INFINITY, lmax = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < KPT; ++q)
+    if (isfinite(sv[q])) {
+      lmin = fminf(lmin, sv[q]);
+      lmax = fmaxf(lmax, sv[q]);
+    }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lmin = fminf(lmin, __shfl_xor_sync(FULL_MASK, lmin, o));
+    lmax = fmaxf(lmax, __shfl_xor_sync(FULL_MASK, lmax, o));
+  }
+  if (lane == 0) {
+    S.wmin[warp] = lmin;
+    S.wmax[warp] = lmax;
+  }
+  __syncthreads();
+  float gmin = INFINITY, gmax = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    gmin = fminf(gmin, S.wmin[w]);
+    gmax = fmaxf(gmax, S.wmax[w]);
+  }
+  gmin = __fadd_rn(gmin, 0.0f);  // -0 -> +0
+  const bool bracket_ok = isfinite(gmin) && isfinite(gmax) && gmin < gmax;
+  // The sampled floor, as in the cluster kernel: the lower edge of the bin where
+  // mu + 3 sqrt(mu) + 6 samples are reached (mu = k nsamp / nv, the samples expected above
+  // tau), with the bins ending lower when a few far samples stretch them.
+  float sc = 1.0f;
+  float thr = -INFINITY;
+  if (bracket_ok) {
+    sc = __fdiv_rn(float(NB), __fsub_rn(gmax, gmin));
+    const float mu = float(k) * float(nsamp) / float(nv);
+    const float want_f = mu + 3.0f * sqrtf(mu) + 6.0f;
+    const uint32_t want = want_f < float(nsamp) ? uint32_t(want_f) : nsamp;
+#pragma unroll
+    for (int q = 0; q < KPT; ++q)
+      if (!isnan(sv[q])) atomicAdd(&S.hist[value_bin(sv[q], gmin, sc)], 1u);
+    __syncthreads();
+    int fb = suffix_cross<T>(S, S.hist, want);
+    const float rf = mu - 4.0f * sqrtf(mu);
+    const int hb = (rf >= 2.0f && fb < NB / 2) ? suffix_cross<T>(S, S.hist, uint32_t(rf)) : -1;
+    if (hb >= 0 && hb < NB / 2) {
+      const float hi = __fadd_rn(gmin, __fdiv_rn(float(hb + 1), sc));
+      sc = __fdiv_rn(float(NB), __fsub_rn(hi, gmin));
+      for (int i = tid; i < NB; i += T) S.hist[i] = 0;
+      __syncthreads();
+#pragma unroll
+      for (int q = 0; q < KPT; ++q)
+        if (!isnan(sv[q])) atomicAdd(&S.hist[value_bin(sv[q], gmin, sc)], 1u);
+      __syncthreads();
+      fb = suffix_cross<T>(S, S.hist, want);
+    }
+    thr = fb > 0 ? __fadd_rn(gmin, __fdiv_rn(float(fb), sc)) : -INFINITY;
+  }
+  const bool alone = (p.flags & FLAG_SPLIT_ALONE) != 0;
+
+  // ---------------------------------------------------------------- verify: publish >= t
+  // One compare against the floor per score (a thread first takes the max of its 8 scores of
+  // the stage); each warp takes its slots with one shared atomic per stage; the published
+  // (score, window index) pairs go straight to the chunk's slot of the workspace.
+  float* const my_v = p.surv_v + size_t(unit) * SPLIT_UNIT_CAP;
+  int32_t* const my_j = p.surv_j + size_t(unit) * SPLIT_UNIT_CAP;
+  bool late = false;
+  for (int32_t s = 0; s < nst; ++s) {
+    const uint32_t slot = uint32_t(s) % SPLIT_NST;
+    const uint32_t ph = (uint32_t(s) / SPLIT_NST) & 1u;
+    if (!mbar_wait_bounded(&S.bar[slot], ph, WAIT_LIMIT_NS)) {
+      mbar_wait_bounded(&S.bar[slot], ph, WAIT_LIMIT_NS);  // let copies land
+      late = true;
+    }
+    const int32_t c0 = v0 + s * STAGE_VEC;
+    float4 vv[VPS];
+    uint32_t lanes = 0xFFFFFFFFu;  // bit 4i+l: lane l of the i-th vector is in the window
+    if (c0 > 0 && c0 + STAGE_VEC <= min(v1, ffull)) {  // an interior stage
+#pragma unroll
+      for (int i = 0; i < VPS; ++i) vv[i] = ring[slot][i * T + tid];
+    } else {
+      lanes = 0;
+#pragma unroll
+      for (int i = 0; i < VPS; ++i) {
+        const int32_t g = c0 + i * T + tid;
+        uint32_t ln = 0;
+        vv[i] = f4_zero();
+        if (g < v1) {
+          if (g < ffull) {
+            vv[i] = ring[slot][i * T + tid];
+            ln = 0xFu;
+          } else {
+            vv[i] = S.tail;
+            ln = (1u << tailn) - 1u;
+          }
+          if (g == 0) ln &= (0xFu << lead) & 0xFu;
+        }
+        lanes |= ln << (4 * i);
+      }
+    }
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < VPS; ++i) mx = fmaxf(mx, fmaxf(fmaxf(vv[i].x, vv[i].y), fmaxf(vv[i].z, vv[i].w)));
+    uint32_t bits = 0;
+    if (mx >= thr) {
+#pragma unroll
+      for (int i = 0; i < VPS; ++i)
+        bits |= (uint32_t(vv[i].x >= thr) | (uint32_t(vv[i].y >= thr) << 1) | (uint32_t(vv[i].z >= thr) << 2) |
+                 (uint32_t(vv[i].w >= thr) << 3))
+                << (4 * i);
+      bits &= lanes;
+    }
+    const uint32_t nhit = __popc(bits);
+    const unsigned lt = lanemask_lt();
+    const unsigned m0 = __ballot_sync(FULL_MASK, nhit & 1u), m1 = __ballot_sync(FULL_MASK, nhit & 2u);
+    uint32_t excl = uint32_t(__popc(m0 & lt)) + (uint32_t(__popc(m1 & lt)) << 1);
+    uint32_t wtot = uint32_t(__popc(m0)) + (uint32_t(__popc(m1)) << 1);
+    if (__any_sync(FULL_MASK, nhit >= 4u)) {
+      const unsigned m2 = __ballot_sync(FULL_MASK, nhit & 4u), m3 = __ballot_sync(FULL_MASK, nhit & 8u);
+      excl += (uint32_t(__popc(m2 & lt)) << 2) + (uint32_t(__popc(m3 & lt)) << 3);
+      wtot += (uint32_t(__popc(m2)) << 2) + (uint32_t(__popc(m3)) << 3);
+    }
+    if (wtot) {
+      uint32_t wbase = 0;
+      if (lane == 0) wbase = atomicAdd(&S.nsurv, wtot);
+      uint32_t at = __shfl_sync(FULL_MASK, wbase, 0) + excl;
+      if (bits && !alone) {
+#pragma unroll
+        for (int i = 0; i < VPS; ++i) {
+          const uint32_t nib = (bits >> (4 * i)) & 0xFu;
+          if (nib) {
+            const int32_t jw = 4 * (c0 + i * T + tid) - lead;  // window index of lane 0
+#pragma unroll
+            for (int l = 0; l < 4; ++l)
+              if ((nib >> l) & 1u) {
+                if (at < uint32_t(SPLIT_UNIT_CAP)) {
+                  my_v[at] = f4_get(vv[i], l);
+                  my_j[at] = jw + l;
+                }
+                ++at;
+              }
+          }
+        }
+      }
+    }
+    if (s + SPLIT_NST < nst) {  // refill this slot once every thread is done with it
+      if (__syncthreads_or(late)) {
+        // drain the stages already in flight, then stop: the row is marked failed
+        for (int32_t d = s + 1; d < nst && d < s + SPLIT_NST; ++d)
+          mbar_wait_bounded(&S.bar[uint32_t(d) % SPLIT_NST], (uint32_t(d) / SPLIT_NST) & 1u, WAIT_LIMIT_NS);
+        late = true;
+        break;
+      }
+      if (tid == 0) issue_stage(s + SPLIT_NST, slot);
+    }
+  }
+  if (__syncthreads_or(late) && tid == 0) S.tout = 1;
+
+  // ---------------------------------------------------------------- publish, last chunk refines
+  // The CTA barrier orders every thread's published pairs before thread 0's fence, and the fence
+  // (cumulative) orders them before the count and the arrival: one device-scope fence per CTA.
+  __syncthreads();
+  if (tid == 0) {
+    p.surv_n[unit] = S.tout ? 0xffffffffu : S.nsurv;  // a failed chunk marks the row
+    __threadfence();
+    const uint32_t old = atomicAdd(p.arrive + row, 1u);
+    const bool last = old + 1u == uint32_t(nunits);
+    if (last) {
+      __threadfence();    // the other chunks' pairs and counts, published before their arrivals
+      p.arrive[row] = 0;  // every chunk of the row has arrived: reset for the next call
+    }
+    S.is_last = last;
+  }
+  __syncthreads();
+  if (!S.is_last) return;
+
+  // The row's published scores: chunk u of the row holds min(n_u, cap) pairs.
+  if (tid == 0) {
+    S.red_n = 0;
+    S.red_over = 0;
+    S.ctr_win = S.ctr_cand = S.ctr_rwin = S.ctr_rtie = 0;
+  }
+  for (int i = tid; i < NB + 4; i += T) S.tot[i] = 0;
+  // The chunks' counts, kept in the samples' histogram (no longer needed) for the walks below.
+  uint32_t* const cnt = S.hist;
+  constexpr int CNT_CACHE = NB + 4;
+  __syncthreads();
+  for (int32_t q = tid; q < nunits; q += T) {
+    const uint32_t n = __ldcg(p.surv_n + unit0 + q);
+    if (q < CNT_CACHE) cnt[q] = n;
+    atomicAdd(&S.red_n, n < uint32_t(SPLIT_UNIT_CAP) ? n : uint32_t(SPLIT_UNIT_CAP));
+    if (n > uint32_t(SPLIT_UNIT_CAP)) atomicOr(&S.red_over, n == 0xffffffffu ? 2u : 1u);
+  }
+  __syncthreads();
+  const uint32_t total = S.red_n;
+  const bool failed = (S.red_over & 2u) != 0;
+  bool ok = !failed && !alone && bracket_ok && S.red_over == 0 && total >= uint32_t(k);
+  // Walk every published pair of the row: f(value, window index), warp-collective with a
+  // CTA-uniform trip count per chunk (warp w takes chunks w, w + NW, ...).  Each lane has eight
+  // pairs in flight at a time, so a chunk of up to 256 pairs costs one round trip to L2.
+  constexpr int PB = 8;
+  auto each_published = [&](auto&& f) {
+    for (int32_t q = warp; q < nunits; q += NW) {
+      const uint32_t uq = unit0 + uint32_t(q);
+      const uint32_t n = min(q < CNT_CACHE ? cnt[q] : __ldcg(p.surv_n + uq), uint32_t(SPLIT_UNIT_CAP));
+      const float* pv = p.surv_v + size_t(uq) * SPLIT_UNIT_CAP;
+      const int32_t* pj = p.surv_j + size_t(uq) * SPLIT_UNIT_CAP;
+      for (uint32_t b0 = 0; b0 < n; b0 += 32 * PB) {
+        float v[PB];
+        int32_t j[PB];
+#pragma unroll
+        for (int e = 0; e < PB; ++e) {
+          const uint32_t i = b0 + uint32_t(32 * e + lane);
+          v[e] = i < n ? __ldcg(pv + i) : 0.f;
+          j[e] = i < n ? __ldcg(pj + i) : 0;
+        }
+#pragma unroll
+        for (int e = 0; e < PB; ++e) f(v[e], j[e], b0 + uint32_t(32 * e + lane) < n);
+      }
+    }
+  };
+  Crossing cr{};
+  if (ok) {
+    each_published([&](float v, int32_t, bool in) {
+      if (in) atomicAdd(&S.tot[value_bin(v, gmin, sc)], 1u);
+    });
+    __syncthreads();
+    cr = scan_crossing<T>(S, uint32_t(k));
+    ok = cr.m <= SPLIT_RING_CAND;  // the crossing bin's members fit the idle ring
+  }
+  if (ok) {
+    // ------------------------------------------------------------ collect + refine
+    const int bstar = cr.bin;
+    float* const cand_v = reinterpret_cast<float*>(&ring[0][0]);
+    int32_t* const cand_j = reinterpret_cast<int32_t*>(&ring[0][0]) + SPLIT_RING_CAND;
+    each_published([&](float e, int32_t jw, bool in) {
+      const int b = in ? value_bin(e, gmin, sc) : -1;
+      const uint32_t ws = warp_alloc_local(&S.ctr_win, b > bstar);
+      if (b > bstar && ws < uint32_t(k)) {  // always below k: counts match the histogram's
+        out[ws] = jw;
+        if (outv) outv[ws] = e;
+      }
+      const uint32_t cs = warp_alloc_local(&S.ctr_cand, b == bstar);
+      if (b == bstar && cs < SPLIT_RING_CAND) {
+        cand_v[cs] = e;
+        cand_j[cs] = jw;
+      }
+    });
+    __syncthreads();
+    const uint32_t need = uint32_t(k) - cr.above;
+    const uint32_t mm = cr.m;
+    if (mm <= uint32_t(RANK_REFINE_MAX)) {
+      // rank of candidate i = candidates ordered before it by (value desc, index asc)
+      for (uint32_t i = tid; i < mm; i += T) {
+        const float v = cand_v[i];
+        const int32_t j = cand_j[i];
+        uint32_t r = 0;
+        for (uint32_t q = 0; q < mm; ++q) {
+          const float w = cand_v[q];
+          r += (w > v) || (w == v && cand_j[q] < j);
+        }
+        if (r < need) {
+          out[cr.above + r] = j;
+          if (outv) outv[cr.above + r] = v;
+        }
+      }
+    } else {
+      // radix select of the need largest order keys among the candidates, 8 bits per pass
+      uint32_t prefix = 0, pmask = 0, rneed = need;
+      bool ge = false;
+      uint32_t* const dh = S.tot;  // the published scores' histogram is no longer needed
+      for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int i = tid; i < 256; i += T) dh[i] = 0;
+        __syncthreads();
+        for (uint32_t i = tid; i < mm; i += T) {
+          const uint32_t key = order_key(cand_v[i]);
+          if ((key & pmask) == prefix) atomicAdd(&dh[(key >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        const DigitCross dc = digit_scan<T>(S, dh, dh, rneed);  // the digit where rneed is reached
+        __syncthreads();
+        prefix |= dc.digit << shift;
+        pmask |= 0xFFu << shift;
+        rneed -= dc.above;
+        if (dc.cnt == rneed) {
+          ge = true;
+          break;
+        }
+      }
+      const uint32_t nties = ge ? 0u : rneed;
+      const uint32_t win_base = cr.above, tie_base = cr.above + (need - nties);
+      for (uint32_t b0 = 0; b0 < mm; b0 += T) {
+        const uint32_t i = b0 + tid;
+        const bool in = i < mm;
+        const uint32_t key = in ? order_key(cand_v[i]) : 0u;
+        const bool win = in && (ge ? (key & pmask) >= prefix : key > prefix);
+        const bool tie = in && !ge && key == prefix;
+        const uint32_t ws = warp_alloc_local(&S.ctr_rwin, win);
+        if (win && win_base + ws < tie_base) {
+          out[win_base + ws] = cand_j[i];
+          if (outv) outv[win_base + ws] = cand_v[i];
+        }
+        const uint32_t ts = warp_alloc_local(&S.ctr_rtie, tie);
+        if (tie && ts < nties) {
+          out[tie_base + ts] = cand_j[i];
+          if (outv) outv[tie_base + ts] = cand_v[i];
+        }
+      }
+    }
+    if (p.row_stats && tid == 0) {
+      int32_t* st = p.row_stats + 4 * int64_t(row);
+      st[0] = PATH_SPLIT;
+      st[1] = int32_t(cr.m);
+      st[2] = nunits;
+      st[3] = int32_t(cr.above);
+    }
+    return;
+  }
+  if (failed) {
+    for (int i = tid; i < k; i += T) out[i] = -2;
+    if (p.row_stats && tid == 0) {
+      int32_t* st = p.row_stats + 4 * int64_t(row);
+      st[0] = PATH_DEVICE_ERROR;
+      st[1] = st[2] = st[3] = 0;
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------------- the row alone
+  // Exact radix select over the order keys of the whole window, one 8-bit digit per pass from
+  // the top, stopping early when the keys above the chosen digit are exactly the ones still
+  // needed or every matching key is equal; then one emission pass.  The window is read with
+  // coalesced 16-byte loads (the lead lanes and the partial last vector masked by position).
+  uint32_t* const dh = S.hist;
+  auto each_window = [&](auto&& f) {  // f(value, window index, valid), warp-collective
+    for (int32_t g0 = 0; g0 < nvec; g0 += 4 * T) {
+      float4 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int32_t g = g0 + i * T + tid;
+        v[i] = g < ffull ? __ldg(reinterpret_cast<const float4*>(base) + g) : f4_zero();
+        if (g == ffull && tailn) {
+          const float* q = base + 4 * size_t(ffull);
+          v[i] = make_float4(q[0], tailn > 1 ? q[1] : qnan, tailn > 2 ? q[2] : qnan, qnan);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int32_t g = g0 + i * T + tid;
+        uint32_t ln = g < ffull ? 0xFu : (g == ffull ? (1u << tailn) - 1u : 0u);
+        if (g == 0) ln &= (0xFu << lead) & 0xFu;
+#pragma unroll
+        for (int l = 0; l < 4; ++l) f(f4_get(v[i], l), 4 * g + l - lead, ((ln >> l) & 1u) != 0);
+      }
+    }
+  };
+  uint32_t prefix = 0, pmask = 0, rneed = uint32_t(k);
+  bool ge = false;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += T) dh[i] = 0;
+    if (tid == 0) {
+      S.kmin_loc = 0xffffffffu;
+      S.kmax_loc = 0u;
+    }
+    __syncthreads();
+    uint32_t tmin = 0xffffffffu, tmax = 0u;
+    each_window([&](float e, int32_t, bool valid) {
+      const uint32_t key = order_key(e);
+      if (valid && (key & pmask) == prefix) {
+        atomicAdd(&dh[(key >> shift) & 255u], 1u);
+        tmin = min(tmin, key);
+        tmax = max(tmax, key);
+      }
+    });
+    tmin = __reduce_min_sync(FULL_MASK, tmin);
+    tmax = __reduce_max_sync(FULL_MASK, tmax);
+    if (lane == 0) {
+      atomicMin(&S.kmin_loc, tmin);
+      atomicMax(&S.kmax_loc, tmax);
+    }
+    __syncthreads();
+    if (S.kmin_loc == S.kmax_loc) {  // every key with this prefix is the same: ties
+      prefix = S.kmin_loc;
+      pmask = 0xffffffffu;
+      __syncthreads();
+      break;
+    }
+    const DigitCross dc = digit_scan<T>(S, dh, dh, rneed);
+    __syncthreads();
+    prefix |= dc.digit << shift;
+    pmask |= 0xFFu << shift;
+    rneed -= dc.above;
+    if (dc.cnt == rneed) {
+      ge = true;
+      break;
+    }
+  }
+  const uint32_t nties = ge ? 0u : rneed;
+  const uint32_t tie_base = uint32_t(k) - nties;
+  each_window([&](float e, int32_t jw, bool valid) {
+    const uint32_t key = order_key(e);
+    const bool win = valid && (ge ? (key & pmask) >= prefix : key > prefix);
+    const bool tie = valid && !ge && key == prefix;
+    const uint32_t ws = warp_alloc_local(&S.ctr_win, win);
+    if (win && ws < tie_base) {
+      out[ws] = jw;
+      if (outv) outv[ws] = e;
+    }
+    const uint32_t ts = warp_alloc_local(&S.ctr_cand, tie);
+    if (tie && ts < nties) {
+      out[tie_base + ts] = jw;
+      if (outv) outv[tie_base + ts] = e;
+    }
+  });
+  if (p.row_stats && tid == 0) {
+    int32_t* st = p.row_stats + 4 * int64_t(row);
+    st[0] = PATH_SPLIT_ALONE;
+    st[1] = int32_t(total);
+    st[2] = nunits;
+    st[3] = 0;
+  }
+}
+
+}  // namespace gvr

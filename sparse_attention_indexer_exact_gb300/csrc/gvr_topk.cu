@@ -13,6 +13,7 @@
 #include <mutex>
 
 #include "gvr_kernel.cuh"
+#include "gvr_split.cuh"
 #include "gvr_topk.h"
 
 namespace {
@@ -55,6 +56,9 @@ cudaError_t set_attributes() {
   if (e == cudaSuccess) e = set_attributes_of<true, false>();
   if (e == cudaSuccess) e = set_attributes_of<false, true>();
   if (e == cudaSuccess) e = set_attributes_of<true, true>();
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gvr::gvr_split_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             gvr::split_smem_bytes());
   return e;
 }
 
@@ -88,7 +92,8 @@ int pow2_ceil(int64_t v) {
   return p;
 }
 
-gvr_status check_common(int64_t row_stride, int64_t num_rows, int32_t k, const gvr_options* o) {
+// ws: the *_ws entry points, which also take the flags that choose between the two kernels.
+gvr_status check_common(int64_t row_stride, int64_t num_rows, int32_t k, const gvr_options* o, bool ws = false) {
   if (num_rows < 0) return GVR_ERR_ARG;
   if (row_stride < 4 || row_stride % 4 != 0 || row_stride >= (int64_t(1) << 31)) return GVR_ERR_STRIDE;
   if (k != 512 && k != 1024 && k != 2048) return GVR_ERR_K;
@@ -98,7 +103,10 @@ gvr_status check_common(int64_t row_stride, int64_t num_rows, int32_t k, const g
     if (o->ring_stages != 0 && (o->ring_stages < gvr::MIN_STAGES || o->ring_stages > gvr::MAX_STAGES))
       return GVR_ERR_ARG;
     if (o->flags & ~(GVR_FLAG_FORCE_RESCUE | GVR_FLAG_NO_FLOOR | GVR_FLAG_ZERO_CAP | GVR_FLAG_RADIX_REFINE |
-                     GVR_FLAG_DETERMINISTIC | GVR_FLAG_SORTED | GVR_FLAG_STREAM_RESCUE | GVR_FLAG_COMPACT_LISTS))
+                     GVR_FLAG_DETERMINISTIC | GVR_FLAG_SORTED | GVR_FLAG_STREAM_RESCUE | GVR_FLAG_COMPACT_LISTS |
+                     GVR_FLAG_CLUSTER_KERNEL | GVR_FLAG_SPLIT_ALONE | GVR_FLAG_SPLIT_KERNEL))
+      return GVR_ERR_ARG;
+    if (!ws && (o->flags & (GVR_FLAG_CLUSTER_KERNEL | GVR_FLAG_SPLIT_ALONE | GVR_FLAG_SPLIT_KERNEL)))
       return GVR_ERR_ARG;
   }
   return GVR_OK;
@@ -264,6 +272,56 @@ gvr_status launch(const gvr::Params& prm, int64_t num_rows, const gvr_options* o
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// ---------------------------------------------------------------- balanced (split) kernel
+// Grid: every SM's share of resident CTAs (one chunk each, one wave).  Workspace layout, fixed
+// for a device: the per-row arrival counters (SPLIT_MAX_ROWS), the per-chunk counts (grid), the
+// published scores and their window indices (grid x SPLIT_UNIT_CAP each).
+int64_t split_grid(int sms, int smem_per_sm, int smem_reserved) {
+  int per_sm = smem_per_sm / (gvr::split_smem_bytes() + smem_reserved);
+  if (per_sm > gvr::SPLIT_CTAS_PER_SM) per_sm = gvr::SPLIT_CTAS_PER_SM;
+  if (per_sm < 1) per_sm = 1;
+  return int64_t(sms) * per_sm;
+}
+
+size_t split_workspace_bytes(int64_t grid) {
+  return size_t(gvr::SPLIT_MAX_ROWS) * 4 + size_t(grid) * 4 + size_t(grid) * gvr::SPLIT_UNIT_CAP * 8;
+}
+
+constexpr int32_t kSplitFlags = GVR_FLAG_SPLIT_ALONE | GVR_FLAG_SPLIT_KERNEL;
+
+// The balanced kernel for this call, or false when the cluster kernel takes it.
+bool use_split(int64_t num_rows, int64_t grid, const gvr_options* o) {
+  const int32_t flags = o ? o->flags : 0;
+  if (flags & GVR_FLAG_CLUSTER_KERNEL) return false;
+  if (flags & ~kSplitFlags) return false;                   // extended modes, cluster diagnostics
+  if (o && (o->cluster_size || o->ring_stages)) return false;  // cluster tuning
+  if (num_rows > gvr::SPLIT_MAX_ROWS || 2 * num_rows > grid) return false;
+  // opt-in: measured slower than the cluster kernel on every workload so far (its fixed chain
+  // of schedule, samples, floor, publish and the last CTA's selection is longer)
+  return (flags & (GVR_FLAG_SPLIT_KERNEL | GVR_FLAG_SPLIT_ALONE)) != 0;
+}
+
+gvr_status launch_split(gvr::SplitParams prm, int64_t grid, void* workspace, void* stream) {
+  unsigned char* w = static_cast<unsigned char*>(workspace);
+  prm.arrive = reinterpret_cast<uint32_t*>(w);
+  prm.surv_n = reinterpret_cast<uint32_t*>(w + size_t(gvr::SPLIT_MAX_ROWS) * 4);
+  prm.surv_v = reinterpret_cast<float*>(w + size_t(gvr::SPLIT_MAX_ROWS) * 4 + size_t(grid) * 4);
+  prm.surv_j = reinterpret_cast<int32_t*>(w + size_t(gvr::SPLIT_MAX_ROWS) * 4 + size_t(grid) * 4 +
+                                          size_t(grid) * gvr::SPLIT_UNIT_CAP * 4);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = size_t(gvr::split_smem_bytes());
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gvr::gvr_split_kernel<true>, prm);
+  return e == cudaSuccess ? GVR_OK : GVR_ERR_LAUNCH;
+}
+
+gvr_status check_workspace(void* workspace, size_t bytes, int64_t grid) {
+  if (!workspace || !aligned(workspace, 16) || bytes < split_workspace_bytes(grid)) return GVR_ERR_WORKSPACE;
+  return GVR_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -405,8 +463,93 @@ const char* gvr_status_string(gvr_status status) {
     case GVR_ERR_K: return "k must be 512, 1024 or 2048";
     case GVR_ERR_ARG: return "invalid argument (row count, next_n, compress_ratio or options)";
     case GVR_ERR_LAUNCH: return "kernel launch failed";
+    case GVR_ERR_WORKSPACE: return "workspace is NULL, misaligned or smaller than gvr_workspace_size";
   }
   return "unknown status";
+}
+
+gvr_status gvr_workspace_size(int32_t sm_count, size_t* bytes) {
+  if (!bytes) return GVR_ERR_NULL;
+  int sms = sm_count, smem_per_sm = kDefaultSmemPerSm, smem_reserved = kDefaultSmemReserved;
+  if (sms <= 0 && device_state(&sms, &smem_per_sm, &smem_reserved) != cudaSuccess) return GVR_ERR_LAUNCH;
+  *bytes = split_workspace_bytes(split_grid(sms, smem_per_sm, smem_reserved));
+  return GVR_OK;
+}
+
+gvr_status topk_decode_ws(const float* logits, int64_t row_stride, int64_t num_rows,
+                          const int32_t* kv_lens, int32_t next_n, int32_t compress_ratio,
+                          int32_t k, int32_t* indices, float* values, void* workspace,
+                          size_t workspace_bytes, void* stream, const gvr_options* options) {
+  gvr_status s = check_common(row_stride, num_rows, k, options, true);
+  if (s != GVR_OK) return s;
+  if (next_n < 1 || compress_ratio < 1) return GVR_ERR_ARG;
+  if (num_rows == 0) return GVR_OK;
+  if (!logits || !kv_lens || !indices) return GVR_ERR_NULL;
+  if (!aligned(logits, 16) || !aligned(indices, 4) || !aligned(kv_lens, 4) ||
+      (values && !aligned(values, 4)))
+    return GVR_ERR_ALIGN;
+  int sms = 0, smem_per_sm = 0, smem_reserved = 0;
+  if (device_state(&sms, &smem_per_sm, &smem_reserved) != cudaSuccess) return GVR_ERR_LAUNCH;
+  const int64_t grid = split_grid(sms, smem_per_sm, smem_reserved);
+  if (!use_split(num_rows, grid, options)) {
+    gvr_options o = options ? *options : gvr_options{};
+    o.flags &= ~(GVR_FLAG_CLUSTER_KERNEL | kSplitFlags);
+    return topk_decode_ex(logits, row_stride, num_rows, kv_lens, next_n, compress_ratio, k, indices, values,
+                          stream, &o);
+  }
+  s = check_workspace(workspace, workspace_bytes, grid);
+  if (s != GVR_OK) return s;
+  gvr::SplitParams prm = {};
+  prm.logits = logits;
+  prm.row_stride = row_stride;
+  prm.kv_lens = kv_lens;
+  prm.indices = indices;
+  prm.values = values;
+  prm.row_stats = options ? options->row_stats : nullptr;
+  prm.num_rows = int32_t(num_rows);
+  prm.next_n = next_n;
+  prm.compress_ratio = compress_ratio;
+  prm.k = k;
+  prm.mode = gvr::MODE_DECODE;
+  prm.flags = (options && (options->flags & GVR_FLAG_SPLIT_ALONE)) ? gvr::FLAG_SPLIT_ALONE : 0;
+  return launch_split(prm, grid, workspace, stream);
+}
+
+gvr_status topk_prefill_ws(const float* logits, int64_t row_stride, int64_t num_rows,
+                           const int32_t* row_starts, const int32_t* row_ends, int32_t k,
+                           int32_t* indices, void* workspace, size_t workspace_bytes, void* stream,
+                           const gvr_options* options) {
+  gvr_status s = check_common(row_stride, num_rows, k, options, true);
+  if (s != GVR_OK) return s;
+  if (num_rows == 0) return GVR_OK;
+  if (!logits || !row_starts || !row_ends || !indices) return GVR_ERR_NULL;
+  if (!aligned(logits, 16) || !aligned(indices, 4) || !aligned(row_starts, 4) || !aligned(row_ends, 4))
+    return GVR_ERR_ALIGN;
+  int sms = 0, smem_per_sm = 0, smem_reserved = 0;
+  if (device_state(&sms, &smem_per_sm, &smem_reserved) != cudaSuccess) return GVR_ERR_LAUNCH;
+  const int64_t grid = split_grid(sms, smem_per_sm, smem_reserved);
+  if (!use_split(num_rows, grid, options)) {
+    gvr_options o = options ? *options : gvr_options{};
+    o.flags &= ~(GVR_FLAG_CLUSTER_KERNEL | kSplitFlags);
+    return topk_prefill_ex(logits, row_stride, num_rows, row_starts, row_ends, k, indices, stream, &o);
+  }
+  s = check_workspace(workspace, workspace_bytes, grid);
+  if (s != GVR_OK) return s;
+  gvr::SplitParams prm = {};
+  prm.logits = logits;
+  prm.row_stride = row_stride;
+  prm.row_starts = row_starts;
+  prm.row_ends = row_ends;
+  prm.indices = indices;
+  prm.values = nullptr;
+  prm.row_stats = options ? options->row_stats : nullptr;
+  prm.num_rows = int32_t(num_rows);
+  prm.next_n = 1;
+  prm.compress_ratio = 1;
+  prm.k = k;
+  prm.mode = gvr::MODE_PREFILL;
+  prm.flags = (options && (options->flags & GVR_FLAG_SPLIT_ALONE)) ? gvr::FLAG_SPLIT_ALONE : 0;
+  return launch_split(prm, grid, workspace, stream);
 }
 
 gvr_status gvr_plan(int64_t row_stride, int64_t num_rows, int32_t k, const gvr_options* options,

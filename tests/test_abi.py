@@ -142,8 +142,9 @@ def test_prefill_argument_errors(lib):
 
 def test_option_errors(lib):
     import sparse_attention_indexer_exact_gb300 as gvr
+    # the kernel-choice flags (256, 512, 1024) belong to the *_ws entry points only
     for bad in (dict(cluster_size=3), dict(cluster_size=32), dict(ring_stages=2), dict(ring_stages=17), dict(reserved=1),
-                dict(flags=256)):
+                dict(flags=256), dict(flags=512), dict(flags=1024), dict(flags=2048)):
         o = gvr.Options(**bad)
         st = lib.topk_decode_ex(ALIGNED, 1024, 4, ALIGNED, 1, 1, K, ALIGNED, None, None, ctypes.byref(o))
         assert st == 5, bad
@@ -207,3 +208,13 @@ def test_binding_refuses_tensors_on_different_devices():
     for name in ("kv_lens", "indices", "values", "pre_idx", "block_max", "row_starts", "row_ends"):
         with pytest.raises(ValueError, match=name):
             gvr._same_device(d0, **{name: on(d1)})
+
+
+def test_workspace_size_for_a_device_shape(lib):
+    # The balanced kernel's workspace: per-row counters, then per chunk (8 CTAs per SM) a count
+    # and 4096 published (score, index) pairs.  Sized without touching a device.
+    size = ctypes.c_size_t(0)
+    assert lib.gvr_workspace_size(152, ctypes.byref(size)) == 0
+    grid = 152 * 8
+    assert size.value == 512 * 4 + grid * 4 + grid * 4096 * 8
+    assert lib.gvr_workspace_size(152, None) == 1
