@@ -64,8 +64,9 @@ typedef enum gvr_status {
   GVR_ERR_K = 4,      /* k is not 512, 1024 or 2048 */
   GVR_ERR_ARG = 5,    /* a negative row count, next_n < 1, compress_ratio < 1, bad options */
   GVR_ERR_LAUNCH = 6,   /* the kernel launch failed (no device, bad configuration, ...) */
-  GVR_ERR_WORKSPACE = 7 /* the workspace is NULL, not 16-byte aligned or smaller than
-                           gvr_workspace_size reports */
+  GVR_ERR_WORKSPACE = 7, /* the workspace is NULL, not 16-byte aligned or smaller than
+                            gvr_workspace_size reports */
+  GVR_ERR_NOALLOC_LIMIT = 8 /* topk_decode_noalloc: more rows than its fixed scratch holds */
 } gvr_status;
 
 /*
@@ -257,6 +258,33 @@ gvr_status topk_prefill_ws(const float* logits, int64_t row_stride, int64_t num_
                            const int32_t* row_starts, const int32_t* row_ends, int32_t k,
                            int32_t* indices, void* workspace, size_t workspace_bytes, void* stream,
                            const gvr_options* options);
+
+/*
+ * Decode top-K that allocates nothing and needs no workspace from the caller.  This entry point
+ * has no counterpart in the pages; it exists for callers that cannot allocate device memory
+ * when they select: an inference engine's plugin or op that is only handed its inputs and
+ * outputs at enqueue time and must not call cudaMalloc there, a serving loop on a fixed memory
+ * arena owned by another allocator, or latency-critical code that cannot afford the device-wide
+ * synchronization cudaMalloc may cause.
+ *
+ * It runs the balanced kernel of topk_decode_ws (same method, same exact results, same argument
+ * rules and errors as topk_decode) on a scratch area the library itself holds: a fixed device
+ * array of about 8 MB, present on every device that loads the library until the process exits.
+ * Limits and behaviour:
+ *   - num_rows must be at most GVR_NOALLOC_MAX_ROWS (128); more returns GVR_ERR_NOALLOC_LIMIT
+ *     before anything is enqueued.
+ *   - The first call on a device looks up the array's device address (once per device, with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the one array.  Each call clears its row counters on `stream` first (one
+ *     small memset, then the kernel), but calls that overlap on the GPU -- different streams
+ *     without an ordering between them, or different host threads -- race on the array and may
+ *     return wrong results; order them, or use topk_decode_ws with one workspace each.
+ *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library routine is called.
+ */
+#define GVR_NOALLOC_MAX_ROWS 128
+gvr_status topk_decode_noalloc(const float* logits, int64_t row_stride, int64_t num_rows,
+                               const int32_t* kv_lens, int32_t next_n, int32_t compress_ratio,
+                               int32_t k, int32_t* indices, float* values, void* stream);
 
 /* Static English text for a status code; never NULL. */
 const char* gvr_status_string(gvr_status status);

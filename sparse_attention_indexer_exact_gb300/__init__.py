@@ -25,7 +25,8 @@ import os
 import threading
 
 __all__ = ["topk_decode", "topk_prefill", "topk_decode_raw", "topk_decode_hinted_raw", "topk_decode_blockskip_raw",
-           "topk_prefill_raw", "topk_decode_ws_raw", "topk_prefill_ws_raw", "workspace_size", "workspace", "plan",
+           "topk_prefill_raw", "topk_decode_ws_raw", "topk_prefill_ws_raw", "topk_decode_noalloc_raw",
+           "workspace_size", "workspace", "plan",
            "Options",
            "GvrError", "library_path", "load_library", "FLAG_FORCE_RESCUE", "FLAG_NO_FLOOR", "FLAG_ZERO_CAP",
            "FLAG_RADIX_REFINE", "FLAG_DETERMINISTIC", "FLAG_SORTED", "FLAG_STREAM_RESCUE", "FLAG_COMPACT_LISTS", "PATH_NAMES",
@@ -44,7 +45,7 @@ PATH_NAMES = {-1: "device_error", 0: "short", 1: "refine", 2: "rescue_bracket", 
 SUPPORTED_K = (512, 1024, 2048)
 EXPORTED_SYMBOLS = ("topk_decode", "topk_prefill", "topk_decode_ex", "topk_prefill_ex", "topk_decode_hinted",
                     "topk_decode_blockskip", "topk_decode_ws", "topk_prefill_ws", "gvr_workspace_size",
-                    "gvr_status_string", "gvr_plan")
+                    "topk_decode_noalloc", "gvr_status_string", "gvr_plan")
 
 
 class GvrError(RuntimeError):
@@ -79,9 +80,10 @@ def _declare(lib):
     lib.topk_decode_ws.argtypes = [p, i64, i64, p, i32, i32, i32, p, p, p, sz, p, ctypes.POINTER(Options)]
     lib.topk_prefill_ws.argtypes = [p, i64, i64, p, p, i32, p, p, sz, p, ctypes.POINTER(Options)]
     lib.gvr_workspace_size.argtypes = [i32, ctypes.POINTER(sz)]
+    lib.topk_decode_noalloc.argtypes = [p, i64, i64, p, i32, i32, i32, p, p, p]
     for f in (lib.topk_decode, lib.topk_decode_ex, lib.topk_decode_hinted, lib.topk_decode_blockskip,
               lib.topk_prefill, lib.topk_prefill_ex, lib.gvr_plan, lib.topk_decode_ws, lib.topk_prefill_ws,
-              lib.gvr_workspace_size):
+              lib.gvr_workspace_size, lib.topk_decode_noalloc):
         f.restype = ctypes.c_int
     lib.gvr_status_string.argtypes = [ctypes.c_int]
     lib.gvr_status_string.restype = ctypes.c_char_p
@@ -179,6 +181,16 @@ def topk_prefill_ws_raw(logits_ptr: int, row_stride: int, num_rows: int, row_sta
                              workspace_ptr, workspace_bytes, stream,
                              ctypes.byref(options) if options is not None else None)
     _check(st)
+
+
+def topk_decode_noalloc_raw(logits_ptr: int, row_stride: int, num_rows: int, kv_lens_ptr: int, next_n: int,
+                            compress_ratio: int, k: int, indices_ptr: int, values_ptr: int | None,
+                            stream: int) -> None:
+    """``topk_decode_noalloc`` on raw device addresses: the library's own fixed scratch, no
+    allocation and no workspace (at most 128 rows; calls that overlap on the GPU race)."""
+    lib = load_library()
+    _check(lib.topk_decode_noalloc(logits_ptr, row_stride, num_rows, kv_lens_ptr, next_n, compress_ratio, k,
+                                   indices_ptr, values_ptr, stream))
 
 
 def workspace_size(sm_count: int = 0) -> int:

@@ -317,6 +317,48 @@ gvr_status launch_split(gvr::SplitParams prm, int64_t grid, void* workspace, voi
   return e == cudaSuccess ? GVR_OK : GVR_ERR_LAUNCH;
 }
 
+// ---------------------------------------------------------------- no-allocation entry point
+// topk_decode_noalloc runs the balanced kernel on a scratch area that the library holds as a
+// device array of fixed size: its grid is capped at kNoAllocGrid chunks, which fixes the bytes.
+constexpr int64_t kNoAllocGrid = 256;
+constexpr size_t kNoAllocCounterBytes = size_t(gvr::SPLIT_MAX_ROWS) * 4;
+constexpr size_t kNoAllocBytes = kNoAllocCounterBytes + size_t(kNoAllocGrid) * 4 +
+                                 size_t(kNoAllocGrid) * gvr::SPLIT_UNIT_CAP * 8;
+static_assert(2 * GVR_NOALLOC_MAX_ROWS <= kNoAllocGrid, "the capped grid holds the row limit");
+
+struct NoAllocState {
+  std::once_flag once;
+  cudaError_t err = cudaSuccess;
+  void* scratch = nullptr;  // the device address of g_noalloc_scratch on this device
+};
+NoAllocState g_noalloc[kMaxDevices];
+
+}  // namespace
+
+// The scratch itself: every device that loads the library holds these bytes until the process
+// exits.  In host code this name is only a host-side stand-in for the device array, so its device
+// address is looked up once per device (noalloc_scratch) and that address is what the kernel gets.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+namespace {
+
+// Device address of the scratch on the current device, looked up on the first call per device
+// (with that device current).
+cudaError_t noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  NoAllocState& st = g_noalloc[dev];
+  std::call_once(st.once, [&st]() {
+    void* p = nullptr;
+    st.err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    st.scratch = st.err == cudaSuccess ? p : nullptr;
+  });
+  *out = st.scratch;
+  return st.err;
+}
+
 gvr_status check_workspace(void* workspace, size_t bytes, int64_t grid) {
   if (!workspace || !aligned(workspace, 16) || bytes < split_workspace_bytes(grid)) return GVR_ERR_WORKSPACE;
   return GVR_OK;
@@ -464,6 +506,7 @@ const char* gvr_status_string(gvr_status status) {
     case GVR_ERR_ARG: return "invalid argument (row count, next_n, compress_ratio or options)";
     case GVR_ERR_LAUNCH: return "kernel launch failed";
     case GVR_ERR_WORKSPACE: return "workspace is NULL, misaligned or smaller than gvr_workspace_size";
+    case GVR_ERR_NOALLOC_LIMIT: return "topk_decode_noalloc takes at most GVR_NOALLOC_MAX_ROWS (128) rows";
   }
   return "unknown status";
 }
@@ -550,6 +593,43 @@ gvr_status topk_prefill_ws(const float* logits, int64_t row_stride, int64_t num_
   prm.mode = gvr::MODE_PREFILL;
   prm.flags = (options && (options->flags & GVR_FLAG_SPLIT_ALONE)) ? gvr::FLAG_SPLIT_ALONE : 0;
   return launch_split(prm, grid, workspace, stream);
+}
+
+gvr_status topk_decode_noalloc(const float* logits, int64_t row_stride, int64_t num_rows,
+                               const int32_t* kv_lens, int32_t next_n, int32_t compress_ratio, int32_t k,
+                               int32_t* indices, float* values, void* stream) {
+  gvr_status s = check_common(row_stride, num_rows, k, nullptr);
+  if (s != GVR_OK) return s;
+  if (next_n < 1 || compress_ratio < 1) return GVR_ERR_ARG;
+  if (num_rows == 0) return GVR_OK;
+  if (num_rows > GVR_NOALLOC_MAX_ROWS) return GVR_ERR_NOALLOC_LIMIT;
+  if (!logits || !kv_lens || !indices) return GVR_ERR_NULL;
+  if (!aligned(logits, 16) || !aligned(indices, 4) || !aligned(kv_lens, 4) ||
+      (values && !aligned(values, 4)))
+    return GVR_ERR_ALIGN;
+  int sms = 0, smem_per_sm = 0, smem_reserved = 0;
+  if (device_state(&sms, &smem_per_sm, &smem_reserved) != cudaSuccess) return GVR_ERR_LAUNCH;
+  int64_t grid = split_grid(sms, smem_per_sm, smem_reserved);
+  if (grid > kNoAllocGrid) grid = kNoAllocGrid;
+  if (2 * num_rows > grid) return GVR_ERR_NOALLOC_LIMIT;  // a device with fewer SMs than 16
+  void* scratch = nullptr;
+  if (noalloc_scratch(&scratch) != cudaSuccess) return GVR_ERR_LAUNCH;
+  // The per-row arrival counters must start at zero.  A completed call leaves them so, but the
+  // array keeps whatever the last call left (one that was cut short, for instance): clear them.
+  if (cudaMemsetAsync(scratch, 0, kNoAllocCounterBytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GVR_ERR_LAUNCH;
+  gvr::SplitParams prm = {};
+  prm.logits = logits;
+  prm.row_stride = row_stride;
+  prm.kv_lens = kv_lens;
+  prm.indices = indices;
+  prm.values = values;
+  prm.num_rows = int32_t(num_rows);
+  prm.next_n = next_n;
+  prm.compress_ratio = compress_ratio;
+  prm.k = k;
+  prm.mode = gvr::MODE_DECODE;
+  return launch_split(prm, grid, scratch, stream);
 }
 
 gvr_status gvr_plan(int64_t row_stride, int64_t num_rows, int32_t k, const gvr_options* options,
