@@ -125,13 +125,24 @@ enum {
    * samples expected above tau) on every launch; by default the host picks them only where
    * they let a two-wave launch run as one wave with half the CTAs per row */
   GVR_FLAG_COMPACT_LISTS = 128,
-  /* *_ws entry points: always the cluster kernel (the workspace is then not touched) */
+  /* always the cluster kernel: for the *_ws entry points not the balanced kernel either (the
+   * workspace is then not touched) */
   GVR_FLAG_CLUSTER_KERNEL = 256,
   /* diagnostics, *_ws entry points: the balanced kernel's last CTA of every long row selects the
    * row alone (the exact path it takes when the published scores cannot decide the row) */
   GVR_FLAG_SPLIT_ALONE = 512,
   /* *_ws entry points: the balanced kernel whenever the call fits it */
-  GVR_FLAG_SPLIT_KERNEL = 1024
+  GVR_FLAG_SPLIT_KERNEL = 1024,
+  /* diagnostics (cluster kernel): the first row's cluster reports a device-side give-up once its
+   * first pass is complete (every bulk copy landed, no wait shortened), so that row's indices
+   * become -2 and its row_stats path GVR_PATH_DEVICE_ERROR while the other rows stay exact --
+   * the failure path without a failure */
+  GVR_FLAG_DIAG_FAIL_ROW0 = 2048,
+  /* opt-in: the short-row kernel for calls it takes (row_stride <= 16384, no other flag, no
+   * cluster or ring setting, no hint or block maxima; others run the cluster kernel): one CTA
+   * of 256 threads holds a whole row in registers.  Exact, but measured slower than the cluster
+   * kernel on every short-row workload tried, so never chosen by default */
+  GVR_FLAG_SHORT_KERNEL = 4096
 };
 
 typedef struct gvr_options {
@@ -165,7 +176,13 @@ enum {
                                    list overflowed: one more read of the row lists the crossing
                                    bin and above per CTA, digit passes over those lists */
   GVR_PATH_SPLIT = 7,           /* balanced kernel: selected from the row's published scores */
-  GVR_PATH_SPLIT_ALONE = 8      /* balanced kernel: the row's last CTA selected it alone */
+  GVR_PATH_SPLIT_ALONE = 8,     /* balanced kernel: the row's last CTA selected it alone */
+  GVR_PATH_NEG_INF_FILL = 9,    /* fewer than k scores above -inf: every other score is a winner,
+                                   the remaining slots take -inf scores (tau = -inf), one pass */
+  GVR_PATH_SHORT_KERNEL = 10,   /* short-row kernel: histogram, crossing bin, refine, all over the
+                                   row held in registers */
+  GVR_PATH_SHORT_RADIX = 11     /* short-row kernel: exact radix select over the row in registers
+                                   (invalid bracket, floor too high, crossing bin too big) */
 };
 
 /* topk_decode with tuning/diagnostic options (NULL = automatic, identical to topk_decode). */

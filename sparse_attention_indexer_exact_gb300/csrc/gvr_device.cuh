@@ -207,3 +207,18 @@ __device__ __forceinline__ void dsmem_red_max(uint32_t addr, uint32_t v) {
 
 }  // namespace gvr
 
+
+namespace gvr {
+
+// Ask L2 to fetch `bytes` (a multiple of 16) of global memory from a 16-byte aligned address.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Orders this thread's earlier generic-proxy view of global memory (data published by other
+// CTAs and acquired through an atomic and a fence) before its later bulk copies that read it.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+}  // namespace gvr

@@ -72,6 +72,7 @@ constexpr int LIST_CAP = LIST_BYTES / 8;
 constexpr int LIST_CAP16 = LIST_BYTES / 6;
 constexpr int LIST_MAX_STAGES = 64;
 constexpr int CAP = 512;              // candidate slots in cluster rank 0
+constexpr uint32_t REC_CAP = LIST_BYTES / 4;  // window indices the first rescue digit pass records
 constexpr int RING_CAND = STAGE_VEC * 16 / 8;  // (score, index) candidates one idle ring stage holds
 constexpr int BULK_BINS = 512;       // first-pass counts of at most this many bins go as bulk adds
 constexpr int RANK_REFINE_MAX = 256;
@@ -103,7 +104,8 @@ enum : int32_t {
   FLAG_DETERMINISTIC = 16,
   FLAG_SORTED = 32,
   FLAG_STREAM_RESCUE = 64,
-  FLAG_COMPACT_LISTS = 128
+  FLAG_COMPACT_LISTS = 128,
+  FLAG_DIAG_FAIL_ROW0 = 2048
 };
 enum : int32_t {
   PATH_DEVICE_ERROR = -1,
@@ -113,7 +115,8 @@ enum : int32_t {
   PATH_RESCUE_OVERFLOW = 3,
   PATH_RESCUE_FORCED = 4,
   PATH_REFINE_CLUSTER = 5,
-  PATH_REFINE_RELIST = 6
+  PATH_REFINE_RELIST = 6,
+  PATH_NEG_INF_FILL = 9
 };
 
 struct Params {
@@ -147,23 +150,6 @@ struct Crossing {
 };
 
 struct alignas(16) Smem {
-  uint32_t hist[NB + 4];           // this CTA's counts (groups of 4 bins read as 16-byte vectors);
-                                   // hist[NB]: 1 when this CTA's list overflowed in pass 1
-  uint32_t tot[NB + 4];            // cluster-wide counts, added here by every CTA of the cluster
-                                   // (tot[NB]: CTAs whose list overflowed); the rescue's two
-                                   // 256-bin digit histograms reuse it
-  union {  // the first-pass list, in one of its two formats
-    struct {
-      float list_v[LIST_CAP];
-      int32_t list_j[LIST_CAP];
-    };
-    struct {
-      float list_v16[LIST_CAP16];
-      uint16_t list_p16[LIST_CAP16];  // stage of the share * 1024 + offset in the stage
-    };
-  };
-  float cand_v[CAP];
-  int32_t cand_j[CAP];
   uint32_t wsum[2][8];
   float wmin[8];
   float whmin[8], whmax[8];        // hinted sampling: smallest / largest finite hinted score per warp
@@ -191,17 +177,36 @@ struct alignas(16) Smem {
   uint32_t ctr_rwin, ctr_rtie;     // rank 0's counters for its own radix refine
   uint32_t rc_win, rc_tie;         // rank 0's counters shared by the cluster in rescue
   uint32_t saved;                  // count of the partial floor bin before the second pass
+  uint32_t rec_n;                  // rescue: members recorded in the first digit pass (may exceed REC_CAP)
   uint32_t tout;                   // this CTA gave up waiting for staged data
   uint32_t err;                    // rank 0: some CTA of the cluster gave up
   uint64_t bar[MAX_STAGES];        // one mbarrier per ring stage
   uint64_t hbar;                   // completes once every CTA's first-pass counts have landed in tot
+  // Last members: hist, tot and the list, then (after padding) the ring -- one contiguous area
+  // that rank 0 reuses at the very end for the sort keys of the sorted output.
+  alignas(16) uint32_t hist[NB + 4];  // this CTA's counts (groups of 4 bins read as 16-byte
+                                      // vectors); hist[NB]: 1 when this CTA's list overflowed
+  uint32_t tot[NB + 4];            // cluster-wide counts, added here by every CTA of the cluster
+                                   // (tot[NB]: CTAs whose list overflowed); the rescue's two
+                                   // 256-bin digit histograms reuse it
+  union {  // the first-pass list, in one of its two formats
+    struct {
+      float list_v[LIST_CAP];
+      int32_t list_j[LIST_CAP];
+    };
+    struct {
+      float list_v16[LIST_CAP16];
+      uint16_t list_p16[LIST_CAP16];  // stage of the share * 1024 + offset in the stage
+    };
+  };
 };
 static_assert(offsetof(Smem, hist) % 16 == 0 && offsetof(Smem, tot) % 16 == 0,
               "histograms are read as 16-byte vectors");
 static_assert(offsetof(Smem, bar) % 8 == 0, "mbarriers must be 8-byte aligned");
 static_assert(2 * 256 + 4 <= NB, "the rescue's digit totals and key bounds live in tot");
-static_assert(offsetof(Smem, wsum) >= sizeof(uint64_t) * MAX_K, "sort keys fit below the scalars");
-static_assert(MIN_STAGES * RING_CAND > CAP, "the ring holds more candidates than the buffer");
+static_assert(RING_CAND >= CAP, "one ring stage holds the candidate buffer");
+static_assert(sizeof(float) * LIST_CAP + sizeof(int32_t) * LIST_CAP == 4 * REC_CAP,
+              "the rescue's record fills exactly the list area");
 
 __device__ __forceinline__ uint32_t* digit_hist(Smem& S, int buf) { return S.tot + 256 * buf; }
 
@@ -214,6 +219,8 @@ struct IntC {
 // destinations, 128-byte aligned).
 constexpr int SMEM_FIXED = int((sizeof(Smem) + 127) / 128 * 128);
 __host__ __device__ constexpr int smem_bytes(int nstage) { return SMEM_FIXED + nstage * STAGE_VEC * 16; }
+static_assert(int(offsetof(Smem, hist)) + int(sizeof(uint64_t)) * MAX_K <= smem_bytes(MIN_STAGES),
+              "the sort keys fit from hist to the end of the smallest ring");
 
 // Monotone bin of a score in [GMIN, GMAX] with NB bins; NaN maps to bin 0.
 __device__ __forceinline__ int value_bin(float v, float gmin, float sc) {
@@ -354,10 +361,6 @@ __device__ __forceinline__ Crossing scan_crossing(SM& S, uint32_t k) {
   return r;
 }
 
-// Sum the 256-bin digit histograms digit_hist(buf) of cluster ranks [c0, c0 + cn) and find the
-// digit d (scanning from 255 down) where the running count reaches `need`; publishes d, the
-// count above d and the count at d in S.dsel / S.dabove / S.dcnt.  Thread t owns digits
-// 255 - DPT t down to 256 - DPT (t + 1).
 // The highest bin b of arr[0..NB) with sum_{bins >= b} arr >= want, or -1 when the total is
 // below want.  Block-collective; thread t owns bins NB-1-(NB/T)t down to NB-(NB/T)(t+1).
 template <int T, class SM>
@@ -478,52 +481,6 @@ __device__ __forceinline__ DigitCross digit_scan(SM& S, const uint32_t* dtot, co
   }
   __syncthreads();
   return DigitCross{S.dsel, S.dabove, S.dcnt, S.dmy_above, S.dmy_at, all};
-}
-
-template <int T>
-__device__ __forceinline__ void digit_cross(Smem& S, int buf, uint32_t c0, uint32_t cn, uint32_t need) {
-  constexpr int DPT = 256 / T;
-  constexpr int NW = T / 32;
-  static_assert(DPT * T == 256 && NW <= 8, "threads must divide 256");
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t cnt[DPT];
-  uint32_t st = 0;
-#pragma unroll
-  for (int j = 0; j < DPT; ++j) {
-    const int d = 255 - DPT * tid - j;
-    const uint32_t local = smem_u32(&digit_hist(S, buf)[d]);
-    uint32_t t = 0;
-    for (uint32_t c = c0; c < c0 + cn; ++c) t += dsmem_ld_u32(dsmem_map(local, c));
-    cnt[j] = t;
-    st += t;
-  }
-  uint32_t incl = st;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t a = __shfl_up_sync(FULL_MASK, incl, o);
-    if (lane >= o) incl += a;
-  }
-  if (lane == 31) S.wsum[0][warp] = incl;
-  __syncthreads();
-  uint32_t before = 0;
-#pragma unroll
-  for (int w = 0; w < NW; ++w)
-    if (w < warp) before += S.wsum[0][w];
-  uint32_t excl = before + incl - st;
-  if (excl < need && excl + st >= need) {
-    bool found = false;
-#pragma unroll
-    for (int j = 0; j < DPT; ++j) {
-      if (!found && excl + cnt[j] >= need) {
-        S.dsel = uint32_t(255 - DPT * tid - j);
-        S.dabove = excl;
-        S.dcnt = cnt[j];
-        found = true;
-      }
-      excl += cnt[j];
-    }
-  }
-  __syncthreads();
 }
 
 // EXT: the extended modes (deterministic ties and sorting, hinted sampling, block skipping) are
@@ -745,6 +702,35 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       for (int l = 0; l < 4; ++l) f(f4_get(v, l), g, ((lanes >> l) & 1u) != 0, l);
     }
   };
+  // The same per-lane walk as stream_pass + each_lane, reading the share straight from global
+  // memory (no ring): f(e, g, valid, l) for every lane of every vector slot, stage by stage, two
+  // stages' loads in flight at a time.  For a pass that must leave the ring alone.
+  auto global_pass = [&](auto&& f) {
+    const float4* const vbase = reinterpret_cast<const float4*>(base);
+    for (int32_t s0 = 0; s0 < nstages; s0 += 2) {
+      float4 v[2][VPS];
+      uint32_t ln[2][VPS];
+      int32_t gg[2][VPS];
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int i = 0; i < VPS; ++i) {
+          const int32_t g = (s0 + q < nstages) ? stage_first(s0 + q) + i * T + tid : nvec;
+          gg[q][i] = g;
+          v[q][i] = g < ffull ? __ldg(vbase + g) : S.tail;
+          uint32_t lanes = g < ffull ? 0xFu : (g < nvec ? (1u << tailn) - 1u : 0u);
+          if (g == 0) lanes &= (0xFu << lead) & 0xFu;
+          ln[q][i] = lanes;
+        }
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+        if (s0 + q < nstages)  // CTA-uniform
+#pragma unroll
+          for (int i = 0; i < VPS; ++i)
+#pragma unroll
+            for (int l = 0; l < 4; ++l) f(f4_get(v[q][i], l), gg[q][i], ((ln[q][i] >> l) & 1u) != 0, l);
+    }
+  };
   // The list: LCAP scores, then their window indices (int32) or, compact, their positions in
   // this CTA's share (16 bits: stage of the share * 1024 + offset in the stage).
   constexpr int LCAP = L16 ? LIST_CAP16 : LIST_CAP;
@@ -800,9 +786,9 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   };
   // Rank 0, block-collective: reorder out[0..k) (and the values) by (value desc, index asc), the
   // order of the plain definition.  k is a power of two; the 64-bit sort keys (inverted order
-  // key, index) live in the histogram / list / candidate area, which no CTA uses any more.
+  // key, index) live in the histogram / list / ring area, which no CTA uses any more.
   auto sort_output = [&]() {
-    uint64_t* sk = reinterpret_cast<uint64_t*>(smem_raw);
+    uint64_t* sk = reinterpret_cast<uint64_t*>(&S.hist[0]);
     __syncthreads();
     for (int i = tid; i < k; i += T) {
       const int32_t j = __ldcg(out + i);  // written by every CTA of the cluster
@@ -1037,10 +1023,12 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
         fb = suffix_cross<T>(S, S.hist, want);
       }
       if (tid == 0) {
-        // any threshold works: bins above bin(t) are complete, bin(t) is partial
-        const float t = fb > 0 ? __fadd_rn(gmin, __fdiv_rn(float(fb), sc)) : -INFINITY;
+        // any threshold works: bins above bin(t) are complete, bin(t) is partial.  A floor in
+        // the lowest bin is -FLT_MAX: every score but -inf (and NaN) is counted and listed, so a
+        // row whose finite scores are fewer than k is decided by the first pass (the -inf fill)
+        const float t = fb > 0 ? __fadd_rn(gmin, __fdiv_rn(float(fb), sc)) : -FLT_MAX;
         S.vthr = t;
-        S.fpart = fb > 0 ? value_bin(t, gmin, sc) : -1;
+        S.fpart = value_bin(t, gmin, sc);
       }
       for (int i = tid; i < NB; i += T) S.hist[i] = 0;
       __syncthreads();
@@ -1116,31 +1104,39 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
         }
       }
     } else {
-      stream_pass(true, [&](uint32_t slot, int32_t c0) {
-        float4 vv[VPS];
-        uint32_t lanes = 0xFFFFFFFFu;  // bit 4i+l: lane l of the i-th vector is in the window
-        if (c0 > 0 && c0 + STAGE_VEC <= ffull) {  // an interior stage: every lane is in the window
-  #pragma unroll
-          for (int i = 0; i < VPS; ++i) vv[i] = ring[slot][i * T + tid];
-        } else {
-          lanes = 0;
-  #pragma unroll
-          for (int i = 0; i < VPS; ++i) {
-            int32_t g;
-            lanes |= stage_vec(slot, c0, i, g, vv[i]) << (4 * i);
+      // One visit covers G stages of the ring (G = 1 here; the visitor also takes a pair, which
+      // measured no faster: the first pass is not bound by the per-visit chain it shares).
+      auto p1_visit = [&](auto g_c, const uint32_t* slots, const int32_t* c0s) {
+        constexpr int G = decltype(g_c)::value;
+        constexpr int NV = VPS * G;  // vectors per thread
+        constexpr int NE = 4 * NV;   // scores per thread
+        float4 vv[NV];
+        uint32_t lanes = 0;  // bit 4v+l: lane l of this thread's v-th vector is in the window
+#pragma unroll
+        for (int q = 0; q < G; ++q) {
+          if (c0s[q] > 0 && c0s[q] + STAGE_VEC <= ffull) {  // an interior stage: every lane is in
+#pragma unroll
+            for (int i = 0; i < VPS; ++i) vv[q * VPS + i] = ring[slots[q]][i * T + tid];
+            lanes |= ((1u << (4 * VPS)) - 1u) << (4 * VPS * q);
+          } else {
+#pragma unroll
+            for (int i = 0; i < VPS; ++i) {
+              int32_t g;
+              lanes |= stage_vec(slots[q], c0s[q], i, g, vv[q * VPS + i]) << (4 * (q * VPS + i));
+            }
           }
         }
-        uint32_t bits = 0;  // bit 4i+l: lane l of this thread's i-th vector is >= thr
-  #pragma unroll
-        for (int i = 0; i < VPS; ++i)
-          bits |= (uint32_t(vv[i].x >= thr) | (uint32_t(vv[i].y >= thr) << 1) | (uint32_t(vv[i].z >= thr) << 2) |
-                   (uint32_t(vv[i].w >= thr) << 3))
-                  << (4 * i);
+        uint32_t bits = 0;  // bit 4v+l: lane l of this thread's v-th vector is >= thr
+#pragma unroll
+        for (int v = 0; v < NV; ++v)
+          bits |= (uint32_t(vv[v].x >= thr) | (uint32_t(vv[v].y >= thr) << 1) | (uint32_t(vv[v].z >= thr) << 2) |
+                   (uint32_t(vv[v].w >= thr) << 3))
+                  << (4 * v);
         bits &= lanes;
         // The warp's exclusive prefix of hit counts from one ballot per bit of the count (the
-        // upper two bits only when some thread has 4 or more hits).
+        // upper bits only when some thread has 4 or more hits).
         const uint32_t nhit = __popc(bits);
-        static_assert(4 * VPS < 16, "hit counts fit in 4 bits");
+        static_assert(NE <= 16, "hit counts fit in 5 bits");
         const unsigned lt = lanemask_lt();
         const unsigned m0 = __ballot_sync(FULL_MASK, nhit & 1u), m1 = __ballot_sync(FULL_MASK, nhit & 2u);
         uint32_t excl = uint32_t(__popc(m0 & lt)) + (uint32_t(__popc(m1 & lt)) << 1);
@@ -1149,18 +1145,23 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
           const unsigned m2 = __ballot_sync(FULL_MASK, nhit & 4u), m3 = __ballot_sync(FULL_MASK, nhit & 8u);
           excl += (uint32_t(__popc(m2 & lt)) << 2) + (uint32_t(__popc(m3 & lt)) << 3);
           wtot += (uint32_t(__popc(m2)) << 2) + (uint32_t(__popc(m3)) << 3);
+          if (NE >= 16) {
+            const unsigned m4 = __ballot_sync(FULL_MASK, nhit & 16u);
+            excl += uint32_t(__popc(m4 & lt)) << 4;
+            wtot += uint32_t(__popc(m4)) << 4;
+          }
         }
         if (wtot == 0) return;  // nothing of this warp reaches the floor
         uint32_t at = wlist + excl;
         wlist += wtot;
         // A warp with a few hits per thread counts them one by one; a dense warp (ties, a low
         // floor) adds its hits with one atomic when they all share a bin, else one per score.
-        const bool dense = __any_sync(FULL_MASK, nhit > uint32_t(SPARSE_MAX));
+        const bool dense = __any_sync(FULL_MASK, nhit > uint32_t(SPARSE_MAX * G));
         if (dense) {
-          uint32_t bj[4 * VPS];
+          uint32_t bj[NE];
           uint32_t bmin = 0xffffffffu, bmax = 0u;
-  #pragma unroll
-          for (int j = 0; j < 4 * VPS; ++j) {
+#pragma unroll
+          for (int j = 0; j < NE; ++j) {
             bj[j] = uint32_t(value_bin(f4_get(vv[j >> 2], j & 3), gmin, sc));
             if ((bits >> j) & 1u) {
               bmin = min(bmin, bj[j]);
@@ -1172,30 +1173,41 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
           if (bmin == bmax) {
             if (lane == 0) atomicAdd(&S.hist[bmin], wtot);
           } else {  // plain atomics: the hardware merges the lanes that share a bin
-  #pragma unroll
-            for (int j = 0; j < 4 * VPS; ++j)
+#pragma unroll
+            for (int j = 0; j < NE; ++j)
               if ((bits >> j) & 1u) atomicAdd(&S.hist[bj[j]], 1u);
           }
         }
         // List the hits (a dense warp only until its segment is full; the counts above are exact).
         if (!dense || wlist - wtot < uint32_t(LSEG)) {
-          const uint32_t kbase = list_key(c0 + tid, 0);  // index field of this thread's lane 0
-          const int32_t jbase = 4 * (c0 + tid) - lead;   // window index of this thread's lane 0
           for (uint32_t rest = bits; rest;) {
-            const int j = __ffs(rest) - 1;
+            const int jb = __ffs(rest) - 1;  // bit: the first or second stage, score j in it
             rest &= rest - 1;
-            const float e = stage_score(slot, c0, j);
+            const bool second = G == 2 && jb >= 4 * VPS;  // selects, not an indexed local array
+            const int j = second ? jb - 4 * VPS : jb;
+            const int32_t c0 = second ? c0s[G - 1] : c0s[0];
+            const float e = stage_score(second ? slots[G - 1] : slots[0], c0, j);
             if (!dense) atomicAdd(&S.hist[value_bin(e, gmin, sc)], 1u);
             if (at < uint32_t(LSEG)) {
               seg_v[at] = e;
-              if constexpr (L16) seg_p[at] = uint16_t(kbase + uint32_t(j >> 2) * (4 * T) + uint32_t(j & 3));
-              else seg_j[at] = jbase + (j >> 2) * (4 * T) + (j & 3);
+              if constexpr (L16)
+                seg_p[at] = uint16_t(list_key(c0 + tid, 0) + uint32_t(j >> 2) * (4 * T) + uint32_t(j & 3));
+              else
+                seg_j[at] = 4 * (c0 + tid) - lead + (j >> 2) * (4 * T) + (j & 3);
             }
             ++at;
           }
         }
+      };
+      stream_pass(true, [&](uint32_t slot, int32_t c0) {
+        const uint32_t sl[1] = {slot};
+        const int32_t c0s[1] = {c0};
+        p1_visit(IntC<1>{}, sl, c0s);
       });
     }
+    // Diagnostics: the first row's rank-0 CTA reports a give-up here, after its first pass has
+    // waited for every stage it issued (nothing in flight), to exercise the failure path.
+    if ((p.flags & FLAG_DIAG_FAIL_ROW0) && row == 0 && rank == 0 && tid == 0) S.tout = 1;
     if (lane == 0) S.list_n[warp] = wlist;
     __syncthreads();
     listed = true;
@@ -1246,7 +1258,11 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     }
     report_timeout();
     cr = scan_crossing<T>(S, uint32_t(k));
-    if (fpart >= 0 && cr.total < uint32_t(k)) {
+    if (thr == -FLT_MAX && cr.total < uint32_t(k) && S.unlisted == 0 && !det) {
+      // Fewer than k scores are >= -FLT_MAX and every CTA listed all of its own: tau = -inf (NaN
+      // aside).  The listed scores are the winners; any k - total of the others fill the rest.
+      path = PATH_NEG_INF_FILL;
+    } else if (fpart >= 0 && cr.total < uint32_t(k)) {
       // Fewer than k scores reached the floor: count the scores below it, push only these new
       // counts, then scan the complete totals.  (When at least k scores reached the floor, tau
       // is at or above it, and a crossing in the partial floor bin needs no second pass: its
@@ -1276,7 +1292,9 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       cr = scan_crossing<T>(S, uint32_t(k));
     }
     const uint32_t cap = (p.flags & FLAG_ZERO_CAP) ? 0u : uint32_t(CAP);
-    if (cr.total < uint32_t(k))
+    if (path == PATH_NEG_INF_FILL) {
+      // decided by the first pass
+    } else if (cr.total < uint32_t(k))
       path = PATH_RESCUE_OVERFLOW;  // NaN in the window (out of contract)
     else if (cr.m > cap && (p.flags & FLAG_ZERO_CAP || det || rounds != 1 || S.unlisted >= UNLISTED_RANK0 ||
                             cr.m > uint32_t(nst) * RING_CAND))
@@ -1291,6 +1309,71 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   // >= thr (this only matters when the crossing is the partial floor bin).
   const float cthr = rounds == 1 ? thr : -INFINITY;
 
+  if (path == PATH_NEG_INF_FILL) {
+    // ------------------------------------------------------------ -inf fill
+    // Winners: every listed score (total of them, cluster-wide).  Ties: k - total of the other
+    // in-window scores, all -inf for a row inside the contract.  Rank 0 hands each CTA a block of
+    // winner slots (its listed count) and of tie slots (its unlisted in-window count); a CTA
+    // walks its share for ties only until its tie slots are written.
+    const uint32_t nwin = cr.total, nties = uint32_t(k) - cr.total;
+    uint32_t my_win = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) my_win += S.list_n[w];
+    if (tid == 0) {
+      uint32_t share = 0;  // in-window scores of this CTA's stages
+      for (int32_t st = 0; st < nstages; ++st) {
+        const int32_t c0 = stage_first(st), c1 = min(c0 + STAGE_VEC, nvec);
+        int32_t n = 4 * (c1 - c0);
+        if (c0 == 0) n -= lead;
+        if (c1 == nvec && tailn) n -= 4 - tailn;
+        share += uint32_t(n);
+      }
+      S.base_above = dsmem_atom_add(dsmem_map(smem_u32(&S.gctr_above), 0), my_win);
+      S.saved = share - my_win;  // this CTA's ties
+      S.base_cand = dsmem_atom_add(dsmem_map(smem_u32(&S.gctr_cand), 0), share - my_win);
+    }
+    __syncthreads();
+    const uint32_t wbase = S.base_above, tbase = S.base_cand, my_eq = S.saved;
+    each_listed([&](float e, int32_t jw, bool in) {
+      const uint32_t ws = warp_alloc_local(&S.ctr_win, in);
+      if (in && wbase + ws < nwin) {
+        out[wbase + ws] = jw;
+        if (outv) outv[wbase + ws] = e;
+      }
+    });
+    const uint32_t my_ties = tbase < nties ? min(my_eq, nties - tbase) : 0u;
+    if (my_ties > 0) {
+      stream_pass(false, [&](uint32_t slot, int32_t c0) {
+        if (S.ctr_cand >= my_ties) return;  // warp-uniform read; the counter only grows
+        uint32_t tm = 0;
+        each_lane(slot, c0, [&](float e, int32_t g, bool valid, int l) {
+          tm |= uint32_t(valid && !(e >= thr)) << (4 * ((g - c0) / T) + l);
+        });
+        uint32_t ts = warp_alloc_n(&S.ctr_cand, __popc(tm));
+        for (uint32_t rest = tm; rest; rest &= rest - 1, ++ts)
+          if (ts < my_ties) {
+            const int j = __ffs(rest) - 1;
+            out[nwin + tbase + ts] = 4 * (c0 + (j >> 2) * T + tid) + (j & 3) - lead;
+            if (outv) outv[nwin + tbase + ts] = stage_score(slot, c0, j);
+          }
+      });
+    }
+    report_timeout();
+    csync();  // rank 0's counters stay alive until every CTA is done with them
+    if (rank == 0) {
+      const bool failed = S.err || S.tout;
+      if (failed)
+        for (int i = tid; i < k; i += T) out[i] = -2;
+      if (stats) {
+        stats[0] = failed ? PATH_DEVICE_ERROR : PATH_NEG_INF_FILL;
+        stats[1] = int32_t(nties);
+        stats[2] = rounds;
+        stats[3] = int32_t(nwin);
+      }
+    }
+    return;
+  }
+
   if (path == PATH_REFINE) {
     // ------------------------------------------------------------ collect
     // Rank 0 hands each CTA a contiguous block of winner slots and of candidate slots.
@@ -1298,11 +1381,14 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     if (tid == 32) S.base_cand = dsmem_atom_add(dsmem_map(smem_u32(&S.gctr_cand), 0), cr.my_cand);
     __syncthreads();
     const int bstar = cr.bin;
+    // The candidates go to rank 0's ring, idle from now on: its first stage holds CAP of them
+    // (scores, then indices), the whole ring up to nst * RING_CAND when rank 0 reads nothing again.
+    // A rank 0 that must read its share again in this collect does so from global memory.
     const bool big = cr.m > uint32_t(CAP);
-    const uint32_t ring_cap = uint32_t(nst) * RING_CAND;  // scores first, then their indices
-    float* const cand_v = big ? reinterpret_cast<float*>(&ring[0][0]) : S.cand_v;
-    int32_t* const cand_j = big ? reinterpret_cast<int32_t*>(&ring[0][0]) + ring_cap : S.cand_j;
+    const uint32_t ring_cap = uint32_t(nst) * RING_CAND;
     const uint32_t cand_cap = big ? ring_cap : uint32_t(CAP);
+    float* const cand_v = reinterpret_cast<float*>(&ring[0][0]);
+    int32_t* const cand_j = reinterpret_cast<int32_t*>(&ring[0][0]) + cand_cap;
     const uint32_t rv = dsmem_map(smem_u32(cand_v), 0);
     const uint32_t rj = dsmem_map(smem_u32(cand_j), 0);
     auto place = [&](float e, int32_t jw, bool valid) {  // warp-collective
@@ -1334,12 +1420,14 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       }
       __syncthreads();
       const float tb = S.vthr;  // scores >= tb are exactly those in bins >= b*
-      stream_pass(false, [&](uint32_t slot, int32_t c0) {
-        each_lane(slot, c0, [&](float e, int32_t g, bool valid, int l) {
-          const bool hit = valid && e >= tb && e >= cthr;
-          if (__any_sync(FULL_MASK, hit)) place(e, 4 * g + l - lead, hit);
-        });
-      });
+      auto visit = [&](float e, int32_t g, bool valid, int l) {
+        const bool hit = valid && e >= tb && e >= cthr;
+        if (__any_sync(FULL_MASK, hit)) place(e, 4 * g + l - lead, hit);
+      };
+      if (rank == 0)
+        global_pass(visit);  // rank 0's ring receives the candidates
+      else
+        stream_pass(false, [&](uint32_t slot, int32_t c0) { each_lane(slot, c0, visit); });
       report_timeout();
     }
     csync();  // every candidate has landed in rank 0's buffer
@@ -1380,13 +1468,13 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
           if (pr) atomicAdd(&digit_hist(S, 0)[(key >> shift) & 255u], 1u);
         }
         __syncthreads();
-        digit_cross<T>(S, 0, rank, 1, rneed);
-        const uint32_t d = S.dsel, ab = S.dabove, cnt = S.dcnt;
-        prefix |= d << shift;
+        // the digit where rneed is reached, from this CTA's own counts (plain shared loads)
+        const DigitCross dc = digit_scan<T>(S, digit_hist(S, 0), digit_hist(S, 0), rneed);
+        prefix |= dc.digit << shift;
         pmask |= 0xFFu << shift;
-        rneed -= ab;
+        rneed -= dc.above;
         __syncthreads();
-        if (cnt == rneed) {
+        if (dc.cnt == rneed) {
           ge = true;
           break;
         }
@@ -1557,10 +1645,16 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   struct Sel {
     uint32_t prefix, pmask, need, my_above, my_at;
     bool ge;
+    bool first_eq;  // the first pass found every admitted key equal (all of them are tau)
   };
   int rpass = 0;  // digit-total buffers alternate over the passes of every selection
-  auto radix_select = [&](auto&& sel, uint32_t need0, uint32_t prefix0, uint32_t pmask0, int shift0) -> Sel {
-    Sel r{prefix0, pmask0, need0, 0u, 0u, false};
+  // record: the first pass also keeps the window indices of up to REC_CAP admitted scores of this
+  // CTA (in the idle list area), so that a tie class found in that pass needs no emission read.
+  int32_t* const rec = reinterpret_cast<int32_t*>(&S.list_v[0]);  // the whole list area: REC_CAP int32
+  auto radix_select = [&](auto&& sel, uint32_t need0, uint32_t prefix0, uint32_t pmask0, int shift0,
+                          bool record) -> Sel {
+    Sel r{prefix0, pmask0, need0, 0u, 0u, false, false};
+    if (tid == 0) S.rec_n = 0;
     for (int shift = shift0; shift >= 0; shift -= 8) {
       const int buf = rpass++ & 1;
       for (int i = tid; i < 256; i += T) dloc[i] = 0;
@@ -1591,6 +1685,26 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
             dmin = min(dmin, d);
             dmax = max(dmax, d);
           }
+        }
+        if (record && shift == shift0 && S.rec_n < REC_CAP) {  // warp-uniform
+          const uint32_t nm = __popc(pm);
+          const unsigned lt = lanemask_lt();
+          uint32_t excl = 0, wtot = 0;
+#pragma unroll
+          for (int b = 0; (1 << b) <= N; ++b) {
+            const unsigned m = __ballot_sync(FULL_MASK, (nm >> b) & 1u);
+            excl += uint32_t(__popc(m & lt)) << b;
+            wtot += uint32_t(__popc(m)) << b;
+          }
+          uint32_t base = 0;
+          if (lane == 0 && wtot) base = atomicAdd(&S.rec_n, wtot);
+          uint32_t at = __shfl_sync(FULL_MASK, base, 0) + excl;
+#pragma unroll
+          for (int j = 0; j < N; ++j)
+            if ((pm >> j) & 1u) {
+              if (at < REC_CAP) rec[at] = jw[j];
+              ++at;
+            }
         }
         dmin = __reduce_min_sync(FULL_MASK, dmin);
         dmax = __reduce_max_sync(FULL_MASK, dmax);
@@ -1675,6 +1789,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
         r.prefix = kmin_all;
         r.pmask = 0xffffffffu;
         r.my_at = dc.my_all;
+        r.first_eq = shift == shift0;
         break;
       }
       r.prefix |= dc.digit << shift;
@@ -1695,7 +1810,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   const Sel t = radix_select([&](float e, int32_t, uint32_t& key) {
     key = order_key(e);
     return key_class(key) == 0;
-  }, seeded ? uint32_t(k) - cr.above : uint32_t(k), tau_prefix, tau_mask, tau_shift);
+  }, seeded ? uint32_t(k) - cr.above : uint32_t(k), tau_prefix, tau_mask, tau_shift, !from_lists);
   const uint32_t prefix = t.prefix, pmask = t.pmask;
   const bool ge = t.ge;
   const uint32_t my_win = (seeded ? cr.my_above : 0u) + t.my_above;  // this CTA's scores above tau
@@ -1713,7 +1828,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       key = ~uint32_t(jw);
       const uint32_t kv = order_key(e);
       return key_class(kv) == 0 && kv == prefix;
-    }, nties, fixed, fixed, 8 * (digits - 1));
+    }, nties, fixed, fixed, 8 * (digits - 1), false);
   }
   auto index_selected = [&](int32_t jw) -> bool {
     const uint32_t key = ~uint32_t(jw);
@@ -1745,7 +1860,16 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       if (outv) outv[tie_base + tbase + ts] = e;
     }
   };
-  if (my_win > 0 || my_ties > 0) {
+  // A tie class found by the first digit pass, with nothing above it in this CTA: the tie slots
+  // come from the indices that pass recorded, without another read of the share.
+  const uint32_t recorded = min(S.rec_n, REC_CAP);
+  if (t.first_eq && !from_lists && !by_index && my_win == 0 && my_ties > 0 && my_ties <= recorded) {
+    for (uint32_t i = tid; i < my_ties; i += T) {
+      const int32_t jw = rec[i];
+      out[tie_base + tbase + i] = jw;
+      if (outv) outv[tie_base + tbase + i] = __ldg(rowp + a + uint32_t(jw));
+    }
+  } else if (my_win > 0 || my_ties > 0) {
     if (from_lists) {
       each_listed([&](float e, int32_t jw, bool in) { emit(e, jw, in); });
     } else {

@@ -36,12 +36,14 @@
 
 namespace gvr {
 
-constexpr int SPLIT_NST = 4;                 // ring stages (4 KB each) per CTA
-constexpr int SPLIT_CTAS_PER_SM = 8;         // occupancy the launch bound and shared memory allow
+constexpr int SPLIT_NST = 6;                 // ring stages (4 KB each) per CTA
+constexpr int SPLIT_CTAS_PER_SM = 6;         // occupancy the launch bound and shared memory allow
 constexpr int SPLIT_UNIT_CAP = 4096;         // scores one chunk can publish
 constexpr int32_t SPLIT_MIN_CHUNK_VEC = 1024;  // 4096 scores: the smallest chunk
 constexpr int SPLIT_MAX_ROWS = 512;          // rows a split launch can schedule
-constexpr uint32_t SPLIT_RING_CAND = SPLIT_NST * STAGE_VEC * 16 / 8;  // (score, index) pairs the ring holds
+constexpr int SPLIT_MAX_UNITS_ROW = 256;     // chunks of one row the last CTA gathers in shared memory
+constexpr int SPLIT_STASH = 4096;            // published (score, index) pairs it gathers at most
+constexpr int FB = 256;                      // bins of the last CTA's histogram of the gathered scores
 constexpr int PATH_SPLIT = 7;                // row_stats: selected from the published scores
 constexpr int PATH_SPLIT_ALONE = 8;          // row_stats: the last CTA selected the row alone
 
@@ -69,14 +71,9 @@ struct SplitParams {
 };
 
 struct alignas(16) SplitSmem {
-  uint32_t hist[NB + 4];  // the samples' histogram (floor)
-  union {
-    uint32_t tot[NB + 4];  // the last CTA: histogram of the row's published scores
-    struct {               // the schedule: every row's window
-      uint32_t nv[SPLIT_MAX_ROWS];
-      uint32_t a[SPLIT_MAX_ROWS];
-    } rows;
-  };
+  uint32_t fh[FB + 4];                    // the last CTA: histogram / digit counts of the gathered scores
+  uint32_t cnt[SPLIT_MAX_UNITS_ROW];      // the last CTA: each chunk's published count
+  uint32_t off[SPLIT_MAX_UNITS_ROW + 1];  // ... and its first slot in the gathered arrays
   uint32_t wsum[2][8];
   float wmin[8], wmax[8];
   Crossing cross;
@@ -90,16 +87,32 @@ struct alignas(16) SplitSmem {
   int32_t sched[7];                  // row, chunk, chunks of the row, first chunk, all chunks, a, nv
   uint32_t is_last;
   uint32_t tout;
+  uint32_t gather_n;                 // the last CTA: gathered slots (chunks padded to 4 entries)
+  float gvmin, gvmax;                // the last CTA: range of the gathered scores
   float4 tail;
   uint64_t bar[SPLIT_NST];
+  uint64_t fbar;                     // the last CTA: the gathering copies have landed
+  // Last members: hist, tot and the ring after them form one contiguous area, which the last
+  // CTA reuses to gather the row's published pairs (values first, then indices).
+  alignas(16) uint32_t hist[NB + 4];  // the samples' histogram (floor)
+  union {
+    uint32_t tot[NB + 4];  // (space: part of the last CTA's gathering area)
+    struct {               // the schedule: every row's window
+      uint32_t nv[SPLIT_MAX_ROWS];
+      uint32_t a[SPLIT_MAX_ROWS];
+    } rows;
+  };
 };
 static_assert(offsetof(SplitSmem, hist) % 16 == 0 && offsetof(SplitSmem, tot) % 16 == 0,
               "histograms are read as 16-byte vectors");
-static_assert(offsetof(SplitSmem, bar) % 8 == 0, "mbarriers must be 8-byte aligned");
+static_assert(offsetof(SplitSmem, bar) % 8 == 0 && offsetof(SplitSmem, fbar) % 8 == 0,
+              "mbarriers must be 8-byte aligned");
 static_assert(2 * SPLIT_MAX_ROWS <= NB + 4, "the schedule fits the histogram it shares memory with");
 
 constexpr int SPLIT_SMEM_FIXED = int((sizeof(SplitSmem) + 127) / 128 * 128);
 __host__ __device__ constexpr int split_smem_bytes() { return SPLIT_SMEM_FIXED + SPLIT_NST * STAGE_VEC * 16; }
+static_assert(split_smem_bytes() - int(offsetof(SplitSmem, hist)) >= 8 * SPLIT_STASH,
+              "hist, tot and the ring hold the gathered pairs");
 
 // Window [a, a + nv) of row r (the same geometry as the cluster kernel's head) from its inputs:
 // decode x = kv_lens[r / next_n]; prefill x = row_starts[r], y = row_ends[r].
@@ -149,6 +162,7 @@ __global__ void __launch_bounds__(THREADS, SPLIT_CTAS_PER_SM) gvr_split_kernel(c
   if (tid == 0) {
 #pragma unroll
     for (int s = 0; s < SPLIT_NST; ++s) mbar_init(&S.bar[s], 1);
+    mbar_init(&S.fbar, 1);
     mbar_init_fence();
   }
 
@@ -327,6 +341,12 @@ __global__ void __launch_bounds__(THREADS, SPLIT_CTAS_PER_SM) gvr_split_kernel(c
   }
   gmin = __fadd_rn(gmin, 0.0f);  // -0 -> +0
   const bool bracket_ok = isfinite(gmin) && isfinite(gmax) && gmin < gmax;
+  // The samples have landed (every thread is past the barrier above): ask L2 for the rest of
+  // the chunk beyond the ring's first stages, so the refills later find it there.
+  if (tid == 0 && nst > SPLIT_NST) {
+    const int32_t c0 = v0 + SPLIT_NST * STAGE_VEC, c1 = min(v1, ffull);
+    if (c1 > c0) bulk_prefetch_l2(base + 4 * size_t(c0), uint32_t(c1 - c0) * 16u);
+  }
   // The sampled floor, as in the cluster kernel: the lower edge of the bin where
   // mu + 3 sqrt(mu) + 6 samples are reached (mu = k nsamp / nv, the samples expected above
   // tau), with the bins ending lower when a few far samples stretch them.
@@ -475,137 +495,235 @@ __global__ void __launch_bounds__(THREADS, SPLIT_CTAS_PER_SM) gvr_split_kernel(c
   __syncthreads();
   if (!S.is_last) return;
 
-  // The row's published scores: chunk u of the row holds min(n_u, cap) pairs.
+  // ------------------------------------------------------------ gather the row's published pairs
+  // Chunk q of the row published min(n_q, cap) pairs.  The last CTA copies them into its shared
+  // memory (hist, tot and the idle ring: values first, then indices) with bulk copies, each
+  // chunk at a 4-entry boundary (its last slots padded and marked with index -1).
+  float* const gv = reinterpret_cast<float*>(&S.hist[0]);
+  int32_t* const gj = reinterpret_cast<int32_t*>(&S.hist[0]) + SPLIT_STASH;
   if (tid == 0) {
     S.red_n = 0;
     S.red_over = 0;
-    S.ctr_win = S.ctr_cand = S.ctr_rwin = S.ctr_rtie = 0;
+    S.ctr_win = S.ctr_cand = 0;  // slot counters of the lone path
   }
-  for (int i = tid; i < NB + 4; i += T) S.tot[i] = 0;
-  // The chunks' counts, kept in the samples' histogram (no longer needed) for the walks below.
-  uint32_t* const cnt = S.hist;
-  constexpr int CNT_CACHE = NB + 4;
   __syncthreads();
-  for (int32_t q = tid; q < nunits; q += T) {
-    const uint32_t n = __ldcg(p.surv_n + unit0 + q);
-    if (q < CNT_CACHE) cnt[q] = n;
-    atomicAdd(&S.red_n, n < uint32_t(SPLIT_UNIT_CAP) ? n : uint32_t(SPLIT_UNIT_CAP));
-    if (n > uint32_t(SPLIT_UNIT_CAP)) atomicOr(&S.red_over, n == 0xffffffffu ? 2u : 1u);
+  const bool gatherable = nunits <= SPLIT_MAX_UNITS_ROW;
+  if (gatherable) {
+    for (int32_t q = tid; q < nunits; q += T) {
+      const uint32_t n = __ldcg(p.surv_n + unit0 + q);
+      S.cnt[q] = n;
+      atomicAdd(&S.red_n, n < uint32_t(SPLIT_UNIT_CAP) ? n : uint32_t(SPLIT_UNIT_CAP));
+      if (n > uint32_t(SPLIT_UNIT_CAP)) atomicOr(&S.red_over, n == 0xffffffffu ? 2u : 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {  // slots: each chunk's count rounded up to 4, in chunk order
+      uint32_t run = 0;
+      for (int32_t q0 = 0; q0 < nunits; q0 += 32) {
+        const int32_t q = q0 + lane;
+        const uint32_t n = q < nunits ? min(S.cnt[q], uint32_t(SPLIT_UNIT_CAP)) : 0u;
+        const uint32_t r4 = (n + 3u) & ~3u;
+        uint32_t incl = r4;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t x = __shfl_up_sync(FULL_MASK, incl, o);
+          if (lane >= o) incl += x;
+        }
+        if (q < nunits) S.off[q] = run + incl - r4;
+        run += __shfl_sync(FULL_MASK, incl, 31);
+      }
+      if (lane == 0) {
+        S.off[nunits] = run;
+        S.gather_n = run;
+      }
+    }
+  } else if (tid == 0) {
+    S.red_over = 1;  // more chunks than the last CTA gathers: the row is selected alone
   }
   __syncthreads();
   const uint32_t total = S.red_n;
   const bool failed = (S.red_over & 2u) != 0;
-  bool ok = !failed && !alone && bracket_ok && S.red_over == 0 && total >= uint32_t(k);
-  // Walk every published pair of the row: f(value, window index), warp-collective with a
-  // CTA-uniform trip count per chunk (warp w takes chunks w, w + NW, ...).  Each lane has eight
-  // pairs in flight at a time, so a chunk of up to 256 pairs costs one round trip to L2.
-  constexpr int PB = 8;
-  auto each_published = [&](auto&& f) {
-    for (int32_t q = warp; q < nunits; q += NW) {
-      const uint32_t uq = unit0 + uint32_t(q);
-      const uint32_t n = min(q < CNT_CACHE ? cnt[q] : __ldcg(p.surv_n + uq), uint32_t(SPLIT_UNIT_CAP));
-      const float* pv = p.surv_v + size_t(uq) * SPLIT_UNIT_CAP;
-      const int32_t* pj = p.surv_j + size_t(uq) * SPLIT_UNIT_CAP;
-      for (uint32_t b0 = 0; b0 < n; b0 += 32 * PB) {
-        float v[PB];
-        int32_t j[PB];
-#pragma unroll
-        for (int e = 0; e < PB; ++e) {
-          const uint32_t i = b0 + uint32_t(32 * e + lane);
-          v[e] = i < n ? __ldcg(pv + i) : 0.f;
-          j[e] = i < n ? __ldcg(pj + i) : 0;
+  const uint32_t gn = gatherable ? S.gather_n : 0u;
+  bool ok = !failed && !alone && S.red_over == 0 && total >= uint32_t(k) && gn <= uint32_t(SPLIT_STASH);
+  if (ok) {
+    if (warp == 0) {
+      if (lane == 0) {
+        fence_proxy_async_global();  // the pairs were published by other CTAs' plain stores
+        mbar_arrive_expect_tx(&S.fbar, gn * 8u);
+      }
+      __syncwarp();
+      for (int32_t q = lane; q < nunits; q += 32) {
+        const uint32_t o = S.off[q], b = (S.off[q + 1] - o) * 4u;
+        if (b) {
+          const size_t src = size_t(unit0 + uint32_t(q)) * SPLIT_UNIT_CAP;
+          fence_proxy_async_global();
+          bulk_copy_g2s(gv + o, p.surv_v + src, b, &S.fbar);
+          bulk_copy_g2s(gj + o, p.surv_j + src, b, &S.fbar);
         }
-#pragma unroll
-        for (int e = 0; e < PB; ++e) f(v[e], j[e], b0 + uint32_t(32 * e + lane) < n);
       }
     }
-  };
+    if (!mbar_wait_bounded(&S.fbar, 0u, WAIT_LIMIT_NS)) {
+      mbar_wait_bounded(&S.fbar, 0u, WAIT_LIMIT_NS);  // let copies land
+      late = true;
+    }
+    if (__syncthreads_or(late)) ok = false;
+  }
+  const bool gave_up = late;
   Crossing cr{};
   if (ok) {
-    each_published([&](float v, int32_t, bool in) {
-      if (in) atomicAdd(&S.tot[value_bin(v, gmin, sc)], 1u);
-    });
+    for (int32_t q = tid; q < nunits; q += T)  // mark the padding slots
+      for (uint32_t e = S.off[q] + min(S.cnt[q], uint32_t(SPLIT_UNIT_CAP)); e < S.off[q + 1]; ++e) gj[e] = -1;
     __syncthreads();
-    cr = scan_crossing<T>(S, uint32_t(k));
-    ok = cr.m <= SPLIT_RING_CAND;  // the crossing bin's members fit the idle ring
-  }
-  if (ok) {
-    // ------------------------------------------------------------ collect + refine
-    const int bstar = cr.bin;
-    float* const cand_v = reinterpret_cast<float*>(&ring[0][0]);
-    int32_t* const cand_j = reinterpret_cast<int32_t*>(&ring[0][0]) + SPLIT_RING_CAND;
-    each_published([&](float e, int32_t jw, bool in) {
-      const int b = in ? value_bin(e, gmin, sc) : -1;
-      const uint32_t ws = warp_alloc_local(&S.ctr_win, b > bstar);
-      if (b > bstar && ws < uint32_t(k)) {  // always below k: counts match the histogram's
-        out[ws] = jw;
-        if (outv) outv[ws] = e;
+    // ---------------------------------------------------------- verify: histogram, crossing bin
+    // FB bins over the gathered scores' own range [vmin, vmax] (monotone bin function).
+    float lo = INFINITY, hi = -INFINITY;
+    for (uint32_t e = tid; e < gn; e += T)
+      if (gj[e] >= 0) {
+        lo = fminf(lo, gv[e]);
+        hi = fmaxf(hi, gv[e]);
       }
-      const uint32_t cs = warp_alloc_local(&S.ctr_cand, b == bstar);
-      if (b == bstar && cs < SPLIT_RING_CAND) {
-        cand_v[cs] = e;
-        cand_j[cs] = jw;
-      }
-    });
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = fminf(lo, __shfl_xor_sync(FULL_MASK, lo, o));
+      hi = fmaxf(hi, __shfl_xor_sync(FULL_MASK, hi, o));
+    }
+    if (lane == 0) {
+      S.wmin[warp] = lo;
+      S.wmax[warp] = hi;
+    }
+    for (int i = tid; i < FB; i += T) S.fh[i] = 0;
     __syncthreads();
-    const uint32_t need = uint32_t(k) - cr.above;
-    const uint32_t mm = cr.m;
-    if (mm <= uint32_t(RANK_REFINE_MAX)) {
-      // rank of candidate i = candidates ordered before it by (value desc, index asc)
-      for (uint32_t i = tid; i < mm; i += T) {
-        const float v = cand_v[i];
-        const int32_t j = cand_j[i];
-        uint32_t r = 0;
-        for (uint32_t q = 0; q < mm; ++q) {
-          const float w = cand_v[q];
-          r += (w > v) || (w == v && cand_j[q] < j);
-        }
-        if (r < need) {
-          out[cr.above + r] = j;
-          if (outv) outv[cr.above + r] = v;
+    lo = INFINITY;
+    hi = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      lo = fminf(lo, S.wmin[w]);
+      hi = fmaxf(hi, S.wmax[w]);
+    }
+    // NaN never reaches the floor; a range that is not finite (+inf / -inf scores) or empty puts
+    // every score in bin 0, where the radix selection below decides them exactly
+    const float fsc = (isfinite(lo) && isfinite(hi) && hi > lo) ? __fdiv_rn(float(FB), __fsub_rn(hi, lo)) : 0.f;
+    auto fbin = [&](float v) -> uint32_t {
+      float x = __fmul_rn(__fsub_rn(v, lo), fsc);
+      x = fminf(fmaxf(x, 0.0f), float(FB - 1));
+      return uint32_t(__float2int_rz(x));
+    };
+    for (uint32_t e = tid; e < gn; e += T)
+      if (gj[e] >= 0) atomicAdd(&S.fh[fbin(gv[e])], 1u);
+    __syncthreads();
+    const DigitCross fc = digit_scan<T>(S, S.fh, S.fh, uint32_t(k));
+    cr.bin = int32_t(fc.digit);
+    cr.above = fc.above;
+    cr.m = fc.cnt;
+    __syncthreads();
+    // ---------------------------------------------------------- refine: radix select in the bin
+    // The need = k - above largest order keys among the crossing bin's members, 8 bits a pass,
+    // stopping once the keys above the chosen digit are exactly the ones needed or every
+    // remaining key is equal.
+    const uint32_t bstar = fc.digit;
+    uint32_t prefix = 0, pmask = 0, rneed = uint32_t(k) - cr.above;
+    bool ge = false;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = tid; i < 256; i += T) S.fh[i] = 0;
+      if (tid == 0) {
+        S.kmin_loc = 0xffffffffu;
+        S.kmax_loc = 0u;
+      }
+      __syncthreads();
+      uint32_t tmin = 0xffffffffu, tmax = 0u;
+      for (uint32_t e = tid; e < gn; e += T) {
+        if (gj[e] < 0) continue;
+        const float v = gv[e];
+        const uint32_t key = order_key(v);
+        if (fbin(v) == bstar && (key & pmask) == prefix) {
+          atomicAdd(&S.fh[(key >> shift) & 255u], 1u);
+          tmin = min(tmin, key);
+          tmax = max(tmax, key);
         }
       }
-    } else {
-      // radix select of the need largest order keys among the candidates, 8 bits per pass
-      uint32_t prefix = 0, pmask = 0, rneed = need;
-      bool ge = false;
-      uint32_t* const dh = S.tot;  // the published scores' histogram is no longer needed
-      for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 256; i += T) dh[i] = 0;
-        __syncthreads();
-        for (uint32_t i = tid; i < mm; i += T) {
-          const uint32_t key = order_key(cand_v[i]);
-          if ((key & pmask) == prefix) atomicAdd(&dh[(key >> shift) & 255u], 1u);
-        }
-        __syncthreads();
-        const DigitCross dc = digit_scan<T>(S, dh, dh, rneed);  // the digit where rneed is reached
-        __syncthreads();
-        prefix |= dc.digit << shift;
-        pmask |= 0xFFu << shift;
-        rneed -= dc.above;
-        if (dc.cnt == rneed) {
-          ge = true;
-          break;
-        }
+      tmin = __reduce_min_sync(FULL_MASK, tmin);
+      tmax = __reduce_max_sync(FULL_MASK, tmax);
+      if (lane == 0) {
+        atomicMin(&S.kmin_loc, tmin);
+        atomicMax(&S.kmax_loc, tmax);
       }
-      const uint32_t nties = ge ? 0u : rneed;
-      const uint32_t win_base = cr.above, tie_base = cr.above + (need - nties);
-      for (uint32_t b0 = 0; b0 < mm; b0 += T) {
-        const uint32_t i = b0 + tid;
-        const bool in = i < mm;
-        const uint32_t key = in ? order_key(cand_v[i]) : 0u;
-        const bool win = in && (ge ? (key & pmask) >= prefix : key > prefix);
-        const bool tie = in && !ge && key == prefix;
-        const uint32_t ws = warp_alloc_local(&S.ctr_rwin, win);
-        if (win && win_base + ws < tie_base) {
-          out[win_base + ws] = cand_j[i];
-          if (outv) outv[win_base + ws] = cand_v[i];
+      __syncthreads();
+      if (S.kmin_loc == S.kmax_loc) {  // every remaining key is the same: ties
+        prefix = S.kmin_loc;
+        pmask = 0xffffffffu;
+        __syncthreads();
+        break;
+      }
+      const DigitCross dc = digit_scan<T>(S, S.fh, S.fh, rneed);
+      __syncthreads();
+      prefix |= dc.digit << shift;
+      pmask |= 0xFFu << shift;
+      rneed -= dc.above;
+      if (dc.cnt == rneed) {
+        ge = true;
+        break;
+      }
+    }
+    // ---------------------------------------------------------- emit
+    // Winners (bins above the crossing bin, or its keys above tau) and the first nties ties, each
+    // thread's own in turn, at offsets from block-wide prefix sums (no per-score atomics).
+    const uint32_t nties = ge ? 0u : rneed;
+    const uint32_t tie_base = uint32_t(k) - nties;
+    auto classify = [&](uint32_t e, bool& win, bool& tie) {
+      win = tie = false;
+      if (gj[e] < 0) return;
+      const float v = gv[e];
+      const uint32_t b = fbin(v);
+      if (b > bstar) {
+        win = true;
+      } else if (b == bstar) {
+        const uint32_t key = order_key(v);
+        win = ge ? (key & pmask) >= prefix : key > prefix;
+        tie = !ge && key == prefix;
+      }
+    };
+    uint32_t nw = 0, nt = 0;
+    for (uint32_t e = tid; e < gn; e += T) {
+      bool win, tie;
+      classify(e, win, tie);
+      nw += win;
+      nt += tie;
+    }
+    uint32_t iw = nw, it = nt;  // inclusive warp scans, then warp offsets
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t a = __shfl_up_sync(FULL_MASK, iw, o), b = __shfl_up_sync(FULL_MASK, it, o);
+      if (lane >= o) {
+        iw += a;
+        it += b;
+      }
+    }
+    if (lane == 31) {
+      S.wsum[0][warp] = iw;
+      S.wsum[1][warp] = it;
+    }
+    __syncthreads();
+    uint32_t ws = iw - nw, ts = it - nt;
+#pragma unroll
+    for (int w = 0; w < NW; ++w)
+      if (w < warp) {
+        ws += S.wsum[0][w];
+        ts += S.wsum[1][w];
+      }
+    for (uint32_t e = tid; e < gn; e += T) {
+      bool win, tie;
+      classify(e, win, tie);
+      if (win) {
+        if (ws < tie_base) {  // always: the winners are exactly k - nties
+          out[ws] = gj[e];
+          if (outv) outv[ws] = gv[e];
         }
-        const uint32_t ts = warp_alloc_local(&S.ctr_rtie, tie);
-        if (tie && ts < nties) {
-          out[tie_base + ts] = cand_j[i];
-          if (outv) outv[tie_base + ts] = cand_v[i];
+        ++ws;
+      } else if (tie) {
+        if (ts < nties) {
+          out[tie_base + ts] = gj[e];
+          if (outv) outv[tie_base + ts] = gv[e];
         }
+        ++ts;
       }
     }
     if (p.row_stats && tid == 0) {
@@ -617,7 +735,7 @@ __global__ void __launch_bounds__(THREADS, SPLIT_CTAS_PER_SM) gvr_split_kernel(c
     }
     return;
   }
-  if (failed) {
+  if (failed || gave_up) {
     for (int i = tid; i < k; i += T) out[i] = -2;
     if (p.row_stats && tid == 0) {
       int32_t* st = p.row_stats + 4 * int64_t(row);

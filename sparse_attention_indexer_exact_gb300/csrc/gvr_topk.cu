@@ -13,6 +13,7 @@
 #include <mutex>
 
 #include "gvr_kernel.cuh"
+#include "gvr_short.cuh"
 #include "gvr_split.cuh"
 #include "gvr_topk.h"
 
@@ -104,10 +105,11 @@ gvr_status check_common(int64_t row_stride, int64_t num_rows, int32_t k, const g
       return GVR_ERR_ARG;
     if (o->flags & ~(GVR_FLAG_FORCE_RESCUE | GVR_FLAG_NO_FLOOR | GVR_FLAG_ZERO_CAP | GVR_FLAG_RADIX_REFINE |
                      GVR_FLAG_DETERMINISTIC | GVR_FLAG_SORTED | GVR_FLAG_STREAM_RESCUE | GVR_FLAG_COMPACT_LISTS |
-                     GVR_FLAG_CLUSTER_KERNEL | GVR_FLAG_SPLIT_ALONE | GVR_FLAG_SPLIT_KERNEL))
+                     GVR_FLAG_CLUSTER_KERNEL | GVR_FLAG_SPLIT_ALONE | GVR_FLAG_SPLIT_KERNEL |
+                     GVR_FLAG_DIAG_FAIL_ROW0 | GVR_FLAG_SHORT_KERNEL))
       return GVR_ERR_ARG;
-    if (!ws && (o->flags & (GVR_FLAG_CLUSTER_KERNEL | GVR_FLAG_SPLIT_ALONE | GVR_FLAG_SPLIT_KERNEL)))
-      return GVR_ERR_ARG;
+    if (!ws && (o->flags & (GVR_FLAG_SPLIT_ALONE | GVR_FLAG_SPLIT_KERNEL))) return GVR_ERR_ARG;
+    if ((o->flags & GVR_FLAG_SHORT_KERNEL) && (o->flags & GVR_FLAG_CLUSTER_KERNEL)) return GVR_ERR_ARG;
   }
   return GVR_OK;
 }
@@ -191,10 +193,13 @@ Geometry plan_geometry(int64_t row_stride, int64_t num_rows, int32_t k, int sms,
   } else {
     const int64_t stages_per_cta = ((need_vec + gvr::STAGE_VEC - 1) / gvr::STAGE_VEC + g.cs - 1) / g.cs;
     const int64_t ctas = num_rows * g.cs;
+    const int per_sm_min = ctas_per_sm(gvr::MIN_STAGES, smem_per_sm, smem_reserved);
     for (int d = gvr::MAX_STAGES; d > gvr::MIN_STAGES; --d) {
       if (d > stages_per_cta) continue;
-      // clusters pack into GPCs, so leave a tenth of the slots as margin
-      if (ctas * 10 <= int64_t(sms) * ctas_per_sm(d, smem_per_sm, smem_reserved) * 9) {
+      // a deeper ring that keeps the occupancy of the shallowest one costs nothing; otherwise,
+      // as clusters pack into GPCs, leave a tenth of the slots as margin
+      const int per_sm = ctas_per_sm(d, smem_per_sm, smem_reserved);
+      if (per_sm >= per_sm_min || ctas * 10 <= int64_t(sms) * per_sm * 9) {
         g.nstage = d;
         break;
       }
@@ -203,9 +208,47 @@ Geometry plan_geometry(int64_t row_stride, int64_t num_rows, int32_t k, int sms,
   return g;
 }
 
+// The short-row kernel takes a plain call (no extended mode, no diagnostics, no cluster tuning)
+// whose rows fit its shared memory; GVR_FLAG_SHORT_KERNEL asks for it, GVR_FLAG_CLUSTER_KERNEL
+// keeps the cluster kernel.
+bool use_short(const gvr::Params& prm, const gvr_options* o) {
+  if (prm.row_stride > gvr::SHORT_MAX || prm.pre_idx || prm.block_max) return false;
+  const int32_t flags = o ? o->flags : 0;
+  if (flags != GVR_FLAG_SHORT_KERNEL) return false;  // opt-in: measured slower than the cluster kernel
+  if (o && (o->cluster_size || o->ring_stages)) return false;
+  return true;
+}
+
+gvr_status launch_short(const gvr::Params& prm, int64_t num_rows, void* stream) {
+  if (num_rows > 0x7fffffffLL) return GVR_ERR_ARG;
+  gvr::ShortParams q = {};
+  q.logits = prm.logits;
+  q.row_stride = prm.row_stride;
+  q.kv_lens = prm.kv_lens;
+  q.row_starts = prm.row_starts;
+  q.row_ends = prm.row_ends;
+  q.indices = prm.indices;
+  q.values = prm.values;
+  q.row_stats = prm.row_stats;
+  q.next_n = prm.next_n;
+  q.compress_ratio = prm.compress_ratio;
+  q.k = prm.k;
+  q.mode = prm.mode;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(num_rows), 1, 1);
+  cfg.blockDim = dim3(gvr::SHORT_THREADS, 1, 1);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  const int vpt = gvr::short_vpt(prm.row_stride);
+  const cudaError_t e = vpt == 4   ? cudaLaunchKernelEx(&cfg, gvr::gvr_short_kernel<4>, q)
+                        : vpt == 8 ? cudaLaunchKernelEx(&cfg, gvr::gvr_short_kernel<8>, q)
+                                   : cudaLaunchKernelEx(&cfg, gvr::gvr_short_kernel<16>, q);
+  return e == cudaSuccess ? GVR_OK : GVR_ERR_LAUNCH;
+}
+
 gvr_status launch(const gvr::Params& prm, int64_t num_rows, const gvr_options* o, void* stream) {
   int sms = 0, smem_per_sm = 0, smem_reserved = 0;
   if (device_state(&sms, &smem_per_sm, &smem_reserved) != cudaSuccess) return GVR_ERR_LAUNCH;
+  if (use_short(prm, o)) return launch_short(prm, num_rows, stream);
   Geometry geo = plan_geometry(prm.row_stride, num_rows, prm.k, sms, smem_per_sm, smem_reserved, o);
   if (geo.cs == 16 && !(o && o->cluster_size == 16)) {
     // A 16-CTA cluster needs 16 SMs of one GPC with room for it: checked once per ring depth,
@@ -258,6 +301,7 @@ gvr_status launch(const gvr::Params& prm, int64_t num_rows, const gvr_options* o
 
   gvr::Params q = prm;
   q.nstage = geo.nstage;
+  q.flags &= ~(GVR_FLAG_CLUSTER_KERNEL | GVR_FLAG_SHORT_KERNEL);
   // the extended instantiation only when a call uses one of its modes
   const bool ext = (q.flags & (gvr::FLAG_DETERMINISTIC | gvr::FLAG_SORTED)) || q.pre_idx || q.block_max;
   cudaError_t e;
@@ -536,7 +580,7 @@ gvr_status topk_decode_ws(const float* logits, int64_t row_stride, int64_t num_r
   const int64_t grid = split_grid(sms, smem_per_sm, smem_reserved);
   if (!use_split(num_rows, grid, options)) {
     gvr_options o = options ? *options : gvr_options{};
-    o.flags &= ~(GVR_FLAG_CLUSTER_KERNEL | kSplitFlags);
+    o.flags &= ~kSplitFlags;
     return topk_decode_ex(logits, row_stride, num_rows, kv_lens, next_n, compress_ratio, k, indices, values,
                           stream, &o);
   }
@@ -573,7 +617,7 @@ gvr_status topk_prefill_ws(const float* logits, int64_t row_stride, int64_t num_
   const int64_t grid = split_grid(sms, smem_per_sm, smem_reserved);
   if (!use_split(num_rows, grid, options)) {
     gvr_options o = options ? *options : gvr_options{};
-    o.flags &= ~(GVR_FLAG_CLUSTER_KERNEL | kSplitFlags);
+    o.flags &= ~kSplitFlags;
     return topk_prefill_ex(logits, row_stride, num_rows, row_starts, row_ends, k, indices, stream, &o);
   }
   s = check_workspace(workspace, workspace_bytes, grid);

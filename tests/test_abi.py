@@ -142,9 +142,10 @@ def test_prefill_argument_errors(lib):
 
 def test_option_errors(lib):
     import sparse_attention_indexer_exact_gb300 as gvr
-    # the kernel-choice flags (256, 512, 1024) belong to the *_ws entry points only
+    # the balanced kernel's flags (512, 1024) belong to the *_ws entry points only; the short-row
+    # and cluster kernels cannot both be forced; 8192 is no flag
     for bad in (dict(cluster_size=3), dict(cluster_size=32), dict(ring_stages=2), dict(ring_stages=17), dict(reserved=1),
-                dict(flags=256), dict(flags=512), dict(flags=1024), dict(flags=2048)):
+                dict(flags=512), dict(flags=1024), dict(flags=256 | 4096), dict(flags=8192)):
         o = gvr.Options(**bad)
         st = lib.topk_decode_ex(ALIGNED, 1024, 4, ALIGNED, 1, 1, K, ALIGNED, None, None, ctypes.byref(o))
         assert st == 5, bad
@@ -168,8 +169,12 @@ def test_plan_geometry(lib, stride, rows, k):
     assert share_vec <= max(8192, -(-(stride // 4) // 16))  # balanced shares
     assert p["threads"] == 128 and 3 <= p["ring_stages"] <= 16
     per_sm = min(7, (228 * 1024) // (p["smem_bytes"] + 1024))
-    if p["ring_stages"] > 3:  # a deeper ring only while every cluster stays resident at once
-        assert rows * cs <= 152 * per_sm
+    per_sm_min = min(7, (228 * 1024) // (gvr.plan(stride, rows, k, gvr.Options(ring_stages=3), sm_count=152)
+                                       ["smem_bytes"] + 1024))
+    if p["ring_stages"] > 3:
+        # a deeper ring only when it keeps the shallowest ring's occupancy, or while every
+        # cluster stays resident at once, and never deeper than the share
+        assert per_sm >= per_sm_min or rows * cs <= 152 * per_sm
         assert p["ring_stages"] <= -(-share_vec // 256)
 
 
@@ -211,10 +216,10 @@ def test_binding_refuses_tensors_on_different_devices():
 
 
 def test_workspace_size_for_a_device_shape(lib):
-    # The balanced kernel's workspace: per-row counters, then per chunk (8 CTAs per SM) a count
+    # The balanced kernel's workspace: per-row counters, then per chunk (6 CTAs per SM) a count
     # and 4096 published (score, index) pairs.  Sized without touching a device.
     size = ctypes.c_size_t(0)
     assert lib.gvr_workspace_size(152, ctypes.byref(size)) == 0
-    grid = 152 * 8
+    grid = 152 * 6
     assert size.value == 512 * 4 + grid * 4 + grid * 4096 * 8
     assert lib.gvr_workspace_size(152, None) == 1

@@ -106,9 +106,11 @@ def test_decode_batch_with_empty_request(gvr):
     assert_decode_exact(gvr, case)
 
 
-def test_prefill_tile_full_size(gvr):
-    st = assert_prefill_exact(gvr, workloads.prefill_tile(), stats=True)
-    assert (st[:, 0] <= 1).all(), "an ordinary N(0,1) tile should never need the rescue"
+@pytest.mark.parametrize("kernel", [0, 4096])
+def test_prefill_tile_full_size(gvr, kernel):
+    # the cluster kernel by default, the short-row kernel (stride 14848 fits it) when asked for
+    st = assert_prefill_exact(gvr, workloads.prefill_tile(), stats=True, options=gvr.Options(flags=kernel))
+    assert np.isin(st[:, 0], [0, 1, 10]).all(), "an ordinary N(0,1) tile should never need the rescue"
 
 
 @pytest.mark.parametrize("variant", workloads.ADVERSARIAL_VARIANTS)
@@ -119,6 +121,8 @@ def test_adversarial_row(gvr, variant):
         assert path == 2  # GMIN == GMAX: invalid bracket
     if variant == "two_valued":
         assert path == 3  # the top bin holds ~n/2 candidates: overflow
+    if variant == "neg_inf_tau":
+        assert path == 9  # fewer than k finite scores: decided by the first pass (-inf fill)
 
 
 @pytest.mark.parametrize("bs,n,k", [(1, 16384, 512), (4, 32768, 1024), (16, 65536, 2048), (4, 131072, 512),
@@ -234,7 +238,11 @@ def test_prefill_misaligned_neg_inf_class(gvr):
                                  np.array([r[2] for r in rows], np.int32), k)
     got, _ = run_prefill(gvr, case)
     assert got.min() >= 0
-    assert_prefill_exact(gvr, case)
+    long_rows = case.window_lengths() > k
+    st = assert_prefill_exact(gvr, case, stats=True)
+    assert (st[long_rows, 0] == 9).all(), st[:, 0]  # cluster kernel, tau = -inf: the -inf fill
+    st = assert_prefill_exact(gvr, case, stats=True, options=gvr.Options(flags=4096))
+    assert (st[long_rows, 0] == 11).all(), st[:, 0]  # short-row kernel: radix over the row
 
 
 def test_prefill_clamped_windows(gvr):
@@ -686,3 +694,88 @@ def test_binding_refuses_narrowed_views(gvr):
     ks = torch.zeros((4,), dtype=torch.int32, device=DEV)
     with pytest.raises(ValueError, match="packed"):
         gvr.topk_prefill(buf[:, :1024], ks, kv, 512)
+
+
+def test_device_error_reporting(gvr):
+    """The failure path, driven by a diagnostic flag instead of a failure: the first row's cluster
+    reports a give-up after its first pass completed; that row reads -2 with the device-error
+    path, every other row is exact."""
+    case = workloads.decode_batch(seed=61, requests=12, next_n=2, cr=4, k=1024, stride=65536,
+                                  kv_lo=8192, kv_hi=262144, boundary=False)
+    for flags in (2048, 2048 | 16, 2048 | 2):
+        got, _, st = run_decode(gvr, case, values=False, options=gvr.Options(flags=flags), stats=True)
+        assert (got[0] == -2).all() and st[0, 0] == -1, (flags, got[0][:8], st[0])
+        ref, _, _ = oracle.topk_decode(case.logits, case.kv_lens, case.next_n, case.compress_ratio, case.k)
+        wins = list(decode_windows(case.logits, case.kv_lens, case.next_n, case.compress_ratio))[1:]
+        bad, why = compare_rows(iter(wins), case.k, got, ref)  # rows 1.. (row indices kept)
+        assert bad == 0, why
+        assert (st[1:, 0] >= 0).all()
+
+
+# ----------------------------------------------------------------------------- short-row kernel
+SHORT, CLUSTER = 4096, 256
+
+
+@pytest.mark.parametrize("kernel", [SHORT, CLUSTER])
+@pytest.mark.parametrize("bs,n,k", [(1, 16384, 512), (4, 16384, 2048), (16, 16384, 1024), (256, 16384, 512),
+                                    (64, 8192, 2048), (3, 4100, 1024)])
+def test_short_stride_cells(gvr, kernel, bs, n, k):
+    """Rows that fit one CTA's registers, through the short-row kernel and the cluster
+    kernel: decode and prefill (every lead), heavy-tailed scores."""
+    st = assert_decode_exact(gvr, workloads.sweep_decode(bs, n, k), options=gvr.Options(flags=kernel), stats=True)
+    if kernel == SHORT:
+        assert np.isin(st[:, 0], [0, 10, 11]).all(), st[:, 0]
+    assert_prefill_exact(gvr, workloads.sweep_prefill(bs, n, k), options=gvr.Options(flags=kernel))
+
+
+@pytest.mark.parametrize("values", [False, True])
+def test_short_kernel_single_row(gvr, values):
+    st = assert_decode_exact(gvr, workloads.single_decode_row(), values=values, stats=True,
+                             options=gvr.Options(flags=SHORT))
+    assert st[0, 0] == 10
+    st = assert_decode_exact(gvr, workloads.single_decode_row(), values=values, stats=True)
+    assert st[0, 0] in (1, 5, 6)  # the default is the cluster kernel
+
+
+def test_short_kernel_tie_heavy_rows(gvr):
+    """Rows the histogram cannot decide take the exact radix over the row in registers:
+    one value, two values, a -inf class holding tau, a +inf class, signed zero at tau, plateaus."""
+    g = np.random.default_rng(71)
+    rows, stride, k = 9, 16384, 1024
+    lg = g.standard_normal((rows, stride)).astype(np.float32)
+    lg[1] = 2.5
+    lg[2] = np.where(g.random(stride) < 0.5, 1.0, 2.0).astype(np.float32)
+    lg[3, g.choice(stride, stride - k + 30, replace=False)] = -np.inf
+    lg[4, g.choice(stride, k - 3, replace=False)] = np.inf
+    lg[5] = -(np.abs(lg[5]) + 1)
+    z = g.choice(stride, 3 * k, replace=False)
+    lg[5, z[:k // 2]] = np.abs(lg[5, z[:k // 2]]) + 1
+    lg[5, z[k // 2:]] = np.where(np.arange(z.size - k // 2) % 2 == 0, np.float32(-0.0), np.float32(0.0))
+    lg[6] = np.round(lg[6] * 3)
+    lg[7] = np.round(lg[7] * 40) / 40
+    lg[8, g.choice(stride, 40, replace=False)] = 1e30  # far outliers stretch the bins
+    case = workloads.DecodeCase("short_ties", lg, np.full(rows, stride, np.int32), 1, 1, k)
+    for kernel in (SHORT, CLUSTER):
+        st = assert_decode_exact(gvr, case, options=gvr.Options(flags=kernel), stats=True)
+        if kernel == SHORT:
+            assert st[1, 0] == 11 and st[2, 0] == 11 and st[3, 0] == 11, st[:, 0]
+
+
+def test_short_kernel_boundaries_and_nan(gvr):
+    g = np.random.default_rng(72)
+    for k in (512, 2048):
+        ns = [0, 1, k - 1, k, k + 1, k + 2, 4097, 16384]
+        stride = 16384
+        lg = g.standard_normal((len(ns), stride)).astype(np.float32)
+        for r, n in enumerate(ns):
+            lg[r, n:] = workloads.DECODE_POISON[np.arange(n, stride) % 3]
+        assert_decode_exact(gvr, workloads.DecodeCase("short_b", lg, np.array(ns, np.int32), 1, 1, k),
+                            options=gvr.Options(flags=SHORT))
+    lg = g.standard_normal((3, 8192)).astype(np.float32)
+    lg[0, ::3] = np.nan
+    lg[1, :] = np.nan
+    lt = torch.from_numpy(lg).to(DEV)
+    idx, _ = gvr.topk_decode(lt, torch.full((3,), 8192, dtype=torch.int32, device=DEV), 1, 1, 512)
+    got = idx.cpu().numpy()
+    for r in range(3):
+        assert got[r].min() >= 0 and got[r].max() < 8192 and np.unique(got[r]).size == 512
