@@ -77,7 +77,6 @@ constexpr int RING_CAND = STAGE_VEC * 16 / 8;  // (score, index) candidates one 
 constexpr int BULK_BINS = 512;       // first-pass counts of at most this many bins go as bulk adds
 constexpr int RANK_REFINE_MAX = 256;
 constexpr uint32_t UNLISTED_RANK0 = 1u << 16;  // marks rank 0's overflowed list in the count  // m at or below: refine by pairwise ranking
-constexpr int SPARSE_MAX = 4;         // above-floor scores of a thread per stage before a warp aggregates
 constexpr int MAX_K = 2048;
 constexpr int MAX_SAMPLES = 2048;     // block64 samples per row at most (32 runs, one per lane)
 
@@ -178,6 +177,9 @@ struct alignas(16) Smem {
   uint32_t rc_win, rc_tie;         // rank 0's counters shared by the cluster in rescue
   uint32_t saved;                  // count of the partial floor bin before the second pass
   uint32_t rec_n;                  // rescue: members recorded in the first digit pass (may exceed REC_CAP)
+  uint32_t hk_min, hk_max;         // the cluster's smallest / largest order key of the first pass's
+                                   // scores >= thr (every CTA adds its own)
+  uint32_t hlisted;                // the cluster's listed first-pass scores
   uint32_t tout;                   // this CTA gave up waiting for staged data
   uint32_t err;                    // rank 0: some CTA of the cluster gave up
   uint64_t bar[MAX_STAGES];        // one mbarrier per ring stage
@@ -861,6 +863,9 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     S.tout = S.err = 0;
     S.unlisted = 0;
     S.relist_n = S.relist_bad = 0;
+    S.hk_min = S.kmin_loc = 0xffffffffu;
+    S.hk_max = S.kmax_loc = 0u;
+    S.hlisted = 0;
     S.cross = Crossing{};
     S.dsel = S.dabove = S.dcnt = 0;
   }
@@ -1104,106 +1109,102 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
         }
       }
     } else {
-      // One visit covers G stages of the ring (G = 1 here; the visitor also takes a pair, which
-      // measured no faster: the first pass is not bound by the per-visit chain it shares).
-      auto p1_visit = [&](auto g_c, const uint32_t* slots, const int32_t* c0s) {
-        constexpr int G = decltype(g_c)::value;
-        constexpr int NV = VPS * G;  // vectors per thread
-        constexpr int NE = 4 * NV;   // scores per thread
-        float4 vv[NV];
-        uint32_t lanes = 0;  // bit 4v+l: lane l of this thread's v-th vector is in the window
+      // One stage per visit, with no warp collective: a thread with scores >= thr takes list
+      // slots for them with one shared-memory atomic on its warp's counter (S.list_n[warp]) and
+      // lists them; their bins are counted once the pass is over, from the list.  A thread that
+      // finds its warp's segment full lists what still fits and from then on only counts its
+      // hits, in a register run of one bin that goes to the histogram when the bin changes (a
+      // tie class costs one atomic per thread for the whole pass).  The counter then exceeds
+      // the segment, which marks the list incomplete; the counts stay exact either way.
+      constexpr int NE = 4 * VPS;
+      bool full = false;                   // this thread saw its warp's segment full
+      uint32_t rb = 0xffffffffu, rrun = 0;  // its run of counted hits in bin rb
+      float rv = __int_as_float(0x7fffffff);  // the run's last value (NaN: none yet)
+      uint32_t hk0 = 0xffffffffu, hk1 = 0u;   // smallest / largest key of its hits
+      stream_pass(true, [&](uint32_t slot, int32_t c0) {
+        float4 vv[VPS];
+        uint32_t lanes;  // bit 4v+l: lane l of this thread's v-th vector is in the window
+        if (c0 > 0 && c0 + STAGE_VEC <= ffull) {  // an interior stage: every lane is in
 #pragma unroll
-        for (int q = 0; q < G; ++q) {
-          if (c0s[q] > 0 && c0s[q] + STAGE_VEC <= ffull) {  // an interior stage: every lane is in
+          for (int i = 0; i < VPS; ++i) vv[i] = ring[slot][i * T + tid];
+          lanes = (1u << NE) - 1u;
+        } else {
+          lanes = 0;
 #pragma unroll
-            for (int i = 0; i < VPS; ++i) vv[q * VPS + i] = ring[slots[q]][i * T + tid];
-            lanes |= ((1u << (4 * VPS)) - 1u) << (4 * VPS * q);
-          } else {
-#pragma unroll
-            for (int i = 0; i < VPS; ++i) {
-              int32_t g;
-              lanes |= stage_vec(slots[q], c0s[q], i, g, vv[q * VPS + i]) << (4 * (q * VPS + i));
-            }
+          for (int i = 0; i < VPS; ++i) {
+            int32_t g;
+            lanes |= stage_vec(slot, c0, i, g, vv[i]) << (4 * i);
           }
         }
         uint32_t bits = 0;  // bit 4v+l: lane l of this thread's v-th vector is >= thr
 #pragma unroll
-        for (int v = 0; v < NV; ++v)
+        for (int v = 0; v < VPS; ++v)
           bits |= (uint32_t(vv[v].x >= thr) | (uint32_t(vv[v].y >= thr) << 1) | (uint32_t(vv[v].z >= thr) << 2) |
                    (uint32_t(vv[v].w >= thr) << 3))
                   << (4 * v);
         bits &= lanes;
-        // The warp's exclusive prefix of hit counts from one ballot per bit of the count (the
-        // upper bits only when some thread has 4 or more hits).
-        const uint32_t nhit = __popc(bits);
-        static_assert(NE <= 16, "hit counts fit in 5 bits");
-        const unsigned lt = lanemask_lt();
-        const unsigned m0 = __ballot_sync(FULL_MASK, nhit & 1u), m1 = __ballot_sync(FULL_MASK, nhit & 2u);
-        uint32_t excl = uint32_t(__popc(m0 & lt)) + (uint32_t(__popc(m1 & lt)) << 1);
-        uint32_t wtot = uint32_t(__popc(m0)) + (uint32_t(__popc(m1)) << 1);
-        if (__any_sync(FULL_MASK, nhit >= 4u)) {
-          const unsigned m2 = __ballot_sync(FULL_MASK, nhit & 4u), m3 = __ballot_sync(FULL_MASK, nhit & 8u);
-          excl += (uint32_t(__popc(m2 & lt)) << 2) + (uint32_t(__popc(m3 & lt)) << 3);
-          wtot += (uint32_t(__popc(m2)) << 2) + (uint32_t(__popc(m3)) << 3);
-          if (NE >= 16) {
-            const unsigned m4 = __ballot_sync(FULL_MASK, nhit & 16u);
-            excl += uint32_t(__popc(m4 & lt)) << 4;
-            wtot += uint32_t(__popc(m4)) << 4;
+        if (!bits) return;
+        if (!full) {
+          const uint32_t nb = uint32_t(__popc(bits));
+          uint32_t at = atomicAdd(&S.list_n[warp], nb);
+          const bool fits = at + nb <= uint32_t(LSEG);
+          const uint32_t end = fits ? at + nb : uint32_t(LSEG);
+          for (; at < end; ++at) {  // list (all of them, or what still fits)
+            const int j = __ffs(bits) - 1;
+            bits &= bits - 1u;
+            seg_v[at] = stage_score(slot, c0, j);
+            if constexpr (L16)
+              seg_p[at] = uint16_t(list_key(c0 + tid, 0) + uint32_t(j >> 2) * (4 * T) + uint32_t(j & 3));
+            else
+              seg_j[at] = 4 * (c0 + tid) - lead + (j >> 2) * (4 * T) + (j & 3);
           }
+          if (fits) return;
+          full = true;
         }
-        if (wtot == 0) return;  // nothing of this warp reaches the floor
-        uint32_t at = wlist + excl;
-        wlist += wtot;
-        // A warp with a few hits per thread counts them one by one; a dense warp (ties, a low
-        // floor) adds its hits with one atomic when they all share a bin, else one per score.
-        const bool dense = __any_sync(FULL_MASK, nhit > uint32_t(SPARSE_MAX * G));
-        if (dense) {
-          uint32_t bj[NE];
-          uint32_t bmin = 0xffffffffu, bmax = 0u;
+        uint32_t same = 0;  // hits equal to the run's last value: same bin, no bin arithmetic
 #pragma unroll
-          for (int j = 0; j < NE; ++j) {
-            bj[j] = uint32_t(value_bin(f4_get(vv[j >> 2], j & 3), gmin, sc));
-            if ((bits >> j) & 1u) {
-              bmin = min(bmin, bj[j]);
-              bmax = max(bmax, bj[j]);
-            }
-          }
-          bmin = __reduce_min_sync(FULL_MASK, bmin);
-          bmax = __reduce_max_sync(FULL_MASK, bmax);
-          if (bmin == bmax) {
-            if (lane == 0) atomicAdd(&S.hist[bmin], wtot);
-          } else {  // plain atomics: the hardware merges the lanes that share a bin
+        for (int j = 0; j < NE; ++j) same |= uint32_t(f4_get(vv[j >> 2], j & 3) == rv) << j;
+        if ((bits & ~same) == 0u) {
+          rrun += uint32_t(__popc(bits));
+          return;
+        }
 #pragma unroll
-            for (int j = 0; j < NE; ++j)
-              if ((bits >> j) & 1u) atomicAdd(&S.hist[bj[j]], 1u);
-          }
-        }
-        // List the hits (a dense warp only until its segment is full; the counts above are exact).
-        if (!dense || wlist - wtot < uint32_t(LSEG)) {
-          for (uint32_t rest = bits; rest;) {
-            const int jb = __ffs(rest) - 1;  // bit: the first or second stage, score j in it
-            rest &= rest - 1;
-            const bool second = G == 2 && jb >= 4 * VPS;  // selects, not an indexed local array
-            const int j = second ? jb - 4 * VPS : jb;
-            const int32_t c0 = second ? c0s[G - 1] : c0s[0];
-            const float e = stage_score(second ? slots[G - 1] : slots[0], c0, j);
-            if (!dense) atomicAdd(&S.hist[value_bin(e, gmin, sc)], 1u);
-            if (at < uint32_t(LSEG)) {
-              seg_v[at] = e;
-              if constexpr (L16)
-                seg_p[at] = uint16_t(list_key(c0 + tid, 0) + uint32_t(j >> 2) * (4 * T) + uint32_t(j & 3));
-              else
-                seg_j[at] = 4 * (c0 + tid) - lead + (j >> 2) * (4 * T) + (j & 3);
+        for (int j = 0; j < NE; ++j)
+          if ((bits >> j) & 1u) {
+            const float e = f4_get(vv[j >> 2], j & 3);
+            if (e != rv) {
+              hk0 = min(hk0, order_key(e));
+              hk1 = max(hk1, order_key(e));
+              const uint32_t b = uint32_t(value_bin(e, gmin, sc));
+              if (b != rb) {
+                if (rrun) atomicAdd(&S.hist[rb], rrun);
+                rb = b;
+                rrun = 0;
+              }
+              rv = e;
             }
-            ++at;
+            ++rrun;
           }
-        }
-      };
-      stream_pass(true, [&](uint32_t slot, int32_t c0) {
-        const uint32_t sl[1] = {slot};
-        const int32_t c0s[1] = {c0};
-        p1_visit(IntC<1>{}, sl, c0s);
       });
+      if (rrun) atomicAdd(&S.hist[rb], rrun);
+      __syncwarp();
+      wlist = S.list_n[warp];
+      // The listed hits' bins, counted once per list entry (the entries past a full segment
+      // were counted during the pass).
+      const uint32_t nl = wlist < uint32_t(LSEG) ? wlist : uint32_t(LSEG);
+      for (uint32_t i = uint32_t(lane); i < nl; i += 32u) {
+        const float e = seg_v[i];
+        atomicAdd(&S.hist[value_bin(e, gmin, sc)], 1u);
+        hk0 = min(hk0, order_key(e));
+        hk1 = max(hk1, order_key(e));
+      }
+      // this CTA's key bounds of the scores >= thr (for a row whose scores >= thr are one value)
+      hk0 = __reduce_min_sync(FULL_MASK, hk0);
+      hk1 = __reduce_max_sync(FULL_MASK, hk1);
+      if (lane == 0 && hk0 <= hk1) {
+        atomicMin(&S.kmin_loc, hk0);
+        atomicMax(&S.kmax_loc, hk1);
+      }
     }
     // Diagnostics: the first row's rank-0 CTA reports a give-up here, after its first pass has
     // waited for every stage it issued (nothing in flight), to exercise the failure path.
@@ -1233,6 +1234,21 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     // (the floor is cluster-uniform, so every CTA expects the same count) and no cluster
     // barrier is needed.  A wide range -- a far outlier stretched the bins, few of them are
     // occupied -- goes bin by bin, only the occupied ones, then a cluster barrier.
+    // This CTA's key bounds and listed count go to every CTA, one thread per destination, after
+    // the counts are on their way (read after a later cluster barrier, only by the rescue).
+    auto publish_bounds = [&]() {
+      if (!bmax_row && uint32_t(tid) < cs) {
+        uint32_t lc = 0;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) lc += min(S.list_n[w], uint32_t(LSEG));
+        const uint32_t c = uint32_t(tid);
+        if (S.kmin_loc <= S.kmax_loc) {
+          dsmem_red_min(dsmem_map(smem_u32(&S.hk_min), c), S.kmin_loc);
+          dsmem_red_max(dsmem_map(smem_u32(&S.hk_max), c), S.kmax_loc);
+        }
+        if (lc) dsmem_red_add(dsmem_map(smem_u32(&S.hlisted), c), lc);
+      }
+    };
     const int fb0 = (fpart > 0 ? fpart : 0) & ~3;
     if (NB - fb0 <= BULK_BINS) {
       const uint32_t pbytes = uint32_t(NB + 4 - fb0) * 4u;
@@ -1246,11 +1262,13 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
                               dsmem_map(smem_u32(&S.hbar), c));
         mbar_arrive_expect_tx(&S.hbar, cs * pbytes);
       }
+      publish_bounds();
       if (!mbar_wait_bounded(&S.hbar, 0, WAIT_LIMIT_NS)) late = true;
       if (__syncthreads_or(late) && tid == 0) S.tout = 1;
       if (tid == 0) S.unlisted = S.tot[NB];
     } else {
       push(fpart > 0 ? fpart : 0, NB - 1);
+      publish_bounds();
       if (tid == 0 && !listed)
         for (uint32_t c = 0; c < cs; ++c)
           dsmem_red_add(dsmem_map(smem_u32(&S.unlisted), c), rank == 0 ? 1u + UNLISTED_RANK0 : 1u);
@@ -1806,101 +1824,127 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     }
     return r;
   };
-  // tau: the k - above largest order keys among the members
-  const Sel t = radix_select([&](float e, int32_t, uint32_t& key) {
-    key = order_key(e);
-    return key_class(key) == 0;
-  }, seeded ? uint32_t(k) - cr.above : uint32_t(k), tau_prefix, tau_mask, tau_shift, !from_lists);
-  const uint32_t prefix = t.prefix, pmask = t.pmask;
-  const bool ge = t.ge;
-  const uint32_t my_win = (seeded ? cr.my_above : 0u) + t.my_above;  // this CTA's scores above tau
-  const uint32_t nties = ge ? 0u : t.need;                           // tie slots
-  // Deterministic mode: the tie slots go to the ties with the smallest window indices, the
-  // nties largest keys ~j among the scores equal to tau.  Keys of indices below 2^(8D) share
-  // their top 32 - 8D bits (all ones), so only D digit passes are needed.
-  bool by_index = false;
-  Sel ix{};
-  if (det && nties > 0) {
-    by_index = true;
-    const int digits = (32 - __clz(int(nv - 1u)) + 7) / 8;
-    const uint32_t fixed = digits < 4 ? (0xffffffffu << (8 * digits)) : 0u;
-    ix = radix_select([&](float e, int32_t jw, uint32_t& key) {
-      key = ~uint32_t(jw);
-      const uint32_t kv = order_key(e);
-      return key_class(kv) == 0 && kv == prefix;
-    }, nties, fixed, fixed, 8 * (digits - 1), false);
-  }
-  auto index_selected = [&](int32_t jw) -> bool {
-    const uint32_t key = ~uint32_t(jw);
-    return ix.ge ? (key & ix.pmask) >= ix.prefix : key >= ix.prefix;
-  };
-  // this CTA's tie candidates for the slots: all its ties, or its index-selected ties
-  const uint32_t my_eq = by_index ? ix.my_above + (ix.ge ? 0u : ix.my_at) : t.my_at;
-  // Emission: rank 0 hands this CTA a block of winner slots and a block of tie slots.
-  const uint32_t tie_base = uint32_t(k) - nties;
-  if (tid == 0) S.base_above = my_win ? dsmem_atom_add(dsmem_map(smem_u32(&S.rc_win), 0), my_win) : 0u;
-  if (tid == 32) S.base_cand = my_eq ? dsmem_atom_add(dsmem_map(smem_u32(&S.rc_tie), 0), my_eq) : 0u;
-  __syncthreads();
-  const uint32_t wbase = S.base_above, tbase = S.base_cand;
-  // ties this CTA writes: its share of the nties slots, in the order the slots were handed out
-  const uint32_t my_ties = tbase < nties ? (my_eq < nties - tbase ? my_eq : nties - tbase) : 0u;
-  auto emit = [&](float e, int32_t jw, bool valid) {  // warp-collective
-    const uint32_t key = order_key(e);
-    const int bc = valid ? key_class(key) : -1;
-    const bool win = bc == 1 || (bc == 0 && (ge ? (key & pmask) >= prefix : key > prefix));
-    const bool tie = bc == 0 && !ge && key == prefix && (!by_index || index_selected(jw));
-    const uint32_t ws = warp_alloc_local(&S.ctr_win, win);
-    if (win && wbase + ws < tie_base) {
-      out[wbase + ws] = jw;
-      if (outv) outv[wbase + ws] = e;
-    }
-    const uint32_t ts = warp_alloc_local(&S.ctr_cand, tie);
-    if (tie && tbase + ts < nties) {
-      out[tie_base + tbase + ts] = jw;
-      if (outv) outv[tie_base + tbase + ts] = e;
-    }
-  };
-  // A tie class found by the first digit pass, with nothing above it in this CTA: the tie slots
-  // come from the indices that pass recorded, without another read of the share.
-  const uint32_t recorded = min(S.rec_n, REC_CAP);
-  if (t.first_eq && !from_lists && !by_index && my_win == 0 && my_ties > 0 && my_ties <= recorded) {
+  // One value above the floor: the first pass found every score >= thr equal (its smallest and
+  // largest keys agree cluster-wide), so the crossing bin's members are one tie class, tau is
+  // that value, nothing lies above it, and any k of them are the selection.  When the lists hold
+  // at least k of them, the tie slots come from the lists: no digit pass, no second read.
+  const bool one_value = seeded && !from_lists && !bmax_row && !det && rounds == 1 && S.hk_min == S.hk_max &&
+                         cr.above == 0 && S.hlisted >= uint32_t(k);
+  if (one_value) {
+    uint32_t lpre[NW + 1];  // listed entries before each warp's segment
+    lpre[0] = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) lpre[w + 1] = lpre[w] + min(S.list_n[w], uint32_t(LSEG));
+    const uint32_t my_eq = lpre[NW];
+    if (tid == 32) S.base_cand = my_eq ? dsmem_atom_add(dsmem_map(smem_u32(&S.rc_tie), 0), my_eq) : 0u;
+    __syncthreads();
+    const uint32_t tbase = S.base_cand;
+    const uint32_t my_ties = tbase < uint32_t(k) ? min(my_eq, uint32_t(k) - tbase) : 0u;
     for (uint32_t i = tid; i < my_ties; i += T) {
-      const int32_t jw = rec[i];
-      out[tie_base + tbase + i] = jw;
-      if (outv) outv[tie_base + tbase + i] = __ldg(rowp + a + uint32_t(jw));
+      uint32_t at = i;  // segment w holds entries lpre[w] ..: static indices only
+#pragma unroll
+      for (int q = 1; q < NW; ++q)
+        if (i >= lpre[q]) at = uint32_t(q * LSEG) + (i - lpre[q]);
+      out[tbase + i] = list_window(at);
+      if (outv) outv[tbase + i] = list_val(at);
     }
-  } else if (my_win > 0 || my_ties > 0) {
-    if (from_lists) {
-      each_listed([&](float e, int32_t jw, bool in) { emit(e, jw, in); });
-    } else {
-      static_assert(4 * VPS < 16, "a thread's slot count per stage fits in 4 bits");
-      stream_pass(false, [&](uint32_t slot, int32_t c0) {
-        // stop visiting once this CTA's slots are all handed out (the counters only grow, and a
-        // warp reads them together; the remaining stages still land and are waited for)
-        if (S.ctr_win >= my_win && S.ctr_cand >= my_ties) return;
-        // Each thread marks its winners and ties of the stage (bit 4i + l), the warp takes its
-        // slots of each kind with one atomic, and each thread writes its own in turn.
-        uint32_t wm = 0, tm = 0;
-        each_lane(slot, c0, [&](float e, int32_t g, bool valid, int l) {
-          const uint32_t key = order_key(e);
-          const int bc = valid ? key_class(key) : -1;
-          const bool win = bc == 1 || (bc == 0 && (ge ? (key & pmask) >= prefix : key > prefix));
-          const bool tie = bc == 0 && !ge && key == prefix && (!by_index || index_selected(4 * g + l - lead));
-          const int j = 4 * ((g - c0) / T) + l;
-          wm |= uint32_t(win) << j;
-          tm |= uint32_t(tie) << j;
+  } else {
+    // tau: the k - above largest order keys among the members
+    const Sel t = radix_select([&](float e, int32_t, uint32_t& key) {
+      key = order_key(e);
+      return key_class(key) == 0;
+    }, seeded ? uint32_t(k) - cr.above : uint32_t(k), tau_prefix, tau_mask, tau_shift, !from_lists);
+    const uint32_t prefix = t.prefix, pmask = t.pmask;
+    const bool ge = t.ge;
+    const uint32_t my_win = (seeded ? cr.my_above : 0u) + t.my_above;  // this CTA's scores above tau
+    const uint32_t nties = ge ? 0u : t.need;                           // tie slots
+    // Deterministic mode: the tie slots go to the ties with the smallest window indices, the
+    // nties largest keys ~j among the scores equal to tau.  Keys of indices below 2^(8D) share
+    // their top 32 - 8D bits (all ones), so only D digit passes are needed.
+    bool by_index = false;
+    Sel ix{};
+    if (det && nties > 0) {
+      by_index = true;
+      const int digits = (32 - __clz(int(nv - 1u)) + 7) / 8;
+      const uint32_t fixed = digits < 4 ? (0xffffffffu << (8 * digits)) : 0u;
+      ix = radix_select([&](float e, int32_t jw, uint32_t& key) {
+        key = ~uint32_t(jw);
+        const uint32_t kv = order_key(e);
+        return key_class(kv) == 0 && kv == prefix;
+      }, nties, fixed, fixed, 8 * (digits - 1), false);
+    }
+    auto index_selected = [&](int32_t jw) -> bool {
+      const uint32_t key = ~uint32_t(jw);
+      return ix.ge ? (key & ix.pmask) >= ix.prefix : key >= ix.prefix;
+    };
+    // this CTA's tie candidates for the slots: all its ties, or its index-selected ties
+    const uint32_t my_eq = by_index ? ix.my_above + (ix.ge ? 0u : ix.my_at) : t.my_at;
+    // Emission: rank 0 hands this CTA a block of winner slots and a block of tie slots.
+    const uint32_t tie_base = uint32_t(k) - nties;
+    if (tid == 0) S.base_above = my_win ? dsmem_atom_add(dsmem_map(smem_u32(&S.rc_win), 0), my_win) : 0u;
+    if (tid == 32) S.base_cand = my_eq ? dsmem_atom_add(dsmem_map(smem_u32(&S.rc_tie), 0), my_eq) : 0u;
+    __syncthreads();
+    const uint32_t wbase = S.base_above, tbase = S.base_cand;
+    // ties this CTA writes: its share of the nties slots, in the order the slots were handed out
+    const uint32_t my_ties = tbase < nties ? (my_eq < nties - tbase ? my_eq : nties - tbase) : 0u;
+    auto emit = [&](float e, int32_t jw, bool valid) {  // warp-collective
+      const uint32_t key = order_key(e);
+      const int bc = valid ? key_class(key) : -1;
+      const bool win = bc == 1 || (bc == 0 && (ge ? (key & pmask) >= prefix : key > prefix));
+      const bool tie = bc == 0 && !ge && key == prefix && (!by_index || index_selected(jw));
+      const uint32_t ws = warp_alloc_local(&S.ctr_win, win);
+      if (win && wbase + ws < tie_base) {
+        out[wbase + ws] = jw;
+        if (outv) outv[wbase + ws] = e;
+      }
+      const uint32_t ts = warp_alloc_local(&S.ctr_cand, tie);
+      if (tie && tbase + ts < nties) {
+        out[tie_base + tbase + ts] = jw;
+        if (outv) outv[tie_base + tbase + ts] = e;
+      }
+    };
+    // A tie class found by the first digit pass, with nothing above it in this CTA: the tie slots
+    // come from the indices that pass recorded, without another read of the share.
+    const uint32_t recorded = min(S.rec_n, REC_CAP);
+    if (t.first_eq && !from_lists && !by_index && my_win == 0 && my_ties > 0 && my_ties <= recorded) {
+      for (uint32_t i = tid; i < my_ties; i += T) {
+        const int32_t jw = rec[i];
+        out[tie_base + tbase + i] = jw;
+        if (outv) outv[tie_base + tbase + i] = __ldg(rowp + a + uint32_t(jw));
+      }
+    } else if (my_win > 0 || my_ties > 0) {
+      if (from_lists) {
+        each_listed([&](float e, int32_t jw, bool in) { emit(e, jw, in); });
+      } else {
+        static_assert(4 * VPS < 16, "a thread's slot count per stage fits in 4 bits");
+        stream_pass(false, [&](uint32_t slot, int32_t c0) {
+          // stop visiting once this CTA's slots are all handed out (the counters only grow, and a
+          // warp reads them together; the remaining stages still land and are waited for)
+          if (S.ctr_win >= my_win && S.ctr_cand >= my_ties) return;
+          // Each thread marks its winners and ties of the stage (bit 4i + l), the warp takes its
+          // slots of each kind with one atomic, and each thread writes its own in turn.
+          uint32_t wm = 0, tm = 0;
+          each_lane(slot, c0, [&](float e, int32_t g, bool valid, int l) {
+            const uint32_t key = order_key(e);
+            const int bc = valid ? key_class(key) : -1;
+            const bool win = bc == 1 || (bc == 0 && (ge ? (key & pmask) >= prefix : key > prefix));
+            const bool tie = bc == 0 && !ge && key == prefix && (!by_index || index_selected(4 * g + l - lead));
+            const int j = 4 * ((g - c0) / T) + l;
+            wm |= uint32_t(win) << j;
+            tm |= uint32_t(tie) << j;
+          });
+          uint32_t ws = warp_alloc_n(&S.ctr_win, __popc(wm));
+          uint32_t ts = warp_alloc_n(&S.ctr_cand, __popc(tm));
+          auto put = [&](int j, uint32_t at) {
+            out[at] = 4 * (c0 + (j >> 2) * T + tid) + (j & 3) - lead;
+            if (outv) outv[at] = stage_score(slot, c0, j);
+          };
+          for (uint32_t rest = wm; rest; rest &= rest - 1, ++ws)
+            if (wbase + ws < tie_base) put(__ffs(rest) - 1, wbase + ws);
+          for (uint32_t rest = tm; rest; rest &= rest - 1, ++ts)
+            if (tbase + ts < nties) put(__ffs(rest) - 1, tie_base + tbase + ts);
         });
-        uint32_t ws = warp_alloc_n(&S.ctr_win, __popc(wm));
-        uint32_t ts = warp_alloc_n(&S.ctr_cand, __popc(tm));
-        auto put = [&](int j, uint32_t at) {
-          out[at] = 4 * (c0 + (j >> 2) * T + tid) + (j & 3) - lead;
-          if (outv) outv[at] = stage_score(slot, c0, j);
-        };
-        for (uint32_t rest = wm; rest; rest &= rest - 1, ++ws)
-          if (wbase + ws < tie_base) put(__ffs(rest) - 1, wbase + ws);
-        for (uint32_t rest = tm; rest; rest &= rest - 1, ++ts)
-          if (tbase + ts < nties) put(__ffs(rest) - 1, tie_base + tbase + ts);
-      });
+      }
     }
   }
   report_timeout();

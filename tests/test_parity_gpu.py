@@ -712,6 +712,31 @@ def test_device_error_reporting(gvr):
         assert (st[1:, 0] >= 0).all()
 
 
+# ----------------------------------------------------------------------------- one value above the floor
+def test_one_value_above_the_floor(gvr):
+    """Rows whose scores at or above the sampled floor are all one value: the tie slots come from
+    the first pass's lists when they hold k of them (half the row one value; a top class of signed
+    zeros), else from the digit passes (3072 ties, all in the share of one CTA of the cluster,
+    more than its lists hold).  Exact with values, and in deterministic mode."""
+    g = np.random.default_rng(81)
+    stride, k = 131072, 2048
+    half = g.standard_normal(stride).astype(np.float32)
+    half[g.random(stride) < 0.5] = 7.0
+    packed = g.standard_normal(stride).astype(np.float32)
+    for s0 in (0, 16384, 32768):  # stage s0 / 1024 of the row: rank 0's for any cluster of <= 16
+        packed[s0:s0 + 1024] = 7.0
+    zeros = -(np.abs(g.standard_normal(stride)) + 1).astype(np.float32)
+    z = g.choice(stride, 5000, replace=False)
+    zeros[z] = np.where(np.arange(z.size) % 2 == 0, np.float32(-0.0), np.float32(0.0))
+    lg = np.stack([half, packed, zeros])
+    case = workloads.DecodeCase("one_value", lg, np.full(3, stride, np.int32), 1, 1, k)
+    st = assert_decode_exact(gvr, case, stats=True)
+    assert (st[:2, 0] == 3).all(), st  # overflow: the lists cannot hold the crossing bin
+    assert st[2, 0] in (1, 5, 6), st  # 5000 ties over every CTA: the lists hold them
+    assert_decode_exact(gvr, case, values=True)
+    assert_decode_exact(gvr, case, options=gvr.Options(flags=16))
+
+
 # ----------------------------------------------------------------------------- short-row kernel
 SHORT, CLUSTER = 4096, 256
 
