@@ -341,7 +341,7 @@ def _launchers(torch, gvr, dev, wsb):
 
 def _cell(tag, case, nbytes, t, peak):
     cm = t["graph_mean"]
-    return {"cell": tag, "bs": case.rows, "n": int(case.meta.get("n", 0)), "k": case.k,
+    return {"cell": tag, "bs": case.rows, "n": int((case.row_lengths() if hasattr(case, "row_lengths") else case.window_lengths()).max()), "k": case.k,
             "cold_us": {k: round(v, 2) for k, v in t.items() if k != "warm"}, "warm_us": round(t["warm"], 2),
             "rows_per_s_cold": case.rows / (cm * 1e-6), "us_per_row_cold": cm / case.rows,
             "algorithmic_bytes": nbytes, "gbs_cold": nbytes / cm / 1e3,
@@ -379,14 +379,21 @@ def tail_check(torch, gvr, dev, wsb, timer, peak, emit=None):
 SWEEP_BIG = [(256, 131072, 512), (256, 131072, 1024), (256, 131072, 2048), (256, 65536, 512)]
 
 
-def extras(torch, gvr, dev, wsb, peak):
+def extras(torch, gvr, dev, wsb, peak, head_case=None):
     """The target configurations beside the headline, one call each at a time, cold and warm:
     the >= 36 MB sweep cells (decode and prefill), the tail check, the single decode row and
-    the 4096-row prefill tile."""
+    the 4096-row prefill tile.  Also the headline batch as one isolated call after an L2 scrub
+    (the per-launch figure a profiler that serialises launches reports)."""
     import workloads
     timer = ColdWarm(torch, dev)
     decode, prefill = _launchers(torch, gvr, dev, wsb)
     out = {}
+    if head_case is not None:
+        t = timer(decode(head_case), reps=16)
+        out["isolated_launch"] = {"event_us": {"median": round(t["median"], 2), "p99": round(t["p99"], 2)},
+                                  "scrub_graph_us": round(t["graph_mean"], 2),
+                                  "note": "one call after a 512 MiB L2 scrub, per-call CUDA events; "
+                                          "the headline times back-to-back graph launches"}
     cells = []
     for bs, n, k in SWEEP_BIG:
         dc = workloads.sweep_decode(bs, n, k)
@@ -638,7 +645,7 @@ def main():
         warm_per = warm_s / args.steps
         del bufs
         torch.cuda.empty_cache()
-        extra = None if args.no_extras else extras(torch, gvr, dev, wsb, peak)
+        extra = None if args.no_extras else extras(torch, gvr, dev, wsb, peak, head_case=case)
         cpu = None
         if not args.no_cpu_baseline:
             secs, cores, runs, total = time_oracle(case, 0, 5, CPU_BASELINE_S)
