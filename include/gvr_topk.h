@@ -142,7 +142,9 @@ enum {
    * cluster or ring setting, no hint or block maxima; others run the cluster kernel): one CTA
    * of 256 threads holds a whole row in registers.  Exact, but measured slower than the cluster
    * kernel on every short-row workload tried, so never chosen by default */
-  GVR_FLAG_SHORT_KERNEL = 4096
+  GVR_FLAG_SHORT_KERNEL = 4096,
+  /* topk_decode_blockskip: skip blocks whatever the samples estimate (the gate is not applied) */
+  GVR_FLAG_BLOCKSKIP_ALWAYS = 8192
 };
 
 typedef struct gvr_options {
@@ -227,10 +229,14 @@ gvr_status topk_decode_hinted(const float* logits, int64_t row_stride, int64_t n
  *                     window are read.
  *   block_max_stride  >= ceil(row_stride / 32) (GVR_ERR_ARG otherwise); block_max 4-byte
  *                     aligned (GVR_ERR_ALIGN), non-NULL when num_rows > 0 (GVR_ERR_NULL).
- * No gate is applied: the pages' shape gate (batch working set and row length) is left to the
- * caller.  The later passes that need every score (the rare second pass below the floor, the
- * row-wide selection) read whole shares as usual.  Every other argument, the ownership rules
- * and the errors are those of topk_decode_ex.
+ * Gate (on the device, per row): once the sampled floor is known, the block64 samples give the
+ * share of 32-score sample halves that reach it, an estimate of the share of blocks the skipping
+ * pass would still read.  Above a quarter the row takes the ordinary staged pass (every block
+ * read at the streaming rate, as topk_decode_ex); at or below it, the first ring stages of each
+ * CTA's share (staged for every row at the start) are read whole and the rest block by block.
+ * GVR_FLAG_BLOCKSKIP_ALWAYS skips the gate.  The later passes that need every score (the rare
+ * second pass below the floor, the row-wide selection) read whole shares as usual.  Every other
+ * argument, the ownership rules and the errors are those of topk_decode_ex.
  */
 gvr_status topk_decode_blockskip(const float* logits, int64_t row_stride, int64_t num_rows,
                                  const int32_t* kv_lens, int32_t next_n, int32_t compress_ratio,

@@ -40,6 +40,7 @@ _lib = None
 FLAG_FORCE_RESCUE, FLAG_NO_FLOOR, FLAG_ZERO_CAP, FLAG_RADIX_REFINE = 1, 2, 4, 8
 FLAG_DETERMINISTIC, FLAG_SORTED, FLAG_STREAM_RESCUE, FLAG_COMPACT_LISTS = 16, 32, 64, 128
 FLAG_CLUSTER_KERNEL, FLAG_SPLIT_ALONE, FLAG_SPLIT_KERNEL, FLAG_DIAG_FAIL_ROW0, FLAG_SHORT_KERNEL = 256, 512, 1024, 2048, 4096
+FLAG_BLOCKSKIP_ALWAYS = 8192
 PATH_NAMES = {-1: "device_error", 0: "short", 1: "refine", 2: "rescue_bracket", 3: "rescue_overflow",
               4: "rescue_forced", 5: "refine_cluster", 6: "refine_relist", 7: "split", 8: "split_alone",
               9: "neg_inf_fill", 10: "short_kernel", 11: "short_radix"}

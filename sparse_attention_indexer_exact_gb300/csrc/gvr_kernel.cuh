@@ -33,15 +33,18 @@
 //    shared-memory lists for the collect step (no second read of the row).  Bins above bin(t)
 //    are then complete, bin(t) itself is partial.  Only when fewer than K scores reach t are
 //    the scores below it counted in a second pass, so the result never depends on the floor.
-//  * ballot-built prefixes for list slots; a warp whose hits share one bin adds them with one
-//    atomic, other warps with one plain shared atomic per hit (the hardware merges the lanes
-//    of one instruction that share a bin).
+//  * no warp collective per stage in the first pass: a thread with hits takes list slots with
+//    one shared atomic on its warp's counter; the hits' bins are counted after the pass, from
+//    the list (hits past a full list in a per-thread register run of one bin).  A tie class
+//    above the floor -- every counted score one value -- is recognised from the cluster's
+//    smallest and largest counted key, and its slots come from the lists.
 //  * the first pass's histogram reaches every CTA of the cluster as TMA bulk reductions into
 //    shared memory, counted on an mbarrier (no cluster barrier).
-//  * four instantiations: the extended modes (EXT: deterministic ties by smallest index and
-//    sorted output, hinted sampling, the block-skip first pass) or not, and the compact lists
-//    (L16: 1024 entries of score and 16-bit share position instead of 768 of score and index,
-//    chosen by the host where they let half as many CTAs hold a row's list) or not.
+//  * six instantiations: the plain one, the extended modes (deterministic ties by smallest
+//    index and sorted output, hinted sampling, the block-skip first pass) or the block-skip
+//    first pass alone; each with or without the compact lists (L16: 1024 entries of score and
+//    16-bit share position instead of 768 of score and index, chosen by the host where they
+//    let half as many CTAs hold a row's list).
 //
 // The bin function is monotone non-decreasing in the score (IEEE round-to-nearest subtract and
 // multiply by a positive scale, clamp, truncate), which is all the crossing-bin logic needs;
@@ -104,7 +107,8 @@ enum : int32_t {
   FLAG_SORTED = 32,
   FLAG_STREAM_RESCUE = 64,
   FLAG_COMPACT_LISTS = 128,
-  FLAG_DIAG_FAIL_ROW0 = 2048
+  FLAG_DIAG_FAIL_ROW0 = 2048,
+  FLAG_BLOCKSKIP_ALWAYS = 8192
 };
 enum : int32_t {
   PATH_DEVICE_ERROR = -1,
@@ -180,6 +184,7 @@ struct alignas(16) Smem {
   uint32_t hk_min, hk_max;         // the cluster's smallest / largest order key of the first pass's
                                    // scores >= thr (every CTA adds its own)
   uint32_t hlisted;                // the cluster's listed first-pass scores
+  uint32_t end_hits, nbr_hits;     // samples at or above the floor's bin in the end runs / their neighbours
   uint32_t tout;                   // this CTA gave up waiting for staged data
   uint32_t err;                    // rank 0: some CTA of the cluster gave up
   uint64_t bar[MAX_STAGES];        // one mbarrier per ring stage
@@ -485,11 +490,15 @@ __device__ __forceinline__ DigitCross digit_scan(SM& S, const uint32_t* dtot, co
   return DigitCross{S.dsel, S.dabove, S.dcnt, S.dmy_above, S.dmy_at, all};
 }
 
-// EXT: the extended modes (deterministic ties and sorting, hinted sampling, block skipping) are
-// compiled in.  The plain instantiation leaves them out, which keeps the common path's code
-// smaller (measured ~3 % faster).
-template <bool EXT, bool L16>
+// X selects what is compiled in: KX_PLAIN none of the extended modes, KX_EXT all of them
+// (deterministic ties and sorting, hinted sampling, block skipping), KX_BLOCKSKIP block skipping
+// alone.  Code a call does not use still costs: the extended instantiation measured ~3 % slower
+// than the plain one on plain calls.
+enum : int { KX_PLAIN = 0, KX_EXT = 1, KX_BLOCKSKIP = 2 };
+template <int X, bool L16>
 __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
+  constexpr bool EXT = X == KX_EXT;
+  constexpr bool BSK = X != KX_PLAIN;  // block maxima may be given
   constexpr int T = THREADS;
   constexpr int NW = T / 32;
   constexpr int KPT = (MAX_K + T - 1) / T;  // samples per thread at most
@@ -625,27 +634,29 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   // its row's indices become -2 at the end, and every later pass returns at once.  At the moment
   // it gives up it issues no more refills and waits (bounded) for the copies already in flight,
   // so none is still writing into its shared memory when it moves on or exits.
-  auto stream_pass = [&](bool primed, auto&& visit) {
+  // nlim < nstages: only the first nlim stages (all primed, none refilled).
+  auto stream_pass = [&](bool primed, auto&& visit, int32_t nlim = -1) {
+    if (nlim < 0) nlim = nstages;
     if (S.tout) return;  // CTA-uniform: written before a barrier that every thread has passed
     if (warp == 0 && !primed && !(ring_resident && loaded))
-      for (int32_t s = lane; s < nst && s < nstages; s += 32) {  // nst <= 16: one pass of lanes
+      for (int32_t s = lane; s < nst && s < nlim; s += 32) {  // nst <= 16: one pass of lanes
         const uint32_t sl = rslot + uint32_t(s);
         issue_stage(s, sl < uint32_t(nst) ? sl : sl - uint32_t(nst));
       }
     uint32_t slot = rslot, ph = rphase;
-    for (int32_t s = 0; s < nstages; ++s) {
+    for (int32_t s = 0; s < nlim; ++s) {
       if (!mbar_wait_bounded(&S.bar[slot], ph, WAIT_LIMIT_NS)) {
         mbar_wait_bounded(&S.bar[slot], ph, WAIT_LIMIT_NS);  // let copies land
         late = true;
       }
       visit(slot, stage_first(s));
       // refill this slot once every thread is done with it, unless some thread gave up waiting
-      const bool refill = s + nst < nstages;
+      const bool refill = s + nst < nlim;
       if (refill ? __syncthreads_or(late) : false) {
         // drain: the stages after this one that are already in flight (no refill was issued
         // for this slot), each waited for once, with the same bound
         uint32_t dsl = slot, dph = ph;
-        for (int32_t d = s + 1; d < nstages && d < s + nst; ++d) {
+        for (int32_t d = s + 1; d < nlim && d < s + nst; ++d) {
           if (++dsl == uint32_t(nst)) {
             dsl = 0;
             dph ^= 1u;
@@ -846,12 +857,13 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
 #pragma unroll
     for (int q = 0; q < KPT; ++q) sh[q] = uint32_t(hpos[q]) < nv ? __ldg(rowp + a + uint32_t(hpos[q])) : qnan;
   }
-  // Block-skip rows (block maxima given) read only the blocks that can reach the floor in the
-  // first pass, so nothing is staged ahead for them.
+  // Block-skip rows (block maxima given) may read only the blocks that can reach the floor in
+  // the first pass; their first ring stages are staged like every row's (the samples decide
+  // later whether skipping pays), and are read whole.
   const float* bmax_row =
-      (EXT && p.mode == MODE_DECODE && p.block_max) ? p.block_max + int64_t(row) * p.bmax_stride : nullptr;
+      (BSK && p.mode == MODE_DECODE && p.block_max) ? p.block_max + int64_t(row) * p.bmax_stride : nullptr;
   // The first ring stages go in flight right behind the samples, one lane of warp 0 per stage.
-  if (warp == 0 && !bmax_row)
+  if (warp == 0)
     for (int32_t s = lane; s < nst && s < nstages; s += 32) issue_stage(s, uint32_t(s));
   // Zero the counters while the samples are in flight (global loads are not waited for here).
   for (int i = tid; i < NB + 4; i += T) S.hist[i] = S.tot[i] = 0;
@@ -866,6 +878,8 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     S.hk_min = S.kmin_loc = 0xffffffffu;
     S.hk_max = S.kmax_loc = 0u;
     S.hlisted = 0;
+    S.rec_n = S.saved = 0;  // the block-skip gate's counts, before their own uses
+    S.end_hits = S.nbr_hits = 0;
     S.cross = Crossing{};
     S.dsel = S.dabove = S.dcnt = 0;
   }
@@ -986,6 +1000,14 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   if (p.flags & FLAG_FORCE_RESCUE) path = PATH_RESCUE_FORCED;
   else if (!bracket_ok) path = PATH_RESCUE_BRACKET;
 
+  // Block-skip gate: skipping pays only while very few blocks reach the floor (the skipping
+  // pass reads its blocks with plain loads, far fewer bytes in flight than the ring's bulk
+  // copies).  The block64 samples are runs of two 32-score halves spread over the row; the
+  // share of the interior halves with a sample at or above the floor estimates the share of
+  // blocks the skipping pass would still read (the same in every CTA of the row: same samples,
+  // same floor).  Above 1/16 the row takes the staged pass.  Counted before the floor's
+  // barrier, read after it.
+  bool skip_blocks = false;
   float sc = 0.f;
   float thr = -INFINITY;  // floor: scores >= thr are counted (and listed) in the first pass
   int fpart = -1;         // bin(thr): the one partially counted bin; -1 = no floor
@@ -1027,16 +1049,77 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
         __syncthreads();
         fb = suffix_cross<T>(S, S.hist, want);
       }
-      if (tid == 0) {
+      // Block-concentrated rows (a sink and recent tokens at the row's two ends, hot blocks in
+      // between) put the first and the last run on the hot ends: the samples over-represent the
+      // top, the floor lands above tau and every such row would count its scores twice.  When
+      // the two end runs hold most of the samples at or above the floor's bin while their
+      // neighbouring runs hold few, the floor is found again from the interior runs alone (the
+      // target scaled to their number) and the lower of the two is kept.  A smooth trend (a
+      // position bias) raises the neighbours too and keeps the floor.  Compiled into the
+      // block-skip instantiations only (the entry point for attention rows of that shape): the
+      // check measured 2-4 % on the plain path's other rows.
+      const bool ends_check = BSK && bmax_row && nblk >= 6;
+      if (ends_check) {
+        uint32_t ec = 0, nc = 0;
+#pragma unroll
+        for (int q = 0; q < KPT; ++q) {
+          if (uint32_t(q * T) >= 128u && uint32_t((q + 1) * T) + 128u <= nsamp) continue;  // no end run here
+          const uint32_t i = uint32_t(q * T + tid), run = i >> 6;
+          if (i < nsamp && !isnan(sv[q]) && value_bin(sv[q], gmin, sc) >= fb) {
+            ec += (run == 0 || run == nblk - 1) ? 1u : 0u;
+            nc += (run == 1 || run == nblk - 2) ? 1u : 0u;
+          }
+        }
+        if (ec) atomicAdd(&S.end_hits, ec);
+        if (nc) atomicAdd(&S.nbr_hits, nc);
+      }
+      if (BSK && bmax_row) {
+        const float tf = fb > 0 ? __fadd_rn(gmin, __fdiv_rn(float(fb), sc)) : -FLT_MAX;  // the floor
+        uint32_t hitq = 0, validq = 0;  // bit q: this warp's 32 samples of slot q reach it / count
+#pragma unroll
+        for (int q = 0; q < KPT; ++q) {  // the end runs (sink, recent tokens) are left out
+          const uint32_t i0 = uint32_t(q * T + 32 * warp);
+          hitq |= uint32_t(sv[q] >= tf) << q;
+          validq |= uint32_t(i0 >= 64u && i0 + 96u <= nsamp) << q;
+        }
+        hitq = __reduce_or_sync(FULL_MASK, hitq) & validq;
+        if (lane == 0) {
+          atomicAdd(&S.rec_n, uint32_t(__popc(hitq)));
+          atomicAdd(&S.saved, uint32_t(__popc(validq)));
+        }
+      }
+      auto set_floor = [&]() {  // tid 0
         // any threshold works: bins above bin(t) are complete, bin(t) is partial.  A floor in
         // the lowest bin is -FLT_MAX: every score but -inf (and NaN) is counted and listed, so a
         // row whose finite scores are fewer than k is decided by the first pass (the -inf fill)
         const float t = fb > 0 ? __fadd_rn(gmin, __fdiv_rn(float(fb), sc)) : -FLT_MAX;
         S.vthr = t;
         S.fpart = value_bin(t, gmin, sc);
-      }
+      };
+      if (tid == 0) set_floor();
       for (int i = tid; i < NB; i += T) S.hist[i] = 0;
       __syncthreads();
+      if (BSK && bmax_row)
+        skip_blocks = (p.flags & FLAG_BLOCKSKIP_ALWAYS) || (S.saved > 0u && 16u * S.rec_n <= S.saved);
+      if (ends_check && 3u * S.end_hits >= 2u * want && S.end_hits >= 4u * (S.nbr_hits + 1u)) {
+        const uint32_t nint = nsamp - 128u;
+        const float mui = float(k) * float(nint) / float(nv);
+        const float wi = mui + 3.0f * sqrtf(mui) + 6.0f;
+        const uint32_t want_i = wi < float(nint) ? uint32_t(wi) : nint;
+#pragma unroll
+        for (int q = 0; q < KPT; ++q) {
+          const uint32_t i = uint32_t(q * T + tid);
+          if (i >= 64u && i + 64u < nsamp && !isnan(sv[q])) atomicAdd(&S.hist[value_bin(sv[q], gmin, sc)], 1u);
+        }
+        __syncthreads();
+        const int fbi = suffix_cross<T>(S, S.hist, want_i);
+        if (fbi < fb) {
+          fb = fbi;
+          if (tid == 0) set_floor();
+        }
+        for (int i = tid; i < NB; i += T) S.hist[i] = 0;
+        __syncthreads();
+      }
       thr = S.vthr;
       fpart = S.fpart;
       if (hints) {
@@ -1064,51 +1147,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     float* const seg_v = (L16 ? S.list_v16 : S.list_v) + warp * LSEG;  // this warp's segment
     int32_t* const seg_j = S.list_j + warp * LSEG;
     uint16_t* const seg_p = S.list_p16 + warp * LSEG;
-    if (bmax_row) {
-      // ---------------------------------------------------------- block-skip first pass
-      // ("Block-skip fast path for self-sampling GVR top-K decode", opt-in row pass): a block
-      // of 32 scores whose bound is below the floor holds no score the first pass counts, so
-      // only the surviving blocks are read, with plain coalesced loads (one block per warp
-      // load, up to 8 in flight per warp).  The counts and lists equal those of the full pass.
-      const int64_t wend = int64_t(a) + nv;  // decode: a = 0, the window is [0, nv)
-      for (int32_t s = warp; s < nstages; s += NW) {  // this CTA's stages, one warp each
-        const int64_t colst = 4 * int64_t(stage_first(s));  // first column (a multiple of 1024)
-        const int64_t bi = (colst >> 5) + lane;              // this lane's block
-        const bool inwin = bi * 32 < wend;
-        const float bm = inwin ? __ldg(bmax_row + bi) : -INFINITY;
-        unsigned surv = __ballot_sync(FULL_MASK, inwin && !(bm < thr));  // NaN bounds survive
-        while (surv) {
-          int32_t blk[8];
-          float v[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            blk[q] = surv ? __ffs(surv) - 1 : -1;
-            surv &= surv - 1u;
-          }
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const int64_t col = colst + 32 * blk[q] + lane;
-            v[q] = (blk[q] >= 0 && col < wend) ? __ldg(rowp + col) : -INFINITY;
-          }
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            if (blk[q] < 0) break;  // warp-uniform
-            const int64_t col = colst + 32 * blk[q] + lane;
-            const bool hit = col < wend && v[q] >= thr;
-            const unsigned hm = __ballot_sync(FULL_MASK, hit);
-            if (!hm) continue;
-            const uint32_t at = wlist + uint32_t(__popc(hm & lanemask_lt()));
-            wlist += uint32_t(__popc(hm));
-            if (hit) atomicAdd(&S.hist[value_bin(v[q], gmin, sc)], 1u);
-            if (hit && at < uint32_t(LSEG)) {
-              seg_v[at] = v[q];
-              if constexpr (L16) seg_p[at] = uint16_t(s * 1024 + 32 * blk[q] + lane);
-              else seg_j[at] = int32_t(col - a);
-            }
-          }
-        }
-      }
-    } else {
+    {
       // One stage per visit, with no warp collective: a thread with scores >= thr takes list
       // slots for them with one shared-memory atomic on its warp's counter (S.list_n[warp]) and
       // lists them; their bins are counted once the pass is over, from the list.  A thread that
@@ -1121,6 +1160,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       uint32_t rb = 0xffffffffu, rrun = 0;  // its run of counted hits in bin rb
       float rv = __int_as_float(0x7fffffff);  // the run's last value (NaN: none yet)
       uint32_t hk0 = 0xffffffffu, hk1 = 0u;   // smallest / largest key of its hits
+      const int32_t ring_stages = skip_blocks ? (nstages < nst ? nstages : nst) : nstages;
       stream_pass(true, [&](uint32_t slot, int32_t c0) {
         float4 vv[VPS];
         uint32_t lanes;  // bit 4v+l: lane l of this thread's v-th vector is in the window
@@ -1185,7 +1225,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
             }
             ++rrun;
           }
-      });
+      }, ring_stages);
       if (rrun) atomicAdd(&S.hist[rb], rrun);
       __syncwarp();
       wlist = S.list_n[warp];
@@ -1204,6 +1244,53 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       if (lane == 0 && hk0 <= hk1) {
         atomicMin(&S.kmin_loc, hk0);
         atomicMax(&S.kmax_loc, hk1);
+      }
+    }
+    if (skip_blocks) {
+      // ---------------------------------------------------------- block-skip first pass
+      // ("Block-skip fast path for self-sampling GVR top-K decode", opt-in row pass): a block
+      // of 32 scores whose bound is below the floor holds no score the first pass counts, so
+      // only the surviving blocks are read, with plain coalesced loads (one block per warp
+      // load, up to 8 in flight per warp).  The counts and lists equal those of the full pass.
+      const int64_t wend = int64_t(a) + nv;  // decode: a = 0, the window is [0, nv)
+      // The stages the ring did not hold, one warp each; the warp's list continues after the
+      // ring part's entries (whose bins are already counted).
+      for (int32_t s = nst + warp; s < nstages; s += NW) {
+        const int64_t colst = 4 * int64_t(stage_first(s));  // first column (a multiple of 1024)
+        const int64_t bi = (colst >> 5) + lane;              // this lane's block
+        const bool inwin = bi * 32 < wend;
+        const float bm = inwin ? __ldg(bmax_row + bi) : -INFINITY;
+        unsigned surv = __ballot_sync(FULL_MASK, inwin && !(bm < thr));  // NaN bounds survive
+        while (surv) {
+          int32_t blk[8];
+          float v[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            blk[q] = surv ? __ffs(surv) - 1 : -1;
+            surv &= surv - 1u;
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int64_t col = colst + 32 * blk[q] + lane;
+            v[q] = (blk[q] >= 0 && col < wend) ? __ldg(rowp + col) : -INFINITY;
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            if (blk[q] < 0) break;  // warp-uniform
+            const int64_t col = colst + 32 * blk[q] + lane;
+            const bool hit = col < wend && v[q] >= thr;
+            const unsigned hm = __ballot_sync(FULL_MASK, hit);
+            if (!hm) continue;
+            const uint32_t at = wlist + uint32_t(__popc(hm & lanemask_lt()));
+            wlist += uint32_t(__popc(hm));
+            if (hit) atomicAdd(&S.hist[value_bin(v[q], gmin, sc)], 1u);
+            if (hit && at < uint32_t(LSEG)) {
+              seg_v[at] = v[q];
+              if constexpr (L16) seg_p[at] = uint16_t(s * 1024 + 32 * blk[q] + lane);
+              else seg_j[at] = int32_t(col - a);
+            }
+          }
+        }
       }
     }
     // Diagnostics: the first row's rank-0 CTA reports a give-up here, after its first pass has
@@ -1619,7 +1706,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   }
   __syncthreads();
   csync();  // every CTA's pushed totals start from zero
-  bool primed = rounds == 0 && !bmax_row;  // the head primed the ring for a row without a first pass
+  bool primed = rounds == 0;  // the head primed the ring for a row without a first pass
   // Bin class of a score for the seeded selection: 1 above the crossing bin, 0 a member of it,
   // -1 below it (or not counted).  Unseeded, every score is a member.
   uint32_t klo = 0, khi = KEY_POS_INF;

@@ -43,20 +43,22 @@ constexpr int kDefaultSmemReserved = 1024;
 constexpr int kMaxCtasPerSm = 7;  // registers: 128 threads x up to 72 registers
 DeviceState g_devices[kMaxDevices];
 
-template <bool EXT, bool L16>
+template <int X, bool L16>
 cudaError_t set_attributes_of() {
-  cudaError_t e = cudaFuncSetAttribute(gvr::gvr_topk_kernel<EXT, L16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(gvr::gvr_topk_kernel<X, L16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        gvr::smem_bytes(gvr::MAX_STAGES));
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gvr::gvr_topk_kernel<EXT, L16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(gvr::gvr_topk_kernel<X, L16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   return e;
 }
 
 cudaError_t set_attributes() {
-  cudaError_t e = set_attributes_of<false, false>();
-  if (e == cudaSuccess) e = set_attributes_of<true, false>();
-  if (e == cudaSuccess) e = set_attributes_of<false, true>();
-  if (e == cudaSuccess) e = set_attributes_of<true, true>();
+  cudaError_t e = set_attributes_of<gvr::KX_PLAIN, false>();
+  if (e == cudaSuccess) e = set_attributes_of<gvr::KX_EXT, false>();
+  if (e == cudaSuccess) e = set_attributes_of<gvr::KX_BLOCKSKIP, false>();
+  if (e == cudaSuccess) e = set_attributes_of<gvr::KX_PLAIN, true>();
+  if (e == cudaSuccess) e = set_attributes_of<gvr::KX_EXT, true>();
+  if (e == cudaSuccess) e = set_attributes_of<gvr::KX_BLOCKSKIP, true>();
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(gvr::gvr_split_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              gvr::split_smem_bytes());
@@ -106,7 +108,7 @@ gvr_status check_common(int64_t row_stride, int64_t num_rows, int32_t k, const g
     if (o->flags & ~(GVR_FLAG_FORCE_RESCUE | GVR_FLAG_NO_FLOOR | GVR_FLAG_ZERO_CAP | GVR_FLAG_RADIX_REFINE |
                      GVR_FLAG_DETERMINISTIC | GVR_FLAG_SORTED | GVR_FLAG_STREAM_RESCUE | GVR_FLAG_COMPACT_LISTS |
                      GVR_FLAG_CLUSTER_KERNEL | GVR_FLAG_SPLIT_ALONE | GVR_FLAG_SPLIT_KERNEL |
-                     GVR_FLAG_DIAG_FAIL_ROW0 | GVR_FLAG_SHORT_KERNEL))
+                     GVR_FLAG_DIAG_FAIL_ROW0 | GVR_FLAG_SHORT_KERNEL | GVR_FLAG_BLOCKSKIP_ALWAYS))
       return GVR_ERR_ARG;
     if (!ws && (o->flags & (GVR_FLAG_SPLIT_ALONE | GVR_FLAG_SPLIT_KERNEL))) return GVR_ERR_ARG;
     if ((o->flags & GVR_FLAG_SHORT_KERNEL) && (o->flags & GVR_FLAG_CLUSTER_KERNEL)) return GVR_ERR_ARG;
@@ -270,7 +272,7 @@ gvr_status launch(const gvr::Params& prm, int64_t num_rows, const gvr_options* o
       qc.attrs = qa;
       qc.numAttrs = 1;
       int n = 0;
-      const cudaError_t qe = cudaOccupancyMaxActiveClusters(&n, gvr::gvr_topk_kernel<false, false>, &qc);
+      const cudaError_t qe = cudaOccupancyMaxActiveClusters(&n, gvr::gvr_topk_kernel<gvr::KX_PLAIN, false>, &qc);
       // a refused query leaves its error in the thread's last-error slot: clear that one only
       if (qe != cudaSuccess) cudaGetLastError();
       f = (qe == cudaSuccess && n > 0) ? 1 : 2;
@@ -302,15 +304,20 @@ gvr_status launch(const gvr::Params& prm, int64_t num_rows, const gvr_options* o
   gvr::Params q = prm;
   q.nstage = geo.nstage;
   q.flags &= ~(GVR_FLAG_CLUSTER_KERNEL | GVR_FLAG_SHORT_KERNEL);
-  // the extended instantiation only when a call uses one of its modes
-  const bool ext = (q.flags & (gvr::FLAG_DETERMINISTIC | gvr::FLAG_SORTED)) || q.pre_idx || q.block_max;
+  // the extended instantiation only when a call uses one of its modes; block skipping alone has
+  // its own, smaller one
+  const int x = ((q.flags & (gvr::FLAG_DETERMINISTIC | gvr::FLAG_SORTED)) || q.pre_idx) ? gvr::KX_EXT
+                : q.block_max                                                         ? gvr::KX_BLOCKSKIP
+                                                                                      : gvr::KX_PLAIN;
   cudaError_t e;
   if (geo.l16)
-    e = ext ? cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<true, true>, q)
-            : cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<false, true>, q);
+    e = x == gvr::KX_EXT         ? cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<gvr::KX_EXT, true>, q)
+        : x == gvr::KX_BLOCKSKIP ? cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<gvr::KX_BLOCKSKIP, true>, q)
+                                 : cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<gvr::KX_PLAIN, true>, q);
   else
-    e = ext ? cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<true, false>, q)
-            : cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<false, false>, q);
+    e = x == gvr::KX_EXT         ? cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<gvr::KX_EXT, false>, q)
+        : x == gvr::KX_BLOCKSKIP ? cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<gvr::KX_BLOCKSKIP, false>, q)
+                                 : cudaLaunchKernelEx(&cfg, gvr::gvr_topk_kernel<gvr::KX_PLAIN, false>, q);
   return e == cudaSuccess ? GVR_OK : GVR_ERR_LAUNCH;
 }
 
@@ -369,6 +376,9 @@ constexpr size_t kNoAllocCounterBytes = size_t(gvr::SPLIT_MAX_ROWS) * 4;
 constexpr size_t kNoAllocBytes = kNoAllocCounterBytes + size_t(kNoAllocGrid) * 4 +
                                  size_t(kNoAllocGrid) * gvr::SPLIT_UNIT_CAP * 8;
 static_assert(2 * GVR_NOALLOC_MAX_ROWS <= kNoAllocGrid, "the capped grid holds the row limit");
+static_assert(int(GVR_FLAG_BLOCKSKIP_ALWAYS) == int(gvr::FLAG_BLOCKSKIP_ALWAYS) &&
+                  int(GVR_FLAG_DIAG_FAIL_ROW0) == int(gvr::FLAG_DIAG_FAIL_ROW0),
+              "the header's flags are the kernel's");
 
 struct NoAllocState {
   std::once_flag once;

@@ -143,9 +143,9 @@ def test_prefill_argument_errors(lib):
 def test_option_errors(lib):
     import sparse_attention_indexer_exact_gb300 as gvr
     # the balanced kernel's flags (512, 1024) belong to the *_ws entry points only; the short-row
-    # and cluster kernels cannot both be forced; 8192 is no flag
+    # and cluster kernels cannot both be forced; 16384 is no flag
     for bad in (dict(cluster_size=3), dict(cluster_size=32), dict(ring_stages=2), dict(ring_stages=17), dict(reserved=1),
-                dict(flags=512), dict(flags=1024), dict(flags=256 | 4096), dict(flags=8192)):
+                dict(flags=512), dict(flags=1024), dict(flags=256 | 4096), dict(flags=16384)):
         o = gvr.Options(**bad)
         st = lib.topk_decode_ex(ALIGNED, 1024, 4, ALIGNED, 1, 1, K, ALIGNED, None, None, ctypes.byref(o))
         assert st == 5, bad

@@ -4,7 +4,8 @@ The block-maxima side tensor bounds every 32-score block of a row's window ("Blo
 path for self-sampling GVR top-K decode", opt-in row pass); the first counting pass reads
 only the blocks whose bound reaches the sampled floor.  For any valid bounds the selection is
 the exact one: exact maxima, loose bounds, +inf (nothing skipped) and NaN bounds (read), on
-every workload, every forced path and in deterministic / sorted mode.
+every workload, every forced path and in deterministic / sorted mode -- through the per-row gate
+and with blocks skipped on every row.
 """
 from __future__ import annotations
 
@@ -55,23 +56,29 @@ def block_bounds(case, kind, seed=0):
     return out
 
 
+ALWAYS = 8192  # GVR_FLAG_BLOCKSKIP_ALWAYS: skip blocks whatever the samples' estimate
+
+
 def assert_blockskip_exact(gvr, case, kind="exact", flags=0, seed=0):
-    bm = block_bounds(case, kind, seed)
+    """Exact with the gate (the samples decide per row between skipping and the staged pass)
+    and with blocks skipped on every row."""
+    bm = torch.from_numpy(block_bounds(case, kind, seed)).to(DEV)
     lg = torch.from_numpy(case.logits).to(DEV)
     kv = torch.from_numpy(case.kv_lens).to(DEV)
-    st = torch.full((case.rows, 4), -7, dtype=torch.int32, device=DEV)
-    opts = gvr.Options(flags=flags)
-    opts.row_stats = st.data_ptr()
-    idx, vals = gvr.topk_decode(lg, kv, case.next_n, case.compress_ratio, case.k, want_values=True, options=opts,
-                                block_max=torch.from_numpy(bm).to(DEV))
-    torch.cuda.synchronize()
-    got, gv = idx.cpu().numpy(), vals.cpu().numpy()
     ref, _, _ = oracle.topk_decode(case.logits, case.kv_lens, case.next_n, case.compress_ratio, case.k)
-    bad, why = compare_rows(decode_windows(case.logits, case.kv_lens, case.next_n, case.compress_ratio), case.k,
-                            got, ref, got_values=gv)
-    assert bad == 0, f"{case.name}/{kind}/{flags}: {bad} inexact rows: {why}"
-    if flags & 32:
-        assert np.array_equal(got, ref)
+    for f in (flags, flags | ALWAYS):
+        st = torch.full((case.rows, 4), -7, dtype=torch.int32, device=DEV)
+        opts = gvr.Options(flags=f)
+        opts.row_stats = st.data_ptr()
+        idx, vals = gvr.topk_decode(lg, kv, case.next_n, case.compress_ratio, case.k, want_values=True, options=opts,
+                                    block_max=bm)
+        torch.cuda.synchronize()
+        got, gv = idx.cpu().numpy(), vals.cpu().numpy()
+        bad, why = compare_rows(decode_windows(case.logits, case.kv_lens, case.next_n, case.compress_ratio), case.k,
+                                got, ref, got_values=gv)
+        assert bad == 0, f"{case.name}/{kind}/{f}: {bad} inexact rows: {why}"
+        if f & 32:
+            assert np.array_equal(got, ref)
     return st.cpu().numpy()
 
 
@@ -85,6 +92,16 @@ def test_blockskip_peaky_batch(gvr, kind):
     """Block-concentrated rows, where most blocks fall below the floor and are never read."""
     assert_blockskip_exact(gvr, workloads.peaky_decode_batch(), kind, seed=8)
     assert_blockskip_exact(gvr, workloads.peaky_decode_batch(requests=8, next_n=3, hot_frac=0.002), kind, 32)
+
+
+def test_blockskip_block_concentrated_floor(gvr):
+    """On block-concentrated rows the two end runs (sink, recent tokens) hold most of the samples
+    at or above the floor while their neighbours hold few: the block-skip instantiation takes the
+    floor again from the interior runs, and most rows need no second counting pass."""
+    case = workloads.peaky_decode_batch(requests=24)
+    st = assert_blockskip_exact(gvr, case, "exact", seed=9)
+    long_rows = case.row_lengths() > case.k
+    assert ((st[long_rows, 2] % 10) == 2).sum() <= long_rows.sum() // 4, st
 
 
 @pytest.mark.parametrize("variant", workloads.ADVERSARIAL_VARIANTS)

@@ -470,8 +470,10 @@ def test_far_outlier_samples_trim_the_bins(gvr):
 
 def test_second_pass_block_concentrated(gvr):
     """Sink, recent tokens and hot blocks: the block64 runs at both row ends over-represent the
-    top, the sampled floor is too high and the rows need the second counting pass (scores below
-    the floor), then the collect reads the share again."""
+    top, the sampled floor of the plain path is too high and the rows need the second counting
+    pass (scores below the floor), then the collect reads the share again.  (Through the
+    block-skip entry point the floor is taken again from the interior runs: see
+    test_blockskip_gpu.py.)"""
     case = workloads.peaky_decode_batch(requests=24)
     st = assert_decode_exact(gvr, case, stats=True)
     long_rows = case.row_lengths() > case.k
