@@ -317,7 +317,8 @@ class ColdWarm:
 
 def _launchers(torch, gvr, dev, wsb):
     """Callables that run one decode / prefill call of a case through the *_ws entry points
-    (the default dispatch: the balanced kernel where it fits, else the cluster kernel)."""
+    (by default the cluster kernel; flags=1024, GVR_FLAG_SPLIT_KERNEL, asks for the balanced
+    kernel where the call fits it)."""
 
     def decode(case, flags=0):
         lg = torch.from_numpy(case.logits).to(dev)
@@ -472,7 +473,7 @@ def run_sweep(args):
         runs = (("cluster", lambda h, lg=lg, kv=kv, idx=idx, case=case: gvr.topk_decode_raw(
                     lg.data_ptr(), case.row_stride, case.rows, kv.data_ptr(), case.next_n, case.compress_ratio,
                     case.k, idx.data_ptr(), None, h)),
-                ("balanced", decode(case)),
+                ("balanced", decode(case, 1024)),
                 ("blockskip_on", lambda h, lg=lg, kv=kv, idx=idx, case=case, bm=bm: gvr.topk_decode_blockskip_raw(
                     lg.data_ptr(), case.row_stride, case.rows, kv.data_ptr(), case.next_n, case.compress_ratio,
                     case.k, bm.data_ptr(), bm.stride(0), idx.data_ptr(), None, h)))
