@@ -1488,12 +1488,18 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     const int bstar = cr.bin;
     // The candidates go to rank 0's ring, idle from now on: its first stage holds CAP of them
     // (scores, then indices), the whole ring up to nst * RING_CAND when rank 0 reads nothing again.
-    // A rank 0 that must read its share again in this collect does so from global memory.
+    // When rank 0 reads its share again in this collect (its list overflowed, or scores below the
+    // floor count), its list area is idle instead: up to CAP candidates go there and rank 0
+    // streams its share through its ring; more candidates keep the ring and rank 0 reads from
+    // global memory.  (Cluster-uniform: the rounds and rank 0's list flag in the pushed counts.)
     const bool big = cr.m > uint32_t(CAP);
+    const bool cand_in_list = !big && (rounds != 1 || S.unlisted >= UNLISTED_RANK0);
     const uint32_t ring_cap = uint32_t(nst) * RING_CAND;
     const uint32_t cand_cap = big ? ring_cap : uint32_t(CAP);
-    float* const cand_v = reinterpret_cast<float*>(&ring[0][0]);
-    int32_t* const cand_j = reinterpret_cast<int32_t*>(&ring[0][0]) + cand_cap;
+    static_assert(sizeof(float) * CAP + sizeof(int32_t) * CAP <= LIST_BYTES, "CAP candidates fit the list area");
+    float* const cand_v = cand_in_list ? &S.list_v[0] : reinterpret_cast<float*>(&ring[0][0]);
+    int32_t* const cand_j = (cand_in_list ? reinterpret_cast<int32_t*>(&S.list_v[0])
+                                          : reinterpret_cast<int32_t*>(&ring[0][0])) + cand_cap;
     const uint32_t rv = dsmem_map(smem_u32(cand_v), 0);
     const uint32_t rj = dsmem_map(smem_u32(cand_j), 0);
     auto place = [&](float e, int32_t jw, bool valid) {  // warp-collective
@@ -1529,10 +1535,51 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
         const bool hit = valid && e >= tb && e >= cthr;
         if (__any_sync(FULL_MASK, hit)) place(e, 4 * g + l - lead, hit);
       };
-      if (rank == 0)
+      // A staged share, with no warp collective: each thread marks its winners and candidates of
+      // the stage, takes their slots with one shared atomic per kind, and writes them.
+      auto collect_stage = [&](uint32_t slot, int32_t c0) {
+        uint32_t wm = 0, cm = 0;
+#pragma unroll
+        for (int i = 0; i < VPS; ++i) {
+          int32_t g;
+          float4 v;
+          const uint32_t ln = stage_vec(slot, c0, i, g, v);
+#pragma unroll
+          for (int l = 0; l < 4; ++l) {
+            const float e = f4_get(v, l);
+            if (((ln >> l) & 1u) && e >= tb && e >= cthr) {
+              const int b = value_bin(e, gmin, sc);
+              wm |= uint32_t(b > bstar) << (4 * i + l);
+              cm |= uint32_t(b == bstar) << (4 * i + l);
+            }
+          }
+        }
+        auto window_of = [&](int j) { return 4 * (c0 + (j >> 2) * T + tid) + (j & 3) - lead; };
+        if (wm) {
+          uint32_t at = S.base_above + atomicAdd(&S.ctr_win, uint32_t(__popc(wm)));
+          for (; wm; wm &= wm - 1u, ++at) {
+            const int j = __ffs(wm) - 1;
+            if (at < uint32_t(k)) {  // always true: counts match the histogram's
+              out[at] = window_of(j);
+              if (outv) outv[at] = stage_score(slot, c0, j);
+            }
+          }
+        }
+        if (cm) {
+          uint32_t c = S.base_cand + atomicAdd(&S.ctr_cand, uint32_t(__popc(cm)));
+          for (; cm; cm &= cm - 1u, ++c) {
+            const int j = __ffs(cm) - 1;
+            if (c < cand_cap) {  // always true: m fits the buffer on this path
+              dsmem_st_u32(rv + 4u * c, __float_as_uint(stage_score(slot, c0, j)));
+              dsmem_st_u32(rj + 4u * c, uint32_t(window_of(j)));
+            }
+          }
+        }
+      };
+      if (rank == 0 && !cand_in_list)
         global_pass(visit);  // rank 0's ring receives the candidates
       else
-        stream_pass(false, [&](uint32_t slot, int32_t c0) { each_lane(slot, c0, visit); });
+        stream_pass(false, collect_stage);
       report_timeout();
     }
     csync();  // every candidate has landed in rank 0's buffer
