@@ -1523,7 +1523,47 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     };
     if (!(rounds == 1 && listed)) rounds += 10;  // diagnostics: collect read the share again
     if (rounds == 1 && listed) {
-      each_listed([&](float e, int32_t jw, bool in) { place(e, jw, in); });
+      // From the list, with no warp collective: each thread counts its entries' winners and
+      // candidates, takes their slots with one shared atomic per kind, then writes them.
+      uint32_t pre[NW + 1];  // segment starts in the concatenated list
+      pre[0] = 0;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) pre[w + 1] = pre[w] + S.list_n[w];
+      auto slot_of = [&](uint32_t i) {  // entry i: its segment's base plus its offset in it
+        uint32_t at = i;
+#pragma unroll
+        for (int w = 1; w < NW; ++w)
+          if (i >= pre[w]) at = uint32_t(w * LSEG) + (i - pre[w]);
+        return at;
+      };
+      uint32_t nw = 0, nc = 0;
+      for (uint32_t i = tid; i < pre[NW]; i += T) {
+        const int b = value_bin(list_val(slot_of(i)), gmin, sc);
+        nw += b > bstar ? 1u : 0u;
+        nc += b == bstar ? 1u : 0u;
+      }
+      if (nw | nc) {
+        uint32_t wat = nw ? S.base_above + atomicAdd(&S.ctr_win, nw) : 0u;
+        uint32_t cat = nc ? S.base_cand + atomicAdd(&S.ctr_cand, nc) : 0u;
+        for (uint32_t i = tid; i < pre[NW]; i += T) {
+          const uint32_t at = slot_of(i);
+          const float e = list_val(at);
+          const int b = value_bin(e, gmin, sc);
+          if (b > bstar) {
+            if (wat < uint32_t(k)) {  // always true: counts match the histogram's
+              out[wat] = list_window(at);
+              if (outv) outv[wat] = e;
+            }
+            ++wat;
+          } else if (b == bstar) {
+            if (cat < cand_cap) {  // always true: m fits the buffer on this path
+              dsmem_st_u32(rv + 4u * cat, __float_as_uint(e));
+              dsmem_st_u32(rj + 4u * cat, uint32_t(list_window(at)));
+            }
+            ++cat;
+          }
+        }
+      }
     } else {  // the list overflowed or scores below the floor count: read the share again
       if (warp == 0) {
         const float t = bstar > 0 ? floor_value(bstar, gmin, sc) : -INFINITY;
