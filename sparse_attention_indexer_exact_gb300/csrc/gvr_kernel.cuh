@@ -1631,11 +1631,19 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     if ((mm <= uint32_t(RANK_REFINE_MAX) && !(p.flags & FLAG_RADIX_REFINE)) || det) {
       // (deterministic mode ranks every candidate set: ties by smallest index)
       // rank of candidate i = number of candidates ordered before it by (value desc, index asc)
+      static_assert(CAP % 4 == 0, "the candidate arrays start 16-byte aligned");
       for (uint32_t i = tid; i < mm; i += T) {
         const float v = cand_v[i];
         const int32_t j = cand_j[i];
         uint32_t r = 0;
-        for (uint32_t q = 0; q < mm; ++q) {
+        uint32_t q = 0;
+        for (; q + 4 <= mm; q += 4) {  // four candidates per pair of 16-byte loads
+          const float4 w = *reinterpret_cast<const float4*>(cand_v + q);
+          const int4 jj = *reinterpret_cast<const int4*>(cand_j + q);
+          r += uint32_t((w.x > v) || (w.x == v && jj.x < j)) + uint32_t((w.y > v) || (w.y == v && jj.y < j)) +
+               uint32_t((w.z > v) || (w.z == v && jj.z < j)) + uint32_t((w.w > v) || (w.w == v && jj.w < j));
+        }
+        for (; q < mm; ++q) {
           const float w = cand_v[q];
           const int32_t jj = cand_j[q];
           r += (w > v) || (w == v && jj < j);
@@ -1646,9 +1654,35 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
         }
       }
     } else {
-      uint32_t prefix = 0, pmask = 0, rneed = need;
+      // The candidates' smallest and largest order key: the digits they share are fixed before
+      // the first digit pass (a crossing bin is narrow, its keys usually share one or two bytes),
+      // and equal keys are all ties at once.
+      uint32_t kmin = 0xffffffffu, kmax = 0u;
+      for (uint32_t i = tid; i < mm; i += T) {
+        const uint32_t key = order_key(cand_v[i]);
+        kmin = min(kmin, key);
+        kmax = max(kmax, key);
+      }
+      kmin = __reduce_min_sync(FULL_MASK, kmin);
+      kmax = __reduce_max_sync(FULL_MASK, kmax);
+      if (tid == 0) {
+        S.kmin_loc = 0xffffffffu;
+        S.kmax_loc = 0u;
+      }
+      __syncthreads();
+      if (lane == 0) {
+        atomicMin(&S.kmin_loc, kmin);
+        atomicMax(&S.kmax_loc, kmax);
+      }
+      __syncthreads();
+      kmin = S.kmin_loc;
+      kmax = S.kmax_loc;
+      const int dfix = kmin == kmax ? 4 : __clz(kmin ^ kmax) / 8;  // whole shared bytes
+      uint32_t prefix = dfix >= 4 ? kmin : (dfix > 0 ? kmin & (0xffffffffu << (32 - 8 * dfix)) : 0u);
+      uint32_t pmask = dfix >= 4 ? 0xffffffffu : (dfix > 0 ? 0xffffffffu << (32 - 8 * dfix) : 0u);
+      uint32_t rneed = need;
       bool ge = false;
-      for (int pass = 0; pass < 4; ++pass) {
+      for (int pass = dfix; pass < 4; ++pass) {
         const int shift = 24 - 8 * pass;
         for (int i = tid; i < 256; i += T) digit_hist(S, 0)[i] = 0;
         __syncthreads();
@@ -1673,23 +1707,33 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       }
       const uint32_t nties = ge ? 0u : rneed;
       const uint32_t win_base = cr.above, tie_base = cr.above + (need - nties);
-      for (uint32_t b0 = 0; b0 < mm; b0 += T) {
-        const uint32_t i = b0 + tid;
-        const bool in = i < mm;
-        const uint32_t key = in ? order_key(cand_v[i]) : 0u;
-        const bool win = in && (ge ? (key & pmask) >= prefix : key > prefix);
-        const bool tie = in && !ge && key == prefix;
-        const uint32_t ws = warp_alloc_local(&S.ctr_rwin, win);
-        if (win && win_base + ws < tie_base) {
-          out[win_base + ws] = cand_j[i];
-          if (outv) outv[win_base + ws] = cand_v[i];
-        }
-        const uint32_t ts = warp_alloc_local(&S.ctr_rtie, tie);
-        if (tie && ts < nties) {
-          out[tie_base + ts] = cand_j[i];
-          if (outv) outv[tie_base + ts] = cand_v[i];
-        }
+      // emission with no warp collective: each thread counts its winners and ties, takes their
+      // slots with one shared atomic per kind, then writes them
+      uint32_t nw = 0, nt = 0;
+      for (uint32_t i = tid; i < mm; i += T) {
+        const uint32_t key = order_key(cand_v[i]);
+        nw += (ge ? (key & pmask) >= prefix : key > prefix) ? 1u : 0u;
+        nt += (!ge && key == prefix) ? 1u : 0u;
       }
+      uint32_t ws = nw ? atomicAdd(&S.ctr_rwin, nw) : 0u;
+      uint32_t ts = nt ? atomicAdd(&S.ctr_rtie, nt) : 0u;
+      if (nw | nt)
+        for (uint32_t i = tid; i < mm; i += T) {
+          const uint32_t key = order_key(cand_v[i]);
+          if (ge ? (key & pmask) >= prefix : key > prefix) {
+            if (win_base + ws < tie_base) {
+              out[win_base + ws] = cand_j[i];
+              if (outv) outv[win_base + ws] = cand_v[i];
+            }
+            ++ws;
+          } else if (!ge && key == prefix) {
+            if (ts < nties) {
+              out[tie_base + ts] = cand_j[i];
+              if (outv) outv[tie_base + ts] = cand_v[i];
+            }
+            ++ts;
+          }
+        }
     }
     __syncthreads();
     const bool failed = S.err || S.tout;
