@@ -164,7 +164,7 @@ struct alignas(16) Smem {
   float wmax[8];
   float4 tail;                     // the partial last vector of the window, NaN-padded
   Crossing cross;
-  float vthr;
+  float vthr, vthr1;
   int32_t fpart;
   uint32_t dsel, dabove, dcnt, dmy_above, dmy_at;
   uint32_t kmin_loc, kmax_loc;     // rescue: smallest / largest key of this CTA's matching scores
@@ -1008,6 +1008,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   // same floor).  Above 1/16 the row takes the staged pass.  Counted before the floor's
   // barrier, read after it.
   bool skip_blocks = false;
+  uint32_t floor_want = 0;  // samples at or above the floor (0: no floor)
   float sc = 0.f;
   float thr = -INFINITY;  // floor: scores >= thr are counted (and listed) in the first pass
   int fpart = -1;         // bin(thr): the one partially counted bin; -1 = no floor
@@ -1021,6 +1022,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       const float mu = float(k) * float(nsamp) / float(nv);
       const float want_f = mu + 3.0f * sqrtf(mu) + 6.0f;
       const uint32_t want = want_f < float(nsamp) ? uint32_t(want_f) : nsamp;
+      floor_want = want;
       // The samples' own histogram on the same bins (in this CTA's private counts, cleared
       // again below): the floor is the lower edge of the bin where `want` samples are reached.
 #pragma unroll
@@ -1144,6 +1146,15 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     // Pass 1 counts (and lists) the scores >= thr; pass 2, only when the crossing falls in
     // the partial bin or below, counts the rest.
     uint32_t wlist = 0;  // scores this warp has appended (warp-uniform; may exceed LSEG)
+    // Dense share: when the floor lets through more of this CTA's scores than its list holds
+    // (by the samples' share above it, with a quarter of margin) -- K = 2048 on a window of a
+    // few thousand scores -- the list would overflow and the collect read the share again
+    // anyway, so the pass only counts from the start: no list slots, no list stores, no walk of
+    // the list after the pass.  The list is marked incomplete.  (A floor of -FLT_MAX keeps
+    // listing: the -inf fill needs every CTA's list.)
+    const bool dense_start = floor_want > 0u && thr > -FLT_MAX &&
+                             uint64_t(4u * floor_want) * uint64_t(nstages) * uint64_t(4 * STAGE_VEC) >
+                                 uint64_t(5u) * nsamp * uint64_t(LCAP);
     float* const seg_v = (L16 ? S.list_v16 : S.list_v) + warp * LSEG;  // this warp's segment
     int32_t* const seg_j = S.list_j + warp * LSEG;
     uint16_t* const seg_p = S.list_p16 + warp * LSEG;
@@ -1156,10 +1167,11 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
       // tie class costs one atomic per thread for the whole pass).  The counter then exceeds
       // the segment, which marks the list incomplete; the counts stay exact either way.
       constexpr int NE = 4 * VPS;
-      bool full = false;                   // this thread saw its warp's segment full
+      bool full = dense_start;             // this thread saw its warp's segment full
+      if (dense_start && lane == 0) S.list_n[warp] = uint32_t(LSEG) + 1u;  // incomplete, holds nothing
       uint32_t rb = 0xffffffffu, rrun = 0;  // its run of counted hits in bin rb
       float rv = __int_as_float(0x7fffffff);  // the run's last value (NaN: none yet)
-      uint32_t hk0 = 0xffffffffu, hk1 = 0u;   // smallest / largest key of its hits
+      float hv0 = INFINITY, hv1 = -INFINITY;  // smallest / largest of its hits (NaN never hits)
       const int32_t ring_stages = skip_blocks ? (nstages < nst ? nstages : nst) : nstages;
       stream_pass(true, [&](uint32_t slot, int32_t c0) {
         float4 vv[VPS];
@@ -1208,37 +1220,40 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
           rrun += uint32_t(__popc(bits));
           return;
         }
+        // Otherwise every hit of the stage is added on its own, with no dependence between them
+        // (all bins first, then one atomic per hit); the stage's first hit becomes the run's value
+        // for the stages after (a tie class then takes the shortcut above).
+        uint32_t bj[NE];
+#pragma unroll
+        for (int j = 0; j < NE; ++j) bj[j] = uint32_t(value_bin(f4_get(vv[j >> 2], j & 3), gmin, sc));
 #pragma unroll
         for (int j = 0; j < NE; ++j)
           if ((bits >> j) & 1u) {
             const float e = f4_get(vv[j >> 2], j & 3);
-            if (e != rv) {
-              hk0 = min(hk0, order_key(e));
-              hk1 = max(hk1, order_key(e));
-              const uint32_t b = uint32_t(value_bin(e, gmin, sc));
-              if (b != rb) {
-                if (rrun) atomicAdd(&S.hist[rb], rrun);
-                rb = b;
-                rrun = 0;
-              }
-              rv = e;
-            }
-            ++rrun;
+            atomicAdd(&S.hist[bj[j]], 1u);
+            hv0 = fminf(hv0, e);
+            hv1 = fmaxf(hv1, e);
           }
+        if (rrun) atomicAdd(&S.hist[rb], rrun);
+        const int jf = __ffs(bits) - 1;
+        rv = stage_score(slot, c0, jf);
+        rb = uint32_t(value_bin(rv, gmin, sc));
+        rrun = 0;
       }, ring_stages);
       if (rrun) atomicAdd(&S.hist[rb], rrun);
       __syncwarp();
       wlist = S.list_n[warp];
       // The listed hits' bins, counted once per list entry (the entries past a full segment
       // were counted during the pass).
-      const uint32_t nl = wlist < uint32_t(LSEG) ? wlist : uint32_t(LSEG);
+      const uint32_t nl = dense_start ? 0u : (wlist < uint32_t(LSEG) ? wlist : uint32_t(LSEG));
       for (uint32_t i = uint32_t(lane); i < nl; i += 32u) {
         const float e = seg_v[i];
         atomicAdd(&S.hist[value_bin(e, gmin, sc)], 1u);
-        hk0 = min(hk0, order_key(e));
-        hk1 = max(hk1, order_key(e));
+        hv0 = fminf(hv0, e);
+        hv1 = fmaxf(hv1, e);
       }
       // this CTA's key bounds of the scores >= thr (for a row whose scores >= thr are one value)
+      uint32_t hk0 = hv0 <= hv1 ? order_key(hv0) : 0xffffffffu, hk1 = hv0 <= hv1 ? order_key(hv1) : 0u;
       hk0 = __reduce_min_sync(FULL_MASK, hk0);
       hk1 = __reduce_max_sync(FULL_MASK, hk1);
       if (lane == 0 && hk0 <= hk1) {
@@ -1326,8 +1341,10 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     auto publish_bounds = [&]() {
       if (!bmax_row && uint32_t(tid) < cs) {
         uint32_t lc = 0;
+        if (!dense_start) {
 #pragma unroll
-        for (int w = 0; w < NW; ++w) lc += min(S.list_n[w], uint32_t(LSEG));
+          for (int w = 0; w < NW; ++w) lc += min(S.list_n[w], uint32_t(LSEG));
+        }
         const uint32_t c = uint32_t(tid);
         if (S.kmin_loc <= S.kmax_loc) {
           dsmem_red_min(dsmem_map(smem_u32(&S.hk_min), c), S.kmin_loc);
@@ -1567,16 +1584,23 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
     } else {  // the list overflowed or scores below the floor count: read the share again
       if (warp == 0) {
         const float t = bstar > 0 ? floor_value(bstar, gmin, sc) : -INFINITY;
-        if (lane == 0) S.vthr = t;
+        const float t1 = bstar < NB - 1 ? floor_value(bstar + 1, gmin, sc) : INFINITY;
+        if (lane == 0) {
+          S.vthr = t;
+          S.vthr1 = t1;
+        }
       }
       __syncthreads();
       const float tb = S.vthr;  // scores >= tb are exactly those in bins >= b*
+      const float tb1 = S.vthr1;  // ... and >= tb1 those in bins > b* (none when b* is the top bin)
+      const bool top = bstar == NB - 1;
       auto visit = [&](float e, int32_t g, bool valid, int l) {
         const bool hit = valid && e >= tb && e >= cthr;
         if (__any_sync(FULL_MASK, hit)) place(e, 4 * g + l - lead, hit);
       };
       // A staged share, with no warp collective: each thread marks its winners and candidates of
-      // the stage, takes their slots with one shared atomic per kind, and writes them.
+      // the stage, takes their slots with one shared atomic per kind, and writes them.  (A warp
+      // prefix of the counts, one atomic per warp, measured slower even on dense rows.)
       auto collect_stage = [&](uint32_t slot, int32_t c0) {
         uint32_t wm = 0, cm = 0;
 #pragma unroll
@@ -1587,10 +1611,10 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
 #pragma unroll
           for (int l = 0; l < 4; ++l) {
             const float e = f4_get(v, l);
-            if (((ln >> l) & 1u) && e >= tb && e >= cthr) {
-              const int b = value_bin(e, gmin, sc);
-              wm |= uint32_t(b > bstar) << (4 * i + l);
-              cm |= uint32_t(b == bstar) << (4 * i + l);
+            if (((ln >> l) & 1u) && e >= tb && e >= cthr) {  // bins are monotone: compares only
+              const bool above = !top && e >= tb1;
+              wm |= uint32_t(above) << (4 * i + l);
+              cm |= uint32_t(!above) << (4 * i + l);
             }
           }
         }
