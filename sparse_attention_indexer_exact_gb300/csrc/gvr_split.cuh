@@ -381,8 +381,8 @@ __global__ void __launch_bounds__(THREADS, SPLIT_CTAS_PER_SM) gvr_split_kernel(c
 
   // ---------------------------------------------------------------- verify: publish >= t
   // One compare against the floor per score (a thread first takes the max of its 8 scores of
-  // the stage); each warp takes its slots with one shared atomic per stage; the published
-  // (score, window index) pairs go straight to the chunk's slot of the workspace.
+  // the stage); a thread with scores at or above it takes their slots with one shared atomic;
+  // the published (score, window index) pairs go straight to the chunk's slot of the workspace.
   float* const my_v = p.surv_v + size_t(unit) * SPLIT_UNIT_CAP;
   int32_t* const my_j = p.surv_j + size_t(unit) * SPLIT_UNIT_CAP;
   bool late = false;
@@ -431,38 +431,18 @@ __global__ void __launch_bounds__(THREADS, SPLIT_CTAS_PER_SM) gvr_split_kernel(c
                 << (4 * i);
       bits &= lanes;
     }
-    const uint32_t nhit = __popc(bits);
-    const unsigned lt = lanemask_lt();
-    const unsigned m0 = __ballot_sync(FULL_MASK, nhit & 1u), m1 = __ballot_sync(FULL_MASK, nhit & 2u);
-    uint32_t excl = uint32_t(__popc(m0 & lt)) + (uint32_t(__popc(m1 & lt)) << 1);
-    uint32_t wtot = uint32_t(__popc(m0)) + (uint32_t(__popc(m1)) << 1);
-    if (__any_sync(FULL_MASK, nhit >= 4u)) {
-      const unsigned m2 = __ballot_sync(FULL_MASK, nhit & 4u), m3 = __ballot_sync(FULL_MASK, nhit & 8u);
-      excl += (uint32_t(__popc(m2 & lt)) << 2) + (uint32_t(__popc(m3 & lt)) << 3);
-      wtot += (uint32_t(__popc(m2)) << 2) + (uint32_t(__popc(m3)) << 3);
-    }
-    if (wtot) {
-      uint32_t wbase = 0;
-      if (lane == 0) wbase = atomicAdd(&S.nsurv, wtot);
-      uint32_t at = __shfl_sync(FULL_MASK, wbase, 0) + excl;
-      if (bits && !alone) {
-#pragma unroll
-        for (int i = 0; i < VPS; ++i) {
-          const uint32_t nib = (bits >> (4 * i)) & 0xFu;
-          if (nib) {
-            const int32_t jw = 4 * (c0 + i * T + tid) - lead;  // window index of lane 0
-#pragma unroll
-            for (int l = 0; l < 4; ++l)
-              if ((nib >> l) & 1u) {
-                if (at < uint32_t(SPLIT_UNIT_CAP)) {
-                  my_v[at] = f4_get(vv[i], l);
-                  my_j[at] = jw + l;
-                }
-                ++at;
-              }
+    static_assert(VPS == 2, "a stage's hit j lies in the thread's first or last vector");
+    if (bits) {  // no warp collective: the thread's slots with one shared atomic
+      uint32_t at = atomicAdd(&S.nsurv, uint32_t(__popc(bits)));
+      if (!alone)
+        for (; bits; bits &= bits - 1u, ++at) {
+          const int j = __ffs(bits) - 1;
+          if (at < uint32_t(SPLIT_UNIT_CAP)) {
+            const float4 v = (j >> 2) == 0 ? vv[0] : vv[VPS - 1];
+            my_v[at] = f4_get(v, j & 3);
+            my_j[at] = 4 * (c0 + (j >> 2) * T + tid) - lead + (j & 3);
           }
         }
-      }
     }
     if (s + SPLIT_NST < nst) {  // refill this slot once every thread is done with it
       if (__syncthreads_or(late)) {
@@ -620,9 +600,40 @@ __global__ void __launch_bounds__(THREADS, SPLIT_CTAS_PER_SM) gvr_split_kernel(c
     // stopping once the keys above the chosen digit are exactly the ones needed or every
     // remaining key is equal.
     const uint32_t bstar = fc.digit;
-    uint32_t prefix = 0, pmask = 0, rneed = uint32_t(k) - cr.above;
+    // A crossing bin of at most SPLIT_MAX_UNITS_ROW members is listed once (their stash slots, in
+    // the per-chunk counts, idle by now) with its smallest and largest key: the digit passes then
+    // read only the members, below the key bytes they all share.
+    const bool compact = cr.m <= uint32_t(SPLIT_MAX_UNITS_ROW);
+    if (tid == 0) {
+      S.kmin_loc = 0xffffffffu;
+      S.kmax_loc = 0u;
+    }
+    __syncthreads();
+    if (compact) {
+      uint32_t tmin = 0xffffffffu, tmax = 0u;
+      for (uint32_t e = tid; e < gn; e += T)
+        if (gj[e] >= 0 && fbin(gv[e]) == bstar) {
+          const uint32_t key = order_key(gv[e]);
+          S.cnt[atomicAdd(&S.ctr_cand, 1u)] = e;  // at most cr.m of them
+          tmin = min(tmin, key);
+          tmax = max(tmax, key);
+        }
+      tmin = __reduce_min_sync(FULL_MASK, tmin);
+      tmax = __reduce_max_sync(FULL_MASK, tmax);
+      if (lane == 0) {
+        atomicMin(&S.kmin_loc, tmin);
+        atomicMax(&S.kmax_loc, tmax);
+      }
+      __syncthreads();
+    }
+    const uint32_t kmin0 = S.kmin_loc, kmax0 = S.kmax_loc;
+    const int dfix = !compact ? 0 : (kmin0 == kmax0 ? 4 : __clz(kmin0 ^ kmax0) / 8);
+    uint32_t prefix = dfix >= 4 ? kmin0 : (dfix > 0 ? kmin0 & (0xffffffffu << (32 - 8 * dfix)) : 0u);
+    uint32_t pmask = dfix >= 4 ? 0xffffffffu : (dfix > 0 ? 0xffffffffu << (32 - 8 * dfix) : 0u);
+    uint32_t rneed = uint32_t(k) - cr.above;
     bool ge = false;
-    for (int shift = 24; shift >= 0; shift -= 8) {
+    __syncthreads();  // every thread has read the bounds before they are reset below
+    for (int shift = 24 - 8 * dfix; shift >= 0; shift -= 8) {
       for (int i = tid; i < 256; i += T) S.fh[i] = 0;
       if (tid == 0) {
         S.kmin_loc = 0xffffffffu;
@@ -630,15 +641,19 @@ __global__ void __launch_bounds__(THREADS, SPLIT_CTAS_PER_SM) gvr_split_kernel(c
       }
       __syncthreads();
       uint32_t tmin = 0xffffffffu, tmax = 0u;
-      for (uint32_t e = tid; e < gn; e += T) {
-        if (gj[e] < 0) continue;
-        const float v = gv[e];
+      auto count = [&](float v) {
         const uint32_t key = order_key(v);
-        if (fbin(v) == bstar && (key & pmask) == prefix) {
+        if ((key & pmask) == prefix) {
           atomicAdd(&S.fh[(key >> shift) & 255u], 1u);
           tmin = min(tmin, key);
           tmax = max(tmax, key);
         }
+      };
+      if (compact) {
+        for (uint32_t i = tid; i < cr.m; i += T) count(gv[S.cnt[i]]);
+      } else {
+        for (uint32_t e = tid; e < gn; e += T)
+          if (gj[e] >= 0 && fbin(gv[e]) == bstar) count(gv[e]);
       }
       tmin = __reduce_min_sync(FULL_MASK, tmin);
       tmax = __reduce_max_sync(FULL_MASK, tmax);
