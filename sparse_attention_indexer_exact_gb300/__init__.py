@@ -29,8 +29,9 @@ __all__ = ["topk_decode", "topk_prefill", "topk_decode_raw", "topk_decode_hinted
            "workspace_size", "workspace", "plan",
            "Options",
            "GvrError", "library_path", "load_library", "FLAG_FORCE_RESCUE", "FLAG_NO_FLOOR", "FLAG_ZERO_CAP",
-           "FLAG_RADIX_REFINE", "FLAG_DETERMINISTIC", "FLAG_SORTED", "FLAG_STREAM_RESCUE", "FLAG_COMPACT_LISTS", "PATH_NAMES",
-           "SUPPORTED_K"]
+           "FLAG_RADIX_REFINE", "FLAG_DETERMINISTIC", "FLAG_SORTED", "FLAG_STREAM_RESCUE", "FLAG_COMPACT_LISTS",
+           "FLAG_CLUSTER_KERNEL", "FLAG_SPLIT_ALONE", "FLAG_SPLIT_KERNEL", "FLAG_DIAG_FAIL_ROW0", "FLAG_SHORT_KERNEL",
+           "FLAG_BLOCKSKIP_ALWAYS", "PATH_NAMES", "SUPPORTED_K"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libgvrtopk.so")
