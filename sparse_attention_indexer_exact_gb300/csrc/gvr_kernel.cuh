@@ -376,12 +376,17 @@ __device__ __forceinline__ int suffix_cross(SM& S, const uint32_t* arr, uint32_t
   constexpr int NW = T / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int lo_bin = NB - BPT * (tid + 1);
+  static_assert(BPT % 4 == 0, "bins per thread are read as 16-byte vectors (arr 16-byte aligned)");
   uint32_t c[BPT];
   uint32_t st = 0;
 #pragma unroll
-  for (int j = 0; j < BPT; ++j) {
-    c[j] = arr[lo_bin + BPT - 1 - j];
-    st += c[j];
+  for (int q = 0; q < BPT / 4; ++q) {
+    const uint4 v = *reinterpret_cast<const uint4*>(arr + lo_bin + 4 * q);
+    c[BPT - 1 - 4 * q] = v.x;  // descending position of bin lo_bin + 4q + e
+    c[BPT - 2 - 4 * q] = v.y;
+    c[BPT - 3 - 4 * q] = v.z;
+    c[BPT - 4 - 4 * q] = v.w;
+    st += v.x + v.y + v.z + v.w;
   }
   uint32_t it = st;
 #pragma unroll
@@ -866,7 +871,11 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
   if (warp == 0)
     for (int32_t s = lane; s < nst && s < nstages; s += 32) issue_stage(s, uint32_t(s));
   // Zero the counters while the samples are in flight (global loads are not waited for here).
-  for (int i = tid; i < NB + 4; i += T) S.hist[i] = S.tot[i] = 0;
+  static_assert((NB + 4) % 4 == 0, "histograms are cleared as 16-byte vectors");
+  for (int i = tid; i < (NB + 4) / 4; i += T) {
+    reinterpret_cast<uint4*>(S.hist)[i] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4*>(S.tot)[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
   if (tid == 0) {
     for (int w = 0; w < NW; ++w) S.list_n[w] = 0;
     S.ctr_win = S.ctr_cand = S.ctr_rwin = S.ctr_rtie = 0;
@@ -1099,7 +1108,7 @@ __global__ void __launch_bounds__(THREADS, 7) gvr_topk_kernel(const Params p) {
         S.fpart = value_bin(t, gmin, sc);
       };
       if (tid == 0) set_floor();
-      for (int i = tid; i < NB; i += T) S.hist[i] = 0;
+      for (int i = tid; i < NB / 4; i += T) reinterpret_cast<uint4*>(S.hist)[i] = make_uint4(0u, 0u, 0u, 0u);
       __syncthreads();
       if (BSK && bmax_row)
         skip_blocks = (p.flags & FLAG_BLOCKSKIP_ALWAYS) || (S.saved > 0u && 16u * S.rec_n <= S.saved);
