@@ -714,6 +714,40 @@ def test_device_error_reporting(gvr):
         assert (st[1:, 0] >= 0).all()
 
 
+# ----------------------------------------------------------------------------- dense shares
+@pytest.mark.parametrize("flags", [0, 128])  # 128: the compact lists
+@pytest.mark.parametrize("cs", [1, 2])
+def test_dense_shares(gvr, flags, cs):
+    """K = 2048 on windows of a few thousand scores with one or two CTAs per row: the floor lets
+    about half of every share through, more than a CTA's list holds, so the first pass only
+    counts (hits added one by one, tie runs by popcount), the collect reads the share again
+    (winners told from candidates by the crossing bin's edges) and rank 0's candidates go to its
+    list area.  Decode with values -- plain, few distinct values, a tie class at the top -- and
+    prefill with every lead."""
+    g = np.random.default_rng(95 + cs)
+    stride, k = 8192, 2048
+    kv = np.array([2049, 2500, 3000, 4096, 4097, 5000, 6000, 7000, 8000, 8191, 8192, 2052], np.int32)
+    lg = g.standard_normal((kv.size, stride)).astype(np.float32)
+    lg[3] = np.round(lg[3] * 2) / 2  # a handful of distinct values: tie runs in the count-only pass
+    lg[7, g.choice(7000, 2600, replace=False)] = 9.0  # a tie class above the rest holds tau
+    for r, n in enumerate(kv):
+        lg[r, n:] = workloads.DECODE_POISON[np.arange(n, stride) % 3]
+    case = workloads.DecodeCase("dense_decode", lg, kv, 1, 1, k)
+    opts = gvr.Options(cluster_size=cs, flags=flags)
+    assert_decode_exact(gvr, case, values=True, options=opts)
+    assert_decode_exact(gvr, case, options=opts)
+    rows = []
+    for r in range(8):
+        ks = 4 * int(g.integers(0, 100)) + r % 4
+        ke = ks + int(g.integers(2100, 7600))
+        row = workloads.PREFILL_POISON[np.arange(stride) % 4].copy()
+        row[ks:ke] = g.standard_normal(ke - ks).astype(np.float32)
+        rows.append((row, ks, ke))
+    pcase = workloads.PrefillCase("dense_prefill", np.stack([x[0] for x in rows]), np.array([x[1] for x in rows], np.int32),
+                                  np.array([x[2] for x in rows], np.int32), k)
+    assert_prefill_exact(gvr, pcase, options=opts)
+
+
 # ----------------------------------------------------------------------------- one value above the floor
 def test_one_value_above_the_floor(gvr):
     """Rows whose scores at or above the sampled floor are all one value: the tie slots come from
