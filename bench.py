@@ -485,6 +485,57 @@ def run_sweep(args):
     return 0
 
 
+def run_prefill_tile(args):
+    """The 4096-row prefill tile alone, through topk_prefill: --steps graph-replayed calls rotating
+    over --copies device copies of the tile (cold L2), CUDA events on the launching stream; one
+    JSON line (not the headline)."""
+    import torch
+    import workloads
+    import sparse_attention_indexer_exact_gb300 as gvr
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (no CPU fallback exists)")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    gvr.load_library()
+    case = workloads.prefill_tile()
+    copies = max(1, args.copies)
+    bufs = [torch.from_numpy(case.logits).to(dev) for _ in range(copies)]
+    ks = torch.from_numpy(case.row_starts).to(dev)
+    ke = torch.from_numpy(case.row_ends).to(dev)
+    idx = torch.empty((case.rows, case.k), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def launch(buf, h):
+        gvr.topk_prefill_raw(buf.data_ptr(), case.row_stride, case.rows, ks.data_ptr(), ke.data_ptr(), case.k,
+                             idx.data_ptr(), h)
+
+    for i in range(args.warmup):
+        launch(bufs[i % copies], stream.cuda_stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        h = torch.cuda.current_stream().cuda_stream
+        for i in range(copies):
+            launch(bufs[i], h)
+    g.replay()
+    torch.cuda.synchronize()
+    reps = max(1, args.steps // copies)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    per = e0.elapsed_time(e1) * 1e3 / (reps * copies)
+    nbytes = prefill_algorithmic_bytes(case)
+    peak, peak_kind = measured_peak_hbm()
+    print(json.dumps({"workload": case.meta.get("workload", "prefill tile"), "rows": case.rows, "k": case.k,
+                      "calls": reps * copies, "copies": copies, "us_per_call": per,
+                      "rows_per_s": case.rows / (per * 1e-6), "algorithmic_bytes": nbytes,
+                      "frac_of_measured": nbytes / per / 1e3 / peak, "peak_kind": peak_kind}))
+    return 0
+
+
 def config_block(case, ws):
     return {"workload": f"decode batch: {case.meta['workload']}", "rows_per_gpu": case.rows,
             "global_rows": case.rows * ws, "k": case.k, "row_stride": case.row_stride,
@@ -509,10 +560,14 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the sweep_big / tail / single_row / prefill_tile keys")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the headline line: every sweep cell and the adversarial tail check")
+    ap.add_argument("--workload", choices=["decode_batch", "prefill_tile"], default="decode_batch",
+                    help="prefill_tile: one line for the 4096-row prefill tile alone (for profiling it)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.sweep:
         return run_sweep(args)
+    if args.workload == "prefill_tile":
+        return run_prefill_tile(args)
 
     import workloads
     ws, rank, local = dist_env()
