@@ -610,7 +610,9 @@ def main():
     st = torch.full((rows, 4), -1, dtype=torch.int32, device=dev)
     launch(bufs[0], stream.cuda_stream, gvr.Options(row_stats=st.data_ptr()))
     torch.cuda.synchronize()
-    kernel = "gvr_split_kernel" if bool(((st[:, 0] == 7) | (st[:, 0] == 8)).any()) else "gvr_topk_kernel"
+    paths = st[:, 0]
+    kernel = ("gvr_split_kernel" if bool(((paths == 7) | (paths == 8)).any()) else
+              "gvr_short_kernel" if bool(((paths == 10) | (paths == 11)).any()) else "gvr_topk_kernel")
 
     def make_graph(buffers):
         g = torch.cuda.CUDAGraph()

@@ -138,10 +138,12 @@ enum {
    * become -2 and its row_stats path GVR_PATH_DEVICE_ERROR while the other rows stay exact --
    * the failure path without a failure */
   GVR_FLAG_DIAG_FAIL_ROW0 = 2048,
-  /* opt-in: the short-row kernel for calls it takes (row_stride <= 16384, no other flag, no
-   * cluster or ring setting, no hint or block maxima; others run the cluster kernel): one CTA
-   * of 256 threads holds a whole row in registers.  Exact, but measured slower than the cluster
-   * kernel on every short-row workload tried, so never chosen by default */
+  /* the short-row kernel for calls it takes (row_stride <= 16384, no flag but
+   * GVR_FLAG_FORCE_RESCUE, no cluster or ring setting, not the hinted or block-skip entry
+   * points; others run the cluster kernel) whatever the row count: one CTA of 1024 threads per
+   * row stages the whole window in shared memory with bulk copies and selects over it.  Calls
+   * with no flag take it by default when row_stride <= 16384 and the rows fit four waves of its
+   * CTAs (two per SM), where it measured faster than the cluster kernel */
   GVR_FLAG_SHORT_KERNEL = 4096,
   /* topk_decode_blockskip: skip blocks whatever the samples estimate (the gate is not applied) */
   GVR_FLAG_BLOCKSKIP_ALWAYS = 8192
@@ -182,9 +184,10 @@ enum {
   GVR_PATH_NEG_INF_FILL = 9,    /* fewer than k scores above -inf: every other score is a winner,
                                    the remaining slots take -inf scores (tau = -inf), one pass */
   GVR_PATH_SHORT_KERNEL = 10,   /* short-row kernel: histogram, crossing bin, refine, all over the
-                                   row held in registers */
-  GVR_PATH_SHORT_RADIX = 11     /* short-row kernel: exact radix select over the row in registers
-                                   (invalid bracket, floor too high, crossing bin too big) */
+                                   window staged in shared memory */
+  GVR_PATH_SHORT_RADIX = 11     /* short-row kernel: exact radix select over the staged window
+                                   (invalid bracket, floor too high, too many scores at or above
+                                   it, crossing bin too big, forced rescue) */
 };
 
 /* topk_decode with tuning/diagnostic options (NULL = automatic, identical to topk_decode). */
@@ -313,9 +316,11 @@ gvr_status topk_decode_noalloc(const float* logits, int64_t row_stride, int64_t 
 const char* gvr_status_string(gvr_status status);
 
 /*
- * The launch geometry the library would choose for a call on the current device (host
- * only, no device work): CTAs per row (cluster size), 4 KB stages of each CTA's shared-memory
- * ring, threads per CTA and dynamic shared memory bytes per CTA.  Returns the GVR_ERR_* code
+ * The launch geometry the library would choose for a plain topk_decode / topk_prefill call on
+ * the current device (host only, no device work): CTAs per row (cluster size), 4 KB stages of
+ * each CTA's shared-memory ring, threads per CTA and dynamic shared memory bytes per CTA.  The
+ * short-row kernel (see GVR_FLAG_SHORT_KERNEL) reads as cluster size 1, ring stages 0 and
+ * 1024 threads.  Returns the GVR_ERR_* code
  * the entry points would return for these arguments.  sm_count > 0 plans for a GB300-class
  * device with that many SMs (228 KB shared memory per SM) without touching a device; any
  * output pointer may be NULL.

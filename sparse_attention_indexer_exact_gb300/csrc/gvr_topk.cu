@@ -62,6 +62,9 @@ cudaError_t set_attributes() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(gvr::gvr_split_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              gvr::split_smem_bytes());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gvr::gvr_short_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(gvr::short_smem_bytes(gvr::SHORT_MAX)));
   return e;
 }
 
@@ -210,15 +213,31 @@ Geometry plan_geometry(int64_t row_stride, int64_t num_rows, int32_t k, int sms,
   return g;
 }
 
-// The short-row kernel takes a plain call (no extended mode, no diagnostics, no cluster tuning)
-// whose rows fit its shared memory; GVR_FLAG_SHORT_KERNEL asks for it, GVR_FLAG_CLUSTER_KERNEL
-// keeps the cluster kernel.
-bool use_short(const gvr::Params& prm, const gvr_options* o) {
-  if (prm.row_stride > gvr::SHORT_MAX || prm.pre_idx || prm.block_max) return false;
-  const int32_t flags = o ? o->flags : 0;
-  if (flags != GVR_FLAG_SHORT_KERNEL) return false;  // opt-in: measured slower than the cluster kernel
+// Short-row kernel CTAs resident per SM (1024 threads of at most 32 registers, two by the launch
+// bound; fewer when its shared memory does not fit twice) and the waves of them it takes by default.
+constexpr int kShortCtasPerSm = 2;
+constexpr int kShortWaves = 4;
+
+int64_t short_slots(int64_t row_stride, int sms, int smem_per_sm, int smem_reserved) {
+  const int by_smem = smem_per_sm / int(gvr::short_smem_bytes(row_stride) + size_t(smem_reserved));
+  return int64_t(sms) * (by_smem < kShortCtasPerSm ? by_smem : kShortCtasPerSm);
+}
+
+// The short-row kernel (one CTA per row, the window resident in shared memory) takes the plain
+// calls -- no flags, no cluster tuning, not the hinted or block-skip entry points -- whose stride
+// fits it and whose rows its CTAs cover in at most kShortWaves waves: measured faster than the
+// cluster kernel there (single rows 13-17 %, batches of 16 to 1024 rows 6-35 %), slower on
+// batches of thousands of rows (the 4096-row prefill tile), where the cluster kernel streams
+// more rows at once.  GVR_FLAG_SHORT_KERNEL (with or without GVR_FLAG_FORCE_RESCUE) asks for it
+// whatever the row count; any other flag keeps the cluster kernel.
+bool use_short(int64_t row_stride, int64_t num_rows, bool plain_entry, int sms, int smem_per_sm,
+               int smem_reserved, const gvr_options* o) {
+  if (row_stride > gvr::SHORT_MAX || !plain_entry) return false;
   if (o && (o->cluster_size || o->ring_stages)) return false;
-  return true;
+  const int32_t flags = o ? o->flags : 0;
+  if ((flags & ~GVR_FLAG_FORCE_RESCUE) == GVR_FLAG_SHORT_KERNEL) return true;
+  if (flags != 0) return false;
+  return num_rows <= kShortWaves * short_slots(row_stride, sms, smem_per_sm, smem_reserved);
 }
 
 gvr_status launch_short(const gvr::Params& prm, int64_t num_rows, void* stream) {
@@ -236,21 +255,21 @@ gvr_status launch_short(const gvr::Params& prm, int64_t num_rows, void* stream) 
   q.compress_ratio = prm.compress_ratio;
   q.k = prm.k;
   q.mode = prm.mode;
+  q.flags = prm.flags & GVR_FLAG_FORCE_RESCUE;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(num_rows), 1, 1);
   cfg.blockDim = dim3(gvr::SHORT_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = gvr::short_smem_bytes(prm.row_stride);
   cfg.stream = static_cast<cudaStream_t>(stream);
-  const int vpt = gvr::short_vpt(prm.row_stride);
-  const cudaError_t e = vpt == 4   ? cudaLaunchKernelEx(&cfg, gvr::gvr_short_kernel<4>, q)
-                        : vpt == 8 ? cudaLaunchKernelEx(&cfg, gvr::gvr_short_kernel<8>, q)
-                                   : cudaLaunchKernelEx(&cfg, gvr::gvr_short_kernel<16>, q);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gvr::gvr_short_kernel, q);
   return e == cudaSuccess ? GVR_OK : GVR_ERR_LAUNCH;
 }
 
 gvr_status launch(const gvr::Params& prm, int64_t num_rows, const gvr_options* o, void* stream) {
   int sms = 0, smem_per_sm = 0, smem_reserved = 0;
   if (device_state(&sms, &smem_per_sm, &smem_reserved) != cudaSuccess) return GVR_ERR_LAUNCH;
-  if (use_short(prm, o)) return launch_short(prm, num_rows, stream);
+  if (use_short(prm.row_stride, num_rows, !prm.pre_idx && !prm.block_max, sms, smem_per_sm, smem_reserved, o))
+    return launch_short(prm, num_rows, stream);
   Geometry geo = plan_geometry(prm.row_stride, num_rows, prm.k, sms, smem_per_sm, smem_reserved, o);
   if (geo.cs == 16 && !(o && o->cluster_size == 16)) {
     // A 16-CTA cluster needs 16 SMs of one GPC with room for it: checked once per ring depth,
@@ -693,6 +712,13 @@ gvr_status gvr_plan(int64_t row_stride, int64_t num_rows, int32_t k, const gvr_o
   if (s != GVR_OK) return s;
   int sms = sm_count, smem_per_sm = kDefaultSmemPerSm, smem_reserved = kDefaultSmemReserved;
   if (sms <= 0 && device_state(&sms, &smem_per_sm, &smem_reserved) != cudaSuccess) return GVR_ERR_LAUNCH;
+  if (use_short(row_stride, num_rows, true, sms, smem_per_sm, smem_reserved, options)) {
+    if (cluster_size) *cluster_size = 1;
+    if (ring_stages) *ring_stages = 0;
+    if (threads) *threads = gvr::SHORT_THREADS;
+    if (smem_bytes) *smem_bytes = int32_t(gvr::short_smem_bytes(row_stride));
+    return GVR_OK;
+  }
   const Geometry geo = plan_geometry(row_stride, num_rows, k, sms, smem_per_sm, smem_reserved, options);
   if (cluster_size) *cluster_size = geo.cs;
   if (ring_stages) *ring_stages = geo.nstage;

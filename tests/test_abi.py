@@ -156,7 +156,13 @@ def test_option_errors(lib):
 @pytest.mark.parametrize("k", [512, 2048])
 def test_plan_geometry(lib, stride, rows, k):
     import sparse_attention_indexer_exact_gb300 as gvr
-    p = gvr.plan(stride, rows, k, sm_count=152)
+    d = gvr.plan(stride, rows, k, sm_count=152)
+    if stride <= 16384 and rows <= 4 * 2 * 152:  # the short-row kernel: four waves of two CTAs per SM
+        assert (d["cluster_size"], d["ring_stages"], d["threads"]) == (1, 0, 1024), d
+        assert 16 * (stride // 4 + 1) < d["smem_bytes"] <= (228 * 1024 - 2 * 1024) // 2, d
+    else:
+        assert d["threads"] == 128, d
+    p = gvr.plan(stride, rows, k, gvr.Options(flags=256), sm_count=152)  # the cluster kernel's geometry
     cs = p["cluster_size"]
     assert cs in (1, 2, 4, 8, 16)
     share_vec = -(-(stride // 4) // cs)
@@ -176,6 +182,20 @@ def test_plan_geometry(lib, stride, rows, k):
         # cluster stays resident at once, and never deeper than the share
         assert per_sm >= per_sm_min or rows * cs <= 152 * per_sm
         assert p["ring_stages"] <= -(-share_vec // 256)
+
+
+def test_plan_short_kernel_policy(lib):
+    """Plain calls go to the short-row kernel while the stride fits it and the rows fit four
+    waves of its CTAs; flags other than its own (and forced rescue) keep the cluster kernel."""
+    import sparse_attention_indexer_exact_gb300 as gvr
+    short = lambda stride, rows, o=None: gvr.plan(stride, rows, 1024, o, sm_count=152)["threads"] == 1024
+    assert short(16384, 1216) and not short(16384, 1217) and not short(16388, 1)
+    assert short(4, 1) and short(8192, 64)
+    assert short(16384, 4096, gvr.Options(flags=4096)) and short(16384, 4096, gvr.Options(flags=4096 | 1))
+    for flags in (1, 2, 4, 8, 16, 32, 64, 128, 256, 2048):
+        assert not short(8192, 1, gvr.Options(flags=flags)), flags
+    assert not short(8192, 1, gvr.Options(cluster_size=2)) and not short(8192, 1, gvr.Options(ring_stages=4))
+    assert short(8192, 1, gvr.Options(row_stats=0))
 
 
 def test_plan_respects_overrides(lib):

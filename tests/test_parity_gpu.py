@@ -239,8 +239,10 @@ def test_prefill_misaligned_neg_inf_class(gvr):
     got, _ = run_prefill(gvr, case)
     assert got.min() >= 0
     long_rows = case.window_lengths() > k
-    st = assert_prefill_exact(gvr, case, stats=True)
+    st = assert_prefill_exact(gvr, case, stats=True, options=gvr.Options(flags=256))
     assert (st[long_rows, 0] == 9).all(), st[:, 0]  # cluster kernel, tau = -inf: the -inf fill
+    st = assert_prefill_exact(gvr, case, stats=True)
+    assert (st[long_rows, 0] == 11).all(), st[:, 0]  # by default the short-row kernel: radix over the row
     st = assert_prefill_exact(gvr, case, stats=True, options=gvr.Options(flags=4096))
     assert (st[long_rows, 0] == 11).all(), st[:, 0]  # short-row kernel: radix over the row
 
@@ -781,7 +783,7 @@ SHORT, CLUSTER = 4096, 256
 @pytest.mark.parametrize("bs,n,k", [(1, 16384, 512), (4, 16384, 2048), (16, 16384, 1024), (256, 16384, 512),
                                     (64, 8192, 2048), (3, 4100, 1024)])
 def test_short_stride_cells(gvr, kernel, bs, n, k):
-    """Rows that fit one CTA's registers, through the short-row kernel and the cluster
+    """Rows that fit one CTA's shared memory, through the short-row kernel and the cluster
     kernel: decode and prefill (every lead), heavy-tailed scores."""
     st = assert_decode_exact(gvr, workloads.sweep_decode(bs, n, k), options=gvr.Options(flags=kernel), stats=True)
     if kernel == SHORT:
@@ -795,11 +797,14 @@ def test_short_kernel_single_row(gvr, values):
                              options=gvr.Options(flags=SHORT))
     assert st[0, 0] == 10
     st = assert_decode_exact(gvr, workloads.single_decode_row(), values=values, stats=True)
-    assert st[0, 0] in (1, 5, 6)  # the default is the cluster kernel
+    assert st[0, 0] == 10  # the default for a row this short
+    st = assert_decode_exact(gvr, workloads.single_decode_row(), values=values, stats=True,
+                             options=gvr.Options(flags=CLUSTER))
+    assert st[0, 0] in (1, 5, 6)
 
 
 def test_short_kernel_tie_heavy_rows(gvr):
-    """Rows the histogram cannot decide take the exact radix over the row in registers:
+    """Rows the histogram cannot decide take the exact radix over the staged row:
     one value, two values, a -inf class holding tau, a +inf class, signed zero at tau, plateaus."""
     g = np.random.default_rng(71)
     rows, stride, k = 9, 16384, 1024
