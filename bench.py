@@ -485,10 +485,11 @@ def run_sweep(args):
     return 0
 
 
-def run_prefill_tile(args):
-    """The 4096-row prefill tile alone, through topk_prefill: --steps graph-replayed calls rotating
-    over --copies device copies of the tile (cold L2), CUDA events on the launching stream; one
-    JSON line (not the headline)."""
+def run_one_workload(args):
+    """One workload alone, for profiling it (not the headline): the 4096-row prefill tile through
+    topk_prefill, or the single 8192-score decode row (K = 512) through topk_decode; --steps
+    graph-replayed calls rotating over --copies device copies, CUDA events on the launching
+    stream; one JSON line."""
     import torch
     import workloads
     import sparse_attention_indexer_exact_gb300 as gvr
@@ -498,17 +499,25 @@ def run_prefill_tile(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     gvr.load_library()
-    case = workloads.prefill_tile()
+    tile = args.workload == "prefill_tile"
+    case = workloads.prefill_tile() if tile else workloads.single_decode_row()
     copies = max(1, args.copies)
     bufs = [torch.from_numpy(case.logits).to(dev) for _ in range(copies)]
-    ks = torch.from_numpy(case.row_starts).to(dev)
-    ke = torch.from_numpy(case.row_ends).to(dev)
     idx = torch.empty((case.rows, case.k), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
+    if tile:
+        ks = torch.from_numpy(case.row_starts).to(dev)
+        ke = torch.from_numpy(case.row_ends).to(dev)
 
-    def launch(buf, h):
-        gvr.topk_prefill_raw(buf.data_ptr(), case.row_stride, case.rows, ks.data_ptr(), ke.data_ptr(), case.k,
-                             idx.data_ptr(), h)
+        def launch(buf, h):
+            gvr.topk_prefill_raw(buf.data_ptr(), case.row_stride, case.rows, ks.data_ptr(), ke.data_ptr(), case.k,
+                                 idx.data_ptr(), h)
+    else:
+        kv = torch.from_numpy(case.kv_lens).to(dev)
+
+        def launch(buf, h):
+            gvr.topk_decode_raw(buf.data_ptr(), case.row_stride, case.rows, kv.data_ptr(), case.next_n,
+                                case.compress_ratio, case.k, idx.data_ptr(), None, h)
 
     for i in range(args.warmup):
         launch(bufs[i % copies], stream.cuda_stream)
@@ -527,9 +536,9 @@ def run_prefill_tile(args):
     e1.record(stream)
     torch.cuda.synchronize()
     per = e0.elapsed_time(e1) * 1e3 / (reps * copies)
-    nbytes = prefill_algorithmic_bytes(case)
+    nbytes = prefill_algorithmic_bytes(case) if tile else algorithmic_bytes(case, False)
     peak, peak_kind = measured_peak_hbm()
-    print(json.dumps({"workload": case.meta.get("workload", "prefill tile"), "rows": case.rows, "k": case.k,
+    print(json.dumps({"workload": case.meta.get("workload", args.workload), "rows": case.rows, "k": case.k,
                       "calls": reps * copies, "copies": copies, "us_per_call": per,
                       "rows_per_s": case.rows / (per * 1e-6), "algorithmic_bytes": nbytes,
                       "frac_of_measured": nbytes / per / 1e3 / peak, "peak_kind": peak_kind}))
@@ -560,14 +569,15 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the sweep_big / tail / single_row / prefill_tile keys")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the headline line: every sweep cell and the adversarial tail check")
-    ap.add_argument("--workload", choices=["decode_batch", "prefill_tile"], default="decode_batch",
-                    help="prefill_tile: one line for the 4096-row prefill tile alone (for profiling it)")
+    ap.add_argument("--workload", choices=["decode_batch", "prefill_tile", "single_row"], default="decode_batch",
+                    help="prefill_tile / single_row: one line for the 4096-row prefill tile or the single "
+                         "8192-score decode row alone (for profiling it)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.sweep:
         return run_sweep(args)
-    if args.workload == "prefill_tile":
-        return run_prefill_tile(args)
+    if args.workload in ("prefill_tile", "single_row"):
+        return run_one_workload(args)
 
     import workloads
     ws, rank, local = dist_env()
