@@ -43,9 +43,10 @@ def _kv_schedule(k, cr, next_n, stride, steps):
     return [np.minimum(starts + s * grow, cr * stride + next_n).astype(np.int32) for s in range(steps)]
 
 
-@pytest.mark.parametrize("flags", [0, 32])
-def test_graph_replay_with_growing_kv_lens(gvr, flags):
-    k, cr, next_n, stride = 1024, 4, 2, 65536
+@pytest.mark.parametrize("stride,flags", [(65536, 0), (65536, 32), (16384, 0)])
+def test_graph_replay_with_growing_kv_lens(gvr, stride, flags):
+    """The cluster kernel (65536-score rows) and, for 16384-score rows, the short-row kernel."""
+    k, cr, next_n = 1024, 4, 2
     sched = _kv_schedule(k, cr, next_n, stride, steps=6)
     reqs = len(sched[0])
     rows = reqs * next_n
@@ -75,6 +76,7 @@ def test_graph_replay_with_growing_kv_lens(gvr, flags):
         gvr.topk_decode(lg, kv, next_n, cr, k, indices=idx, values=vals, options=opts)
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
+    assert (gvr.plan(stride, rows, k, opts)["threads"] == 1024) == (stride <= 16384)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         gvr.topk_decode(lg, kv, next_n, cr, k, indices=idx, values=vals, options=opts)
