@@ -21,6 +21,10 @@
  * bracket finds the bin that crosses tau; the members of that bin go to a bounded candidate
  * buffer and an exact refine picks the remaining winners; an invalid bracket or an overflowing
  * buffer sends the row to an exact radix rescue that runs on every CTA of the row's cluster.
+ * Which kernel runs is decided on the host from row_stride, num_rows and the options alone: a
+ * cluster of CTAs per row streaming the window through a shared-memory ring, or, for plain
+ * calls with row_stride <= 16384 and at most four waves of rows, one CTA per row holding the
+ * whole window in shared memory (GVR_FLAG_SHORT_KERNEL); the results are exact either way.
  *
  * Conventions shared by every entry point.
  *   - All pointers except `options` are DEVICE pointers into memory the caller owns.  The
