@@ -137,13 +137,14 @@ enum {
   GVR_FLAG_SPLIT_ALONE = 512,
   /* *_ws entry points: the balanced kernel whenever the call fits it */
   GVR_FLAG_SPLIT_KERNEL = 1024,
-  /* diagnostics (cluster kernel): the first row's cluster reports a device-side give-up once its
-   * first pass is complete (every bulk copy landed, no wait shortened), so that row's indices
-   * become -2 and its row_stats path GVR_PATH_DEVICE_ERROR while the other rows stay exact --
-   * the failure path without a failure */
+  /* diagnostics: the first row's cluster reports a device-side give-up once its first pass is
+   * complete (every bulk copy landed, no wait shortened) -- with GVR_FLAG_SHORT_KERNEL the
+   * short-row kernel's CTA of row 0, once its window has landed -- so that row's indices become
+   * -2 and its row_stats path GVR_PATH_DEVICE_ERROR while the other rows stay exact: the failure
+   * path without a failure */
   GVR_FLAG_DIAG_FAIL_ROW0 = 2048,
   /* the short-row kernel for calls it takes (row_stride <= 16384, no flag but
-   * GVR_FLAG_FORCE_RESCUE, no cluster or ring setting, not the hinted or block-skip entry
+   * GVR_FLAG_FORCE_RESCUE or GVR_FLAG_DIAG_FAIL_ROW0, no cluster or ring setting, not the hinted or block-skip entry
    * points; others run the cluster kernel) whatever the row count: one CTA of 1024 threads per
    * row stages the whole window in shared memory with bulk copies and selects over it.  Calls
    * with no flag take it by default when row_stride <= 16384 and the rows fit four waves of its

@@ -50,7 +50,7 @@ struct ShortParams {
   int32_t compress_ratio;
   int32_t k;
   int32_t mode;
-  int32_t flags;              // FLAG_FORCE_RESCUE or 0
+  int32_t flags;              // FLAG_FORCE_RESCUE, FLAG_DIAG_FAIL_ROW0 or 0
 };
 
 struct alignas(16) ShortSmem {
@@ -323,6 +323,8 @@ __global__ void __launch_bounds__(SHORT_THREADS, 2) gvr_short_kernel(const Short
   // ---------------------------------------------------------------- wait for the window
   // Warp 0 waits on the copies' mbarrier; the CTA barrier passes what it saw on to the others.
   if (warp == 0 && !mbar_wait_bounded(&S.bar, 0, WAIT_LIMIT_NS)) S.tout = 1;
+  // diagnostics: row 0 reports a give-up once its window has landed (no copy in flight)
+  if (tid == 0 && (p.flags & FLAG_DIAG_FAIL_ROW0) && row == 0) S.tout = 1;
   __syncthreads();
   if (S.tout) {  // gave up: wait (bounded) for the copies still in flight, then mark the row
     if (tid == 0) mbar_wait_bounded(&S.bar, 0, WAIT_LIMIT_NS);

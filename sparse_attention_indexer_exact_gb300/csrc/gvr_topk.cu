@@ -228,14 +228,15 @@ int64_t short_slots(int64_t row_stride, int sms, int smem_per_sm, int smem_reser
 // fits it and whose rows its CTAs cover in at most kShortWaves waves: measured faster than the
 // cluster kernel there (single rows 13-17 %, batches of 16 to 1024 rows 6-35 %), slower on
 // batches of thousands of rows (the 4096-row prefill tile), where the cluster kernel streams
-// more rows at once.  GVR_FLAG_SHORT_KERNEL (with or without GVR_FLAG_FORCE_RESCUE) asks for it
-// whatever the row count; any other flag keeps the cluster kernel.
+// more rows at once.  GVR_FLAG_SHORT_KERNEL (with or without GVR_FLAG_FORCE_RESCUE and
+// GVR_FLAG_DIAG_FAIL_ROW0) asks for it whatever the row count; any other flag keeps the cluster
+// kernel.
 bool use_short(int64_t row_stride, int64_t num_rows, bool plain_entry, int sms, int smem_per_sm,
                int smem_reserved, const gvr_options* o) {
   if (row_stride > gvr::SHORT_MAX || !plain_entry) return false;
   if (o && (o->cluster_size || o->ring_stages)) return false;
   const int32_t flags = o ? o->flags : 0;
-  if ((flags & ~GVR_FLAG_FORCE_RESCUE) == GVR_FLAG_SHORT_KERNEL) return true;
+  if ((flags & ~(GVR_FLAG_FORCE_RESCUE | GVR_FLAG_DIAG_FAIL_ROW0)) == GVR_FLAG_SHORT_KERNEL) return true;
   if (flags != 0) return false;
   return num_rows <= kShortWaves * short_slots(row_stride, sms, smem_per_sm, smem_reserved);
 }
@@ -255,7 +256,7 @@ gvr_status launch_short(const gvr::Params& prm, int64_t num_rows, void* stream) 
   q.compress_ratio = prm.compress_ratio;
   q.k = prm.k;
   q.mode = prm.mode;
-  q.flags = prm.flags & GVR_FLAG_FORCE_RESCUE;
+  q.flags = prm.flags & (GVR_FLAG_FORCE_RESCUE | GVR_FLAG_DIAG_FAIL_ROW0);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(num_rows), 1, 1);
   cfg.blockDim = dim3(gvr::SHORT_THREADS, 1, 1);

@@ -827,6 +827,40 @@ def test_short_kernel_tie_heavy_rows(gvr):
             assert st[1, 0] == 11 and st[2, 0] == 11 and st[3, 0] == 11, st[:, 0]
 
 
+def test_short_kernel_device_error_reporting(gvr):
+    """The short-row kernel's failure path, driven by the diagnostic flag: row 0 reports a give-up
+    once its window has landed; it reads -2 with the device-error path, every other row is exact."""
+    case = workloads.sweep_decode(8, 16384, 1024)
+    for flags in (SHORT | 2048, SHORT | 2048 | 1):
+        got, _, st = run_decode(gvr, case, values=False, options=gvr.Options(flags=flags), stats=True)
+        assert (got[0] == -2).all() and st[0, 0] == -1, (flags, got[0][:8], st[0])
+        ref, _, _ = oracle.topk_decode(case.logits, case.kv_lens, case.next_n, case.compress_ratio, case.k)
+        wins = list(decode_windows(case.logits, case.kv_lens, case.next_n, case.compress_ratio))[1:]
+        bad, why = compare_rows(iter(wins), case.k, got, ref)  # rows 1.. (row indices kept)
+        assert bad == 0, why
+        assert np.isin(st[1:, 0], [10, 11]).all(), st[:, 0]
+
+
+def test_short_kernel_list_overflow(gvr):
+    """A cluster of high scores that the block64 samples never see: the floor lets through more
+    scores than the kernel lists (4096), and the row takes the exact radix over the window."""
+    g = np.random.default_rng(73)
+    stride, k = 16384, 512
+    lg = g.standard_normal((2, stride)).astype(np.float32)
+    nsamp, nv = 512, stride  # K samples in K/64 runs of 64 (the row needs no more)
+    nblk = nsamp // 64
+    sampled = np.zeros(stride, bool)
+    for b in range(nblk):
+        st0 = b * (nv - 64) // (nblk - 1)
+        sampled[st0:st0 + 64] = True
+    hidden = np.flatnonzero(~sampled)[:6000]
+    lg[0, hidden] = (5.0 + g.random(hidden.size)).astype(np.float32)
+    lg[1, hidden[:3000]] = (5.0 + g.random(3000)).astype(np.float32)  # below the list's capacity
+    case = workloads.DecodeCase("hidden_cluster", lg, np.full(2, stride, np.int32), 1, 1, k)
+    st = assert_decode_exact(gvr, case, values=True, stats=True)
+    assert st[0, 0] == 11, st[:, 0]
+
+
 def test_short_kernel_boundaries_and_nan(gvr):
     g = np.random.default_rng(72)
     for k in (512, 2048):
