@@ -192,6 +192,9 @@ def test_plan_short_kernel_policy(lib):
     assert short(16384, 1216) and not short(16384, 1217) and not short(16388, 1)
     assert short(4, 1) and short(8192, 64)
     assert short(16384, 4096, gvr.Options(flags=4096)) and short(16384, 4096, gvr.Options(flags=4096 | 1))
+    assert short(8192, 1, gvr.Options(flags=4096 | 2048)) and short(8192, 1, gvr.Options(flags=4096 | 2048 | 1))
+    for flags in (4096 | 16, 4096 | 32, 4096 | 128, 4096 | 2):  # its flag with another: the cluster kernel
+        assert not short(8192, 1, gvr.Options(flags=flags)), flags
     for flags in (1, 2, 4, 8, 16, 32, 64, 128, 256, 2048):
         assert not short(8192, 1, gvr.Options(flags=flags)), flags
     assert not short(8192, 1, gvr.Options(cluster_size=2)) and not short(8192, 1, gvr.Options(ring_stages=4))
